@@ -1,0 +1,181 @@
+"""fp64 CPU oracle for packed mixed-mask variable-length attention.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
+package.  The CUDA library never imports, links or calls it, and it imports
+nothing from the CUDA library.
+
+The arithmetic lives in ``pk_oracle.c`` (plain C, fp64, OpenMP over rows);
+this module only compiles it with gcc and marshals numpy arrays through
+ctypes.  What it computes, with the passages it follows, is stated at the top
+of ``pk_oracle.c``:
+
+* packing over ``cu_seqlens`` with no cross-sequence attention
+  ("[RFC]: HunyuanImage 3.0 deployment", Proposed Change, P0 "Packed
+  Attention for Multi-Request Batching");
+* the generalized causal mask, text causal and image tokens seeing their
+  whole own segment (same page, P0 "Attention mask challenge"; "Model
+  structure", item 1), materialised densely per sequence;
+* grouped-query heads, query head h reading key/value head h // (Hq // Hkv);
+* fp64 scores, a max-subtracted natural-log LSE and the softmax-weighted
+  sum of V.
+
+Every function here is pinned by ``tests/test_oracle.py`` against closed
+forms, library special cases (textbook causal and full attention), a
+hand-derived mask fixture and invariants.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pk_oracle.c")
+_LIB_DIR = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_LIB_DIR, "libpk_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+TEXT = 0
+IMAGE = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile ``pk_oracle.c`` into ``_build/libpk_oracle.so`` with gcc."""
+    os.makedirs(_LIB_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        u16p = ctypes.POINTER(ctypes.c_uint16)
+        f64p = ctypes.POINTER(ctypes.c_double)
+        lib.pko_validate.argtypes = [i32p, ctypes.c_int32, i32p, ctypes.c_int32]
+        lib.pko_validate.restype = ctypes.c_int
+        lib.pko_mask_dense.argtypes = [i32p, ctypes.c_int32, i32p, ctypes.c_int32,
+                                       ctypes.c_int32, ctypes.POINTER(ctypes.c_uint8)]
+        lib.pko_mask_dense.restype = ctypes.c_int
+        lib.pko_visible_pairs.argtypes = [i32p, ctypes.c_int32, i32p, ctypes.c_int32]
+        lib.pko_visible_pairs.restype = ctypes.c_int64
+        lib.pko_attention.argtypes = [u16p, u16p, u16p, i32p, ctypes.c_int32, i32p,
+                                      ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                      ctypes.c_int32, ctypes.c_double, i32p,
+                                      ctypes.c_int32, f64p, f64p, ctypes.c_int32]
+        lib.pko_attention.restype = ctypes.c_int
+        lib.pko_bf16_to_double.argtypes = [ctypes.c_uint16]
+        lib.pko_bf16_to_double.restype = ctypes.c_double
+        lib.pko_max_threads.argtypes = []
+        lib.pko_max_threads.restype = ctypes.c_int32
+        _lib = lib
+        return lib
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _ptr(a: np.ndarray, ct):
+    return a.ctypes.data_as(ctypes.POINTER(ct))
+
+
+def _segs_array(segments) -> np.ndarray:
+    arr = _i32(segments).reshape(-1, 3) if len(segments) else np.zeros((0, 3), np.int32)
+    return np.ascontiguousarray(arr)
+
+
+def _bits(x) -> np.ndarray:
+    """bf16 tensor / uint16 array -> contiguous uint16 bit patterns."""
+    if isinstance(x, np.ndarray):
+        assert x.dtype == np.uint16
+        return np.ascontiguousarray(x)
+    import torch  # local: only for tensors handed in by tests
+    assert x.dtype == torch.bfloat16 and x.device.type == "cpu"
+    return np.ascontiguousarray(x.contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def bf16_to_double(bits: int) -> float:
+    return float(_load().pko_bf16_to_double(ctypes.c_uint16(bits)))
+
+
+def validate(cu_seqlens, segments) -> int:
+    cu = _i32(cu_seqlens)
+    sg = _segs_array(segments)
+    return int(_load().pko_validate(_ptr(cu, ctypes.c_int32), len(cu) - 1,
+                                    _ptr(sg, ctypes.c_int32), sg.shape[0]))
+
+
+def dense_mask(cu_seqlens, segments, s: int) -> np.ndarray:
+    """The explicit L x L bool mask of sequence ``s`` (row = query)."""
+    cu = _i32(cu_seqlens)
+    sg = _segs_array(segments)
+    L = int(cu[s + 1] - cu[s])
+    M = np.zeros((L, L), dtype=np.uint8)
+    rc = _load().pko_mask_dense(_ptr(cu, ctypes.c_int32), len(cu) - 1,
+                                _ptr(sg, ctypes.c_int32), sg.shape[0], s,
+                                _ptr(M, ctypes.c_uint8))
+    if rc:
+        raise ValueError(f"oracle: invalid descriptors (code {rc})")
+    return M.astype(bool)
+
+
+def visible_pairs(cu_seqlens, segments) -> int:
+    """Visible (query, key) pairs of the pack for one head."""
+    cu = _i32(cu_seqlens)
+    sg = _segs_array(segments)
+    n = int(_load().pko_visible_pairs(_ptr(cu, ctypes.c_int32), len(cu) - 1,
+                                      _ptr(sg, ctypes.c_int32), sg.shape[0]))
+    if n < 0:
+        raise ValueError("oracle: invalid descriptors")
+    return n
+
+
+def attention(q, k, v, cu_seqlens, segments, hq: int, hkv: int, d: int,
+              scale: float, rows=None, nthreads: int = 0):
+    """fp64 packed masked attention.
+
+    q: bf16 [T, hq, d]; k, v: bf16 [T, hkv, d] (torch CPU tensors or uint16
+    bit arrays).  Returns (out fp64 [R, hq, d], lse fp64 [hq, R]) with R = T,
+    or R = len(rows) when ``rows`` lists global token indices.
+    """
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    cu = _i32(cu_seqlens)
+    sg = _segs_array(segments)
+    T = int(cu[-1])
+    assert qb.size == T * hq * d and kb.size == T * hkv * d and vb.size == T * hkv * d
+    if rows is None:
+        R, rp, nr = T, None, 0
+    else:
+        rr = _i32(rows)
+        R, rp, nr = rr.size, _ptr(rr, ctypes.c_int32), rr.size
+    out = np.zeros((R, hq, d), dtype=np.float64)
+    lse = np.zeros((hq, R), dtype=np.float64)
+    rc = _load().pko_attention(_ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16),
+                               _ptr(vb, ctypes.c_uint16), _ptr(cu, ctypes.c_int32),
+                               len(cu) - 1, _ptr(sg, ctypes.c_int32), sg.shape[0],
+                               hq, hkv, d, float(scale), rp, nr,
+                               _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double),
+                               int(nthreads))
+    if rc:
+        raise ValueError(f"oracle: invalid arguments (code {rc})")
+    return out, lse
+
+
+def max_threads() -> int:
+    return int(_load().pko_max_threads())

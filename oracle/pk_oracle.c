@@ -1,0 +1,266 @@
+/*
+ * pk_oracle.c -- plain, slow, fp64 CPU oracle for packed variable-length
+ * attention with the HunyuanImage-3.0 "generalized causal" mask.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file; only the tests, the smoke check and the CPU-baseline leg
+ * of the benchmark do.  It shares no code with the CUDA library.
+ *
+ * What it computes (the plain definition, no tiling, no fusion):
+ *
+ *   Packing.  Requests are packed back to back into one token stream; the
+ *   sequence s owns tokens [cu_seqlens[s], cu_seqlens[s+1]).  No attention
+ *   crosses sequences and nothing is padded.
+ *     -- "[RFC]: HunyuanImage 3.0 deployment", Proposed Change, P0
+ *        "Packed Attention for Multi-Request Batching": contiguous packing
+ *        with cu_seqlens replaces batch duplication, padding and the
+ *        explicit (bsz,1,seqlen,seqlen) mask (Motivation, item (1)).
+ *
+ *   Mask.  Inside a sequence of length L, query row i sees key j iff
+ *        j <= i                                  (text tokens are causal)
+ *     or seg(i) is an IMAGE segment and seg(j) == seg(i)
+ *                                  (image tokens see their whole own segment)
+ *     -- same page, P0 bullet "Attention mask challenge" (generalized causal
+ *        attention: text causal, image bidirectional) and "Model structure",
+ *        item 1 (image patches attend to each other simultaneously).
+ *     The dense L x L mask is materialised per sequence, exactly as the
+ *     replaced path would.
+ *
+ *   Heads.  Query head h reads key/value head g = h / (Hq / Hkv)
+ *     (grouped-query attention, contiguous groups).
+ *
+ *   Scores, LSE, output (fp64 throughout, from the bf16 input values):
+ *        s_ij  = scale * sum_c q[i,h,c] * k[j,g,c]
+ *        lse_i = ln sum_{j visible} exp(s_ij)      (max-subtracted)
+ *        o_i   = sum_{j visible} exp(s_ij - lse_i) * v[j,g,:]
+ *
+ * Layouts: q [T][Hq][d], k and v [T][Hkv][d] as raw bf16 bit patterns
+ * (uint16); out [rows][Hq][d] fp64; lse [Hq][rows] fp64, where rows is T for
+ * the full call or n_rows for the sampled call.  Segments are int32 triples
+ * {start (global token index), len, type (0 = text, 1 = image)}.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define PKO_TEXT 0
+#define PKO_IMAGE 1
+
+/* bf16 -> double: a bf16 value is the top 16 bits of an IEEE binary32. */
+double pko_bf16_to_double(uint16_t bits) {
+  uint32_t u = ((uint32_t)bits) << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* Descriptor check: cu_seqlens starts at 0 and never decreases; segments are
+ * in order, non-empty, typed 0/1, and tile every sequence exactly.
+ * Returns 0 when valid, a positive code otherwise. */
+int pko_validate(const int32_t* cu, int32_t num_seqs, const int32_t* segs,
+                 int32_t num_segs) {
+  if (num_seqs < 0 || num_segs < 0) return 1;
+  if (cu[0] != 0) return 2;
+  for (int32_t s = 0; s < num_seqs; ++s)
+    if (cu[s + 1] < cu[s]) return 3;
+  int32_t g = 0;
+  for (int32_t s = 0; s < num_seqs; ++s) {
+    int32_t pos = cu[s];
+    while (pos < cu[s + 1]) {
+      if (g >= num_segs) return 4;
+      const int32_t* sg = segs + 3 * g;
+      if (sg[0] != pos || sg[1] <= 0) return 5;
+      if (sg[2] != PKO_TEXT && sg[2] != PKO_IMAGE) return 6;
+      if (sg[0] + sg[1] > cu[s + 1]) return 7;
+      pos += sg[1];
+      ++g;
+    }
+  }
+  if (g != num_segs) return 8;
+  return 0;
+}
+
+/* Segment index of every token of the pack (explicit lookup table). */
+static int32_t* segment_of_tokens(int32_t T, const int32_t* segs,
+                                  int32_t num_segs) {
+  int32_t* seg_of = (int32_t*)malloc(sizeof(int32_t) * (size_t)(T > 0 ? T : 1));
+  for (int32_t g = 0; g < num_segs; ++g)
+    for (int32_t t = segs[3 * g]; t < segs[3 * g] + segs[3 * g + 1]; ++t)
+      seg_of[t] = g;
+  return seg_of;
+}
+
+/* One row of the dense mask of sequence s: row_out[j] = 1 iff the i-th token
+ * of s (0-based inside s) sees the j-th token of s. */
+static void mask_row(int32_t b, int32_t L, int32_t i, const int32_t* seg_of,
+                     const int32_t* segs, uint8_t* row_out) {
+  int32_t gi = seg_of[b + i];
+  int is_image = segs[3 * gi + 2] == PKO_IMAGE;
+  for (int32_t j = 0; j < L; ++j) {
+    int causal = j <= i;
+    int own_image_segment = is_image && seg_of[b + j] == gi;
+    row_out[j] = (uint8_t)(causal || own_image_segment);
+  }
+}
+
+/* Dense bool mask of sequence s, M[i*L + j], L = cu[s+1]-cu[s]. */
+int pko_mask_dense(const int32_t* cu, int32_t num_seqs, const int32_t* segs,
+                   int32_t num_segs, int32_t s, uint8_t* M) {
+  int rc = pko_validate(cu, num_seqs, segs, num_segs);
+  if (rc) return rc;
+  if (s < 0 || s >= num_seqs) return 9;
+  int32_t T = cu[num_seqs];
+  int32_t* seg_of = segment_of_tokens(T, segs, num_segs);
+  int32_t b = cu[s], L = cu[s + 1] - cu[s];
+  for (int32_t i = 0; i < L; ++i) mask_row(b, L, i, seg_of, segs, M + (size_t)i * L);
+  free(seg_of);
+  return 0;
+}
+
+/* Number of visible (query, key) pairs of the whole pack, per head, counted
+ * from the dense mask rule. */
+int64_t pko_visible_pairs(const int32_t* cu, int32_t num_seqs,
+                          const int32_t* segs, int32_t num_segs) {
+  if (pko_validate(cu, num_seqs, segs, num_segs)) return -1;
+  int32_t T = cu[num_seqs];
+  int32_t* seg_of = segment_of_tokens(T, segs, num_segs);
+  int64_t total = 0;
+  for (int32_t s = 0; s < num_seqs; ++s) {
+    int32_t b = cu[s], L = cu[s + 1] - cu[s];
+    uint8_t* row = (uint8_t*)malloc((size_t)(L > 0 ? L : 1));
+    for (int32_t i = 0; i < L; ++i) {
+      mask_row(b, L, i, seg_of, segs, row);
+      for (int32_t j = 0; j < L; ++j) total += row[j];
+    }
+    free(row);
+  }
+  free(seg_of);
+  return total;
+}
+
+/* Attention of one query row (all query heads) over its sequence, given the
+ * row of the dense mask.  q_row points at q[i][0][0]; k_seq / v_seq at the
+ * first token of the sequence.  Writes out_row[Hq][d] and lse[h*lse_stride]. */
+static void attend_row(const uint16_t* q_row, const uint16_t* k_seq,
+                       const uint16_t* v_seq, const uint8_t* mrow, int32_t L,
+                       int32_t Hq, int32_t Hkv, int32_t d, double scale,
+                       double* out_row, double* lse, int64_t lse_stride,
+                       double* s_buf, double* qd) {
+  int32_t group = Hq / Hkv;
+  for (int32_t h = 0; h < Hq; ++h) {
+    int32_t g = h / group;
+    for (int32_t c = 0; c < d; ++c)
+      qd[c] = pko_bf16_to_double(q_row[(size_t)h * d + c]);
+    double m = -INFINITY;
+    for (int32_t j = 0; j < L; ++j) {
+      if (!mrow[j]) continue;
+      const uint16_t* kj = k_seq + ((size_t)j * Hkv + g) * d;
+      double acc = 0.0;
+      for (int32_t c = 0; c < d; ++c) acc += qd[c] * pko_bf16_to_double(kj[c]);
+      s_buf[j] = scale * acc;
+      if (s_buf[j] > m) m = s_buf[j];
+    }
+    double denom = 0.0;
+    for (int32_t j = 0; j < L; ++j)
+      if (mrow[j]) denom += exp(s_buf[j] - m);
+    double lse_h = m + log(denom);
+    lse[(int64_t)h * lse_stride] = lse_h;
+    double* o = out_row + (size_t)h * d;
+    for (int32_t c = 0; c < d; ++c) o[c] = 0.0;
+    for (int32_t j = 0; j < L; ++j) {
+      if (!mrow[j]) continue;
+      double p = exp(s_buf[j] - lse_h);
+      const uint16_t* vj = v_seq + ((size_t)j * Hkv + g) * d;
+      for (int32_t c = 0; c < d; ++c) o[c] += p * pko_bf16_to_double(vj[c]);
+    }
+  }
+}
+
+/*
+ * Packed masked attention.
+ *   rows == NULL : every token; out [T][Hq][d], lse [Hq][T].  The dense mask
+ *                  of each sequence is built in full before its rows run.
+ *   rows != NULL : only the listed global token indices (any order);
+ *                  out [n_rows][Hq][d], lse [Hq][n_rows].  Each listed row
+ *                  builds its own row of the dense mask.
+ * nthreads <= 0 uses the OpenMP default.  Returns 0 or a validation code.
+ */
+int pko_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                  const int32_t* cu, int32_t num_seqs, const int32_t* segs,
+                  int32_t num_segs, int32_t Hq, int32_t Hkv, int32_t d,
+                  double scale, const int32_t* rows, int32_t n_rows,
+                  double* out, double* lse, int32_t nthreads) {
+  int rc = pko_validate(cu, num_seqs, segs, num_segs);
+  if (rc) return rc;
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return 10;
+  int32_t T = cu[num_seqs];
+  int32_t* seg_of = segment_of_tokens(T, segs, num_segs);
+  int32_t Lmax = 0;
+  for (int32_t s = 0; s < num_seqs; ++s)
+    if (cu[s + 1] - cu[s] > Lmax) Lmax = cu[s + 1] - cu[s];
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#endif
+  if (rows == NULL) {
+    for (int32_t s = 0; s < num_seqs; ++s) {
+      int32_t b = cu[s], L = cu[s + 1] - cu[s];
+      if (L == 0) continue;
+      uint8_t* M = (uint8_t*)malloc((size_t)L * L);
+      for (int32_t i = 0; i < L; ++i) mask_row(b, L, i, seg_of, segs, M + (size_t)i * L);
+#pragma omp parallel
+      {
+        double* s_buf = (double*)malloc(sizeof(double) * (size_t)L);
+        double* qd = (double*)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 4)
+        for (int32_t i = 0; i < L; ++i) {
+          int32_t t = b + i;
+          attend_row(q + (size_t)t * Hq * d, k + (size_t)b * Hkv * d,
+                     v + (size_t)b * Hkv * d, M + (size_t)i * L, L, Hq, Hkv, d,
+                     scale, out + (size_t)t * Hq * d, lse + t, T, s_buf, qd);
+        }
+        free(s_buf);
+        free(qd);
+      }
+      free(M);
+    }
+  } else {
+    for (int32_t r = 0; r < n_rows; ++r)
+      if (rows[r] < 0 || rows[r] >= T) { free(seg_of); return 11; }
+#pragma omp parallel
+    {
+      double* s_buf = (double*)malloc(sizeof(double) * (size_t)(Lmax > 0 ? Lmax : 1));
+      double* qd = (double*)malloc(sizeof(double) * (size_t)d);
+      uint8_t* mrow = (uint8_t*)malloc((size_t)(Lmax > 0 ? Lmax : 1));
+#pragma omp for schedule(dynamic, 1)
+      for (int32_t r = 0; r < n_rows; ++r) {
+        int32_t t = rows[r];
+        int32_t s = 0;
+        while (cu[s + 1] <= t) ++s;
+        int32_t b = cu[s], L = cu[s + 1] - cu[s];
+        mask_row(b, L, t - b, seg_of, segs, mrow);
+        attend_row(q + (size_t)t * Hq * d, k + (size_t)b * Hkv * d,
+                   v + (size_t)b * Hkv * d, mrow, L, Hq, Hkv, d, scale,
+                   out + (size_t)r * Hq * d, lse + r, n_rows, s_buf, qd);
+      }
+      free(s_buf);
+      free(qd);
+      free(mrow);
+    }
+  }
+  free(seg_of);
+  return 0;
+}
+
+/* Threads the OpenMP runtime would use (reported with the CPU baseline). */
+int32_t pko_max_threads(void) {
+#ifdef _OPENMP
+  return (int32_t)omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
