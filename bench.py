@@ -1,0 +1,413 @@
+"""Benchmark: packed mixed-mask attention, useful TFLOP/s on one GB300.
+
+One step = one pk_attn_fwd launch over the whole pack (all heads, all
+sequences) with inputs already resident in HBM; the plan is built once,
+outside the timed region (it is reused by every layer and denoising step).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line on rank 0.  ``--impl reference`` times the fp64 CPU
+oracle (the only reference that exists for this path) on a bounded row
+sample of the same workload.  Under torchrun each rank runs its own replica
+of the pack (independent packs: weak scaling, no collective on the data
+path); the timed region is bracketed by barriers and the max over ranks is
+reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "packed mixed-mask attention useful TFLOP/s & tokens/s; % of bf16 dense peak"
+NOMINAL_BF16_TFLOPS = 2250.0
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+KERNEL_SOURCES = ["packed_varlen_masked_gb300/csrc/pk_attn.cu",
+                  "packed_varlen_masked_gb300/csrc/tmem_ops.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "pk_attn_fwd_d128_mixed_resolution_traffic.md")
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            tf = d.get("bf16_tflops") or d.get("bf16_tflops_burst")
+            gb = d.get("hbm_gbs")
+            if tf and gb:
+                return {"bf16_tflops": float(tf), "hbm_gbs": float(gb),
+                        "bf16_tflops_sustained": d.get("bf16_tflops_sustained"),
+                        "source": "measured"}
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def load_traffic():
+    """Per-launch DRAM bytes from the committed ncu summary, valid only while
+    the kernel source is unchanged since the capture."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    text = open(TRAFFIC_FILE).read()
+    m_sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
+    m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_b or m_sha.group(1) != kernel_source_sha():
+        return None
+    return float(m_b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reference_arm(args, pack, rank, world):
+    """fp64 CPU oracle, as it stands, on bounded row samples of the pack."""
+    if rank != 0:
+        return
+    import oracle
+    import torch
+    import packed_varlen_masked_gb300 as pk  # planner only (host): FLOP count per row
+    q, k, v = W.make_qkv(pack)
+    plan = pk.Plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d, num_ctas=1,
+                   upload=False)
+    lim = plan.kv_limit()
+    cu = pack.cu_seqlens
+    seq_start = np.repeat(cu[:-1], np.diff(cu))
+    keys = (lim - seq_start + 1).astype(np.float64)
+    rng = np.random.default_rng(0)
+    # calibrate: rows per ~2 s step
+    probe = rng.integers(0, pack.total_tokens, size=32).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, cu, pack.segments, pack.hq, pack.hkv, pack.d, pack.scale, rows=probe)
+    dt = time.perf_counter() - t0
+    n_rows = int(max(16, min(4096, 32 * 2.0 / max(dt, 1e-6))))
+    times, flops = [], []
+    for step in range(args.warmup + args.steps):
+        rows = rng.integers(0, pack.total_tokens, size=n_rows).astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.attention(q, k, v, cu, pack.segments, pack.hq, pack.hkv, pack.d, pack.scale, rows=rows)
+        t = time.perf_counter() - t0
+        if step >= args.warmup:
+            times.append(t)
+            flops.append(4.0 * pack.d * pack.hq * keys[rows].sum())
+    total_t = sum(times)
+    tflops = sum(flops) / total_t / 1e12
+    cores = oracle.max_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total_t / len(times), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": dict(pack.describe(), l2="CPU run"),
+        "tokens_per_s": (n_rows * len(times)) / total_t,
+        "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n_rows} uniformly drawn query rows (all {pack.hq} heads) per step"},
+        "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(pack, seconds: float = 12.0):
+    """The oracle as it stands, on a bounded sample of the same workload."""
+    import oracle
+    import packed_varlen_masked_gb300 as pk
+    q, k, v = W.make_qkv(pack)
+    plan = pk.Plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d, num_ctas=1,
+                   upload=False)
+    lim = plan.kv_limit()
+    cu = pack.cu_seqlens
+    keys = (lim - np.repeat(cu[:-1], np.diff(cu)) + 1).astype(np.float64)
+    rng = np.random.default_rng(1)
+    probe = rng.integers(0, pack.total_tokens, size=32).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, cu, pack.segments, pack.hq, pack.hkv, pack.d, pack.scale, rows=probe)
+    dt = time.perf_counter() - t0
+    n_rows = int(max(32, min(20000, 32 * seconds / max(dt, 1e-6))))
+    rows = rng.integers(0, pack.total_tokens, size=n_rows).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, cu, pack.segments, pack.hq, pack.hkv, pack.d, pack.scale, rows=rows)
+    t = time.perf_counter() - t0
+    fl = 4.0 * pack.d * pack.hq * keys[rows].sum()
+    return {"value": fl / t / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+            "kind": "oracle", "seconds": t,
+            "sample": f"{n_rows} uniformly drawn query rows x {pack.hq} heads of the workload"}
+
+
+def sweep(pk, torch, stream, dev):
+    """Timing-only pass over every workload (device-generated inputs)."""
+    res = {}
+    for name, fn in W.CONFIGS.items():
+        pack = fn()
+        g = torch.Generator(device=dev).manual_seed(0)
+        T = pack.total_tokens
+        q = torch.randn(T, pack.hq, pack.d, device=dev, generator=g).bfloat16() * pack.q_mult
+        k = torch.randn(T, pack.hkv, pack.d, device=dev, generator=g).bfloat16()
+        v = torch.randn(T, pack.hkv, pack.d, device=dev, generator=g).bfloat16()
+        plan = pk.plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d, device=dev)
+        out = torch.empty_like(q)
+        lse = torch.empty(pack.hq, T, dtype=torch.float32, device=dev)
+        for _ in range(3):
+            pk.attn_fwd(q, k, v, plan, pack.scale, out=out, lse=lse)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        n = 10
+        torch.cuda.synchronize()
+        ev[0].record(stream)
+        for _ in range(n):
+            pk.attn_fwd(q, k, v, plan, pack.scale, out=out, lse=lse)
+        ev[1].record(stream)
+        torch.cuda.synchronize()
+        ms = ev[0].elapsed_time(ev[1]) / n
+        fl = plan.useful_flops
+        res[name] = {"ms": round(ms, 4), "useful_tflops": round(fl / ms / 1e9, 1),
+                     "tokens_per_s": round(T / ms * 1e3), "total_tokens": T}
+        del q, k, v, out, lse, plan
+        torch.cuda.empty_cache()
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mixed_resolution", choices=sorted(W.CONFIGS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world, rank, local = dist_setup(args)
+    pack = W.CONFIGS[args.workload]()
+
+    if args.impl == "reference":
+        return reference_arm(args, pack, rank, world)
+
+    import torch
+    import packed_varlen_masked_gb300 as pk
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist_mod.init_process_group("nccl", device_id=dev)
+        dist = dist_mod
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    q, k, v = W.make_qkv(pack)
+    q, k, v = q.to(dev), k.to(dev), v.to(dev)
+    plan = pk.plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty(pack.hq, pack.total_tokens, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    for _ in range(args.warmup):
+        pk.attn_fwd(q, k, v, plan, pack.scale, out=out, lse=lse, status=status)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} during warm-up")
+
+    # timed region: K launches, an event pair around each launch on the
+    # launching stream (per-launch duration for the roofline)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t_all = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    with ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                      else local) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        t_all[0].record(stream)
+        for i in range(args.steps):
+            evs[i][0].record(stream)
+            pk.attn_fwd(q, k, v, plan, pack.scale, out=out, lse=lse, status=status)
+            evs[i][1].record(stream)
+        t_all[1].record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    total_ms = t_all[0].elapsed_time(t_all[1])
+    launch_ms = [a.elapsed_time(b) for a, b in evs]
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the timed region")
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    flops = plan.useful_flops
+    ms_step = total_ms / args.steps
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    tokens_per_s = world * pack.total_tokens * args.steps / (total_ms * 1e-3)
+
+    # end to end through the public host-buffer call
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: t.cpu().pin_memory()
+        qh, kh, vh = pin(q), pin(k), pin(v)
+        oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        bufs = {"q": q, "k": k, "v": v, "out": out, "lse": lse}
+        for _ in range(args.warmup):
+            pk.attn_fwd_host(qh, kh, vh, plan, pack.scale, bufs, oh, lh)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            pk.attn_fwd_host(qh, kh, vh, plan, pack.scale, bufs, oh, lh)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e_ms = e0.elapsed_time(e1)
+        if dist is not None:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * flops * args.steps / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": e_ms / args.steps,
+               "h2d_bytes_per_step": int((q.numel() + k.numel() + v.numel()) * 2),
+               "d2h_bytes_per_step": int(out.numel() * 2 + lse.numel() * 4)}
+
+    per_workload = None
+    if not args.no_sweep and rank == 0:
+        per_workload = sweep(pk, torch, stream, dev)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    peaks = load_peaks()
+    avg_launch_ms = statistics.mean(launch_ms)
+    achieved = flops / (avg_launch_ms * 1e-3) / 1e12
+    traffic = load_traffic()
+    info = plan.info
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline(pack)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": dict(pack.describe(), parallelism=f"replicas{world}",
+                       l2="inputs larger than L2 (q %.0f MB, k+v %.0f MB)" % (
+                           q.numel() * 2 / 1e6, (k.numel() + v.numel()) * 2 / 1e6),
+                       useful_flops_per_step=flops,
+                       padded_dense_mask_flops_per_step=4.0 * pack.d * pack.hq * len(pack.seqs)
+                       * pack.max_seqlen ** 2),
+        "tokens_per_s": round(tokens_per_s),
+        "pct_of_nominal_bf16_peak": round(100 * value / world / NOMINAL_BF16_TFLOPS, 2),
+        "pct_of_measured_bf16_peak": round(100 * value / world / peaks["bf16_tflops"], 2),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": traffic,
+                     "peak_source": peaks["source"] + " (bf16 burst)",
+                     "kernel": "pk_attn_fwd_kernel<128>", "launch_ms_mean": round(avg_launch_ms, 4),
+                     "launch_ms_min": round(min(launch_ms), 4)},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+        "plan": {k2: info[k2] for k2 in ("num_items", "num_ctas", "num_full_tiles",
+                                          "num_partial_tiles")},
+        "per_workload": per_workload,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

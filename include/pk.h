@@ -1,0 +1,189 @@
+/*
+ * pk.h -- C ABI of the packed mixed-mask variable-length attention library
+ * for GB300 (sm_103a).
+ *
+ * The operation ("[RFC]: HunyuanImage 3.0 deployment", Proposed Change, P0
+ * "Packed Attention for Multi-Request Batching"): requests of different
+ * resolutions are packed back to back into one token stream described by
+ * cu_seqlens, with no padding and no explicit (bsz,1,seqlen,seqlen) mask
+ * (Motivation, item (1)).  Each packed sequence carries the model's
+ * generalized causal mask (same page, P0 "Attention mask challenge";
+ * "Model structure", item 1):
+ *
+ *   query i of a sequence sees key j of the same sequence iff
+ *     j <= i, or i lies in an IMAGE segment and j lies in that same segment.
+ *
+ * Nothing attends across sequences.  Query head h reads key/value head
+ * h / (hq / hkv) (grouped-query attention, contiguous groups).
+ *
+ *   out[t,h,:] = sum_j softmax_j(scale * q[t,h,:].k[j,g,:]) v[j,g,:]
+ *   lse[h,t]   = ln sum_j exp(scale * q[t,h,:].k[j,g,:])   (visible j only)
+ *
+ * Tensors (all caller-owned device memory, bf16 = IEEE bfloat16):
+ *   q   [T][hq][d]   bf16, rows contiguous, 16-byte aligned base
+ *   k,v [T][hkv][d]  bf16, rows contiguous, 16-byte aligned base
+ *   out [T][hq][d]   bf16, written for every token
+ *   lse [hq][T]      fp32, natural log, written for every token
+ * where T = cu_seqlens[num_seqs].
+ *
+ * Ownership: the library never allocates device memory.  A plan owns host
+ * memory only; its device image lives in a caller-allocated buffer of
+ * pk_plan_device_bytes() bytes that must outlive every launch using it.
+ * Thread safety: a plan is read-only after pk_plan_upload; concurrent
+ * launches on one plan are safe.
+ */
+#ifndef PK_H_
+#define PK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA stream (identical to cudaStream_t / CUstream). */
+typedef struct CUstream_st* pk_stream_t;
+
+typedef enum pk_status {
+  PK_OK = 0,
+  PK_ERR_INVALID_ARG = 1,   /* malformed descriptors, null pointer, bad size */
+  PK_ERR_UNSUPPORTED = 2,   /* head_dim not in {64, 128}, device not sm_103 */
+  PK_ERR_ALIGNMENT = 3,     /* a tensor base is not 16-byte aligned */
+  PK_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
+  PK_ERR_TIMEOUT = 5,       /* device: a bounded wait ran out (in dev_status) */
+  PK_ERR_DEVICE_CHECK = 6,  /* device: an internal consistency check failed */
+  PK_ERR_NOT_UPLOADED = 7   /* plan has no device image yet */
+} pk_status;
+
+typedef enum pk_seg_type { PK_TEXT = 0, PK_IMAGE = 1 } pk_seg_type;
+
+/* One segment of a sequence: tokens [start, start+len) of the packed stream
+ * (global token index), all TEXT or all IMAGE.  Adjacent IMAGE segments are
+ * distinct images: neither sees the other's later tokens. */
+typedef struct pk_segment {
+  int32_t start;
+  int32_t len;
+  int32_t type;
+} pk_segment;
+
+typedef struct pk_plan pk_plan;
+
+/* Summary of a plan (host data, for callers and tests). */
+typedef struct pk_plan_info {
+  int32_t total_tokens;     /* T */
+  int32_t num_seqs;
+  int32_t hq, hkv, head_dim;
+  int32_t num_items;        /* work items: (q-tile, kv head, query-head pair) */
+  int32_t num_ctas;         /* persistent CTAs launched by pk_attn_fwd */
+  int32_t num_full_tiles;   /* (item, k-tile) visits with no mask math */
+  int32_t num_partial_tiles;/* (item, k-tile) visits with per-element mask */
+  int32_t reserved;
+  int64_t visible_pairs;    /* per query head */
+  double useful_flops;      /* 4 * d * hq * visible_pairs */
+} pk_plan_info;
+
+/* Device work item, 32 bytes, as stored in the plan image (exposed for
+ * tests and tools).  A work item is one 128-row query tile of one sequence
+ * for up to two query heads of the same key/value head. */
+typedef struct pk_work_item {
+  int32_t q_start;   /* global token index of the tile's first query row */
+  int32_t q_rows;    /* valid query rows in the tile, 1..128 */
+  int32_t kv_start;  /* global token index of the sequence's first key */
+  int32_t n_kt;      /* 128-key tiles visited, from kv_start upwards */
+  int32_t n_full;    /* leading tiles visible to every valid row (no mask) */
+  int32_t hq0;       /* query head of slot 0 */
+  int32_t hq1;       /* query head of slot 1, or -1 when the slot is empty */
+  int32_t hkv;       /* key/value head shared by both slots */
+} pk_work_item;
+
+/*
+ * Build a plan (host only, no device work).
+ *   cu_seqlens : host int32[num_seqs+1]; cu_seqlens[0] == 0, non-decreasing.
+ *                Empty sequences are allowed and produce no work.
+ *   segs       : host pk_segment[num_segs], in token order, non-empty, tiling
+ *                every sequence exactly (no segment crosses a sequence end).
+ *   hq, hkv    : query / key-value heads, hq % hkv == 0.
+ *   head_dim   : 64 or 128 (else PK_ERR_UNSUPPORTED).
+ *   num_ctas   : persistent CTAs to schedule for; 0 = the current device's
+ *                SM count (needs a CUDA device).
+ * On success *out owns a new plan (free with pk_plan_destroy).  On failure
+ * *out is set to NULL and a status is returned.
+ */
+pk_status pk_plan_create(const int32_t* cu_seqlens, int32_t num_seqs,
+                         const pk_segment* segs, int32_t num_segs, int32_t hq,
+                         int32_t hkv, int32_t head_dim, int32_t num_ctas,
+                         pk_plan** out);
+
+/* Bytes of the device image of the plan (work list, per-CTA offsets and the
+ * per-token key limit). */
+size_t pk_plan_device_bytes(const pk_plan* plan);
+
+/* Copy the plan's device image into dev_buf (caller-owned, >= 256-byte
+ * aligned, >= pk_plan_device_bytes bytes) on `stream`, and remember dev_buf.
+ * Asynchronous: the plan's host memory stays valid until destroy. */
+pk_status pk_plan_upload(pk_plan* plan, void* dev_buf, size_t bytes,
+                         pk_stream_t stream);
+
+/*
+ * Launch the attention forward on `stream` (asynchronous).
+ *   q, k, v   : device bf16 tensors as described above.
+ *   out, lse  : device outputs as described above.
+ *   scale     : softmax scale, finite and > 0 (usually 1/sqrt(head_dim)).
+ *   dev_status: nullable device int32; on a device-side failure the kernel
+ *               writes PK_ERR_TIMEOUT / PK_ERR_DEVICE_CHECK there (the caller
+ *               zeroes it; it is never cleared by the library).
+ * Argument and launch errors are returned synchronously.  Requires a device
+ * of compute capability 10.3 (GB300).
+ */
+pk_status pk_attn_fwd(const pk_plan* plan, const void* q, const void* k,
+                      const void* v, void* out, float* lse, float scale,
+                      pk_stream_t stream, int32_t* dev_status);
+
+/*
+ * End-to-end variant for callers holding host buffers: copies q, k, v from
+ * host memory into the caller's device buffers, runs pk_attn_fwd, and copies
+ * out and lse back into host memory, all on `stream` (asynchronous; pinned
+ * host memory makes the copies truly asynchronous).  Device buffers are the
+ * caller's (same shapes as pk_attn_fwd); host buffers must stay valid until
+ * the stream reaches the end of this call's work.
+ */
+pk_status pk_attn_fwd_host(const pk_plan* plan, const void* q_host,
+                           const void* k_host, const void* v_host,
+                           void* out_host, float* lse_host, void* q_dev,
+                           void* k_dev, void* v_dev, void* out_dev,
+                           float* lse_dev, float scale, pk_stream_t stream,
+                           int32_t* dev_status);
+
+void pk_plan_destroy(pk_plan* plan);
+
+const char* pk_status_string(pk_status status);
+
+/* 4 * head_dim * hq * (visible (query, key) pairs per head). */
+double pk_plan_useful_flops(const pk_plan* plan);
+
+pk_status pk_plan_get_info(const pk_plan* plan, pk_plan_info* info);
+
+/* Host copies of plan internals, for tests: the per-token key limit
+ * (global index of the last visible key, int32[T]) and the CTA-ordered work
+ * list (pk_work_item[num_items]) with per-CTA offsets (int32[num_ctas+1]). */
+pk_status pk_plan_get_kv_limit(const pk_plan* plan, int32_t* out, int64_t n);
+pk_status pk_plan_get_items(const pk_plan* plan, pk_work_item* items,
+                            int64_t n_items, int32_t* cta_offsets,
+                            int64_t n_offsets);
+
+/* Upper bound of every device-side wait, in nanoseconds (default 4e9).
+ * Process-wide; applies to launches made after the call. */
+void pk_set_wait_timeout_ns(uint64_t ns);
+
+/* Self-test of the bounded wait: launches one CTA that waits on a barrier
+ * nothing arrives at, for at most `timeout_ns`, and writes PK_ERR_TIMEOUT to
+ * dev_status when the wait runs out. */
+pk_status pk_debug_wait_timeout(int32_t* dev_status, uint64_t timeout_ns,
+                                pk_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PK_H_ */

@@ -1,0 +1,24 @@
+"""Packed mixed-mask variable-length attention for GB300 (sm_103a).
+
+Thin ctypes binding over the C ABI declared in ``include/pk.h``: argument
+marshalling only.  Every step of the computation runs in the library's CUDA
+kernels; there is no CPU or PyTorch fallback, and importing this package
+fails loudly when the compiled library is missing.
+
+    plan = pk.plan(cu_seqlens, segments, hq, hkv, head_dim)   # host planner
+    out, lse = pk.attn_fwd(q, k, v, plan, scale)               # one launch
+
+``segments`` is a sequence of (start, length, type) triples in token order,
+type 0 = text (causal), 1 = image (sees its whole own segment).  PyTorch
+provides device memory and the current stream.
+"""
+from __future__ import annotations
+
+from ._native import (PK_ERR_ALIGNMENT, PK_ERR_CUDA, PK_ERR_DEVICE_CHECK,  # noqa: F401
+                      PK_ERR_INVALID_ARG, PK_ERR_NOT_UPLOADED, PK_ERR_TIMEOUT,
+                      PK_ERR_UNSUPPORTED, PK_OK, PKError, lib_path, load)
+from .api import (IMAGE, TEXT, Plan, attn_fwd, attn_fwd_host,  # noqa: F401
+                  debug_wait_timeout, plan, set_wait_timeout_ns)
+
+__all__ = ["plan", "Plan", "attn_fwd", "attn_fwd_host", "PKError", "TEXT", "IMAGE",
+           "set_wait_timeout_ns", "debug_wait_timeout", "load", "lib_path"]

@@ -1,0 +1,206 @@
+"""User-facing calls: ``plan`` / ``Plan`` and ``attn_fwd`` (argument
+marshalling around the C ABI; all computation happens in the library)."""
+from __future__ import annotations
+
+import ctypes
+import math
+from typing import Optional, Sequence, Tuple
+
+import numpy as np
+
+from ._native import PlanInfo, Segment, WorkItem, check, load
+
+TEXT = 0
+IMAGE = 1
+
+
+def _segments_struct(segments) -> Tuple[ctypes.Array, int]:
+    arr = np.asarray(segments, dtype=np.int64).reshape(-1, 3)
+    n = arr.shape[0]
+    segs = (Segment * max(n, 1))()
+    for i, (st, ln, ty) in enumerate(arr.tolist()):
+        segs[i] = Segment(int(st), int(ln), int(ty))
+    return segs, n
+
+
+class Plan:
+    """A host plan (tile classes + longest-work-first schedule) and, once
+    uploaded, its device image in a PyTorch-allocated buffer.
+
+    Build it once per pack composition and reuse it for every layer and
+    denoising step: it is read-only after upload.
+    """
+
+    def __init__(self, cu_seqlens, segments, hq: int, hkv: int, head_dim: int,
+                 num_ctas: int = 0, device=None, upload: bool = True):
+        self._lib = load()
+        self._h = ctypes.c_void_p()
+        cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+        if cu.ndim != 1 or cu.size < 1:
+            raise ValueError("cu_seqlens must be a 1-D array with at least one entry")
+        segs, n = _segments_struct(segments)
+        check(self._lib.pk_plan_create(cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                       cu.size - 1, segs, n, int(hq), int(hkv), int(head_dim),
+                                       int(num_ctas), ctypes.byref(self._h)),
+              "pk_plan_create")
+        self.hq, self.hkv, self.head_dim = int(hq), int(hkv), int(head_dim)
+        self.total_tokens = int(cu[-1])
+        self._buf = None
+        if upload:
+            self.upload(device)
+
+    # -- lifetime -----------------------------------------------------------
+    def close(self) -> None:
+        if getattr(self, "_h", None) is not None and self._h.value:
+            self._lib.pk_plan_destroy(self._h)
+            self._h = ctypes.c_void_p()
+        self._buf = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def handle(self) -> ctypes.c_void_p:
+        return self._h
+
+    # -- device image -------------------------------------------------------
+    @property
+    def device_bytes(self) -> int:
+        return int(self._lib.pk_plan_device_bytes(self._h))
+
+    def upload(self, device=None) -> None:
+        import torch
+        dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        nbytes = self.device_bytes
+        buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        check(self._lib.pk_plan_upload(self._h, ctypes.c_void_p(buf.data_ptr()), nbytes,
+                                       ctypes.c_void_p(stream)), "pk_plan_upload")
+        self._buf = buf
+
+    @property
+    def device_buffer(self):
+        return self._buf
+
+    # -- introspection --------------------------------------------------------
+    @property
+    def info(self) -> dict:
+        pi = PlanInfo()
+        check(self._lib.pk_plan_get_info(self._h, ctypes.byref(pi)), "pk_plan_get_info")
+        return {name: getattr(pi, name) for name, _ in PlanInfo._fields_ if name != "reserved"}
+
+    @property
+    def useful_flops(self) -> float:
+        return float(self._lib.pk_plan_useful_flops(self._h))
+
+    def kv_limit(self) -> np.ndarray:
+        out = np.zeros(max(self.total_tokens, 1), dtype=np.int32)
+        check(self._lib.pk_plan_get_kv_limit(self._h, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                              out.size), "pk_plan_get_kv_limit")
+        return out[: self.total_tokens]
+
+    def items(self) -> Tuple[np.ndarray, np.ndarray]:
+        """(items int32 [n, 8] in CTA order, cta_offsets int32 [num_ctas + 1]).
+        Columns: q_start, q_rows, kv_start, n_kt, n_full, hq0, hq1, hkv."""
+        info = self.info
+        n, g = info["num_items"], info["num_ctas"]
+        items = (WorkItem * max(n, 1))()
+        offs = np.zeros(g + 1, dtype=np.int32)
+        check(self._lib.pk_plan_get_items(self._h, items, n,
+                                           offs.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                           g + 1), "pk_plan_get_items")
+        arr = np.frombuffer(bytes(items), dtype=np.int32).reshape(-1, 8)[:n].copy()
+        return arr, offs
+
+
+def plan(cu_seqlens, segments, hq: int, hkv: int, head_dim: int, num_ctas: int = 0,
+         device=None) -> Plan:
+    return Plan(cu_seqlens, segments, hq, hkv, head_dim, num_ctas=num_ctas, device=device)
+
+
+def _check_tensor(t, name, shape):
+    import torch
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA bfloat16 tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def attn_fwd(q, k, v, plan: Plan, scale: Optional[float] = None, out=None, lse=None,
+             status=None, check_status: bool = False):
+    """Packed mixed-mask attention forward on the current CUDA stream.
+
+    q [T, hq, d], k and v [T, hkv, d] bf16 CUDA tensors.  Returns
+    (out bf16 [T, hq, d], lse fp32 [hq, T]).  With ``check_status`` the call
+    synchronises and raises if the kernel reported a device-side failure.
+    """
+    import torch
+    T, hq, hkv, d = plan.total_tokens, plan.hq, plan.hkv, plan.head_dim
+    _check_tensor(q, "q", (T, hq, d))
+    _check_tensor(k, "k", (T, hkv, d))
+    _check_tensor(v, "v", (T, hkv, d))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check_tensor(out, "out", (T, hq, d))
+    if lse is None:
+        lse = torch.empty(hq, T, dtype=torch.float32, device=q.device)
+    elif lse.dtype != torch.float32 or tuple(lse.shape) != (hq, T) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 tensor of shape [hq, T]")
+    if check_status and status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=q.device)
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    lib = plan._lib
+    check(lib.pk_attn_fwd(plan.handle, ctypes.c_void_p(q.data_ptr()),
+                          ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()),
+                          ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(lse.data_ptr()),
+                          float(scale), ctypes.c_void_p(stream),
+                          ctypes.c_void_p(status.data_ptr() if status is not None else 0)),
+          "pk_attn_fwd")
+    if check_status:
+        torch.cuda.current_stream(q.device).synchronize()
+        check(int(status.item()), "pk_attn_fwd (device)")
+    return out, lse
+
+
+def attn_fwd_host(q_host, k_host, v_host, plan: Plan, scale: float, dev_buffers: dict,
+                  out_host, lse_host, status=None):
+    """End-to-end call from host buffers (ideally pinned): copies q/k/v to the
+    caller's device buffers, runs the attention and copies out/lse back, all
+    on the current stream.  ``dev_buffers`` holds CUDA tensors 'q', 'k', 'v',
+    'out', 'lse' of the pk_attn_fwd shapes."""
+    import torch
+    for name, t in (("q_host", q_host), ("k_host", k_host), ("v_host", v_host),
+                    ("out_host", out_host), ("lse_host", lse_host)):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous host tensor")
+    db = dev_buffers
+    stream = torch.cuda.current_stream(db["q"].device).cuda_stream
+    check(plan._lib.pk_attn_fwd_host(
+        plan.handle, ctypes.c_void_p(q_host.data_ptr()), ctypes.c_void_p(k_host.data_ptr()),
+        ctypes.c_void_p(v_host.data_ptr()), ctypes.c_void_p(out_host.data_ptr()),
+        ctypes.c_void_p(lse_host.data_ptr()), ctypes.c_void_p(db["q"].data_ptr()),
+        ctypes.c_void_p(db["k"].data_ptr()), ctypes.c_void_p(db["v"].data_ptr()),
+        ctypes.c_void_p(db["out"].data_ptr()), ctypes.c_void_p(db["lse"].data_ptr()),
+        float(scale), ctypes.c_void_p(stream),
+        ctypes.c_void_p(status.data_ptr() if status is not None else 0)), "pk_attn_fwd_host")
+    return out_host, lse_host
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    load().pk_set_wait_timeout_ns(int(ns))
+
+
+def debug_wait_timeout(status, timeout_ns: int) -> None:
+    """Launch the bounded-wait self-test kernel (see pk.h)."""
+    import torch
+    stream = torch.cuda.current_stream(status.device).cuda_stream
+    check(load().pk_debug_wait_timeout(ctypes.c_void_p(status.data_ptr()), int(timeout_ns),
+                                       ctypes.c_void_p(stream)), "pk_debug_wait_timeout")

@@ -1,0 +1,71 @@
+"""Build the in-tree shared library ``_build/libpk.so`` with nvcc for sm_103a.
+
+Two translation units: the host planner (``csrc/pk_plan.cpp``) and the CUDA
+kernels plus launcher (``csrc/pk_attn.cu``).  They compile in parallel and
+are linked against the shared CUDA runtime (the one PyTorch loads too).
+"""
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+BUILD = os.path.join(PKG, "_build")
+LIB = os.path.join(BUILD, "libpk.so")
+SOURCES = ["pk_plan.cpp", "pk_attn.cu"]
+HEADERS = [os.path.join(CSRC, "pk_internal.h"), os.path.join(CSRC, "tmem_ops.cuh"),
+           os.path.join(INCLUDE, "pk.h")]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def nvcc() -> str:
+    for cand in (os.environ.get("CUDA_HOME", ""), "/usr/local/cuda"):
+        if cand and os.path.exists(os.path.join(cand, "bin", "nvcc")):
+            return os.path.join(cand, "bin", "nvcc")
+    found = shutil.which("nvcc")
+    if not found:
+        raise RuntimeError("nvcc not found")
+    return found
+
+
+def _stale() -> bool:
+    if not os.path.exists(LIB):
+        return True
+    t = os.path.getmtime(LIB)
+    deps = [os.path.join(CSRC, s) for s in SOURCES] + HEADERS + [__file__]
+    return any(os.path.getmtime(p) > t for p in deps)
+
+
+def build(force: bool = False, verbose_ptxas: bool = False) -> str:
+    if not force and not _stale():
+        return LIB
+    os.makedirs(BUILD, exist_ok=True)
+    cc = nvcc()
+    common = ["-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
+
+    def compile_one(src: str) -> str:
+        obj = os.path.join(BUILD, src + f".{os.getpid()}.o")
+        cmd = [cc, *ARCH, "-lineinfo", *common, "-c", os.path.join(CSRC, src), "-o", obj]
+        if verbose_ptxas and src.endswith(".cu"):
+            cmd.insert(1, "-Xptxas=-v")
+        subprocess.run(cmd, check=True)
+        return obj
+
+    with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+        objs = list(ex.map(compile_one, SOURCES))
+    tmp = LIB + f".tmp{os.getpid()}"
+    subprocess.run([cc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs], check=True)
+    for o in objs:
+        os.remove(o)
+    os.replace(tmp, LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv))

@@ -1,0 +1,762 @@
+// Packed mixed-mask variable-length attention forward for GB300 (sm_103a).
+//
+// What it computes is the operation of "[RFC]: HunyuanImage 3.0 deployment"
+// (Proposed Change, P0 "Packed Attention for Multi-Request Batching" and its
+// "Attention mask challenge" bullet): attention over sequences packed back to
+// back by cu_seqlens, each with the generalized causal mask (text causal,
+// image tokens also seeing their whole own segment), with grouped-query
+// heads.  The host planner turns the mask into a per-token key limit and a
+// list of 128-row query tiles, each visiting a prefix of 128-key tiles that
+// are either fully visible (no mask math) or partial (per-element compare).
+//
+// Kernel organisation (one persistent CTA per SM, 12 warps):
+//   warp 0      TMA producer: Q tiles of the two query-head slots, then a
+//               ring of K and V tiles (128-byte swizzled, one box per 64
+//               columns of the head dimension).
+//   warp 1      allocates the 512 TMEM columns; one thread issues every
+//               tcgen05.mma: S = Q K^T (both operands K-major in shared
+//               memory) and O += P V (P read from TMEM, V MN-major in shared
+//               memory), and signals with tcgen05.commit.
+//   warps 4-7   softmax for slot 0, warps 8-11 for slot 1: thread r owns row
+//               r of its slot's S, O and P in TMEM.  Online softmax in base 2
+//               with a lazily moved running maximum, P written back to TMEM
+//               as bf16 over the S columns, epilogue O / l -> bf16 and the
+//               natural-log LSE.
+// The two slots are two query heads that share one key/value head, so each
+// K/V tile feeds four 128x128 MMAs and the tensor pipe alternates between the
+// slots while the other slot's softmax runs.
+//
+// TMEM columns: S0 [0,128)  S1 [128,256)  O0 [256,256+D)  O1 [256+D,256+2D);
+// P of slot s is stored as bf16 pairs in the first 64 columns of S_s.
+//
+// Every mbarrier wait is bounded in time; on expiry the kernel records
+// PK_ERR_TIMEOUT, raises a CTA-local abort flag so the other roles stop, lets
+// in-flight copies and MMAs land, frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "pk_internal.h"
+#include "tmem_ops.cuh"
+
+namespace pk {
+namespace dev {
+
+constexpr int kThreads = 384;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 64 bf16
+
+template <int D>
+struct Cfg {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kTileBytes = 128 * D * 2;
+  // Stage count keeps shared memory above half an SM, so that exactly one
+  // CTA (and one 512-column TMEM allocation) lives on each SM.
+  static constexpr int kStages = D == 128 ? 2 : 4;
+  static constexpr uint32_t kColS0 = 0, kColS1 = 128;
+  static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = 2 * kTileBytes;
+  static constexpr int kOffV = kOffK + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  // barrier indices
+  static constexpr int kQFull = 0, kQEmpty = 1;
+  static constexpr int kKFull = 2, kKEmpty = kKFull + kStages;
+  static constexpr int kVFull = kKEmpty + kStages, kVEmpty = kVFull + kStages;
+  static constexpr int kSFull = kVEmpty + kStages;  // [2]
+  static constexpr int kPReady = kSFull + 2;        // [2]
+  static constexpr int kOFull = kPReady + 2;        // [2]
+  static constexpr int kOFree = kOFull + 2;         // [2]
+  static constexpr int kMmaDone = kOFree + 2;
+  static constexpr int kNumBars = kMmaDone + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  static_assert(kSmemBytes > 114 * 1024, "one CTA per SM");
+};
+
+// Instruction descriptors of tcgen05.mma kind::f16 (dense, f32 accumulate,
+// bf16 A and B): bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16),
+// 10-12 B format (1 = bf16), 15/16 A/B major (0 = K-major, 1 = MN-major),
+// 17-22 N >> 3, 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor (tcgen05 form): start address, leading and
+// stride byte offsets (all >> 4), version 1 at bit 46, 128-byte swizzle (2)
+// at bits 61-63.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+struct WaitCtl {
+  volatile int* abort_flag;  // CTA-local, shared memory
+  int32_t* status;           // device status word, may be null
+  uint64_t limit_ns;
+};
+
+// Slow path of a bounded wait: poll until the phase completes, the CTA has
+// aborted, or the time limit passes (then record the timeout and abort).
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, WaitCtl c,
+                                            bool honour_abort) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 15u) == 0) {
+      if (honour_abort && *c.abort_flag) return false;
+      if (globaltimer_ns() - t0 > c.limit_ns) {
+        *c.abort_flag = 1;
+        if (c.status) atomicCAS(c.status, 0, (int32_t)PK_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& c) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, c, true);
+}
+// Drain wait used on the abort path: ignores the abort flag, still bounded.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, const WaitCtl& c) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, c, false);
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+// D(tmem) (+)= A(smem desc) * B(smem desc)
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D(tmem) (+)= A(tmem) * B(smem desc)
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// {lo -> bits 0-15, hi -> bits 16-31}, round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+struct KernelParams {
+  const pk_work_item* items;
+  const int32_t* cta_offsets;
+  const int32_t* kv_limit;
+  uint8_t* out;   // bf16 [T][hq][D]
+  float* lse;     // [hq][T]
+  int32_t* status;
+  int32_t T;
+  int32_t hq;
+  float scale_log2;  // softmax scale * log2(e)
+  uint64_t wait_limit_ns;
+};
+
+// S(tmem) = Q K^T over the head dimension: D/16 MMAs of 128x128x16.  Both
+// tiles are K-major with 128-byte swizzle: row r of a 64-column box sits at
+// r*128 bytes, 8-row groups 1024 bytes apart; the k-th 16-column step starts
+// 32*(k%4) bytes into box k/4.
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+  constexpr uint32_t idesc = make_idesc(128, 128, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (uint32_t)(kk >> 2) * kBoxBytes + (uint32_t)(kk & 3) * 32u;
+    mma_ss(d_tmem, sdesc(q_smem + off, 16, 1024), sdesc(k_smem + off, 16, 1024), idesc,
+           kk > 0 ? 1u : 0u);
+  }
+}
+
+// O(tmem) (+)= P V: 8 MMAs of 128 x D x 16.  P (bf16 pairs) is read from
+// TMEM, 8 columns per 16 keys.  V is MN-major with 128-byte swizzle: 16 keys
+// span 2048 bytes, and the second 64-column box (D = 128) is 16384 bytes on.
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
+                                         bool accumulate) {
+  constexpr uint32_t idesc = make_idesc(128, D, true);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    mma_ts(d_tmem, p_tmem + (uint32_t)kk * 8u,
+           sdesc(v_smem + (uint32_t)kk * 2048u, kBoxBytes, 1024), idesc,
+           (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+template <int D>
+__device__ void producer_role(const KernelParams& p, const CUtensorMap* tm_q,
+                              const CUtensorMap* tm_k, const CUtensorMap* tm_v, uint32_t sbase,
+                              int beg, int end, const WaitCtl& wc) {
+  using C = Cfg<D>;
+  auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
+  uint32_t kv_iter = 0, item_iter = 0;
+  uint32_t k_armed = 0, v_armed = 0, q_armed = 0;
+  bool ok = true;
+  for (int it = beg; it < end && ok; ++it, ++item_iter) {
+    const pk_work_item w = p.items[it];
+    if (!(ok = mbar_wait(bar(C::kQEmpty), (item_iter & 1u) ^ 1u, wc))) break;
+    const bool two = w.hq1 >= 0;
+    mbar_arrive_expect_tx(bar(C::kQFull), (two ? 2u : 1u) * C::kTileBytes);
+    ++q_armed;
+#pragma unroll
+    for (int h = 0; h < C::kHalves; ++h) {
+      tma_load_3d(sbase + C::kOffQ + h * kBoxBytes, tm_q, bar(C::kQFull), h * 64, w.hq0,
+                  w.q_start);
+      if (two)
+        tma_load_3d(sbase + C::kOffQ + C::kTileBytes + h * kBoxBytes, tm_q, bar(C::kQFull),
+                    h * 64, w.hq1, w.q_start);
+    }
+    for (int j = 0; j < w.n_kt; ++j, ++kv_iter) {
+      const uint32_t st = kv_iter % C::kStages, ph = (kv_iter / C::kStages) & 1u;
+      const int row = w.kv_start + j * 128;
+      if (!(ok = mbar_wait(bar(C::kKEmpty + st), ph ^ 1u, wc))) break;
+      mbar_arrive_expect_tx(bar(C::kKFull + st), C::kTileBytes);
+      ++k_armed;
+#pragma unroll
+      for (int h = 0; h < C::kHalves; ++h)
+        tma_load_3d(sbase + C::kOffK + st * C::kTileBytes + h * kBoxBytes, tm_k,
+                    bar(C::kKFull + st), h * 64, w.hkv, row);
+      if (!(ok = mbar_wait(bar(C::kVEmpty + st), ph ^ 1u, wc))) break;
+      mbar_arrive_expect_tx(bar(C::kVFull + st), C::kTileBytes);
+      ++v_armed;
+#pragma unroll
+      for (int h = 0; h < C::kHalves; ++h)
+        tma_load_3d(sbase + C::kOffV + st * C::kTileBytes + h * kBoxBytes, tm_v,
+                    bar(C::kVFull + st), h * 64, w.hkv, row);
+    }
+  }
+  if (!ok) {
+    // Aborted: let every copy already issued land before the CTA may exit.
+    // The last kStages armings of a ring are the only ones that can be open,
+    // and each is the most recent arming of its stage.
+    for (uint32_t k = 1; k <= (uint32_t)C::kStages && k <= k_armed; ++k) {
+      const uint32_t i = k_armed - k;
+      mbar_wait_drain(bar(C::kKFull + i % C::kStages), (i / C::kStages) & 1u, wc);
+    }
+    for (uint32_t k = 1; k <= (uint32_t)C::kStages && k <= v_armed; ++k) {
+      const uint32_t i = v_armed - k;
+      mbar_wait_drain(bar(C::kVFull + i % C::kStages), (i / C::kStages) & 1u, wc);
+    }
+    if (q_armed) mbar_wait_drain(bar(C::kQFull), (q_armed - 1u) & 1u, wc);
+  }
+}
+
+template <int D>
+__device__ void mma_role(const KernelParams& p, uint32_t sbase, uint32_t tmem, int beg, int end,
+                         const WaitCtl& wc) {
+  using C = Cfg<D>;
+  auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
+  const uint32_t q0 = sbase + C::kOffQ, q1 = sbase + C::kOffQ + C::kTileBytes;
+  const uint32_t tS0 = tmem + C::kColS0, tS1 = tmem + C::kColS1;
+  const uint32_t tO0 = tmem + C::kColO0, tO1 = tmem + C::kColO1;
+  uint32_t kv_iter = 0, item_iter = 0;
+  uint32_t pr_ph0 = 0, pr_ph1 = 0, of_cnt0 = 0, of_cnt1 = 0;
+  bool ok = true;
+  for (int it = beg; it < end && ok; ++it, ++item_iter) {
+    const pk_work_item w = p.items[it];
+    const bool two = w.hq1 >= 0;
+    const int n = w.n_kt;
+    if (!(ok = mbar_wait(bar(C::kQFull), item_iter & 1u, wc))) break;
+    {
+      const uint32_t st = kv_iter % C::kStages, ph = (kv_iter / C::kStages) & 1u;
+      if (!(ok = mbar_wait(bar(C::kKFull + st), ph, wc))) break;
+      tc_fence_after();
+      const uint32_t ks = sbase + C::kOffK + st * C::kTileBytes;
+      issue_qk<D>(tS0, q0, ks);
+      tc_commit(bar(C::kSFull + 0));
+      if (two) {
+        issue_qk<D>(tS1, q1, ks);
+        tc_commit(bar(C::kSFull + 1));
+      }
+      tc_commit(bar(C::kKEmpty + st));
+      if (n == 1) tc_commit(bar(C::kQEmpty));  // last use of Q issued
+    }
+    for (int j = 1; j <= n; ++j) {
+      const uint32_t ip = kv_iter + (uint32_t)j - 1u;
+      const uint32_t stp = ip % C::kStages, php = (ip / C::kStages) & 1u;
+      const uint32_t vs = sbase + C::kOffV + stp * C::kTileBytes;
+      uint32_t stj = 0, ks = 0;
+      if (j < n) {
+        const uint32_t ij = kv_iter + (uint32_t)j;
+        stj = ij % C::kStages;
+        if (!(ok = mbar_wait(bar(C::kKFull + stj), (ij / C::kStages) & 1u, wc))) break;
+        ks = sbase + C::kOffK + stj * C::kTileBytes;
+      }
+      if (!(ok = mbar_wait(bar(C::kVFull + stp), php, wc))) break;
+      // slot 0
+      if (!(ok = mbar_wait(bar(C::kPReady + 0), pr_ph0, wc))) break;
+      pr_ph0 ^= 1u;
+      if (j == 1 && !(ok = mbar_wait(bar(C::kOFree + 0), (of_cnt0 & 1u) ^ 1u, wc))) break;
+      tc_fence_after();
+      issue_pv<D>(tO0, tS0, vs, j > 1);
+      if (j < n) {
+        issue_qk<D>(tS0, q0, ks);
+        tc_commit(bar(C::kSFull + 0));
+      } else {
+        tc_commit(bar(C::kOFull + 0));
+      }
+      // slot 1
+      if (two) {
+        if (!(ok = mbar_wait(bar(C::kPReady + 1), pr_ph1, wc))) break;
+        pr_ph1 ^= 1u;
+        if (j == 1 && !(ok = mbar_wait(bar(C::kOFree + 1), (of_cnt1 & 1u) ^ 1u, wc))) break;
+        tc_fence_after();
+        issue_pv<D>(tO1, tS1, vs, j > 1);
+        if (j < n) {
+          issue_qk<D>(tS1, q1, ks);
+          tc_commit(bar(C::kSFull + 1));
+        } else {
+          tc_commit(bar(C::kOFull + 1));
+        }
+      }
+      tc_commit(bar(C::kVEmpty + stp));
+      if (j < n) tc_commit(bar(C::kKEmpty + stj));
+      if (j == n - 1) tc_commit(bar(C::kQEmpty));  // last use of Q issued
+    }
+    if (!ok) break;
+    ++of_cnt0;
+    if (two) ++of_cnt1;
+    kv_iter += (uint32_t)n;
+  }
+  // Every MMA issued must finish before TMEM is released.
+  tc_commit(bar(C::kMmaDone));
+  mbar_wait_drain(bar(C::kMmaDone), 0, wc);
+}
+
+template <int D>
+__device__ void softmax_role(const KernelParams& p, int slot, uint32_t sbase, uint32_t tmem,
+                             int beg, int end, const WaitCtl& wc) {
+  using C = Cfg<D>;
+  auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+  const int r = quad * 32 + lane;
+  const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+  const uint32_t tS = tmem + lane_base + (slot ? C::kColS1 : C::kColS0);
+  const uint32_t tO = tmem + lane_base + (slot ? C::kColO1 : C::kColO0);
+  const float sl2 = p.scale_log2;
+  uint32_t sf_ph = 0, of_ph = 0;
+  for (int it = beg; it < end; ++it) {
+    const pk_work_item w = p.items[it];
+    if (slot == 1 && w.hq1 < 0) continue;
+    const int h = slot ? w.hq1 : w.hq0;
+    const bool valid = r < w.q_rows;
+    const int lim = p.kv_limit[w.q_start + (valid ? r : w.q_rows - 1)];
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < w.n_kt; ++j) {
+      ok = mbar_wait(bar(C::kSFull + slot), sf_ph, wc);
+      ok = __all_sync(0xffffffffu, ok);
+      sf_ph ^= 1u;
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[128];
+      tmem_ld_x128(tS, sr);
+      float x[128];
+#pragma unroll
+      for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c]);
+      if (j >= w.n_full) {
+        const int nvis = lim - (w.kv_start + j * 128) + 1;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) x[c] = c < nvis ? x[c] : -INFINITY;
+      }
+      float mx = x[0];
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
+      const float m_new = mx * sl2;
+      if (j == 0) {
+        m_used = m_new;
+      } else {
+        const bool need = m_new > m_used + 8.0f;
+        if (__any_sync(0xffffffffu, need)) {
+          const float f = need ? ex2(m_used - m_new) : 1.0f;
+          if (need) {
+            m_used = m_new;
+            l *= f;
+          }
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld_x32(tO + (uint32_t)c0, o);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * f);
+            tmem_st_x32(tO + (uint32_t)c0, o);
+          }
+        }
+      }
+      const float neg = -m_used;
+      uint32_t pp[64];
+      float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+      for (int c = 0; c < 128; c += 2) {
+        const float p0 = ex2(fmaf(x[c], sl2, neg));
+        const float p1 = ex2(fmaf(x[c + 1], sl2, neg));
+        sum0 += p0;
+        sum1 += p1;
+        pp[c >> 1] = pack_bf16x2(p0, p1);
+      }
+      l += sum0 + sum1;
+      tmem_st_x64(tS, pp);
+      tc_fence_before();
+      mbar_arrive(bar(C::kPReady + slot));
+    }
+    if (!ok) break;
+    ok = mbar_wait(bar(C::kOFull + slot), of_ph, wc);
+    ok = __all_sync(0xffffffffu, ok);
+    of_ph ^= 1u;
+    if (!ok) break;
+    tc_fence_after();
+    const float inv_l = 1.0f / l;
+    uint8_t* orow = p.out + (((size_t)(w.q_start + r) * (size_t)p.hq + (size_t)h) * D) * 2;
+#pragma unroll
+    for (int c0 = 0; c0 < D; c0 += 32) {
+      uint32_t o[32];
+      tmem_ld_x32(tO + (uint32_t)c0, o);
+      uint32_t b[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        b[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv_l, __uint_as_float(o[2 * c + 1]) * inv_l);
+      if (valid) {
+        uint4* dst = reinterpret_cast<uint4*>(orow + (size_t)c0 * 2);
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          dst[v] = make_uint4(b[4 * v], b[4 * v + 1], b[4 * v + 2], b[4 * v + 3]);
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(bar(C::kOFree + slot));
+    if (valid)
+      p.lse[(size_t)h * (size_t)p.T + (size_t)(w.q_start + r)] =
+          (m_used + __log2f(l)) * 0.69314718055994530942f;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    pk_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const KernelParams p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1 KB alignment
+  uint8_t* sgen = smem_raw + (sbase - raw);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(sgen + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + C::kOffMisc + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::kQFull), 1);
+    mbar_init(bar(C::kQEmpty), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar(C::kKFull + s), 1);
+      mbar_init(bar(C::kKEmpty + s), 1);
+      mbar_init(bar(C::kVFull + s), 1);
+      mbar_init(bar(C::kVEmpty + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(C::kSFull + s), 1);
+      mbar_init(bar(C::kPReady + s), 128);
+      mbar_init(bar(C::kOFull + s), 1);
+      mbar_init(bar(C::kOFree + s), 128);
+    }
+    mbar_init(bar(C::kMmaDone), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_holder)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const int beg = p.cta_offsets[blockIdx.x], end = p.cta_offsets[blockIdx.x + 1];
+  const WaitCtl wc{abort_flag, p.status, p.wait_limit_ns};
+
+  if (warp == 0) {
+    if (lane == 0) producer_role<D>(p, &tm_q, &tm_k, &tm_v, sbase, beg, end, wc);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) mma_role<D>(p, sbase, tmem, beg, end, wc);
+    __syncwarp();
+  } else if (warp >= 4) {
+    softmax_role<D>(p, (warp - 4) >> 2, sbase, tmem, beg, end, wc);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// One CTA waits on a barrier that nothing arrives at; the bounded wait must
+// give up, record PK_ERR_TIMEOUT and return.
+__global__ void pk_wait_timeout_kernel(int32_t* status, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar_storage;
+  __shared__ int abort_flag;
+  const uint32_t bar = smem_u32(&bar_storage);
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const WaitCtl wc{&abort_flag, status, limit_ns};
+    mbar_wait(bar, 0, wc);
+  }
+  __syncthreads();
+}
+
+}  // namespace dev
+}  // namespace pk
+
+namespace {
+
+std::atomic<uint64_t> g_wait_limit_ns{4000000000ull};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult qres;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &qres) == cudaSuccess &&
+        qres == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// [T][H][D] bf16 viewed as a 3-D tensor (D, H, T); boxes of 64 x 1 x 128
+// with 128-byte swizzle; rows past T read as zeros.
+bool make_map(CUtensorMap* m, const void* base, int H, int T, int D) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+  const cuuint32_t box[3] = {64, 1, 128};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Device capability check, cached per device ordinal.
+pk_status check_device() {
+  static std::mutex mu;
+  static int verdict[64];  // 0 unknown, 1 ok, 2 unsupported
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return PK_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= 64) return PK_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(mu);
+  if (verdict[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return PK_ERR_CUDA;
+    }
+    verdict[dev] = (major == 10 && minor == 3) ? 1 : 2;
+  }
+  return verdict[dev] == 1 ? PK_OK : PK_ERR_UNSUPPORTED;
+}
+
+template <int D>
+pk_status launch(const pk_plan* plan, const void* q, const void* k, const void* v, void* out,
+                 float* lse, float scale, cudaStream_t stream, int32_t* dev_status) {
+  using C = pk::dev::Cfg<D>;
+  CUtensorMap tq, tk, tv;
+  if (!make_map(&tq, q, plan->hq, plan->T, D) || !make_map(&tk, k, plan->hkv, plan->T, D) ||
+      !make_map(&tv, v, plan->hkv, plan->T, D))
+    return PK_ERR_CUDA;
+  if (cudaFuncSetAttribute(pk::dev::pk_attn_fwd_kernel<D>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::kSmemBytes) != cudaSuccess) {
+    cudaGetLastError();
+    return PK_ERR_CUDA;
+  }
+  const uint8_t* img = static_cast<const uint8_t*>(plan->dev);
+  pk::dev::KernelParams kp;
+  kp.items = reinterpret_cast<const pk_work_item*>(img + plan->layout.items_off);
+  kp.cta_offsets = reinterpret_cast<const int32_t*>(img + plan->layout.cta_off_off);
+  kp.kv_limit = reinterpret_cast<const int32_t*>(img + plan->layout.kvlim_off);
+  kp.out = static_cast<uint8_t*>(out);
+  kp.lse = lse;
+  kp.status = dev_status;
+  kp.T = plan->T;
+  kp.hq = plan->hq;
+  kp.scale_log2 = scale * 1.4426950408889634f;
+  kp.wait_limit_ns = g_wait_limit_ns.load();
+  pk::dev::pk_attn_fwd_kernel<D><<<plan->num_ctas, pk::dev::kThreads, C::kSmemBytes, stream>>>(
+      tq, tk, tv, kp);
+  if (cudaGetLastError() != cudaSuccess) return PK_ERR_CUDA;
+  return PK_OK;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+void pk_set_wait_timeout_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : 1); }
+
+pk_status pk_attn_fwd(const pk_plan* plan, const void* q, const void* k, const void* v,
+                      void* out, float* lse, float scale, pk_stream_t stream,
+                      int32_t* dev_status) {
+  if (plan == nullptr) return PK_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return PK_ERR_INVALID_ARG;
+  if (plan->T == 0 || plan->items.empty()) return PK_OK;
+  if (plan->dev == nullptr) return PK_ERR_NOT_UPLOADED;
+  if (!q || !k || !v || !out || !lse) return PK_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return PK_ERR_ALIGNMENT;
+  pk_status st = check_device();
+  if (st != PK_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (plan->head_dim == 128) return launch<128>(plan, q, k, v, out, lse, scale, s, dev_status);
+  if (plan->head_dim == 64) return launch<64>(plan, q, k, v, out, lse, scale, s, dev_status);
+  return PK_ERR_UNSUPPORTED;
+}
+
+pk_status pk_attn_fwd_host(const pk_plan* plan, const void* q_host, const void* k_host,
+                           const void* v_host, void* out_host, float* lse_host, void* q_dev,
+                           void* k_dev, void* v_dev, void* out_dev, float* lse_dev, float scale,
+                           pk_stream_t stream, int32_t* dev_status) {
+  if (plan == nullptr) return PK_ERR_INVALID_ARG;
+  if (plan->T == 0) return PK_OK;
+  if (!q_host || !k_host || !v_host || !out_host || !lse_host) return PK_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t T = (size_t)plan->T, d = (size_t)plan->head_dim;
+  const size_t qb = T * plan->hq * d * 2, kvb = T * plan->hkv * d * 2;
+  const size_t lb = T * plan->hq * sizeof(float);
+  if (!q_dev || !k_dev || !v_dev || !out_dev || !lse_dev) return PK_ERR_INVALID_ARG;
+  if (cudaMemcpyAsync(q_dev, q_host, qb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(k_dev, k_host, kvb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(v_dev, v_host, kvb, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+    cudaGetLastError();
+    return PK_ERR_CUDA;
+  }
+  pk_status st = pk_attn_fwd(plan, q_dev, k_dev, v_dev, out_dev, lse_dev, scale, stream,
+                             dev_status);
+  if (st != PK_OK) return st;
+  if (cudaMemcpyAsync(out_host, out_dev, qb, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemcpyAsync(lse_host, lse_dev, lb, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+    cudaGetLastError();
+    return PK_ERR_CUDA;
+  }
+  return PK_OK;
+}
+
+pk_status pk_debug_wait_timeout(int32_t* dev_status, uint64_t timeout_ns, pk_stream_t stream) {
+  if (dev_status == nullptr) return PK_ERR_INVALID_ARG;
+  pk_status st = check_device();
+  if (st != PK_OK) return st;
+  pk::dev::pk_wait_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      dev_status, timeout_ns ? timeout_ns : 1);
+  if (cudaGetLastError() != cudaSuccess) return PK_ERR_CUDA;
+  return PK_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,68 @@
+"""The C-ABI library loads and exports every symbol ``include/pk.h``
+declares; host-side argument checks (no device work)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import packed_varlen_masked_gb300 as pk
+from packed_varlen_masked_gb300 import _native
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "pk.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pk_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ["pk_plan_create", "pk_plan_upload", "pk_attn_fwd", "pk_plan_destroy",
+                     "pk_plan_device_bytes", "pk_status_string", "pk_plan_useful_flops"]:
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(pk.lib_path())
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_every_declared_symbol():
+    assert set(_declared_functions()) <= set(_native.SIGNATURES)
+
+
+def test_status_strings():
+    lib = pk.load()
+    for code in range(8):
+        assert lib.pk_status_string(code)
+    assert lib.pk_status_string(pk.PK_ERR_TIMEOUT).decode() == "device wait timed out"
+
+
+def test_null_and_bad_arguments_are_rejected_without_a_device():
+    lib = pk.load()
+    out = ctypes.c_void_p()
+    assert lib.pk_plan_create(None, 1, None, 0, 4, 4, 64, 4, ctypes.byref(out)) == pk.PK_ERR_INVALID_ARG
+    assert lib.pk_plan_device_bytes(None) == 0
+    assert lib.pk_attn_fwd(None, None, None, None, None, None, 0.125, None, None) == pk.PK_ERR_INVALID_ARG
+    plan = pk.Plan([0, 3], [(0, 3, 0)], 2, 2, 64, num_ctas=2, upload=False)
+    # scale must be finite and positive
+    for bad in (0.0, -1.0, float("nan"), float("inf")):
+        assert lib.pk_attn_fwd(plan.handle, None, None, None, None, None, bad, None, None) \
+            == pk.PK_ERR_INVALID_ARG
+    # not uploaded yet
+    assert lib.pk_attn_fwd(plan.handle, 16, 16, 16, 16, 16, 0.125, None, None) == pk.PK_ERR_NOT_UPLOADED
+    assert lib.pk_plan_upload(plan.handle, None, 0, None) == pk.PK_ERR_INVALID_ARG
+
+
+def test_upload_rejects_small_or_misaligned_buffers_before_touching_memory():
+    lib = pk.load()
+    plan = pk.Plan([0, 300], [(0, 300, 1)], 4, 2, 128, num_ctas=4, upload=False)
+    n = plan.device_bytes
+    assert n > 0 and n % 256 == 0
+    assert lib.pk_plan_upload(plan.handle, 4096, n - 1, None) == pk.PK_ERR_INVALID_ARG
+    assert lib.pk_plan_upload(plan.handle, 4096 + 16, n, None) == pk.PK_ERR_ALIGNMENT

@@ -1,0 +1,165 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on
+the same seeded inputs.  Tolerance: max |out_gpu - out_oracle| <= 1e-2 on
+the bf16 outputs and <= 1e-3 on the fp32 natural-log LSE."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import packed_varlen_masked_gb300 as pk
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+OUT_TOL = 1e-2
+LSE_TOL = 1e-3
+
+
+def _gpu(pack, q, k, v, plan=None):
+    if plan is None:
+        plan = pk.plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d)
+    out, lse = pk.attn_fwd(q.cuda(), k.cuda(), v.cuda(), plan, pack.scale, check_status=True)
+    return out.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def _compare(pack, out_g, lse_g, out_o, lse_o, rows=None):
+    if rows is not None:
+        out_g, lse_g = out_g[rows], lse_g[:, rows]
+    assert np.isfinite(out_g).all() and np.isfinite(lse_g).all()
+    e_out = float(np.abs(out_g - out_o).max()) if out_o.size else 0.0
+    e_lse = float(np.abs(lse_g - lse_o).max()) if lse_o.size else 0.0
+    print(f"{pack.name}: max|dout|={e_out:.3e} max|dlse|={e_lse:.3e} max|o|={np.abs(out_o).max() if out_o.size else 0:.3f}")
+    assert e_out <= OUT_TOL, e_out
+    assert e_lse <= LSE_TOL, e_lse
+
+
+def _full(pack, q=None, k=None, v=None):
+    if q is None:
+        q, k, v = W.make_qkv(pack)
+    out_o, lse_o = oracle.attention(q, k, v, pack.cu_seqlens, pack.segments, pack.hq,
+                                    pack.hkv, pack.d, pack.scale)
+    out_g, lse_g = _gpu(pack, q, k, v)
+    _compare(pack, out_g, lse_g, out_o, lse_o)
+
+
+def _small_packs():
+    rng = np.random.default_rng(2024)
+    packs = []
+    for i, (hq, hkv, d) in enumerate([(8, 2, 128), (8, 2, 64), (6, 2, 128), (4, 4, 64),
+                                      (2, 1, 128), (3, 3, 64)]):
+        packs.append(W.random_pack(rng, 4, 700, hq=hq, hkv=hkv, d=d, name=f"rand{i}-h{hq}-{hkv}-d{d}"))
+    packs.append(W.Pack("ragged-tails", [[(W.TEXT, 1)], [], [(W.IMAGE, 1)], [(W.IMAGE, 129)],
+                                         [(W.TEXT, 128), (W.IMAGE, 129), (W.TEXT, 3)],
+                                         [(W.IMAGE, 255), (W.TEXT, 1)], [(W.TEXT, 383)]],
+                        hq=4, hkv=2, d=128, seed=5))
+    packs.append(W.Pack("adjacent-images", [[(W.TEXT, 40), (W.IMAGE, 200), (W.IMAGE, 200),
+                                             (W.IMAGE, 300), (W.TEXT, 7)]],
+                        hq=8, hkv=2, d=128, seed=6))
+    packs.append(W.Pack("all-text-causal", [[(W.TEXT, 513)], [(W.TEXT, 77)]], hq=4, hkv=2, d=128, seed=7))
+    packs.append(W.Pack("all-image-full", [[(W.IMAGE, 513)], [(W.IMAGE, 77)]], hq=4, hkv=2, d=64, seed=8))
+    packs.append(W.Pack("sharp-q8", [[(W.TEXT, 100), (W.IMAGE, 400)], [(W.TEXT, 30), (W.IMAGE, 256)]],
+                        hq=8, hkv=2, d=128, seed=9, q_mult=8.0))
+    return packs
+
+
+@pytest.mark.parametrize("pack", _small_packs(), ids=lambda p: p.name)
+def test_small_packs_full(pack):
+    _full(pack)
+
+
+def test_tiny_config_full():
+    _full(W.tiny_pack())
+
+
+def test_cfg_pair_config_full():
+    _full(W.cfg_pair())
+
+
+@pytest.mark.parametrize("name,budget", [("mixed_resolution", 384), ("highres_edit", 192),
+                                         ("skewed", 384)])
+def test_full_size_configs_sampled(name, budget):
+    """Full-size packs in the benchmark's launch configuration (one CTA per
+    SM), compared on a deterministic row sample that includes every sequence
+    and segment edge and rows on both sides of 128-row tile edges."""
+    pack = W.CONFIGS[name]()
+    q, k, v = W.make_qkv(pack)
+    rows = W.sample_rows(pack, budget)
+    out_o, lse_o = oracle.attention(q, k, v, pack.cu_seqlens, pack.segments, pack.hq,
+                                    pack.hkv, pack.d, pack.scale, rows=rows)
+    out_g, lse_g = _gpu(pack, q, k, v)
+    _compare(pack, out_g, lse_g, out_o, lse_o, rows=rows)
+
+
+def test_growing_maximum_rescales_output():
+    """Scores that grow key tile after key tile force the running maximum to
+    move by more than the lazy-rescale threshold many times."""
+    pack = W.Pack("growing", [[(W.IMAGE, 1024)], [(W.TEXT, 640)]], hq=2, hkv=1, d=64, seed=3)
+    q, k, v = W.make_qkv(pack)
+    T = pack.total_tokens
+    ramp = torch.linspace(0.0, 6.0, T).view(T, 1, 1)
+    k = (k.float() * 0.1 + ramp).bfloat16()
+    q = torch.ones_like(q) * 0.5
+    _full(pack, q, k, v)
+
+
+def test_every_row_written_and_guard_bands_untouched():
+    pack = W.Pack("guard", [[(W.TEXT, 50), (W.IMAGE, 200)], [(W.TEXT, 3)], [(W.IMAGE, 130)]],
+                  hq=4, hkv=2, d=128, seed=11)
+    q, k, v = W.make_qkv(pack)
+    T, G = pack.total_tokens, 4096
+    plan = pk.plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d)
+    out_buf = torch.full((T * pack.hq * pack.d + 2 * G,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse_buf = torch.full((T * pack.hq + 2 * G,), float("nan"), dtype=torch.float32, device="cuda")
+    out = out_buf[G:G + T * pack.hq * pack.d].view(T, pack.hq, pack.d)
+    lse = lse_buf[G:G + T * pack.hq].view(pack.hq, T)
+    pk.attn_fwd(q.cuda(), k.cuda(), v.cuda(), plan, pack.scale, out=out, lse=lse, check_status=True)
+    assert torch.isfinite(out).all() and torch.isfinite(lse).all()
+    assert torch.isnan(out_buf[:G]).all() and torch.isnan(out_buf[-G:]).all()
+    assert torch.isnan(lse_buf[:G]).all() and torch.isnan(lse_buf[-G:]).all()
+
+
+def test_deterministic_and_plan_reusable():
+    pack = W.mixed_resolution(seed=3, requests=2)
+    q, k, v = W.make_qkv(pack, device="cuda")
+    plan = pk.plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d)
+    o1, l1 = pk.attn_fwd(q, k, v, plan, pack.scale, check_status=True)
+    o2, l2 = pk.attn_fwd(q, k, v, plan, pack.scale, check_status=True)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    # same plan, other inputs
+    q2 = torch.randn_like(q, dtype=torch.float32).bfloat16()
+    o3, _ = pk.attn_fwd(q2, k, v, plan, pack.scale, check_status=True)
+    assert not torch.equal(o1, o3)
+
+
+def test_single_token_and_empty_pack():
+    pack = W.Pack("one", [[(W.TEXT, 1)]], hq=2, hkv=1, d=64, seed=1)
+    _full(pack)
+    empty = pk.plan([0, 0], [], 2, 1, 64)
+    z = torch.zeros(0, 2, 64, dtype=torch.bfloat16, device="cuda")
+    zk = torch.zeros(0, 1, 64, dtype=torch.bfloat16, device="cuda")
+    out, lse = pk.attn_fwd(z, zk, zk, empty, 0.125, check_status=True)
+    assert out.shape == (0, 2, 64) and lse.shape == (2, 0)
+
+
+def test_misaligned_tensor_rejected_before_launch():
+    pack = W.Pack("mis", [[(W.TEXT, 64)]], hq=2, hkv=2, d=64, seed=1)
+    plan = pk.plan(pack.cu_seqlens, pack.segments, 2, 2, 64)
+    lib = pk.load()
+    base = torch.zeros(64 * 2 * 64 + 8, dtype=torch.bfloat16, device="cuda")
+    good = base[:64 * 2 * 64]
+    lse = torch.zeros(2, 64, dtype=torch.float32, device="cuda")
+    import ctypes
+    st = lib.pk_attn_fwd(plan.handle, ctypes.c_void_p(base.data_ptr() + 2), ctypes.c_void_p(good.data_ptr()),
+                         ctypes.c_void_p(good.data_ptr()), ctypes.c_void_p(good.data_ptr()),
+                         ctypes.c_void_p(lse.data_ptr()), 0.125, None, None)
+    assert st == pk.PK_ERR_ALIGNMENT
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pk.debug_wait_timeout(status, 2_000_000)  # 2 ms
+    torch.cuda.synchronize()
+    assert int(status.item()) == pk.PK_ERR_TIMEOUT
+    _full(W.Pack("after-timeout", [[(W.TEXT, 20), (W.IMAGE, 150)]], hq=2, hkv=1, d=64, seed=2))
