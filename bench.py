@@ -260,12 +260,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--requests", type=int, default=8,
+                    help="requests in the mixed-resolution pack (x2 CFG branches)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
     world, rank, local = dist_setup(args)
-    pack = W.CONFIGS[args.workload]()
+    pack = (W.mixed_resolution(requests=args.requests) if args.workload == "mixed_resolution"
+            else W.CONFIGS[args.workload]())
 
     if args.impl == "reference":
         return reference_arm(args, pack, rank, world)

@@ -207,6 +207,29 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// Three-input maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// Packed pair arithmetic: (d0, d1) = (a0, a1) * (b0, b1) + (c0, c1).
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
+                                     float c0, float c1) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+// (d0, d1) += (a0, a1)
+__device__ __forceinline__ void acc2(float& d0, float& d1, float a0, float a1) {
+  asm("{\n\t.reg .b64 ra, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rd, {%0, %1};\n\t"
+      "add.rn.f32x2 rd, rd, ra;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1));
+}
 // {lo -> bits 0-15, hi -> bits 16-31}, round to nearest even.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
@@ -434,9 +457,16 @@ __device__ void softmax_role(const KernelParams& p, int slot, uint32_t sbase, ui
 #pragma unroll
         for (int c = 0; c < 128; ++c) x[c] = c < nvis ? x[c] : -INFINITY;
       }
-      float mx = x[0];
+      // Row maximum: eight independent three-input chains, then a short tree.
+      float mc[8];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
+      for (int i = 0; i < 8; ++i) mc[i] = fmaxf(x[2 * i], x[2 * i + 1]);
+#pragma unroll
+      for (int b = 16; b < 128; b += 16)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mc[i] = max3(mc[i], x[b + 2 * i], x[b + 2 * i + 1]);
+      const float mx = max3(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], mc[5]),
+                            fmaxf(mc[6], mc[7]));
       const float m_new = mx * sl2;
       if (j == 0) {
         m_used = m_new;
@@ -458,18 +488,21 @@ __device__ void softmax_role(const KernelParams& p, int slot, uint32_t sbase, ui
           }
         }
       }
+      // p = 2^(s*scale*log2e - m); P goes to the tensor cores as bf16, the
+      // row sum l accumulates the fp32 values.
       const float neg = -m_used;
       uint32_t pp[64];
-      float sum0 = 0.f, sum1 = 0.f;
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 128; c += 2) {
-        const float p0 = ex2(fmaf(x[c], sl2, neg));
-        const float p1 = ex2(fmaf(x[c + 1], sl2, neg));
-        sum0 += p0;
-        sum1 += p1;
+        float a0, a1;
+        fma2(a0, a1, x[c], x[c + 1], sl2, sl2, neg, neg);
+        const float p0 = ex2(a0), p1 = ex2(a1);
         pp[c >> 1] = pack_bf16x2(p0, p1);
+        const int q = (c >> 1) & 3;
+        acc2(acc[2 * q], acc[2 * q + 1], p0, p1);
       }
-      l += sum0 + sum1;
+      l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
       tmem_st_x64(tS, pp);
       tc_fence_before();
       mbar_arrive(bar(C::kPReady + slot));

@@ -1,6 +1,11 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on
-the same seeded inputs.  Tolerance: max |out_gpu - out_oracle| <= 1e-2 on
-the bf16 outputs and <= 1e-3 on the fp32 natural-log LSE."""
+the same seeded inputs.
+
+Tolerance: |out_gpu - out_oracle| <= 1e-2 + half a bf16 ulp of out_oracle
+on every bf16 output element (the 1e-2 bounds the kernel's arithmetic; the
+half ulp is the rounding of the output to bf16 itself, 0.0078 for |o| in
+[2, 4) and 0.0156 for |o| in [4, 8), which no bf16 result can avoid), and
+|lse_gpu - lse_oracle| <= 1e-3 on the fp32 natural-log LSE."""
 import math
 
 import numpy as np
@@ -24,14 +29,25 @@ def _gpu(pack, q, k, v, plan=None):
     return out.float().cpu().numpy(), lse.cpu().numpy()
 
 
+def _half_ulp_bf16(x):
+    """Half a bf16 unit in the last place at |x| (8 significant bits)."""
+    a = np.maximum(np.abs(x), np.finfo(np.float32).tiny)
+    return 0.5 * np.exp2(np.floor(np.log2(a)) - 7)
+
+
 def _compare(pack, out_g, lse_g, out_o, lse_o, rows=None):
     if rows is not None:
         out_g, lse_g = out_g[rows], lse_g[:, rows]
     assert np.isfinite(out_g).all() and np.isfinite(lse_g).all()
-    e_out = float(np.abs(out_g - out_o).max()) if out_o.size else 0.0
-    e_lse = float(np.abs(lse_g - lse_o).max()) if lse_o.size else 0.0
-    print(f"{pack.name}: max|dout|={e_out:.3e} max|dlse|={e_lse:.3e} max|o|={np.abs(out_o).max() if out_o.size else 0:.3f}")
-    assert e_out <= OUT_TOL, e_out
+    if out_o.size == 0:
+        return
+    err = np.abs(out_g - out_o)
+    e_out = float(err.max())
+    e_lse = float(np.abs(lse_g - lse_o).max())
+    excess = float((err - _half_ulp_bf16(out_o)).max())
+    print(f"{pack.name}: max|dout|={e_out:.3e} max(|dout|-ulp/2)={excess:.3e} "
+          f"max|dlse|={e_lse:.3e} max|o|={np.abs(out_o).max():.3f}")
+    assert (err <= OUT_TOL + _half_ulp_bf16(out_o)).all(), (e_out, excess)
     assert e_lse <= LSE_TOL, e_lse
 
 
