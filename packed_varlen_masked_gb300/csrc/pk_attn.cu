@@ -10,8 +10,9 @@
 // are either fully visible (no mask math) or partial (per-element compare).
 //
 // Kernel organisation (one persistent CTA per SM, 12 warps):
-//   warp 0      TMA producer: Q tiles of the two query-head slots, then a
-//               ring of K and V tiles (128-byte swizzled, one box per 64
+//   warp 0      TMA producer of the Q tiles of the two query-head slots and
+//               of a 3-stage ring of K tiles; warp 2: TMA producer of a
+//               2-stage ring of V tiles (128-byte swizzled boxes, one per 64
 //               columns of the head dimension).
 //   warp 1      allocates the 512 TMEM columns; one thread issues every
 //               tcgen05.mma: S = Q K^T (both operands K-major in shared
@@ -54,20 +55,22 @@ template <int D>
 struct Cfg {
   static constexpr int kHalves = D / 64;
   static constexpr int kTileBytes = 128 * D * 2;
-  // Stage count keeps shared memory above half an SM, so that exactly one
-  // CTA (and one 512-column TMEM allocation) lives on each SM.
-  static constexpr int kStages = D == 128 ? 2 : 4;
+  // Ring depths: K gets one stage more than V (a key tile is needed a half
+  // period before its value tile).  Shared memory stays above half an SM, so
+  // that exactly one CTA (and one 512-column TMEM allocation) lives per SM.
+  static constexpr int kKStages = D == 128 ? 3 : 4;
+  static constexpr int kVStages = D == 128 ? 2 : 4;
   static constexpr uint32_t kColS0 = 0, kColS1 = 128;
   static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = 2 * kTileBytes;
-  static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  static constexpr int kOffV = kOffK + kKStages * kTileBytes;
+  static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
   // barrier indices
   static constexpr int kQFull = 0, kQEmpty = 1;
-  static constexpr int kKFull = 2, kKEmpty = kKFull + kStages;
-  static constexpr int kVFull = kKEmpty + kStages, kVEmpty = kVFull + kStages;
-  static constexpr int kSFull = kVEmpty + kStages;  // [2]
+  static constexpr int kKFull = 2, kKEmpty = kKFull + kKStages;
+  static constexpr int kVFull = kKEmpty + kKStages, kVEmpty = kVFull + kVStages;
+  static constexpr int kSFull = kVEmpty + kVStages;  // [2]
   static constexpr int kPReady = kSFull + 2;        // [2]
   static constexpr int kOFull = kPReady + 2;        // [2]
   static constexpr int kOFree = kOFull + 2;         // [2]
@@ -167,6 +170,26 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
+}
+// Same copy with an L2 eviction-priority policy (from createpolicy).
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar, int c0, int c1, int c2,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
 }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -280,14 +303,18 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
   }
 }
 
+// Q/K producer (one thread): per item the two query tiles, then the ring of
+// key tiles.  Keys and values are re-read by the other query heads of the
+// group and by neighbouring query tiles, so they are kept in L2 (evict-last);
+// each query tile is read once (evict-first).
 template <int D>
-__device__ void producer_role(const KernelParams& p, const CUtensorMap* tm_q,
-                              const CUtensorMap* tm_k, const CUtensorMap* tm_v, uint32_t sbase,
-                              int beg, int end, const WaitCtl& wc) {
+__device__ void producer_qk_role(const KernelParams& p, const CUtensorMap* tm_q,
+                                 const CUtensorMap* tm_k, uint32_t sbase, int beg, int end,
+                                 const WaitCtl& wc) {
   using C = Cfg<D>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
-  uint32_t kv_iter = 0, item_iter = 0;
-  uint32_t k_armed = 0, v_armed = 0, q_armed = 0;
+  const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
+  uint32_t kv_iter = 0, item_iter = 0, k_armed = 0, q_armed = 0;
   bool ok = true;
   for (int it = beg; it < end && ok; ++it, ++item_iter) {
     const pk_work_item w = p.items[it];
@@ -297,44 +324,63 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tm_q,
     ++q_armed;
 #pragma unroll
     for (int h = 0; h < C::kHalves; ++h) {
-      tma_load_3d(sbase + C::kOffQ + h * kBoxBytes, tm_q, bar(C::kQFull), h * 64, w.hq0,
-                  w.q_start);
+      tma_load_3d_hint(sbase + C::kOffQ + h * kBoxBytes, tm_q, bar(C::kQFull), h * 64, w.hq0,
+                       w.q_start, stream);
       if (two)
-        tma_load_3d(sbase + C::kOffQ + C::kTileBytes + h * kBoxBytes, tm_q, bar(C::kQFull),
-                    h * 64, w.hq1, w.q_start);
+        tma_load_3d_hint(sbase + C::kOffQ + C::kTileBytes + h * kBoxBytes, tm_q, bar(C::kQFull),
+                         h * 64, w.hq1, w.q_start, stream);
     }
     for (int j = 0; j < w.n_kt; ++j, ++kv_iter) {
-      const uint32_t st = kv_iter % C::kStages, ph = (kv_iter / C::kStages) & 1u;
-      const int row = w.kv_start + j * 128;
+      const uint32_t st = kv_iter % C::kKStages, ph = (kv_iter / C::kKStages) & 1u;
       if (!(ok = mbar_wait(bar(C::kKEmpty + st), ph ^ 1u, wc))) break;
       mbar_arrive_expect_tx(bar(C::kKFull + st), C::kTileBytes);
       ++k_armed;
 #pragma unroll
       for (int h = 0; h < C::kHalves; ++h)
-        tma_load_3d(sbase + C::kOffK + st * C::kTileBytes + h * kBoxBytes, tm_k,
-                    bar(C::kKFull + st), h * 64, w.hkv, row);
+        tma_load_3d_hint(sbase + C::kOffK + st * C::kTileBytes + h * kBoxBytes, tm_k,
+                         bar(C::kKFull + st), h * 64, w.hkv, w.kv_start + j * 128, keep);
+    }
+  }
+  if (!ok) {
+    // Aborted: let every copy already issued land before the CTA may exit.
+    // The last kKStages armings of the ring are the only ones that can be
+    // open, and each is the most recent arming of its stage.
+    for (uint32_t k = 1; k <= (uint32_t)C::kKStages && k <= k_armed; ++k) {
+      const uint32_t i = k_armed - k;
+      mbar_wait_drain(bar(C::kKFull + i % C::kKStages), (i / C::kKStages) & 1u, wc);
+    }
+    if (q_armed) mbar_wait_drain(bar(C::kQFull), (q_armed - 1u) & 1u, wc);
+  }
+}
+
+// V producer (one thread of another warp): the ring of value tiles, so that
+// a value tile waiting for its stage never holds back the next key tile.
+template <int D>
+__device__ void producer_v_role(const KernelParams& p, const CUtensorMap* tm_v, uint32_t sbase,
+                                int beg, int end, const WaitCtl& wc) {
+  using C = Cfg<D>;
+  auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
+  const uint64_t keep = l2_policy_evict_last();
+  uint32_t kv_iter = 0, v_armed = 0;
+  bool ok = true;
+  for (int it = beg; it < end && ok; ++it) {
+    const pk_work_item w = p.items[it];
+    for (int j = 0; j < w.n_kt; ++j, ++kv_iter) {
+      const uint32_t st = kv_iter % C::kVStages, ph = (kv_iter / C::kVStages) & 1u;
       if (!(ok = mbar_wait(bar(C::kVEmpty + st), ph ^ 1u, wc))) break;
       mbar_arrive_expect_tx(bar(C::kVFull + st), C::kTileBytes);
       ++v_armed;
 #pragma unroll
       for (int h = 0; h < C::kHalves; ++h)
-        tma_load_3d(sbase + C::kOffV + st * C::kTileBytes + h * kBoxBytes, tm_v,
-                    bar(C::kVFull + st), h * 64, w.hkv, row);
+        tma_load_3d_hint(sbase + C::kOffV + st * C::kTileBytes + h * kBoxBytes, tm_v,
+                         bar(C::kVFull + st), h * 64, w.hkv, w.kv_start + j * 128, keep);
     }
   }
   if (!ok) {
-    // Aborted: let every copy already issued land before the CTA may exit.
-    // The last kStages armings of a ring are the only ones that can be open,
-    // and each is the most recent arming of its stage.
-    for (uint32_t k = 1; k <= (uint32_t)C::kStages && k <= k_armed; ++k) {
-      const uint32_t i = k_armed - k;
-      mbar_wait_drain(bar(C::kKFull + i % C::kStages), (i / C::kStages) & 1u, wc);
-    }
-    for (uint32_t k = 1; k <= (uint32_t)C::kStages && k <= v_armed; ++k) {
+    for (uint32_t k = 1; k <= (uint32_t)C::kVStages && k <= v_armed; ++k) {
       const uint32_t i = v_armed - k;
-      mbar_wait_drain(bar(C::kVFull + i % C::kStages), (i / C::kStages) & 1u, wc);
+      mbar_wait_drain(bar(C::kVFull + i % C::kVStages), (i / C::kVStages) & 1u, wc);
     }
-    if (q_armed) mbar_wait_drain(bar(C::kQFull), (q_armed - 1u) & 1u, wc);
   }
 }
 
@@ -355,7 +401,7 @@ __device__ void mma_role(const KernelParams& p, uint32_t sbase, uint32_t tmem, i
     const int n = w.n_kt;
     if (!(ok = mbar_wait(bar(C::kQFull), item_iter & 1u, wc))) break;
     {
-      const uint32_t st = kv_iter % C::kStages, ph = (kv_iter / C::kStages) & 1u;
+      const uint32_t st = kv_iter % C::kKStages, ph = (kv_iter / C::kKStages) & 1u;
       if (!(ok = mbar_wait(bar(C::kKFull + st), ph, wc))) break;
       tc_fence_after();
       const uint32_t ks = sbase + C::kOffK + st * C::kTileBytes;
@@ -370,13 +416,13 @@ __device__ void mma_role(const KernelParams& p, uint32_t sbase, uint32_t tmem, i
     }
     for (int j = 1; j <= n; ++j) {
       const uint32_t ip = kv_iter + (uint32_t)j - 1u;
-      const uint32_t stp = ip % C::kStages, php = (ip / C::kStages) & 1u;
+      const uint32_t stp = ip % C::kVStages, php = (ip / C::kVStages) & 1u;
       const uint32_t vs = sbase + C::kOffV + stp * C::kTileBytes;
       uint32_t stj = 0, ks = 0;
       if (j < n) {
         const uint32_t ij = kv_iter + (uint32_t)j;
-        stj = ij % C::kStages;
-        if (!(ok = mbar_wait(bar(C::kKFull + stj), (ij / C::kStages) & 1u, wc))) break;
+        stj = ij % C::kKStages;
+        if (!(ok = mbar_wait(bar(C::kKFull + stj), (ij / C::kKStages) & 1u, wc))) break;
         ks = sbase + C::kOffK + stj * C::kTileBytes;
       }
       if (!(ok = mbar_wait(bar(C::kVFull + stp), php, wc))) break;
@@ -447,27 +493,44 @@ __device__ void softmax_role(const KernelParams& p, int slot, uint32_t sbase, ui
       sf_ph ^= 1u;
       if (!ok) break;
       tc_fence_after();
-      uint32_t sr[128];
-      tmem_ld_x128(tS, sr);
-      float x[128];
-#pragma unroll
-      for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c]);
+      // Partial tile: overwrite the scores of keys past this row's limit with
+      // -inf in TMEM, so the passes below carry no mask state.
       if (j >= w.n_full) {
         const int nvis = lim - (w.kv_start + j * 128) + 1;
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t cm[32];
+          tmem_ld_x32(tS + (uint32_t)(32 * ch), cm);
 #pragma unroll
-        for (int c = 0; c < 128; ++c) x[c] = c < nvis ? x[c] : -INFINITY;
+          for (int c = 0; c < 32; ++c)
+            cm[c] = (32 * ch + c < nvis) ? cm[c] : 0xff800000u;  // -inf
+          tmem_st_x32(tS + (uint32_t)(32 * ch), cm);
+        }
       }
-      // Row maximum: eight independent three-input chains, then a short tree.
-      float mc[8];
+      // Row maximum over the 128 scores from four 32-column TMEM loads,
+      // double buffered; eight independent three-input max chains.
+      uint32_t ca[32], cb[32];
+      float m_new;
+      {
+        float mc[8] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY,
+                       -INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        tmem_ld_x32_async(tS, ca);
+        tmem_wait_ld_x32(ca);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mc[i] = fmaxf(x[2 * i], x[2 * i + 1]);
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t(&cur)[32] = (ch & 1) ? cb : ca;
+          uint32_t(&nxt)[32] = (ch & 1) ? ca : cb;
+          if (ch < 3) tmem_ld_x32_async(tS + (uint32_t)(32 * (ch + 1)), nxt);
 #pragma unroll
-      for (int b = 16; b < 128; b += 16)
+          for (int b0 = 0; b0 < 32; b0 += 16)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mc[i] = max3(mc[i], x[b + 2 * i], x[b + 2 * i + 1]);
-      const float mx = max3(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], mc[5]),
-                            fmaxf(mc[6], mc[7]));
-      const float m_new = mx * sl2;
+            for (int i = 0; i < 8; ++i)
+              mc[i] = max3(mc[i], __uint_as_float(cur[b0 + 2 * i]),
+                           __uint_as_float(cur[b0 + 2 * i + 1]));
+          if (ch < 3) tmem_wait_ld_x32(nxt);
+        }
+        m_new = max3(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7])) * sl2;
+      }
       if (j == 0) {
         m_used = m_new;
       } else {
@@ -488,22 +551,34 @@ __device__ void softmax_role(const KernelParams& p, int slot, uint32_t sbase, ui
           }
         }
       }
-      // p = 2^(s*scale*log2e - m); P goes to the tensor cores as bf16, the
-      // row sum l accumulates the fp32 values.
+      // p = 2^(s*scale*log2e - m), in four 32-column chunks re-read from
+      // TMEM (the next chunk's load overlaps this chunk's exponentials).  P
+      // of chunk c (bf16 pairs) lands in columns [16c, 16c+16) of S, below
+      // every column still to be read.  The row sum l accumulates fp32 p.
       const float neg = -m_used;
-      uint32_t pp[64];
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      tmem_ld_x32_async(tS, ca);
+      tmem_wait_ld_x32(ca);
 #pragma unroll
-      for (int c = 0; c < 128; c += 2) {
-        float a0, a1;
-        fma2(a0, a1, x[c], x[c + 1], sl2, sl2, neg, neg);
-        const float p0 = ex2(a0), p1 = ex2(a1);
-        pp[c >> 1] = pack_bf16x2(p0, p1);
-        const int q = (c >> 1) & 3;
-        acc2(acc[2 * q], acc[2 * q + 1], p0, p1);
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t(&cur)[32] = (ch & 1) ? cb : ca;
+        uint32_t(&nxt)[32] = (ch & 1) ? ca : cb;
+        if (ch < 3) tmem_ld_x32_async(tS + (uint32_t)(32 * (ch + 1)), nxt);
+        uint32_t pp[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float a0, a1;
+          fma2(a0, a1, __uint_as_float(cur[c]), __uint_as_float(cur[c + 1]), sl2, sl2, neg, neg);
+          const float p0 = ex2(a0), p1 = ex2(a1);
+          pp[c >> 1] = pack_bf16x2(p0, p1);
+          const int q = (c >> 1) & 3;
+          acc2(acc[2 * q], acc[2 * q + 1], p0, p1);
+        }
+        tmem_st_x16_async(tS + (uint32_t)(16 * ch), pp);
+        if (ch < 3) tmem_wait_ld_x32(nxt);
       }
       l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-      tmem_st_x64(tS, pp);
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(C::kPReady + slot));
     }
@@ -556,9 +631,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar(C::kQFull), 1);
     mbar_init(bar(C::kQEmpty), 1);
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(bar(C::kKFull + s), 1);
       mbar_init(bar(C::kKEmpty + s), 1);
+    }
+    for (int s = 0; s < C::kVStages; ++s) {
       mbar_init(bar(C::kVFull + s), 1);
       mbar_init(bar(C::kVEmpty + s), 1);
     }
@@ -590,7 +667,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtl wc{abort_flag, p.status, p.wait_limit_ns};
 
   if (warp == 0) {
-    if (lane == 0) producer_role<D>(p, &tm_q, &tm_k, &tm_v, sbase, beg, end, wc);
+    if (lane == 0) producer_qk_role<D>(p, &tm_q, &tm_k, sbase, beg, end, wc);
+    __syncwarp();
+  } else if (warp == 2) {
+    if (lane == 0) producer_v_role<D>(p, &tm_v, sbase, beg, end, wc);
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) mma_role<D>(p, sbase, tmem, beg, end, wc);
