@@ -47,7 +47,7 @@
 namespace pk {
 namespace dev {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 64 bf16
 
@@ -55,31 +55,35 @@ template <int D>
 struct Cfg {
   static constexpr int kHalves = D / 64;
   static constexpr int kTileBytes = 128 * D * 2;
-  // Ring depths: K gets one stage more than V (a key tile is needed a half
-  // period before its value tile).  Shared memory stays above half an SM, so
-  // that exactly one CTA (and one 512-column TMEM allocation) lives per SM.
+  // Rings: two query tiles (the next unit's loads during this one), three
+  // key tiles, two value tiles.  Shared memory stays above half an SM, so
+  // exactly one CTA (and one 512-column TMEM allocation) lives on each SM.
   static constexpr int kKStages = D == 128 ? 3 : 4;
   static constexpr int kVStages = D == 128 ? 2 : 4;
-  static constexpr uint32_t kColS0 = 0, kColS1 = 128;
-  static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
+  // TMEM columns: S double buffer, P double buffer (bf16 pairs), O.
+  static constexpr uint32_t kColS0 = 0;    // S(t) in [128*(t%2), +128)
+  static constexpr uint32_t kColP0 = 256;  // P(t) in [256 + 64*(t%2), +64)
+  static constexpr uint32_t kColO = 384;   // O in [384, 384 + D)
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = 2 * kTileBytes;
   static constexpr int kOffV = kOffK + kKStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
   // barrier indices
-  static constexpr int kQFull = 0, kQEmpty = 1;
-  static constexpr int kKFull = 2, kKEmpty = kKFull + kKStages;
+  static constexpr int kQFull = 0, kQEmpty = 2;  // [2] each
+  static constexpr int kKFull = 4, kKEmpty = kKFull + kKStages;
   static constexpr int kVFull = kKEmpty + kKStages, kVEmpty = kVFull + kVStages;
   static constexpr int kSFull = kVEmpty + kVStages;  // [2]
-  static constexpr int kPReady = kSFull + 2;        // [2]
-  static constexpr int kOFull = kPReady + 2;        // [2]
-  static constexpr int kOFree = kOFull + 2;         // [2]
-  static constexpr int kMmaDone = kOFree + 2;
-  static constexpr int kNumBars = kMmaDone + 1;
+  static constexpr int kSFree = kSFull + 2;          // [2]
+  static constexpr int kPReady = kSFree + 2;         // [2]
+  static constexpr int kPvDone = kPReady + 2;        // [2]
+  static constexpr int kOFree = kPvDone + 2;
+  static constexpr int kMmaDone = kOFree + 1;  // [2]: one per MMA issuer
+  static constexpr int kNumBars = kMmaDone + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   static_assert(kSmemBytes > 114 * 1024, "one CTA per SM");
+  static_assert(kColO + D <= 512, "TMEM budget");
 };
 
 // Instruction descriptors of tcgen05.mma kind::f16 (dense, f32 accumulate,
@@ -273,18 +277,42 @@ struct KernelParams {
   uint64_t wait_limit_ns;
 };
 
+// A unit of work is one query head of a work item: a 128-row query tile that
+// streams the key/value tiles of its sequence.  A CTA runs the heads of each
+// of its items back to back, so the second head's keys and values come from
+// L2.  Every role walks the same unit sequence.
+struct UnitIter {
+  const pk_work_item* items;
+  int it, end, slot;
+  pk_work_item w;
+  __device__ UnitIter(const pk_work_item* items_, int beg, int end_)
+      : items(items_), it(beg), end(end_), slot(0) {
+    if (it < end) w = items[it];
+  }
+  __device__ bool valid() const { return it < end; }
+  __device__ int head() const { return slot ? w.hq1 : w.hq0; }
+  __device__ void next() {
+    if (slot == 0 && w.hq1 >= 0) {
+      slot = 1;
+      return;
+    }
+    slot = 0;
+    if (++it < end) w = items[it];
+  }
+};
+
 // S(tmem) = Q K^T over the head dimension: D/16 MMAs of 128x128x16.  Both
 // tiles are K-major with 128-byte swizzle: row r of a 64-column box sits at
 // r*128 bytes, 8-row groups 1024 bytes apart; the k-th 16-column step starts
-// 32*(k%4) bytes into box k/4.
+// 32*(k%4) bytes into box k/4.  q_desc / k_desc describe the tiles' first
+// byte; a step only adds its byte offset / 16 to the start-address field.
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
   constexpr uint32_t idesc = make_idesc(128, 128, false);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (uint32_t)(kk >> 2) * kBoxBytes + (uint32_t)(kk & 3) * 32u;
-    mma_ss(d_tmem, sdesc(q_smem + off, 16, 1024), sdesc(k_smem + off, 16, 1024), idesc,
-           kk > 0 ? 1u : 0u);
+    const uint64_t off = (uint64_t)(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
+    mma_ss(d_tmem, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -292,21 +320,19 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint3
 // TMEM, 8 columns per 16 keys.  V is MN-major with 128-byte swizzle: 16 keys
 // span 2048 bytes, and the second 64-column box (D = 128) is 16384 bytes on.
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
                                          bool accumulate) {
   constexpr uint32_t idesc = make_idesc(128, D, true);
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    mma_ts(d_tmem, p_tmem + (uint32_t)kk * 8u,
-           sdesc(v_smem + (uint32_t)kk * 2048u, kBoxBytes, 1024), idesc,
+  for (int kk = 0; kk < 8; ++kk)
+    mma_ts(d_tmem, p_tmem + (uint32_t)kk * 8u, v_desc + (uint64_t)(kk * (2048 >> 4)), idesc,
            (accumulate || kk > 0) ? 1u : 0u);
-  }
 }
 
-// Q/K producer (one thread): per item the two query tiles, then the ring of
-// key tiles.  Keys and values are re-read by the other query heads of the
-// group and by neighbouring query tiles, so they are kept in L2 (evict-last);
-// each query tile is read once (evict-first).
+// Q/K producer (one thread): per unit its query tile (double buffered), then
+// the ring of key tiles.  Keys and values are re-read by the other query
+// heads of the group and by neighbouring query tiles, so they are kept in L2
+// (evict-last); a query tile is read once (evict-first).
 template <int D>
 __device__ void producer_qk_role(const KernelParams& p, const CUtensorMap* tm_q,
                                  const CUtensorMap* tm_k, uint32_t sbase, int beg, int end,
@@ -314,24 +340,20 @@ __device__ void producer_qk_role(const KernelParams& p, const CUtensorMap* tm_q,
   using C = Cfg<D>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
   const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
-  uint32_t kv_iter = 0, item_iter = 0, k_armed = 0, q_armed = 0;
+  uint32_t g = 0, u = 0, k_armed = 0, q_armed = 0;
   bool ok = true;
-  for (int it = beg; it < end && ok; ++it, ++item_iter) {
-    const pk_work_item w = p.items[it];
-    if (!(ok = mbar_wait(bar(C::kQEmpty), (item_iter & 1u) ^ 1u, wc))) break;
-    const bool two = w.hq1 >= 0;
-    mbar_arrive_expect_tx(bar(C::kQFull), (two ? 2u : 1u) * C::kTileBytes);
+  for (UnitIter ui(p.items, beg, end); ui.valid() && ok; ui.next(), ++u) {
+    const pk_work_item& w = ui.w;
+    const uint32_t qb = u & 1u;
+    if (!(ok = mbar_wait(bar(C::kQEmpty + qb), ((u >> 1) & 1u) ^ 1u, wc))) break;
+    mbar_arrive_expect_tx(bar(C::kQFull + qb), C::kTileBytes);
     ++q_armed;
 #pragma unroll
-    for (int h = 0; h < C::kHalves; ++h) {
-      tma_load_3d_hint(sbase + C::kOffQ + h * kBoxBytes, tm_q, bar(C::kQFull), h * 64, w.hq0,
-                       w.q_start, stream);
-      if (two)
-        tma_load_3d_hint(sbase + C::kOffQ + C::kTileBytes + h * kBoxBytes, tm_q, bar(C::kQFull),
-                         h * 64, w.hq1, w.q_start, stream);
-    }
-    for (int j = 0; j < w.n_kt; ++j, ++kv_iter) {
-      const uint32_t st = kv_iter % C::kKStages, ph = (kv_iter / C::kKStages) & 1u;
+    for (int h = 0; h < C::kHalves; ++h)
+      tma_load_3d_hint(sbase + C::kOffQ + qb * C::kTileBytes + h * kBoxBytes, tm_q,
+                       bar(C::kQFull + qb), h * 64, ui.head(), w.q_start, stream);
+    for (int j = 0; j < w.n_kt; ++j, ++g) {
+      const uint32_t st = g % C::kKStages, ph = (g / C::kKStages) & 1u;
       if (!(ok = mbar_wait(bar(C::kKEmpty + st), ph ^ 1u, wc))) break;
       mbar_arrive_expect_tx(bar(C::kKFull + st), C::kTileBytes);
       ++k_armed;
@@ -343,13 +365,16 @@ __device__ void producer_qk_role(const KernelParams& p, const CUtensorMap* tm_q,
   }
   if (!ok) {
     // Aborted: let every copy already issued land before the CTA may exit.
-    // The last kKStages armings of the ring are the only ones that can be
-    // open, and each is the most recent arming of its stage.
+    // The last kKStages armings of the ring (and the last two of Q) are the
+    // only ones that can be open, each the most recent arming of its stage.
     for (uint32_t k = 1; k <= (uint32_t)C::kKStages && k <= k_armed; ++k) {
       const uint32_t i = k_armed - k;
       mbar_wait_drain(bar(C::kKFull + i % C::kKStages), (i / C::kKStages) & 1u, wc);
     }
-    if (q_armed) mbar_wait_drain(bar(C::kQFull), (q_armed - 1u) & 1u, wc);
+    for (uint32_t k = 1; k <= 2u && k <= q_armed; ++k) {
+      const uint32_t i = q_armed - k;
+      mbar_wait_drain(bar(C::kQFull + (i & 1u)), (i >> 1) & 1u, wc);
+    }
   }
 }
 
@@ -361,12 +386,12 @@ __device__ void producer_v_role(const KernelParams& p, const CUtensorMap* tm_v, 
   using C = Cfg<D>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
   const uint64_t keep = l2_policy_evict_last();
-  uint32_t kv_iter = 0, v_armed = 0;
+  uint32_t g = 0, v_armed = 0;
   bool ok = true;
-  for (int it = beg; it < end && ok; ++it) {
-    const pk_work_item w = p.items[it];
-    for (int j = 0; j < w.n_kt; ++j, ++kv_iter) {
-      const uint32_t st = kv_iter % C::kVStages, ph = (kv_iter / C::kVStages) & 1u;
+  for (UnitIter ui(p.items, beg, end); ui.valid() && ok; ui.next()) {
+    const pk_work_item& w = ui.w;
+    for (int j = 0; j < w.n_kt; ++j, ++g) {
+      const uint32_t st = g % C::kVStages, ph = (g / C::kVStages) & 1u;
       if (!(ok = mbar_wait(bar(C::kVEmpty + st), ph ^ 1u, wc))) break;
       mbar_arrive_expect_tx(bar(C::kVFull + st), C::kTileBytes);
       ++v_armed;
@@ -384,164 +409,136 @@ __device__ void producer_v_role(const KernelParams& p, const CUtensorMap* tm_v, 
   }
 }
 
+// MMA issue is split between two threads (a tcgen05.mma costs its issuing
+// thread about as long as a third of the 128x128x16 product itself, and two
+// threads of different warps issue concurrently).  Key tile t of the CTA's
+// stream (t counts across units) computes S(t) into S buffer t%2; after the
+// softmax has written P(t) into P buffer t%2, O += P(t) V(t).
+//
+// S issuer (warp 1): S(t) needs K(t) loaded and S buffer t%2 released by the
+// softmax of tile t-2, so it runs up to two tiles ahead of the softmax and
+// the tensor pipe computes S(t+2) while the softmax works on tile t.
 template <int D>
-__device__ void mma_role(const KernelParams& p, uint32_t sbase, uint32_t tmem, int beg, int end,
-                         const WaitCtl& wc) {
+__device__ void mma_s_role(const KernelParams& p, uint32_t sbase, uint32_t tmem, int beg,
+                           int end, const WaitCtl& wc) {
   using C = Cfg<D>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
-  const uint32_t q0 = sbase + C::kOffQ, q1 = sbase + C::kOffQ + C::kTileBytes;
-  const uint32_t tS0 = tmem + C::kColS0, tS1 = tmem + C::kColS1;
-  const uint32_t tO0 = tmem + C::kColO0, tO1 = tmem + C::kColO1;
-  uint32_t kv_iter = 0, item_iter = 0;
-  uint32_t pr_ph0 = 0, pr_ph1 = 0, of_cnt0 = 0, of_cnt1 = 0;
+  const uint64_t q_desc0 = sdesc(sbase + C::kOffQ, 16, 1024);
+  const uint64_t k_desc0 = sdesc(sbase + C::kOffK, 16, 1024);
+  constexpr uint64_t kTileDesc = (uint64_t)(C::kTileBytes >> 4);
+  uint32_t t = 0, u = 0;
   bool ok = true;
-  for (int it = beg; it < end && ok; ++it, ++item_iter) {
-    const pk_work_item w = p.items[it];
-    const bool two = w.hq1 >= 0;
-    const int n = w.n_kt;
-    if (!(ok = mbar_wait(bar(C::kQFull), item_iter & 1u, wc))) break;
-    {
-      const uint32_t st = kv_iter % C::kKStages, ph = (kv_iter / C::kKStages) & 1u;
-      if (!(ok = mbar_wait(bar(C::kKFull + st), ph, wc))) break;
+  for (UnitIter ui(p.items, beg, end); ui.valid() && ok; ui.next(), ++u) {
+    const uint32_t n = (uint32_t)ui.w.n_kt, qb = u & 1u;
+    if (!(ok = mbar_wait(bar(C::kQFull + qb), (u >> 1) & 1u, wc))) break;
+    for (uint32_t j = 0; j < n; ++j, ++t) {
+      const uint32_t kst = t % C::kKStages, b = t & 1u;
+      if (!(ok = mbar_wait(bar(C::kKFull + kst), (t / C::kKStages) & 1u, wc))) break;
+      if (t >= 2 && !(ok = mbar_wait(bar(C::kSFree + b), ((t >> 1) - 1u) & 1u, wc))) break;
       tc_fence_after();
-      const uint32_t ks = sbase + C::kOffK + st * C::kTileBytes;
-      issue_qk<D>(tS0, q0, ks);
-      tc_commit(bar(C::kSFull + 0));
-      if (two) {
-        issue_qk<D>(tS1, q1, ks);
-        tc_commit(bar(C::kSFull + 1));
-      }
-      tc_commit(bar(C::kKEmpty + st));
-      if (n == 1) tc_commit(bar(C::kQEmpty));  // last use of Q issued
+      issue_qk<D>(tmem + C::kColS0 + b * 128u, q_desc0 + qb * kTileDesc,
+                  k_desc0 + kst * kTileDesc);
+      tc_commit(bar(C::kSFull + b));
+      tc_commit(bar(C::kKEmpty + kst));
+      if (j + 1 == n) tc_commit(bar(C::kQEmpty + qb));  // last use of this Q buffer
     }
-    for (int j = 1; j <= n; ++j) {
-      const uint32_t ip = kv_iter + (uint32_t)j - 1u;
-      const uint32_t stp = ip % C::kVStages, php = (ip / C::kVStages) & 1u;
-      const uint32_t vs = sbase + C::kOffV + stp * C::kTileBytes;
-      uint32_t stj = 0, ks = 0;
-      if (j < n) {
-        const uint32_t ij = kv_iter + (uint32_t)j;
-        stj = ij % C::kKStages;
-        if (!(ok = mbar_wait(bar(C::kKFull + stj), (ij / C::kKStages) & 1u, wc))) break;
-        ks = sbase + C::kOffK + stj * C::kTileBytes;
-      }
-      if (!(ok = mbar_wait(bar(C::kVFull + stp), php, wc))) break;
-      // slot 0
-      if (!(ok = mbar_wait(bar(C::kPReady + 0), pr_ph0, wc))) break;
-      pr_ph0 ^= 1u;
-      if (j == 1 && !(ok = mbar_wait(bar(C::kOFree + 0), (of_cnt0 & 1u) ^ 1u, wc))) break;
-      tc_fence_after();
-      issue_pv<D>(tO0, tS0, vs, j > 1);
-      if (j < n) {
-        issue_qk<D>(tS0, q0, ks);
-        tc_commit(bar(C::kSFull + 0));
-      } else {
-        tc_commit(bar(C::kOFull + 0));
-      }
-      // slot 1
-      if (two) {
-        if (!(ok = mbar_wait(bar(C::kPReady + 1), pr_ph1, wc))) break;
-        pr_ph1 ^= 1u;
-        if (j == 1 && !(ok = mbar_wait(bar(C::kOFree + 1), (of_cnt1 & 1u) ^ 1u, wc))) break;
-        tc_fence_after();
-        issue_pv<D>(tO1, tS1, vs, j > 1);
-        if (j < n) {
-          issue_qk<D>(tS1, q1, ks);
-          tc_commit(bar(C::kSFull + 1));
-        } else {
-          tc_commit(bar(C::kOFull + 1));
-        }
-      }
-      tc_commit(bar(C::kVEmpty + stp));
-      if (j < n) tc_commit(bar(C::kKEmpty + stj));
-      if (j == n - 1) tc_commit(bar(C::kQEmpty));  // last use of Q issued
-    }
-    if (!ok) break;
-    ++of_cnt0;
-    if (two) ++of_cnt1;
-    kv_iter += (uint32_t)n;
   }
-  // Every MMA issued must finish before TMEM is released.
-  tc_commit(bar(C::kMmaDone));
-  mbar_wait_drain(bar(C::kMmaDone), 0, wc);
+  // Every MMA this thread issued must finish before TMEM is released.
+  tc_commit(bar(C::kMmaDone + 0));
+  mbar_wait_drain(bar(C::kMmaDone + 0), 0, wc);
 }
 
+// P V issuer (warp 3): O (+)= P(t) V(t) needs V(t) loaded and P(t) written;
+// a unit's first product overwrites O, after the previous unit's O was read.
 template <int D>
-__device__ void softmax_role(const KernelParams& p, int slot, uint32_t sbase, uint32_t tmem,
-                             int beg, int end, const WaitCtl& wc) {
+__device__ void mma_pv_role(const KernelParams& p, uint32_t sbase, uint32_t tmem, int beg,
+                            int end, const WaitCtl& wc) {
+  using C = Cfg<D>;
+  auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
+  const uint64_t v_desc0 = sdesc(sbase + C::kOffV, kBoxBytes, 1024);
+  constexpr uint64_t kTileDesc = (uint64_t)(C::kTileBytes >> 4);
+  uint32_t t = 0, u = 0;
+  bool ok = true;
+  for (UnitIter ui(p.items, beg, end); ui.valid() && ok; ui.next(), ++u) {
+    const uint32_t n = (uint32_t)ui.w.n_kt;
+    for (uint32_t j = 0; j < n; ++j, ++t) {
+      const uint32_t vst = t % C::kVStages, b = t & 1u;
+      if (!(ok = mbar_wait(bar(C::kVFull + vst), (t / C::kVStages) & 1u, wc))) break;
+      if (!(ok = mbar_wait(bar(C::kPReady + b), (t >> 1) & 1u, wc))) break;
+      if (j == 0 && !(ok = mbar_wait(bar(C::kOFree), (u & 1u) ^ 1u, wc))) break;
+      tc_fence_after();
+      issue_pv<D>(tmem + C::kColO, tmem + C::kColP0 + b * 64u, v_desc0 + vst * kTileDesc, j > 0);
+      tc_commit(bar(C::kPvDone + b));
+      tc_commit(bar(C::kVEmpty + vst));
+    }
+  }
+  tc_commit(bar(C::kMmaDone + 1));
+  mbar_wait_drain(bar(C::kMmaDone + 1), 0, wc);
+}
+
+// Softmax warpgroup (warps 4-7): thread r owns row r of S, P and O in TMEM.
+template <int D>
+__device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint32_t tmem, int beg,
+                             int end, const WaitCtl& wc) {
   using C = Cfg<D>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;  // TMEM lane quadrant this warp may access
   const int r = quad * 32 + lane;
   const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-  const uint32_t tS = tmem + lane_base + (slot ? C::kColS1 : C::kColS0);
-  const uint32_t tO = tmem + lane_base + (slot ? C::kColO1 : C::kColO0);
+  const uint32_t tO = tmem + lane_base + C::kColO;
   const float sl2 = p.scale_log2;
-  uint32_t sf_ph = 0, of_ph = 0;
-  for (int it = beg; it < end; ++it) {
-    const pk_work_item w = p.items[it];
-    if (slot == 1 && w.hq1 < 0) continue;
-    const int h = slot ? w.hq1 : w.hq0;
+  uint32_t g = 0;
+  bool ok = true;
+  for (UnitIter ui(p.items, beg, end); ui.valid() && ok; ui.next()) {
+    const pk_work_item& w = ui.w;
+    const int h = ui.head();
     const bool valid = r < w.q_rows;
     const int lim = p.kv_limit[w.q_start + (valid ? r : w.q_rows - 1)];
     float m_used = -INFINITY, l = 0.f;
-    bool ok = true;
     for (int j = 0; j < w.n_kt; ++j) {
-      ok = mbar_wait(bar(C::kSFull + slot), sf_ph, wc);
-      ok = __all_sync(0xffffffffu, ok);
-      sf_ph ^= 1u;
+      const uint32_t t = g + (uint32_t)j, b = t & 1u;
+      const uint32_t tS = tmem + lane_base + C::kColS0 + b * 128u;
+      const uint32_t tP = tmem + lane_base + C::kColP0 + b * 64u;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kSFull + b), (t >> 1) & 1u, wc));
       if (!ok) break;
       tc_fence_after();
-      // Partial tile: overwrite the scores of keys past this row's limit with
-      // -inf in TMEM, so the passes below carry no mask state.
-      if (j >= w.n_full) {
+      uint32_t sr[128];
+      tmem_ld_x128(tS, sr);
+      // S buffer b may now take S(t+2).
+      tc_fence_before();
+      mbar_arrive(bar(C::kSFree + b));
+      if (j >= w.n_full) {  // partial tile: keys past this row's limit are -inf
         const int nvis = lim - (w.kv_start + j * 128) + 1;
-#pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t cm[32];
-          tmem_ld_x32(tS + (uint32_t)(32 * ch), cm);
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            cm[c] = (32 * ch + c < nvis) ? cm[c] : 0xff800000u;  // -inf
-          tmem_st_x32(tS + (uint32_t)(32 * ch), cm);
-        }
+        for (int c = 0; c < 128; ++c) sr[c] = c < nvis ? sr[c] : 0xff800000u;
       }
-      // Row maximum over the 128 scores from four 32-column TMEM loads,
-      // double buffered; eight independent three-input max chains.
-      uint32_t ca[32], cb[32];
-      float m_new;
-      {
-        float mc[8] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY,
-                       -INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        tmem_ld_x32_async(tS, ca);
-        tmem_wait_ld_x32(ca);
+      float mc[8];
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t(&cur)[32] = (ch & 1) ? cb : ca;
-          uint32_t(&nxt)[32] = (ch & 1) ? ca : cb;
-          if (ch < 3) tmem_ld_x32_async(tS + (uint32_t)(32 * (ch + 1)), nxt);
+      for (int i = 0; i < 8; ++i) mc[i] = fmaxf(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]));
 #pragma unroll
-          for (int b0 = 0; b0 < 32; b0 += 16)
+      for (int b0 = 16; b0 < 128; b0 += 16)
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              mc[i] = max3(mc[i], __uint_as_float(cur[b0 + 2 * i]),
-                           __uint_as_float(cur[b0 + 2 * i + 1]));
-          if (ch < 3) tmem_wait_ld_x32(nxt);
-        }
-        m_new = max3(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7])) * sl2;
-      }
+        for (int i = 0; i < 8; ++i)
+          mc[i] = max3(mc[i], __uint_as_float(sr[b0 + 2 * i]), __uint_as_float(sr[b0 + 2 * i + 1]));
+      const float m_new =
+          max3(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7])) * sl2;
       if (j == 0) {
         m_used = m_new;
       } else {
         const bool need = m_new > m_used + 8.0f;
         if (__any_sync(0xffffffffu, need)) {
+          // O must hold P(t-1) V(t-1) before it is rescaled.
+          const uint32_t tp = t - 1u;
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kPvDone + (tp & 1u)), (tp >> 1) & 1u, wc));
+          if (!ok) break;
+          tc_fence_after();
           const float f = need ? ex2(m_used - m_new) : 1.0f;
           if (need) {
             m_used = m_new;
             l *= f;
           }
-#pragma unroll
+#pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t o[32];
             tmem_ld_x32(tO + (uint32_t)c0, o);
@@ -551,41 +548,35 @@ __device__ void softmax_role(const KernelParams& p, int slot, uint32_t sbase, ui
           }
         }
       }
-      // p = 2^(s*scale*log2e - m), in four 32-column chunks re-read from
-      // TMEM (the next chunk's load overlaps this chunk's exponentials).  P
-      // of chunk c (bf16 pairs) lands in columns [16c, 16c+16) of S, below
-      // every column still to be read.  The row sum l accumulates fp32 p.
+      // p = 2^(s*scale*log2e - m): P to the tensor cores as bf16 pairs, the
+      // row sum l in fp32.
       const float neg = -m_used;
+      uint32_t pp[64];
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      tmem_ld_x32_async(tS, ca);
-      tmem_wait_ld_x32(ca);
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t(&cur)[32] = (ch & 1) ? cb : ca;
-        uint32_t(&nxt)[32] = (ch & 1) ? ca : cb;
-        if (ch < 3) tmem_ld_x32_async(tS + (uint32_t)(32 * (ch + 1)), nxt);
-        uint32_t pp[16];
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float a0, a1;
-          fma2(a0, a1, __uint_as_float(cur[c]), __uint_as_float(cur[c + 1]), sl2, sl2, neg, neg);
-          const float p0 = ex2(a0), p1 = ex2(a1);
-          pp[c >> 1] = pack_bf16x2(p0, p1);
-          const int q = (c >> 1) & 3;
-          acc2(acc[2 * q], acc[2 * q + 1], p0, p1);
-        }
-        tmem_st_x16_async(tS + (uint32_t)(16 * ch), pp);
-        if (ch < 3) tmem_wait_ld_x32(nxt);
+      for (int c = 0; c < 128; c += 2) {
+        float a0, a1;
+        fma2(a0, a1, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]), sl2, sl2, neg, neg);
+        const float p0 = ex2(a0), p1 = ex2(a1);
+        pp[c >> 1] = pack_bf16x2(p0, p1);
+        const int q = (c >> 1) & 3;
+        acc2(acc[2 * q], acc[2 * q + 1], p0, p1);
       }
       l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-      tmem_wait_st();
+      // P buffer b held P(t-2): its product must have been read.
+      if (t >= 2) {
+        const uint32_t tp = t - 2u;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kPvDone + b), (tp >> 1) & 1u, wc));
+        if (!ok) break;
+        tc_fence_after();
+      }
+      tmem_st_x64(tP, pp);
       tc_fence_before();
-      mbar_arrive(bar(C::kPReady + slot));
+      mbar_arrive(bar(C::kPReady + b));
     }
     if (!ok) break;
-    ok = mbar_wait(bar(C::kOFull + slot), of_ph, wc);
-    ok = __all_sync(0xffffffffu, ok);
-    of_ph ^= 1u;
+    const uint32_t tl = g + (uint32_t)w.n_kt - 1u;  // the unit's last product
+    ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kPvDone + (tl & 1u)), (tl >> 1) & 1u, wc));
     if (!ok) break;
     tc_fence_after();
     const float inv_l = 1.0f / l;
@@ -594,22 +585,23 @@ __device__ void softmax_role(const KernelParams& p, int slot, uint32_t sbase, ui
     for (int c0 = 0; c0 < D; c0 += 32) {
       uint32_t o[32];
       tmem_ld_x32(tO + (uint32_t)c0, o);
-      uint32_t b[16];
+      uint32_t bb[16];
 #pragma unroll
       for (int c = 0; c < 16; ++c)
-        b[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv_l, __uint_as_float(o[2 * c + 1]) * inv_l);
+        bb[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv_l, __uint_as_float(o[2 * c + 1]) * inv_l);
       if (valid) {
         uint4* dst = reinterpret_cast<uint4*>(orow + (size_t)c0 * 2);
 #pragma unroll
         for (int v = 0; v < 4; ++v)
-          dst[v] = make_uint4(b[4 * v], b[4 * v + 1], b[4 * v + 2], b[4 * v + 3]);
+          dst[v] = make_uint4(bb[4 * v], bb[4 * v + 1], bb[4 * v + 2], bb[4 * v + 3]);
       }
     }
     tc_fence_before();
-    mbar_arrive(bar(C::kOFree + slot));
+    mbar_arrive(bar(C::kOFree));
     if (valid)
       p.lse[(size_t)h * (size_t)p.T + (size_t)(w.q_start + r)] =
           (m_used + __log2f(l)) * 0.69314718055994530942f;
+    g += (uint32_t)w.n_kt;
   }
 }
 
@@ -629,8 +621,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(C::kQFull), 1);
-    mbar_init(bar(C::kQEmpty), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(C::kQFull + s), 1);
+      mbar_init(bar(C::kQEmpty + s), 1);
+      mbar_init(bar(C::kSFull + s), 1);
+      mbar_init(bar(C::kSFree + s), 128);
+      mbar_init(bar(C::kPReady + s), 128);
+      mbar_init(bar(C::kPvDone + s), 1);
+    }
     for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(bar(C::kKFull + s), 1);
       mbar_init(bar(C::kKEmpty + s), 1);
@@ -639,13 +637,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(C::kVFull + s), 1);
       mbar_init(bar(C::kVEmpty + s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(C::kSFull + s), 1);
-      mbar_init(bar(C::kPReady + s), 128);
-      mbar_init(bar(C::kOFull + s), 1);
-      mbar_init(bar(C::kOFree + s), 128);
-    }
-    mbar_init(bar(C::kMmaDone), 1);
+    mbar_init(bar(C::kOFree), 128);
+    mbar_init(bar(C::kMmaDone + 0), 1);
+    mbar_init(bar(C::kMmaDone + 1), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     tma_prefetch_desc(&tm_q);
@@ -669,14 +663,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) producer_qk_role<D>(p, &tm_q, &tm_k, sbase, beg, end, wc);
     __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) mma_s_role<D>(p, sbase, tmem, beg, end, wc);
+    __syncwarp();
   } else if (warp == 2) {
     if (lane == 0) producer_v_role<D>(p, &tm_v, sbase, beg, end, wc);
     __syncwarp();
-  } else if (warp == 1) {
-    if (lane == 0) mma_role<D>(p, sbase, tmem, beg, end, wc);
+  } else if (warp == 3) {
+    if (lane == 0) mma_pv_role<D>(p, sbase, tmem, beg, end, wc);
     __syncwarp();
-  } else if (warp >= 4) {
-    softmax_role<D>(p, (warp - 4) >> 2, sbase, tmem, beg, end, wc);
+  } else {
+    softmax_role<D>(p, sbase, tmem, beg, end, wc);
   }
 
   tc_fence_before();
