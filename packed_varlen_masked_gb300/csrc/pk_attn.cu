@@ -9,26 +9,28 @@
 // list of 128-row query tiles, each visiting a prefix of 128-key tiles that
 // are either fully visible (no mask math) or partial (per-element compare).
 //
-// Kernel organisation (one persistent CTA per SM, 12 warps):
-//   warp 0      TMA producer of the Q tiles of the two query-head slots and
-//               of a 3-stage ring of K tiles; warp 2: TMA producer of a
-//               2-stage ring of V tiles (128-byte swizzled boxes, one per 64
+// Kernel organisation (one persistent CTA per SM, 8 warps).  The CTA runs
+// its work items' query heads ("units") one after another; a unit is a
+// 128-row query tile streaming the key/value tiles of its sequence.
+//   warp 0      TMA producer of the query tiles (double buffered) and of a
+//               3-stage ring of key tiles; warp 2: TMA producer of a 2-stage
+//               ring of value tiles (128-byte swizzled boxes, one per 64
 //               columns of the head dimension).
 //   warp 1      allocates the 512 TMEM columns; one thread issues every
-//               tcgen05.mma: S = Q K^T (both operands K-major in shared
-//               memory) and O += P V (P read from TMEM, V MN-major in shared
-//               memory), and signals with tcgen05.commit.
-//   warps 4-7   softmax for slot 0, warps 8-11 for slot 1: thread r owns row
-//               r of its slot's S, O and P in TMEM.  Online softmax in base 2
-//               with a lazily moved running maximum, P written back to TMEM
-//               as bf16 over the S columns, epilogue O / l -> bf16 and the
+//               S(t) = Q K(t)^T (both operands K-major in shared memory).
+//   warp 3      one thread issues every O += P(t) V(t) (P read from TMEM, V
+//               MN-major in shared memory).  A tcgen05.mma costs its issuing
+//               thread a large part of the product's own time, and two
+//               issuers in different warps work concurrently.
+//   warps 4-7   softmax: thread r owns row r of S, P and O in TMEM.  Online
+//               softmax in base 2 with a lazily moved running maximum, P
+//               written as bf16 pairs, epilogue O / l -> bf16 and the
 //               natural-log LSE.
-// The two slots are two query heads that share one key/value head, so each
-// K/V tile feeds four 128x128 MMAs and the tensor pipe alternates between the
-// slots while the other slot's softmax runs.
-//
-// TMEM columns: S0 [0,128)  S1 [128,256)  O0 [256,256+D)  O1 [256+D,256+2D);
-// P of slot s is stored as bf16 pairs in the first 64 columns of S_s.
+// TMEM columns: S double buffer [0,256), P double buffer [256,384), O
+// [384,384+D).  Because S(t) and P(t) live in different columns and both are
+// double buffered, the S issuer computes S(t+2) as soon as the softmax has
+// read S(t), and the tensor pipe runs S(t+2) and P(t-1)V(t-1) while the
+// softmax works on tile t.
 //
 // Every mbarrier wait is bounded in time; on expiry the kernel records
 // PK_ERR_TIMEOUT, raises a CTA-local abort flag so the other roles stop, lets
@@ -50,6 +52,9 @@ namespace dev {
 constexpr int kThreads = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 64 bf16
+// Growth of a row's maximum (log2 units) tolerated before O and l are
+// rescaled: exponentials run against a stale maximum while it lags by less.
+constexpr float kRescaleLog2 = 16.0f;
 
 template <int D>
 struct Cfg {
@@ -122,6 +127,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
@@ -513,29 +529,60 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint32_t tme
 #pragma unroll
         for (int c = 0; c < 128; ++c) sr[c] = c < nvis ? sr[c] : 0xff800000u;
       }
-      float mc[8];
+      // P buffer b last held P(t-2); test early whether its product has
+      // been read, so the barrier latency hides under the exponentials.
+      const uint32_t tpp = t - 2u;
+      const bool p_free = t < 2 || mbar_test_wait(bar(C::kPvDone + b), (tpp >> 1) & 1u);
+      // p = 2^(s*scale*log2e - m) as bf16 pairs for the tensor cores, the
+      // row sum l in fp32.  After a unit's first tile, the exponentials use
+      // the running maximum m_used and track this tile's maximum on the fly;
+      // only when the tile maximum passes m_used + kRescaleLog2 (p above
+      // 2^16) does the row take the new maximum, rescale O and l, and
+      // recompute the tile from the scores still in registers.  P (bf16), O
+      // and l (fp32) keep their relative precision at any scale, so the
+      // only limit on the threshold is range: O <= L * 2^16 * max|v|.
+      uint32_t pp[64];
+      float acc[8];
+      auto exp_pass = [&](float neg, bool track) -> float {
+        float mc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mc[i] = fmaxf(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]));
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
 #pragma unroll
-      for (int b0 = 16; b0 < 128; b0 += 16)
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          mc[i] = max3(mc[i], __uint_as_float(sr[b0 + 2 * i]), __uint_as_float(sr[b0 + 2 * i + 1]));
-      const float m_new =
-          max3(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7])) * sl2;
+        for (int c = 0; c < 128; c += 2) {
+          const float x0 = __uint_as_float(sr[c]), x1 = __uint_as_float(sr[c + 1]);
+          if (track) mc[(c >> 1) & 3] = max3(mc[(c >> 1) & 3], x0, x1);
+          float a0, a1;
+          fma2(a0, a1, x0, x1, sl2, sl2, neg, neg);
+          const float p0 = ex2(a0), p1 = ex2(a1);
+          pp[c >> 1] = pack_bf16x2(p0, p1);
+          const int q = (c >> 1) & 3;
+          acc2(acc[2 * q], acc[2 * q + 1], p0, p1);
+        }
+        return fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3])) * sl2;
+      };
       if (j == 0) {
-        m_used = m_new;
+        float mc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mc[i] = fmaxf(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]));
+#pragma unroll
+        for (int b0 = 16; b0 < 128; b0 += 16)
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            mc[i] = max3(mc[i], __uint_as_float(sr[b0 + 2 * i]), __uint_as_float(sr[b0 + 2 * i + 1]));
+        m_used = max3(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7])) * sl2;
+        exp_pass(-m_used, false);
       } else {
-        const bool need = m_new > m_used + 8.0f;
+        const float m_tile = exp_pass(-m_used, true);
+        const bool need = m_tile > m_used + kRescaleLog2;
         if (__any_sync(0xffffffffu, need)) {
           // O must hold P(t-1) V(t-1) before it is rescaled.
           const uint32_t tp = t - 1u;
           ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kPvDone + (tp & 1u)), (tp >> 1) & 1u, wc));
           if (!ok) break;
           tc_fence_after();
-          const float f = need ? ex2(m_used - m_new) : 1.0f;
+          const float f = need ? ex2(m_used - m_tile) : 1.0f;
           if (need) {
-            m_used = m_new;
+            m_used = m_tile;
             l *= f;
           }
 #pragma unroll 1
@@ -546,30 +593,15 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint32_t tme
             for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * f);
             tmem_st_x32(tO + (uint32_t)c0, o);
           }
+          exp_pass(-m_used, false);
         }
       }
-      // p = 2^(s*scale*log2e - m): P to the tensor cores as bf16 pairs, the
-      // row sum l in fp32.
-      const float neg = -m_used;
-      uint32_t pp[64];
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int c = 0; c < 128; c += 2) {
-        float a0, a1;
-        fma2(a0, a1, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]), sl2, sl2, neg, neg);
-        const float p0 = ex2(a0), p1 = ex2(a1);
-        pp[c >> 1] = pack_bf16x2(p0, p1);
-        const int q = (c >> 1) & 3;
-        acc2(acc[2 * q], acc[2 * q + 1], p0, p1);
-      }
       l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-      // P buffer b held P(t-2): its product must have been read.
-      if (t >= 2) {
-        const uint32_t tp = t - 2u;
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kPvDone + b), (tp >> 1) & 1u, wc));
+      if (!__all_sync(0xffffffffu, p_free)) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kPvDone + b), (tpp >> 1) & 1u, wc));
         if (!ok) break;
-        tc_fence_after();
       }
+      tc_fence_after();
       tmem_st_x64(tP, pp);
       tc_fence_before();
       mbar_arrive(bar(C::kPReady + b));

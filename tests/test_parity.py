@@ -5,7 +5,13 @@ Tolerance: |out_gpu - out_oracle| <= 1e-2 + half a bf16 ulp of out_oracle
 on every bf16 output element (the 1e-2 bounds the kernel's arithmetic; the
 half ulp is the rounding of the output to bf16 itself, 0.0078 for |o| in
 [2, 4) and 0.0156 for |o| in [4, 8), which no bf16 result can avoid), and
-|lse_gpu - lse_oracle| <= 1e-3 on the fp32 natural-log LSE."""
+|lse_gpu - lse_oracle| <= 1e-3 on the fp32 natural-log LSE.
+
+Inputs sharper than any stated workload (q scaled beyond x4) are held to the
+bound the arithmetic itself gives instead of 1e-2: P enters the P V product
+as bf16, so each softmax weight carries a relative error of up to 2^-9, and
+|o_gpu - o| <= 2^-9 * max|v| before the output rounding; the test allows
+2^-8 * max|v| for the exp2 approximation and fp32 accumulation on top."""
 import math
 
 import numpy as np
@@ -35,7 +41,15 @@ def _half_ulp_bf16(x):
     return 0.5 * np.exp2(np.floor(np.log2(a)) - 7)
 
 
-def _compare(pack, out_g, lse_g, out_o, lse_o, rows=None):
+def _arith_tol(pack, v):
+    """1e-2 for the stated workloads; for sharper inputs the bf16-P bound."""
+    if pack.q_mult <= 4.0:
+        return OUT_TOL
+    vmax = float(v.float().abs().max()) if v is not None else 0.0
+    return max(OUT_TOL, 2.0 ** -8 * vmax)
+
+
+def _compare(pack, out_g, lse_g, out_o, lse_o, rows=None, v=None):
     if rows is not None:
         out_g, lse_g = out_g[rows], lse_g[:, rows]
     assert np.isfinite(out_g).all() and np.isfinite(lse_g).all()
@@ -47,7 +61,7 @@ def _compare(pack, out_g, lse_g, out_o, lse_o, rows=None):
     excess = float((err - _half_ulp_bf16(out_o)).max())
     print(f"{pack.name}: max|dout|={e_out:.3e} max(|dout|-ulp/2)={excess:.3e} "
           f"max|dlse|={e_lse:.3e} max|o|={np.abs(out_o).max():.3f}")
-    assert (err <= OUT_TOL + _half_ulp_bf16(out_o)).all(), (e_out, excess)
+    assert (err <= _arith_tol(pack, v) + _half_ulp_bf16(out_o)).all(), (e_out, excess)
     assert e_lse <= LSE_TOL, e_lse
 
 
@@ -57,7 +71,7 @@ def _full(pack, q=None, k=None, v=None):
     out_o, lse_o = oracle.attention(q, k, v, pack.cu_seqlens, pack.segments, pack.hq,
                                     pack.hkv, pack.d, pack.scale)
     out_g, lse_g = _gpu(pack, q, k, v)
-    _compare(pack, out_g, lse_g, out_o, lse_o)
+    _compare(pack, out_g, lse_g, out_o, lse_o, v=v)
 
 
 def _small_packs():
