@@ -535,32 +535,29 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint32_t tme
       const bool p_free = t < 2 || mbar_test_wait(bar(C::kPvDone + b), (tpp >> 1) & 1u);
       // p = 2^(s*scale*log2e - m) as bf16 pairs for the tensor cores, the
       // row sum l in fp32.  After a unit's first tile, the exponentials use
-      // the running maximum m_used and track this tile's maximum on the fly;
-      // only when the tile maximum passes m_used + kRescaleLog2 (p above
-      // 2^16) does the row take the new maximum, rescale O and l, and
-      // recompute the tile from the scores still in registers.  P (bf16), O
-      // and l (fp32) keep their relative precision at any scale, so the
-      // only limit on the threshold is range: O <= L * 2^16 * max|v|.
+      // the running maximum m_used as it stands.  Every p is non-negative, so
+      // none can pass 2^kRescaleLog2 unless the tile's sum does: only then is
+      // the tile maximum computed, and if it passes m_used + kRescaleLog2
+      // the row takes it, rescales O and l, and recomputes the tile from the
+      // scores still in registers.  P (bf16), O and l (fp32) keep their
+      // relative precision at any scale, so the only limit on the threshold
+      // is range: O <= L * 2^16 * max|v|.
       uint32_t pp[64];
       float acc[8];
-      auto exp_pass = [&](float neg, bool track) -> float {
-        float mc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      auto exp_pass = [&](float neg) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0.f;
 #pragma unroll
         for (int c = 0; c < 128; c += 2) {
-          const float x0 = __uint_as_float(sr[c]), x1 = __uint_as_float(sr[c + 1]);
-          if (track) mc[(c >> 1) & 3] = max3(mc[(c >> 1) & 3], x0, x1);
           float a0, a1;
-          fma2(a0, a1, x0, x1, sl2, sl2, neg, neg);
+          fma2(a0, a1, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]), sl2, sl2, neg, neg);
           const float p0 = ex2(a0), p1 = ex2(a1);
           pp[c >> 1] = pack_bf16x2(p0, p1);
           const int q = (c >> 1) & 3;
           acc2(acc[2 * q], acc[2 * q + 1], p0, p1);
         }
-        return fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3])) * sl2;
       };
-      if (j == 0) {
+      auto row_max = [&]() {
         float mc[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) mc[i] = fmaxf(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]));
@@ -569,13 +566,19 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint32_t tme
 #pragma unroll
           for (int i = 0; i < 8; ++i)
             mc[i] = max3(mc[i], __uint_as_float(sr[b0 + 2 * i]), __uint_as_float(sr[b0 + 2 * i + 1]));
-        m_used = max3(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7])) * sl2;
-        exp_pass(-m_used, false);
-      } else {
-        const float m_tile = exp_pass(-m_used, true);
+        return max3(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7])) * sl2;
+      };
+      constexpr float kRescaleSum = 65536.0f;  // 2^kRescaleLog2
+      if (j == 0) m_used = row_max();
+      exp_pass(-m_used);
+      const float tile_sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+      if (__any_sync(0xffffffffu, !(tile_sum <= kRescaleSum))) {
+        // Rare: some row's maximum may have outgrown m_used.
+        const float m_tile = row_max();
         const bool need = m_tile > m_used + kRescaleLog2;
         if (__any_sync(0xffffffffu, need)) {
-          // O must hold P(t-1) V(t-1) before it is rescaled.
+          // O must hold P(t-1) V(t-1) before it is rescaled (j > 0 here: the
+          // first tile's maximum is exact).
           const uint32_t tp = t - 1u;
           ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kPvDone + (tp & 1u)), (tp >> 1) & 1u, wc));
           if (!ok) break;
@@ -593,7 +596,7 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint32_t tme
             for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * f);
             tmem_st_x32(tO + (uint32_t)c0, o);
           }
-          exp_pass(-m_used, false);
+          exp_pass(-m_used);
         }
       }
       l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
