@@ -506,6 +506,7 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint32_t tme
   const float sl2 = p.scale_log2;
   uint32_t g = 0;
   bool ok = true;
+  bool s_ready = false;  // S(t) of the next tile already seen complete
   for (UnitIter ui(p.items, beg, end); ui.valid() && ok; ui.next()) {
     const pk_work_item& w = ui.w;
     const int h = ui.head();
@@ -516,8 +517,10 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint32_t tme
       const uint32_t t = g + (uint32_t)j, b = t & 1u;
       const uint32_t tS = tmem + lane_base + C::kColS0 + b * 128u;
       const uint32_t tP = tmem + lane_base + C::kColP0 + b * 64u;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kSFull + b), (t >> 1) & 1u, wc));
-      if (!ok) break;
+      if (!s_ready) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kSFull + b), (t >> 1) & 1u, wc));
+        if (!ok) break;
+      }
       tc_fence_after();
       uint32_t sr[128];
       tmem_ld_x128(tS, sr);
@@ -533,6 +536,9 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint32_t tme
       // been read, so the barrier latency hides under the exponentials.
       const uint32_t tpp = t - 2u;
       const bool p_free = t < 2 || mbar_test_wait(bar(C::kPvDone + b), (tpp >> 1) & 1u);
+      // Likewise whether S(t+1) has landed (S(t+3) cannot complete before
+      // this softmax frees S(t+1)'s buffer, so a yes stays valid).
+      const bool s_next = mbar_test_wait(bar(C::kSFull + (b ^ 1u)), ((t + 1u) >> 1) & 1u);
       // p = 2^(s*scale*log2e - m) as bf16 pairs for the tensor cores, the
       // row sum l in fp32.  After a unit's first tile, the exponentials use
       // the running maximum m_used as it stands.  Every p is non-negative, so
@@ -572,7 +578,12 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint32_t tme
       if (j == 0) m_used = row_max();
       exp_pass(-m_used);
       const float tile_sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-      if (__any_sync(0xffffffffu, !(tile_sum <= kRescaleSum))) {
+      // One warp vote for: a possible rescale (bit 0), P buffer still busy
+      // (bit 1), next S not yet seen (bit 2).
+      const unsigned votes = __reduce_or_sync(
+          0xffffffffu, (!(tile_sum <= kRescaleSum) ? 1u : 0u) | (p_free ? 0u : 2u) | (s_next ? 0u : 4u));
+      s_ready = (votes & 4u) == 0u;
+      if (votes & 1u) {
         // Rare: some row's maximum may have outgrown m_used.
         const float m_tile = row_max();
         const bool need = m_tile > m_used + kRescaleLog2;
@@ -600,7 +611,7 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint32_t tme
         }
       }
       l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-      if (!__all_sync(0xffffffffu, p_free)) {
+      if (votes & 2u) {
         ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kPvDone + b), (tpp >> 1) & 1u, wc));
         if (!ok) break;
       }
