@@ -218,6 +218,72 @@ def cpu_baseline(pack, seconds: float = 12.0):
             "sample": f"{n_rows} uniformly drawn query rows x {pack.hq} heads of the workload"}
 
 
+def replaced_path(torch, pack, q, k, v, ours_out, steps=3):
+    """Time the path the pages replace: every sequence padded to the longest
+    one, an explicit (bsz, 1, L, L) bool mask, torch SDPA.  Measurement
+    only: its output is compared with ours on valid rows, never used."""
+    import torch.nn.functional as F
+    cu = pack.cu_seqlens
+    S, L = len(pack.seqs), pack.max_seqlen
+    dev = q.device
+    group = pack.hq // pack.hkv
+    qp = torch.zeros(S, pack.hq, L, pack.d, dtype=q.dtype, device=dev)
+    kp = torch.zeros(S, pack.hq, L, pack.d, dtype=q.dtype, device=dev)  # KV heads repeated
+    vp = torch.zeros_like(kp)
+    mask = torch.zeros(S, 1, L, L, dtype=torch.bool, device=dev)
+    for s_idx, seq in enumerate(pack.seqs):
+        b, e = int(cu[s_idx]), int(cu[s_idx + 1])
+        n = e - b
+        qp[s_idx, :, :n] = q[b:e].transpose(0, 1)
+        kp[s_idx, :, :n] = k[b:e].repeat_interleave(group, dim=1).transpose(0, 1)
+        vp[s_idx, :, :n] = v[b:e].repeat_interleave(group, dim=1).transpose(0, 1)
+        # the model's mask: causal, plus each image segment sees itself
+        pos = torch.arange(L, device=dev)
+        m = pos[None, :] <= pos[:, None]
+        start = 0
+        for typ, ln in seq:
+            if typ == W.IMAGE:
+                m[start:start + ln, start:start + ln] = True
+            start += ln
+        m[n:, :] = False
+        m[:, n:] = False
+        m[torch.arange(n, L, device=dev), torch.arange(n, L, device=dev)] = True  # padded rows: no NaN
+        mask[s_idx, 0] = m
+    from torch.nn.attention import SDPBackend, sdpa_kernel
+
+    def run():
+        # the memory-efficient kernel takes an arbitrary mask; never the
+        # math fallback, which would materialise every score
+        with sdpa_kernel([SDPBackend.EFFICIENT_ATTENTION]):
+            return F.scaled_dot_product_attention(qp, kp, vp, attn_mask=mask, scale=pack.scale)
+    try:
+        o = run()
+    except RuntimeError as exc:
+        del qp, kp, vp, mask
+        torch.cuda.empty_cache()
+        return {"impl": "torch SDPA (memory-efficient backend), padded", "unavailable": str(exc)[:200]}
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        o = run()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    # agreement with our output on the valid rows
+    err = 0.0
+    for s_idx in range(S):
+        b, e = int(cu[s_idx]), int(cu[s_idx + 1])
+        err = max(err, float((o[s_idx, :, :e - b].transpose(0, 1).float() - ours_out[b:e].float())
+                             .abs().max()))
+    res = {"impl": "torch SDPA, padded to the longest sequence, explicit (bsz,1,L,L) bool mask",
+           "ms": round(ms, 3), "max_abs_diff_vs_ours": round(err, 5),
+           "mask_bytes": int(mask.numel()), "padded_tokens": int(S * L)}
+    del qp, kp, vp, mask, o
+    torch.cuda.empty_cache()
+    return res
+
+
 def sweep(pk, torch, stream, dev):
     """Timing-only pass over every workload (device-generated inputs)."""
     res = {}
@@ -260,6 +326,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-replaced", action="store_true",
+                    help="skip timing the replaced padded + explicit-mask SDPA path")
     ap.add_argument("--requests", type=int, default=8,
                     help="requests in the mixed-resolution pack (x2 CFG branches)")
     args = ap.parse_args()
@@ -365,6 +433,12 @@ def main():
     per_workload = None
     if not args.no_sweep and rank == 0:
         per_workload = sweep(pk, torch, stream, dev)
+    replaced = None
+    if not args.no_replaced and rank == 0:
+        pk.attn_fwd(q, k, v, plan, pack.scale, out=out, lse=lse)
+        torch.cuda.synchronize()
+        replaced = replaced_path(torch, pack, q, k, v, out)
+        replaced["speedup_of_packed"] = round(replaced["ms"] / ms_step, 2)
 
     if rank != 0:
         if dist is not None:
@@ -406,6 +480,7 @@ def main():
         "plan": {k2: info[k2] for k2 in ("num_items", "num_ctas", "num_full_tiles",
                                           "num_partial_tiles")},
         "per_workload": per_workload,
+        "replaced_path": replaced,
     }
     print(json.dumps(line), flush=True)
     if dist is not None:

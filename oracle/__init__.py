@@ -179,3 +179,71 @@ def attention(q, k, v, cu_seqlens, segments, hq: int, hkv: int, d: int,
 
 def max_threads() -> int:
     return int(_load().pko_max_threads())
+
+
+def _load_general():
+    lib = _load()
+    if not hasattr(lib, "_general_ready"):
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        u16p = ctypes.POINTER(ctypes.c_uint16)
+        f64p = ctypes.POINTER(ctypes.c_double)
+        lib.pko_attention_general.argtypes = [
+            u16p, u16p, u16p, i32p, i32p, i32p, i32p, ctypes.c_int32, i32p, i32p, i32p, i32p,
+            ctypes.c_int32, i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+            ctypes.c_int32, ctypes.c_int32, ctypes.c_double, f64p, f64p, ctypes.c_int32]
+        lib.pko_attention_general.restype = ctypes.c_int
+        lib.pko_lse_merge.argtypes = [f64p, f64p, ctypes.c_int32, ctypes.c_int32,
+                                      ctypes.c_int32, ctypes.c_int32, f64p, f64p]
+        lib.pko_lse_merge.restype = None
+        lib._general_ready = True
+    return lib
+
+
+def attention_general(q, k, v, cu_seqlens_q, cu_seqlens_k, q_pos0, k_pos0, seq_segments,
+                      hq: int, hkv: int, d: int, scale: float, block_table=None,
+                      block: int = 128, nthreads: int = 0):
+    """fp64 attention of queries over keys that are position ranges of their
+    sequences (see pk_oracle.c).  ``seq_segments``: (seq, start, len, type)
+    rows in sequence-position space.  ``block_table`` [S, blocks_per_seq]
+    places key position p of sequence s at pool row table[s, p // block] *
+    block + p % block.  Returns (out [Tq, hq, d], lse [hq, Tq]); rows that
+    see no key get out 0 and lse -inf."""
+    lib = _load_general()
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    cq, ck = _i32(cu_seqlens_q), _i32(cu_seqlens_k)
+    qp, kp = _i32(q_pos0), _i32(k_pos0)
+    sg = _i32(seq_segments).reshape(-1, 4)
+    cols = [np.ascontiguousarray(sg[:, i]) for i in range(4)]
+    S = len(cq) - 1
+    Tq = int(cq[-1])
+    if block_table is None:
+        bt, bps, bp = None, 0, None
+    else:
+        bt = _i32(block_table).reshape(S, -1)
+        bps = bt.shape[1]
+        bp = _ptr(np.ascontiguousarray(bt), ctypes.c_int32)
+    out = np.zeros((Tq, hq, d), dtype=np.float64)
+    lse = np.zeros((hq, Tq), dtype=np.float64)
+    rc = lib.pko_attention_general(
+        _ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16), _ptr(vb, ctypes.c_uint16),
+        _ptr(cq, ctypes.c_int32), _ptr(ck, ctypes.c_int32), _ptr(qp, ctypes.c_int32),
+        _ptr(kp, ctypes.c_int32), S, *[_ptr(c, ctypes.c_int32) for c in cols], sg.shape[0],
+        bp, bps, block, hq, hkv, d, float(scale), _ptr(out, ctypes.c_double),
+        _ptr(lse, ctypes.c_double), int(nthreads))
+    if rc:
+        raise ValueError(f"oracle: invalid arguments (code {rc})")
+    return out, lse
+
+
+def lse_merge(o_parts, lse_parts):
+    """Merge partial attentions over disjoint key sets: o_parts [C, T, H, d],
+    lse_parts [C, H, T] (fp64) -> (out [T, H, d], lse [H, T])."""
+    lib = _load_general()
+    o = np.ascontiguousarray(np.asarray(o_parts, dtype=np.float64))
+    l = np.ascontiguousarray(np.asarray(lse_parts, dtype=np.float64))
+    C, T, H, d = o.shape
+    out = np.zeros((T, H, d), dtype=np.float64)
+    lse = np.zeros((H, T), dtype=np.float64)
+    lib.pko_lse_merge(_ptr(o, ctypes.c_double), _ptr(l, ctypes.c_double), C, T, H, d,
+                      _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double))
+    return out, lse

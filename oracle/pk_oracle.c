@@ -264,3 +264,166 @@ int32_t pko_max_threads(void) {
   return 1;
 #endif
 }
+
+/*
+ * General form, for queries and keys that are position ranges of their
+ * sequences (the cached-prefix hand-over of "[RFC]: HunyuanImage 3.0
+ * deployment", Proposed Change, P0 "KV Cache Transfer Integration for DiT":
+ * image queries attend to a text prefix whose keys/values come from the AR
+ * stage; and key chunks of one sequence, as a ring of devices holds them).
+ *
+ *   seg_seq/seg_start/seg_len/seg_type [G]: segments of every sequence in its
+ *       own position space, ordered, tiling [0, L_s) of each sequence.
+ *   cu_q [S+1]: packed query rows; query i of sequence s has position
+ *       q_pos0[s] + i.
+ *   cu_k [S+1]: key rows per sequence; key j of sequence s has position
+ *       k_pos0[s] + j and lives at packed row cu_k[s] + j, or, when
+ *       block_table is given, at pool row
+ *       block_table[s*blocks_per_seq + p/block] * block + p % block with
+ *       p = k_pos0[s] + j.
+ *   Query position pq sees key position pk iff the dense mask of the whole
+ *   sequence has (pq, pk) set.  A query that sees no key of the range gets
+ *   out = 0 and lse = -inf.
+ * q: [Tq][Hq][d], k/v: [rows][Hkv][d] bf16 bits; out [Tq][Hq][d], lse [Hq][Tq].
+ */
+int pko_attention_general(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                          const int32_t* cu_q, const int32_t* cu_k, const int32_t* q_pos0,
+                          const int32_t* k_pos0, int32_t num_seqs, const int32_t* seg_seq,
+                          const int32_t* seg_start, const int32_t* seg_len,
+                          const int32_t* seg_type, int32_t num_segs,
+                          const int32_t* block_table, int32_t blocks_per_seq, int32_t block,
+                          int32_t Hq, int32_t Hkv, int32_t d, double scale, double* out,
+                          double* lse, int32_t nthreads) {
+  if (num_seqs < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || d <= 0) return 10;
+  if (cu_q[0] != 0 || cu_k[0] != 0) return 2;
+  int32_t* L = (int32_t*)calloc((size_t)(num_seqs > 0 ? num_seqs : 1), sizeof(int32_t));
+  int32_t* first_seg = (int32_t*)malloc(sizeof(int32_t) * (size_t)(num_seqs + 1));
+  for (int32_t s = 0; s <= num_seqs; ++s) first_seg[s] = num_segs;
+  for (int32_t g = 0; g < num_segs; ++g) {
+    int32_t s = seg_seq[g];
+    if (s < 0 || s >= num_seqs || seg_len[g] <= 0 || seg_start[g] != L[s] ||
+        (seg_type[g] != PKO_TEXT && seg_type[g] != PKO_IMAGE) ||
+        (g > 0 && seg_seq[g - 1] > s)) {
+      free(L); free(first_seg); return 5;
+    }
+    if (first_seg[s] == num_segs) first_seg[s] = g;
+    L[s] += seg_len[g];
+  }
+  for (int32_t s = 0; s < num_seqs; ++s) {
+    int32_t nq = cu_q[s + 1] - cu_q[s], nk = cu_k[s + 1] - cu_k[s];
+    if (nq < 0 || nk < 0 || q_pos0[s] < 0 || k_pos0[s] < 0 || q_pos0[s] + nq > L[s] ||
+        k_pos0[s] + nk > L[s]) {
+      free(L); free(first_seg); return 3;
+    }
+  }
+  const int32_t Tq = cu_q[num_seqs];
+  const int32_t group = Hq / Hkv;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#endif
+  for (int32_t s = 0; s < num_seqs; ++s) {
+    const int32_t Ls = L[s], nq = cu_q[s + 1] - cu_q[s], nk = cu_k[s + 1] - cu_k[s];
+    if (nq == 0) continue;
+    /* segment index of every position, then the dense mask rows of the queries */
+    int32_t* seg_of = (int32_t*)malloc(sizeof(int32_t) * (size_t)(Ls > 0 ? Ls : 1));
+    for (int32_t g = first_seg[s]; g < num_segs && seg_seq[g] == s; ++g)
+      for (int32_t p = seg_start[g]; p < seg_start[g] + seg_len[g]; ++p) seg_of[p] = g;
+#pragma omp parallel
+    {
+      uint8_t* mrow = (uint8_t*)malloc((size_t)(Ls > 0 ? Ls : 1));
+      double* sbuf = (double*)malloc(sizeof(double) * (size_t)(nk > 0 ? nk : 1));
+      double* qd = (double*)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 4)
+      for (int32_t i = 0; i < nq; ++i) {
+        const int32_t pq = q_pos0[s] + i, t = cu_q[s] + i;
+        const int32_t gi = seg_of[pq];
+        const int is_image = seg_type[gi] == PKO_IMAGE;
+        for (int32_t pk = 0; pk < Ls; ++pk)
+          mrow[pk] = (uint8_t)(pk <= pq || (is_image && seg_of[pk] == gi));
+        for (int32_t h = 0; h < Hq; ++h) {
+          const int32_t g = h / group;
+          for (int32_t c = 0; c < d; ++c) qd[c] = pko_bf16_to_double(q[((size_t)t * Hq + h) * d + c]);
+          double m = -INFINITY;
+          for (int32_t j = 0; j < nk; ++j) {
+            const int32_t pk = k_pos0[s] + j;
+            if (!mrow[pk]) continue;
+            size_t row = block_table
+                ? (size_t)block_table[(size_t)s * blocks_per_seq + pk / block] * block + pk % block
+                : (size_t)(cu_k[s] + j);
+            const uint16_t* kj = k + (row * Hkv + g) * d;
+            double acc = 0.0;
+            for (int32_t c = 0; c < d; ++c) acc += qd[c] * pko_bf16_to_double(kj[c]);
+            sbuf[j] = scale * acc;
+            if (sbuf[j] > m) m = sbuf[j];
+          }
+          double* o = out + ((size_t)t * Hq + h) * d;
+          for (int32_t c = 0; c < d; ++c) o[c] = 0.0;
+          if (m == -INFINITY) {
+            lse[(size_t)h * Tq + t] = -INFINITY;
+            continue;
+          }
+          double den = 0.0;
+          for (int32_t j = 0; j < nk; ++j)
+            if (mrow[k_pos0[s] + j]) den += exp(sbuf[j] - m);
+          const double l = m + log(den);
+          lse[(size_t)h * Tq + t] = l;
+          for (int32_t j = 0; j < nk; ++j) {
+            const int32_t pk = k_pos0[s] + j;
+            if (!mrow[pk]) continue;
+            size_t row = block_table
+                ? (size_t)block_table[(size_t)s * blocks_per_seq + pk / block] * block + pk % block
+                : (size_t)(cu_k[s] + j);
+            const uint16_t* vj = v + (row * Hkv + g) * d;
+            const double pw = exp(sbuf[j] - l);
+            for (int32_t c = 0; c < d; ++c) o[c] += pw * pko_bf16_to_double(vj[c]);
+          }
+        }
+      }
+      free(mrow);
+      free(sbuf);
+      free(qd);
+    }
+    free(seg_of);
+  }
+  free(L);
+  free(first_seg);
+  return 0;
+}
+
+/*
+ * Merge of partial attentions over disjoint key sets of the same queries
+ * (the combination a ring of devices performs, "Parallelism Acceleration
+ * Guide", Ring Attention): with per-part log-sum-exps lse_c and normalised
+ * outputs o_c,
+ *     lse = ln sum_c exp(lse_c),   o = sum_c exp(lse_c - lse) o_c.
+ * Parts with lse_c = -inf contribute nothing; if every part is -inf the
+ * result is o = 0, lse = -inf.  o_parts [C][T][H][d], lse_parts [C][H][T]
+ * (fp64); out [T][H][d], lse [H][T].
+ */
+void pko_lse_merge(const double* o_parts, const double* lse_parts, int32_t C, int32_t T,
+                   int32_t H, int32_t d, double* out, double* lse) {
+  for (int32_t t = 0; t < T; ++t)
+    for (int32_t h = 0; h < H; ++h) {
+      double m = -INFINITY;
+      for (int32_t c = 0; c < C; ++c) {
+        const double lc = lse_parts[((size_t)c * H + h) * T + t];
+        if (lc > m) m = lc;
+      }
+      double* o = out + ((size_t)t * H + h) * d;
+      for (int32_t x = 0; x < d; ++x) o[x] = 0.0;
+      if (m == -INFINITY) {
+        lse[(size_t)h * T + t] = -INFINITY;
+        continue;
+      }
+      double den = 0.0;
+      for (int32_t c = 0; c < C; ++c) den += exp(lse_parts[((size_t)c * H + h) * T + t] - m);
+      const double L = m + log(den);
+      lse[(size_t)h * T + t] = L;
+      for (int32_t c = 0; c < C; ++c) {
+        const double w = exp(lse_parts[((size_t)c * H + h) * T + t] - L);
+        if (w == 0.0) continue;
+        const double* oc = o_parts + (((size_t)c * T + t) * H + h) * d;
+        for (int32_t x = 0; x < d; ++x) o[x] += w * oc[x];
+      }
+    }
+}

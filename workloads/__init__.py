@@ -202,3 +202,60 @@ def sample_rows(pack: Pack, budget: int, seed: int = 1, tile: int = 128) -> np.n
     rand = rng.integers(0, T, size=n_rand).tolist() if T > 0 else []
     rows = np.unique(np.asarray(structural + rand, dtype=np.int32))
     return rows[:budget]
+
+
+def seq_segments(pack: Pack) -> np.ndarray:
+    """[G, 4] int32 (seq, start, len, type): segments in each sequence's own
+    position space."""
+    out = []
+    for s, seq in enumerate(pack.seqs):
+        pos = 0
+        for typ, n in seq:
+            out.append((s, pos, n, typ))
+            pos += n
+    return np.asarray(out, dtype=np.int32).reshape(-1, 4)
+
+
+def prefix_split(pack: Pack):
+    """Cached-prefix layout of a pack: per sequence the queries are the tokens
+    from its first image segment on (the tokens being generated), the keys
+    are the whole sequence (text prefix handed over + image).  Returns
+    (q_rows: global token indices of the queries, cu_seqlens_q, q_pos0)."""
+    cu = pack.cu_seqlens
+    rows, cu_q, q_pos0 = [], [0], []
+    for s, seq in enumerate(pack.seqs):
+        first_img = 0
+        for typ, n in seq:
+            if typ == IMAGE:
+                break
+            first_img += n
+        L = int(cu[s + 1] - cu[s])
+        first_img = min(first_img, L)
+        rows.extend(range(int(cu[s]) + first_img, int(cu[s + 1])))
+        cu_q.append(cu_q[-1] + L - first_img)
+        q_pos0.append(first_img)
+    return np.asarray(rows, dtype=np.int64), np.asarray(cu_q, np.int32), np.asarray(q_pos0, np.int32)
+
+
+def paged_layout(pack: Pack, rng: np.random.Generator, block: int = 128, spare: int = 3):
+    """A shuffled block pool holding every sequence's keys: returns
+    (block_table [S, blocks_per_seq] int32, pool_rows: for every pool row the
+    global token it holds, or -1)."""
+    cu = pack.cu_seqlens
+    S = len(cu) - 1
+    nblocks = [(int(cu[s + 1] - cu[s]) + block - 1) // block for s in range(S)]
+    bps = max(nblocks) if nblocks else 0
+    total = sum(nblocks) + spare
+    perm = rng.permutation(total)
+    table = np.zeros((S, max(bps, 1)), dtype=np.int32)
+    pool_rows = -np.ones(total * block, dtype=np.int64)
+    k = 0
+    for s in range(S):
+        for b in range(nblocks[s]):
+            pb = int(perm[k]); k += 1
+            table[s, b] = pb
+            for r in range(block):
+                t = int(cu[s]) + b * block + r
+                if t < int(cu[s + 1]):
+                    pool_rows[pb * block + r] = t
+    return table, pool_rows
