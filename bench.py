@@ -150,14 +150,9 @@ def reference_arm(args, pack, rank, world):
         return
     import oracle
     import torch
-    import packed_varlen_masked_gb300 as pk  # planner only (host): FLOP count per row
     q, k, v = W.make_qkv(pack)
-    plan = pk.Plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d, num_ctas=1,
-                   upload=False)
-    lim = plan.kv_limit()
     cu = pack.cu_seqlens
-    seq_start = np.repeat(cu[:-1], np.diff(cu))
-    keys = (lim - seq_start + 1).astype(np.float64)
+    keys = oracle.row_keys(cu, pack.segments).astype(np.float64)  # FLOP count per row
     rng = np.random.default_rng(0)
     # calibrate: rows per ~2 s step
     probe = rng.integers(0, pack.total_tokens, size=32).astype(np.int32)
@@ -195,13 +190,9 @@ def reference_arm(args, pack, rank, world):
 def cpu_baseline(pack, seconds: float = 12.0):
     """The oracle as it stands, on a bounded sample of the same workload."""
     import oracle
-    import packed_varlen_masked_gb300 as pk
     q, k, v = W.make_qkv(pack)
-    plan = pk.Plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d, num_ctas=1,
-                   upload=False)
-    lim = plan.kv_limit()
     cu = pack.cu_seqlens
-    keys = (lim - np.repeat(cu[:-1], np.diff(cu)) + 1).astype(np.float64)
+    keys = oracle.row_keys(cu, pack.segments).astype(np.float64)  # FLOP count per row
     rng = np.random.default_rng(1)
     probe = rng.integers(0, pack.total_tokens, size=32).astype(np.int32)
     t0 = time.perf_counter()

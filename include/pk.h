@@ -20,11 +20,14 @@
  *   lse[h,t]   = ln sum_j exp(scale * q[t,h,:].k[j,g,:])   (visible j only)
  *
  * Tensors (all caller-owned device memory, bf16 = IEEE bfloat16):
- *   q   [T][hq][d]   bf16, rows contiguous, 16-byte aligned base
- *   k,v [T][hkv][d]  bf16, rows contiguous, 16-byte aligned base
- *   out [T][hq][d]   bf16, written for every token
- *   lse [hq][T]      fp32, natural log, written for every token
- * where T = cu_seqlens[num_seqs].
+ *   q   [Tq][hq][d]  bf16, rows contiguous, 16-byte aligned base
+ *   k,v [Tk][hkv][d] bf16, rows contiguous, 16-byte aligned base
+ *   out [Tq][hq][d]  bf16, written for every query row
+ *   lse [hq][Tq]     fp32, natural log, written for every query row
+ * With pk_plan_create, Tq = Tk = cu_seqlens[num_seqs].  With
+ * pk_plan_create_layout, Tq = cu_seqlens_q[num_seqs] and Tk = num_kv_rows.
+ * A query row that sees no key of its key range (possible only when the
+ * range starts after position 0) gets out = 0 and lse = -inf.
  *
  * Ownership: the library never allocates device memory.  A plan owns host
  * memory only; its device image lives in a caller-allocated buffer of
@@ -67,6 +70,43 @@ typedef struct pk_segment {
   int32_t type;
 } pk_segment;
 
+/* A segment in its sequence's own position space: positions [start,
+ * start+len) of sequence `seq`, all TEXT or all IMAGE. */
+typedef struct pk_seq_segment {
+  int32_t seq;
+  int32_t start;
+  int32_t len;
+  int32_t type;
+} pk_seq_segment;
+
+/*
+ * General layout ("[RFC]: HunyuanImage 3.0 deployment", Proposed Change, P0
+ * "KV Cache Transfer Integration for DiT": the text prefix's keys/values come
+ * from the AR stage, so the queries of a step are a subset of positions of
+ * the sequence; and the page-table keys of the recipe's paged-KV mode).
+ * Sequence s covers positions [0, L_s), tiled by its segments (segs ordered
+ * by seq, then start).  Its queries are the packed rows
+ * [cu_seqlens_q[s], cu_seqlens_q[s+1]) at positions q_pos0[s] + i; its keys
+ * are positions k_pos0[s] + j, j < cu_seqlens_k[s+1] - cu_seqlens_k[s],
+ * stored at row cu_seqlens_k[s] + j of k/v (block_table == NULL), or at row
+ * block_table[s * blocks_per_seq + p / 128] * 128 + p % 128 for position p
+ * (paged: 128-row blocks, k_pos0[s] a multiple of 128, num_kv_rows the pool
+ * rows, a multiple of 128).  q_pos0 / k_pos0 may be NULL (all zero).  The
+ * mask is the one of the whole sequence.  All pointers are host memory.
+ */
+typedef struct pk_layout {
+  int32_t num_seqs;
+  const int32_t* cu_seqlens_q;
+  const int32_t* q_pos0;
+  const int32_t* cu_seqlens_k;
+  const int32_t* k_pos0;
+  const pk_seq_segment* segs;
+  int32_t num_segs;
+  const int32_t* block_table;
+  int32_t blocks_per_seq;
+  int32_t num_kv_rows;
+} pk_layout;
+
 typedef struct pk_plan pk_plan;
 
 /* Summary of a plan (host data, for callers and tests). */
@@ -78,7 +118,7 @@ typedef struct pk_plan_info {
   int32_t num_ctas;         /* persistent CTAs launched by pk_attn_fwd */
   int32_t num_full_tiles;   /* (item, k-tile) visits with no mask math */
   int32_t num_partial_tiles;/* (item, k-tile) visits with per-element mask */
-  int32_t reserved;
+  int32_t kv_rows;          /* Tk: rows of the key/value tensors */
   int64_t visible_pairs;    /* per query head */
   double useful_flops;      /* 4 * d * hq * visible_pairs */
 } pk_plan_info;
@@ -89,7 +129,8 @@ typedef struct pk_plan_info {
 typedef struct pk_work_item {
   int32_t q_start;   /* global token index of the tile's first query row */
   int32_t q_rows;    /* valid query rows in the tile, 1..128 */
-  int32_t kv_start;  /* global token index of the sequence's first key */
+  int32_t kv_start;  /* contiguous keys: row of the key range's first key;
+                        paged: index of its first block in the block table */
   int32_t n_kt;      /* 128-key tiles visited, from kv_start upwards */
   int32_t n_full;    /* leading tiles visible to every valid row (no mask) */
   int32_t hq0;       /* query head of slot 0 */
@@ -115,8 +156,14 @@ pk_status pk_plan_create(const int32_t* cu_seqlens, int32_t num_seqs,
                          int32_t hkv, int32_t head_dim, int32_t num_ctas,
                          pk_plan** out);
 
-/* Bytes of the device image of the plan (work list, per-CTA offsets and the
- * per-token key limit). */
+/* Same planner for a general layout (see pk_layout); head_dim and num_ctas
+ * as for pk_plan_create.  Keys may be paged only with head_dim 64 or 128 and
+ * 128-row blocks. */
+pk_status pk_plan_create_layout(const pk_layout* layout, int32_t hq, int32_t hkv,
+                                int32_t head_dim, int32_t num_ctas, pk_plan** out);
+
+/* Bytes of the device image of the plan (work list, per-CTA offsets, the
+ * per-row key limit and, for paged keys, the block table). */
 size_t pk_plan_device_bytes(const pk_plan* plan);
 
 /* Copy the plan's device image into dev_buf (caller-owned, >= 256-byte
@@ -164,9 +211,10 @@ double pk_plan_useful_flops(const pk_plan* plan);
 
 pk_status pk_plan_get_info(const pk_plan* plan, pk_plan_info* info);
 
-/* Host copies of plan internals, for tests: the per-token key limit
- * (global index of the last visible key, int32[T]) and the CTA-ordered work
- * list (pk_work_item[num_items]) with per-CTA offsets (int32[num_ctas+1]). */
+/* Host copies of plan internals, for tests: the per-row key limit (index of
+ * the last visible key within the row's key range, -1 for none; int32[Tq])
+ * and the CTA-ordered work list (pk_work_item[num_items]) with per-CTA
+ * offsets (int32[num_ctas+1]). */
 pk_status pk_plan_get_kv_limit(const pk_plan* plan, int32_t* out, int64_t n);
 pk_status pk_plan_get_items(const pk_plan* plan, pk_work_item* items,
                             int64_t n_items, int32_t* cta_offsets,

@@ -74,6 +74,9 @@ def _load():
         lib.pko_mask_dense.restype = ctypes.c_int
         lib.pko_visible_pairs.argtypes = [i32p, ctypes.c_int32, i32p, ctypes.c_int32]
         lib.pko_visible_pairs.restype = ctypes.c_int64
+        lib.pko_row_keys.argtypes = [i32p, ctypes.c_int32, i32p, ctypes.c_int32,
+                                     ctypes.POINTER(ctypes.c_int64)]
+        lib.pko_row_keys.restype = ctypes.c_int
         lib.pko_attention.argtypes = [u16p, u16p, u16p, i32p, ctypes.c_int32, i32p,
                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                       ctypes.c_int32, ctypes.c_double, i32p,
@@ -144,6 +147,18 @@ def visible_pairs(cu_seqlens, segments) -> int:
     if n < 0:
         raise ValueError("oracle: invalid descriptors")
     return n
+
+
+def row_keys(cu_seqlens, segments) -> np.ndarray:
+    """Visible keys of every query row (int64 [T]): row sums of the mask."""
+    cu = _i32(cu_seqlens)
+    sg = _segs_array(segments)
+    out = np.zeros(max(int(cu[-1]), 1), dtype=np.int64)
+    rc = _load().pko_row_keys(_ptr(cu, ctypes.c_int32), len(cu) - 1, _ptr(sg, ctypes.c_int32),
+                              sg.shape[0], _ptr(out, ctypes.c_int64))
+    if rc:
+        raise ValueError("oracle: invalid descriptors")
+    return out[: int(cu[-1])]
 
 
 def attention(q, k, v, cu_seqlens, segments, hq: int, hkv: int, d: int,

@@ -143,6 +143,28 @@ int64_t pko_visible_pairs(const int32_t* cu, int32_t num_seqs,
   return total;
 }
 
+/* Visible keys of every query row of the pack (row sums of the dense mask),
+ * out[T]; returns 0, or -1 for invalid descriptors. */
+int pko_row_keys(const int32_t* cu, int32_t num_seqs, const int32_t* segs,
+                 int32_t num_segs, int64_t* out) {
+  if (pko_validate(cu, num_seqs, segs, num_segs)) return -1;
+  int32_t T = cu[num_seqs];
+  int32_t* seg_of = segment_of_tokens(T, segs, num_segs);
+  for (int32_t s = 0; s < num_seqs; ++s) {
+    int32_t b = cu[s], L = cu[s + 1] - cu[s];
+    uint8_t* row = (uint8_t*)malloc((size_t)(L > 0 ? L : 1));
+    for (int32_t i = 0; i < L; ++i) {
+      mask_row(b, L, i, seg_of, segs, row);
+      int64_t n = 0;
+      for (int32_t j = 0; j < L; ++j) n += row[j];
+      out[b + i] = n;
+    }
+    free(row);
+  }
+  free(seg_of);
+  return 0;
+}
+
 /* Attention of one query row (all query heads) over its sequence, given the
  * row of the dense mask.  q_row points at q[i][0][0]; k_seq / v_seq at the
  * first token of the sequence.  Writes out_row[Hq][d] and lse[h*lse_stride]. */

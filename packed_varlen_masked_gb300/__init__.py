@@ -18,7 +18,7 @@ from ._native import (PK_ERR_ALIGNMENT, PK_ERR_CUDA, PK_ERR_DEVICE_CHECK,  # noq
                       PK_ERR_INVALID_ARG, PK_ERR_NOT_UPLOADED, PK_ERR_TIMEOUT,
                       PK_ERR_UNSUPPORTED, PK_OK, PKError, lib_path, load)
 from .api import (IMAGE, TEXT, Plan, attn_fwd, attn_fwd_host,  # noqa: F401
-                  debug_wait_timeout, plan, set_wait_timeout_ns)
+                  debug_wait_timeout, plan, plan_layout, set_wait_timeout_ns)
 
-__all__ = ["plan", "Plan", "attn_fwd", "attn_fwd_host", "PKError", "TEXT", "IMAGE",
+__all__ = ["plan", "plan_layout", "Plan", "attn_fwd", "attn_fwd_host", "PKError", "TEXT", "IMAGE",
            "set_wait_timeout_ns", "debug_wait_timeout", "load", "lib_path"]

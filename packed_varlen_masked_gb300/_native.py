@@ -30,12 +30,28 @@ class Segment(ctypes.Structure):
     _fields_ = [("start", ctypes.c_int32), ("len", ctypes.c_int32), ("type", ctypes.c_int32)]
 
 
+class SeqSegment(ctypes.Structure):
+    _fields_ = [("seq", ctypes.c_int32), ("start", ctypes.c_int32), ("len", ctypes.c_int32),
+                ("type", ctypes.c_int32)]
+
+
+_I32P = ctypes.POINTER(ctypes.c_int32)
+
+
+class Layout(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32), ("cu_seqlens_q", _I32P), ("q_pos0", _I32P),
+                ("cu_seqlens_k", _I32P), ("k_pos0", _I32P),
+                ("segs", ctypes.POINTER(SeqSegment)), ("num_segs", ctypes.c_int32),
+                ("block_table", _I32P), ("blocks_per_seq", ctypes.c_int32),
+                ("num_kv_rows", ctypes.c_int32)]
+
+
 class PlanInfo(ctypes.Structure):
     _fields_ = [("total_tokens", ctypes.c_int32), ("num_seqs", ctypes.c_int32),
                 ("hq", ctypes.c_int32), ("hkv", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("num_items", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
                 ("num_full_tiles", ctypes.c_int32), ("num_partial_tiles", ctypes.c_int32),
-                ("reserved", ctypes.c_int32), ("visible_pairs", ctypes.c_int64),
+                ("kv_rows", ctypes.c_int32), ("visible_pairs", ctypes.c_int64),
                 ("useful_flops", ctypes.c_double)]
 
 
@@ -51,6 +67,9 @@ SIGNATURES = {
     "pk_plan_create": (ctypes.c_int, [_i32p, ctypes.c_int32, ctypes.POINTER(Segment),
                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                       ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(_vp)]),
+    "pk_plan_create_layout": (ctypes.c_int, [ctypes.POINTER(Layout), ctypes.c_int32,
+                                             ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                             ctypes.POINTER(_vp)]),
     "pk_plan_device_bytes": (ctypes.c_size_t, [_vp]),
     "pk_plan_upload": (ctypes.c_int, [_vp, _vp, ctypes.c_size_t, _vp]),
     "pk_attn_fwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),

@@ -8,7 +8,7 @@ from typing import Optional, Sequence, Tuple
 
 import numpy as np
 
-from ._native import PlanInfo, Segment, WorkItem, check, load
+from ._native import Layout, PlanInfo, Segment, SeqSegment, WorkItem, check, load
 
 TEXT = 0
 IMAGE = 1
@@ -32,20 +32,29 @@ class Plan:
     """
 
     def __init__(self, cu_seqlens, segments, hq: int, hkv: int, head_dim: int,
-                 num_ctas: int = 0, device=None, upload: bool = True):
+                 num_ctas: int = 0, device=None, upload: bool = True, _layout=None):
         self._lib = load()
         self._h = ctypes.c_void_p()
-        cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
-        if cu.ndim != 1 or cu.size < 1:
-            raise ValueError("cu_seqlens must be a 1-D array with at least one entry")
-        segs, n = _segments_struct(segments)
-        check(self._lib.pk_plan_create(cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
-                                       cu.size - 1, segs, n, int(hq), int(hkv), int(head_dim),
-                                       int(num_ctas), ctypes.byref(self._h)),
-              "pk_plan_create")
         self.hq, self.hkv, self.head_dim = int(hq), int(hkv), int(head_dim)
-        self.total_tokens = int(cu[-1])
         self._buf = None
+        if _layout is not None:
+            lay, keep = _layout
+            check(self._lib.pk_plan_create_layout(ctypes.byref(lay), self.hq, self.hkv,
+                                                  self.head_dim, int(num_ctas),
+                                                  ctypes.byref(self._h)), "pk_plan_create_layout")
+            del keep
+        else:
+            cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+            if cu.ndim != 1 or cu.size < 1:
+                raise ValueError("cu_seqlens must be a 1-D array with at least one entry")
+            segs, n = _segments_struct(segments)
+            check(self._lib.pk_plan_create(cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                           cu.size - 1, segs, n, self.hq, self.hkv,
+                                           self.head_dim, int(num_ctas), ctypes.byref(self._h)),
+                  "pk_plan_create")
+        info = self.info
+        self.total_tokens = int(info["total_tokens"])
+        self.kv_rows = int(info["kv_rows"])
         if upload:
             self.upload(device)
 
@@ -90,7 +99,7 @@ class Plan:
     def info(self) -> dict:
         pi = PlanInfo()
         check(self._lib.pk_plan_get_info(self._h, ctypes.byref(pi)), "pk_plan_get_info")
-        return {name: getattr(pi, name) for name, _ in PlanInfo._fields_ if name != "reserved"}
+        return {name: getattr(pi, name) for name, _ in PlanInfo._fields_}
 
     @property
     def useful_flops(self) -> float:
@@ -121,6 +130,37 @@ def plan(cu_seqlens, segments, hq: int, hkv: int, head_dim: int, num_ctas: int =
     return Plan(cu_seqlens, segments, hq, hkv, head_dim, num_ctas=num_ctas, device=device)
 
 
+def plan_layout(cu_seqlens_q, cu_seqlens_k, seq_segments, hq: int, hkv: int, head_dim: int,
+                q_pos0=None, k_pos0=None, block_table=None, num_kv_rows: Optional[int] = None,
+                num_ctas: int = 0, device=None, upload: bool = True) -> Plan:
+    """Plan for queries and keys that are position ranges of their sequences
+    (cached prefix, key chunks) and optionally paged keys (see pk_layout in
+    include/pk.h).  ``seq_segments``: (seq, start, len, type) rows in each
+    sequence's position space; ``block_table`` [num_seqs, blocks_per_seq]
+    of 128-row pool blocks."""
+    i32 = lambda a: np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+    p32 = lambda a: a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)) if a is not None else None
+    cq, ck = i32(cu_seqlens_q), i32(cu_seqlens_k)
+    S = cq.size - 1
+    qp = i32(q_pos0) if q_pos0 is not None else None
+    kp = i32(k_pos0) if k_pos0 is not None else None
+    sg = np.asarray(seq_segments, dtype=np.int64).reshape(-1, 4)
+    segs = (SeqSegment * max(sg.shape[0], 1))()
+    for i, (a, b, c, d) in enumerate(sg.tolist()):
+        segs[i] = SeqSegment(int(a), int(b), int(c), int(d))
+    bt = i32(block_table).reshape(S, -1) if block_table is not None else None
+    if num_kv_rows is None:
+        if bt is not None:
+            raise ValueError("num_kv_rows (pool rows) is required with a block table")
+        num_kv_rows = int(ck[-1])
+    lay = Layout(S, p32(cq), p32(qp), p32(ck), p32(kp), segs, sg.shape[0],
+                 p32(bt) if bt is not None else None, bt.shape[1] if bt is not None else 0,
+                 int(num_kv_rows))
+    keep = (cq, ck, qp, kp, segs, bt)
+    return Plan(None, None, hq, hkv, head_dim, num_ctas=num_ctas, device=device, upload=upload,
+                _layout=(lay, keep))
+
+
 def _check_tensor(t, name, shape):
     import torch
     if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda:
@@ -141,9 +181,10 @@ def attn_fwd(q, k, v, plan: Plan, scale: Optional[float] = None, out=None, lse=N
     """
     import torch
     T, hq, hkv, d = plan.total_tokens, plan.hq, plan.hkv, plan.head_dim
+    Tk = plan.kv_rows
     _check_tensor(q, "q", (T, hq, d))
-    _check_tensor(k, "k", (T, hkv, d))
-    _check_tensor(v, "v", (T, hkv, d))
+    _check_tensor(k, "k", (Tk, hkv, d))
+    _check_tensor(v, "v", (Tk, hkv, d))
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:

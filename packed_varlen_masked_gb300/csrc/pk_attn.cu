@@ -283,7 +283,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 struct KernelParams {
   const pk_work_item* items;
   const int32_t* cta_offsets;
-  const int32_t* kv_limit;
+  const int32_t* kv_limit;       // per query row: last visible key of its range, -1 none
+  const int32_t* block_table;    // paged keys: physical 128-row block of each key tile; else null
   uint8_t* out;   // bf16 [T][hq][D]
   float* lse;     // [hq][T]
   int32_t* status;
@@ -292,6 +293,13 @@ struct KernelParams {
   float scale_log2;  // softmax scale * log2(e)
   uint64_t wait_limit_ns;
 };
+
+// First key/value row of key tile j of a work item: contiguous keys start
+// at kv_start; paged keys take the block of the item's key range from the
+// block table (blocks are one key tile, 128 rows).
+__device__ __forceinline__ int key_tile_row(const KernelParams& p, const pk_work_item& w, int j) {
+  return p.block_table ? p.block_table[w.kv_start + j] * 128 : w.kv_start + j * 128;
+}
 
 // A unit of work is one query head of a work item: a 128-row query tile that
 // streams the key/value tiles of its sequence.  A CTA runs the heads of each
@@ -376,7 +384,7 @@ __device__ void producer_qk_role(const KernelParams& p, const CUtensorMap* tm_q,
 #pragma unroll
       for (int h = 0; h < C::kHalves; ++h)
         tma_load_3d_hint(sbase + C::kOffK + st * C::kTileBytes + h * kBoxBytes, tm_k,
-                         bar(C::kKFull + st), h * 64, w.hkv, w.kv_start + j * 128, keep);
+                         bar(C::kKFull + st), h * 64, w.hkv, key_tile_row(p, w, j), keep);
     }
   }
   if (!ok) {
@@ -414,7 +422,7 @@ __device__ void producer_v_role(const KernelParams& p, const CUtensorMap* tm_v, 
 #pragma unroll
       for (int h = 0; h < C::kHalves; ++h)
         tma_load_3d_hint(sbase + C::kOffV + st * C::kTileBytes + h * kBoxBytes, tm_v,
-                         bar(C::kVFull + st), h * 64, w.hkv, w.kv_start + j * 128, keep);
+                         bar(C::kVFull + st), h * 64, w.hkv, key_tile_row(p, w, j), keep);
     }
   }
   if (!ok) {
@@ -528,7 +536,7 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint32_t tme
       tc_fence_before();
       mbar_arrive(bar(C::kSFree + b));
       if (j >= w.n_full) {  // partial tile: keys past this row's limit are -inf
-        const int nvis = lim - (w.kv_start + j * 128) + 1;
+        const int nvis = lim - j * 128 + 1;
 #pragma unroll
         for (int c = 0; c < 128; ++c) sr[c] = c < nvis ? sr[c] : 0xff800000u;
       }
@@ -576,7 +584,8 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint32_t tme
       };
       constexpr float kRescaleSum = 65536.0f;  // 2^kRescaleLog2
       if (j == 0) m_used = row_max();
-      exp_pass(-m_used);
+      // A row that sees no key of its range keeps m_used = -inf and p = 0.
+      exp_pass(m_used == -INFINITY ? 0.0f : -m_used);
       const float tile_sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
       // One warp vote for: a possible rescale (bit 0), P buffer still busy
       // (bit 1), next S not yet seen (bit 2).
@@ -607,7 +616,7 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint32_t tme
             for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * f);
             tmem_st_x32(tO + (uint32_t)c0, o);
           }
-          exp_pass(-m_used);
+          exp_pass(m_used == -INFINITY ? 0.0f : -m_used);
         }
       }
       l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
@@ -625,7 +634,7 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint32_t tme
     ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kPvDone + (tl & 1u)), (tl >> 1) & 1u, wc));
     if (!ok) break;
     tc_fence_after();
-    const float inv_l = 1.0f / l;
+    const float inv_l = l > 0.f ? 1.0f / l : 0.f;  // a row without keys writes zeros
     uint8_t* orow = p.out + (((size_t)(w.q_start + r) * (size_t)p.hq + (size_t)h) * D) * 2;
 #pragma unroll
     for (int c0 = 0; c0 < D; c0 += 32) {
@@ -646,7 +655,7 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint32_t tme
     mbar_arrive(bar(C::kOFree));
     if (valid)
       p.lse[(size_t)h * (size_t)p.T + (size_t)(w.q_start + r)] =
-          (m_used + __log2f(l)) * 0.69314718055994530942f;
+          l > 0.f ? (m_used + __log2f(l)) * 0.69314718055994530942f : -INFINITY;
     g += (uint32_t)w.n_kt;
   }
 }
@@ -822,8 +831,8 @@ pk_status launch(const pk_plan* plan, const void* q, const void* k, const void* 
                  float* lse, float scale, cudaStream_t stream, int32_t* dev_status) {
   using C = pk::dev::Cfg<D>;
   CUtensorMap tq, tk, tv;
-  if (!make_map(&tq, q, plan->hq, plan->T, D) || !make_map(&tk, k, plan->hkv, plan->T, D) ||
-      !make_map(&tv, v, plan->hkv, plan->T, D))
+  if (!make_map(&tq, q, plan->hq, plan->T, D) || !make_map(&tk, k, plan->hkv, plan->Tk, D) ||
+      !make_map(&tv, v, plan->hkv, plan->Tk, D))
     return PK_ERR_CUDA;
   if (cudaFuncSetAttribute(pk::dev::pk_attn_fwd_kernel<D>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -836,6 +845,8 @@ pk_status launch(const pk_plan* plan, const void* q, const void* k, const void* 
   kp.items = reinterpret_cast<const pk_work_item*>(img + plan->layout.items_off);
   kp.cta_offsets = reinterpret_cast<const int32_t*>(img + plan->layout.cta_off_off);
   kp.kv_limit = reinterpret_cast<const int32_t*>(img + plan->layout.kvlim_off);
+  kp.block_table =
+      plan->paged ? reinterpret_cast<const int32_t*>(img + plan->layout.table_off) : nullptr;
   kp.out = static_cast<uint8_t*>(out);
   kp.lse = lse;
   kp.status = dev_status;
@@ -864,6 +875,7 @@ pk_status pk_attn_fwd(const pk_plan* plan, const void* q, const void* k, const v
   if (!(scale > 0.f) || !std::isfinite(scale)) return PK_ERR_INVALID_ARG;
   if (plan->T == 0 || plan->items.empty()) return PK_OK;
   if (plan->dev == nullptr) return PK_ERR_NOT_UPLOADED;
+  if (plan->Tk <= 0) return PK_ERR_INVALID_ARG;  // queries need a key/value tensor to map
   if (!q || !k || !v || !out || !lse) return PK_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u))
@@ -884,8 +896,8 @@ pk_status pk_attn_fwd_host(const pk_plan* plan, const void* q_host, const void* 
   if (plan->T == 0) return PK_OK;
   if (!q_host || !k_host || !v_host || !out_host || !lse_host) return PK_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const size_t T = (size_t)plan->T, d = (size_t)plan->head_dim;
-  const size_t qb = T * plan->hq * d * 2, kvb = T * plan->hkv * d * 2;
+  const size_t T = (size_t)plan->T, Tk = (size_t)plan->Tk, d = (size_t)plan->head_dim;
+  const size_t qb = T * plan->hq * d * 2, kvb = Tk * plan->hkv * d * 2;
   const size_t lb = T * plan->hq * sizeof(float);
   if (!q_dev || !k_dev || !v_dev || !out_dev || !lse_dev) return PK_ERR_INVALID_ARG;
   if (cudaMemcpyAsync(q_dev, q_host, qb, cudaMemcpyHostToDevice, s) != cudaSuccess ||

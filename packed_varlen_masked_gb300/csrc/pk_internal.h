@@ -15,23 +15,30 @@ constexpr size_t kImageAlign = 256;
 
 static_assert(sizeof(pk_work_item) == 32, "work item is 32 bytes");
 
+constexpr int kKeyBlock = 128;  // rows per block of a paged key/value pool
+
 struct PlanImageLayout {
   size_t items_off = 0;    // pk_work_item[num_items], CTA-ordered
   size_t cta_off_off = 0;  // int32[num_ctas + 1]
-  size_t kvlim_off = 0;    // int32[T]
+  size_t kvlim_off = 0;    // int32[Tq]: last visible key index of the row's key range, -1 none
+  size_t table_off = 0;    // int32[num_seqs * blocks_per_seq] when keys are paged
   size_t bytes = 0;
 };
 
 }  // namespace pk
 
 struct pk_plan {
-  int32_t T = 0;
+  int32_t T = 0;          // query rows (Tq)
+  int32_t Tk = 0;         // rows of the key/value tensors (contiguous keys or pool)
+  bool paged = false;     // keys/values read through the block table
+  int32_t blocks_per_seq = 0;
+  std::vector<int32_t> block_table;
   int32_t num_seqs = 0;
   int32_t hq = 0, hkv = 0, head_dim = 0;
   int32_t num_ctas = 0;
   int32_t num_full_tiles = 0, num_partial_tiles = 0;
   int64_t visible_pairs = 0;
-  std::vector<int32_t> kv_limit;           // [T] global index of last visible key
+  std::vector<int32_t> kv_limit;           // [Tq] last visible key of the row's key range, -1 none
   std::vector<pk_work_item> items;         // CTA-ordered
   std::vector<int32_t> cta_offsets;        // [num_ctas + 1]
   pk::PlanImageLayout layout;

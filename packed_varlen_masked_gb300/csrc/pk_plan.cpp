@@ -1,17 +1,18 @@
-// Host planner: descriptor validation, per-token key limit, tile
+// Host planner: descriptor validation, per-row key limit, tile
 // classification and the longest-work-first persistent schedule.
 //
 // The mask of "[RFC]: HunyuanImage 3.0 deployment" (Proposed Change, P0
-// "Attention mask challenge"; "Model structure", item 1) lets query i of a
-// sequence see key j iff j <= i, or i and j share i's IMAGE segment.  Because
-// an image segment starts at or before i, the union of the causal prefix and
-// the own segment is itself a prefix of the sequence: row i sees exactly keys
-// [seq_start, kv_limit[i]] with
-//     kv_limit[i] = i                      for a text token,
-//     kv_limit[i] = (end of i's segment)-1 for an image token.
-// kv_limit never decreases along a sequence and kv_limit[i] >= i, so every
-// row sees at least the sequence's first key.  The page's "block-sparse mask"
-// option then becomes a per-tile classification over 128 x 128 tiles:
+// "Attention mask challenge"; "Model structure", item 1) lets position x of a
+// sequence see position y iff y <= x, or x and y share x's IMAGE segment.
+// Because an image segment starts at or before x, the union of the causal
+// prefix and the own segment is itself a prefix of the sequence: x sees
+// exactly positions [0, lim(x)] with
+//     lim(x) = x                      for a text token,
+//     lim(x) = (end of x's segment)-1 for an image token.
+// lim never decreases along a sequence and lim(x) >= x.  A query row sees the
+// prefix of its key range up to lim(x) (none if the range starts after it),
+// stored as an index into the range.  The page's "block-sparse mask" option
+// then becomes a per-tile classification over 128 x 128 tiles:
 //   skipped  : no row of the query tile sees any key of the key tile
 //              (never enumerated: the visited key tiles are a prefix),
 //   full     : every valid row sees every key of the tile (no mask math),
@@ -29,70 +30,87 @@
 
 namespace {
 
-pk_status validate(const int32_t* cu, int32_t num_seqs, const pk_segment* segs,
-                   int32_t num_segs, int32_t hq, int32_t hkv, int32_t d) {
-  if (num_seqs < 0 || num_segs < 0 || cu == nullptr) return PK_ERR_INVALID_ARG;
-  if (num_segs > 0 && segs == nullptr) return PK_ERR_INVALID_ARG;
-  if (hq <= 0 || hkv <= 0 || hq % hkv != 0) return PK_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return PK_ERR_UNSUPPORTED;
-  if (cu[0] != 0) return PK_ERR_INVALID_ARG;
-  for (int32_t s = 0; s < num_seqs; ++s)
-    if (cu[s + 1] < cu[s]) return PK_ERR_INVALID_ARG;
-  // Tokens are addressed with int32 and tiles may overhang the end by 127.
-  if (cu[num_seqs] > INT32_MAX - 2 * pk::kTileQ) return PK_ERR_INVALID_ARG;
-  int32_t g = 0;
-  for (int32_t s = 0; s < num_seqs; ++s) {
-    int32_t pos = cu[s];
-    while (pos < cu[s + 1]) {
-      if (g >= num_segs) return PK_ERR_INVALID_ARG;
-      const pk_segment& sg = segs[g];
-      if (sg.start != pos || sg.len <= 0) return PK_ERR_INVALID_ARG;
-      if (sg.type != PK_TEXT && sg.type != PK_IMAGE) return PK_ERR_INVALID_ARG;
-      if (sg.len > cu[s + 1] - pos) return PK_ERR_INVALID_ARG;
-      pos += sg.len;
-      ++g;
-    }
-  }
-  if (g != num_segs) return PK_ERR_INVALID_ARG;
-  return PK_OK;
-}
-
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Relative cost of a work item for the longest-processing-time schedule:
-// one unit per visited key tile, masked tiles a little dearer, a fixed
-// per-item cost (query loads, pipeline fill, epilogue), and single-slot items
-// doing half of the tensor work.
+// one unit per visited key tile and query head (the CTA runs the item's two
+// heads one after the other), masked tiles a little dearer, and a fixed
+// per-head cost (query load, pipeline fill, epilogue).
 double item_cost(const pk_work_item& w) {
-  double c = w.n_full * 1.0 + (w.n_kt - w.n_full) * 1.3 + 3.0;
-  return w.hq1 >= 0 ? c : 0.55 * c;
+  const double per_head = w.n_full * 1.0 + (w.n_kt - w.n_full) * 1.3 + 3.0;
+  return w.hq1 >= 0 ? 2.0 * per_head : per_head;
 }
 
-}  // namespace
-
-extern "C" {
-
-const char* pk_status_string(pk_status st) {
-  switch (st) {
-    case PK_OK: return "ok";
-    case PK_ERR_INVALID_ARG: return "invalid argument";
-    case PK_ERR_UNSUPPORTED: return "unsupported configuration";
-    case PK_ERR_ALIGNMENT: return "misaligned tensor";
-    case PK_ERR_CUDA: return "CUDA error";
-    case PK_ERR_TIMEOUT: return "device wait timed out";
-    case PK_ERR_DEVICE_CHECK: return "device consistency check failed";
-    case PK_ERR_NOT_UPLOADED: return "plan not uploaded";
+// Validation of the general layout; fills seg_first[s] (first segment of s)
+// and seq_len[s] (positions covered by its segments).
+pk_status validate_layout(const pk_layout& L, int32_t hq, int32_t hkv, int32_t d,
+                          std::vector<int32_t>& seg_first, std::vector<int32_t>& seq_len) {
+  const int32_t S = L.num_seqs;
+  if (S < 0 || L.num_segs < 0 || L.cu_seqlens_q == nullptr || L.cu_seqlens_k == nullptr)
+    return PK_ERR_INVALID_ARG;
+  if (L.num_segs > 0 && L.segs == nullptr) return PK_ERR_INVALID_ARG;
+  if (hq <= 0 || hkv <= 0 || hq % hkv != 0) return PK_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return PK_ERR_UNSUPPORTED;
+  const int32_t* cq = L.cu_seqlens_q;
+  const int32_t* ck = L.cu_seqlens_k;
+  if (cq[0] != 0 || ck[0] != 0) return PK_ERR_INVALID_ARG;
+  for (int32_t s = 0; s < S; ++s)
+    if (cq[s + 1] < cq[s] || ck[s + 1] < ck[s]) return PK_ERR_INVALID_ARG;
+  // Rows are addressed with int32 and tiles may overhang the end by 127.
+  if (cq[S] > INT32_MAX - 2 * pk::kTileQ || L.num_kv_rows > INT32_MAX - 2 * pk::kTileK ||
+      L.num_kv_rows < 0)
+    return PK_ERR_INVALID_ARG;
+  seg_first.assign(S, -1);
+  seq_len.assign(S, 0);
+  int32_t prev = -1;
+  for (int32_t g = 0; g < L.num_segs; ++g) {
+    const pk_seq_segment& sg = L.segs[g];
+    if (sg.seq < 0 || sg.seq >= S || sg.seq < prev) return PK_ERR_INVALID_ARG;
+    if (sg.len <= 0 || (sg.type != PK_TEXT && sg.type != PK_IMAGE)) return PK_ERR_INVALID_ARG;
+    if (sg.start != seq_len[sg.seq] || sg.len > INT32_MAX / 2 - seq_len[sg.seq])
+      return PK_ERR_INVALID_ARG;
+    if (seg_first[sg.seq] < 0) seg_first[sg.seq] = g;
+    seq_len[sg.seq] += sg.len;
+    prev = sg.seq;
   }
-  return "unknown status";
+  for (int32_t s = 0; s < S; ++s) {
+    const int32_t q0 = L.q_pos0 ? L.q_pos0[s] : 0, k0 = L.k_pos0 ? L.k_pos0[s] : 0;
+    const int32_t nq = cq[s + 1] - cq[s], nk = ck[s + 1] - ck[s];
+    if (q0 < 0 || k0 < 0 || q0 > seq_len[s] - nq || k0 > seq_len[s] - nk) return PK_ERR_INVALID_ARG;
+  }
+  if (L.block_table != nullptr) {
+    if (L.blocks_per_seq <= 0 || L.num_kv_rows % pk::kKeyBlock) return PK_ERR_INVALID_ARG;
+    const int32_t pool_blocks = L.num_kv_rows / pk::kKeyBlock;
+    for (int32_t s = 0; s < S; ++s) {
+      const int32_t k0 = L.k_pos0 ? L.k_pos0[s] : 0, nk = ck[s + 1] - ck[s];
+      if (nk == 0) continue;
+      if (k0 % pk::kKeyBlock) return PK_ERR_INVALID_ARG;
+      const int32_t b0 = k0 / pk::kKeyBlock, nb = (nk + pk::kKeyBlock - 1) / pk::kKeyBlock;
+      if (b0 + nb > L.blocks_per_seq) return PK_ERR_INVALID_ARG;
+      for (int32_t b = b0; b < b0 + nb; ++b) {
+        const int32_t pb = L.block_table[(size_t)s * L.blocks_per_seq + b];
+        if (pb < 0 || pb >= pool_blocks) return PK_ERR_INVALID_ARG;
+      }
+    }
+    for (int32_t s = 0; s < S; ++s)
+      if (ck[s + 1] == ck[s] && cq[s + 1] > cq[s]) {
+        // rows without keys read table entry 0 (all masked): it must be valid
+        if (S == 0 || L.block_table[0] < 0 || L.block_table[0] >= pool_blocks)
+          return PK_ERR_INVALID_ARG;
+      }
+  } else if (L.num_kv_rows < ck[S]) {
+    return PK_ERR_INVALID_ARG;
+  }
+  if (cq[S] > 0 && L.num_kv_rows == 0) return PK_ERR_INVALID_ARG;  // no key tensor to read
+  return PK_OK;
 }
 
-pk_status pk_plan_create(const int32_t* cu, int32_t num_seqs,
-                         const pk_segment* segs, int32_t num_segs, int32_t hq,
-                         int32_t hkv, int32_t d, int32_t num_ctas,
-                         pk_plan** out) {
+pk_status build_plan(const pk_layout& L, int32_t hq, int32_t hkv, int32_t d, int32_t num_ctas,
+                     pk_plan** out) {
   if (out == nullptr) return PK_ERR_INVALID_ARG;
   *out = nullptr;
-  pk_status st = validate(cu, num_seqs, segs, num_segs, hq, hkv, d);
+  std::vector<int32_t> seg_first, seq_len;
+  pk_status st = validate_layout(L, hq, hkv, d, seg_first, seq_len);
   if (st != PK_OK) return st;
   if (num_ctas < 0) return PK_ERR_INVALID_ARG;
   if (num_ctas == 0) {
@@ -108,38 +126,63 @@ pk_status pk_plan_create(const int32_t* cu, int32_t num_seqs,
 
   pk_plan* p = new (std::nothrow) pk_plan();
   if (p == nullptr) return PK_ERR_INVALID_ARG;
-  const int32_t T = cu[num_seqs];
-  p->T = T;
-  p->num_seqs = num_seqs;
+  const int32_t S = L.num_seqs;
+  const int32_t* cq = L.cu_seqlens_q;
+  const int32_t* ck = L.cu_seqlens_k;
+  const int32_t Tq = cq[S];
+  p->T = Tq;
+  p->Tk = L.num_kv_rows;
+  p->paged = L.block_table != nullptr;
+  p->blocks_per_seq = p->paged ? L.blocks_per_seq : 0;
+  if (p->paged)
+    p->block_table.assign(L.block_table, L.block_table + (size_t)S * L.blocks_per_seq);
+  p->num_seqs = S;
   p->hq = hq;
   p->hkv = hkv;
   p->head_dim = d;
 
-  // Per-token key limit (global index of the last visible key).
-  p->kv_limit.resize(T);
-  for (int32_t g = 0; g < num_segs; ++g) {
-    const pk_segment& sg = segs[g];
-    for (int32_t t = sg.start; t < sg.start + sg.len; ++t)
-      p->kv_limit[t] = sg.type == PK_IMAGE ? sg.start + sg.len - 1 : t;
+  // Per query row: last visible key of its sequence's key range, as an
+  // index into that range (-1: the row sees none of it).  The key limit of
+  // position x is x for text and the end of x's segment minus one for image.
+  p->kv_limit.assign(Tq, -1);
+  for (int32_t s = 0; s < S; ++s) {
+    const int32_t nq = cq[s + 1] - cq[s], nk = ck[s + 1] - ck[s];
+    if (nq == 0) continue;
+    const int32_t q0 = L.q_pos0 ? L.q_pos0[s] : 0, k0 = L.k_pos0 ? L.k_pos0[s] : 0;
+    int32_t g = seg_first[s];
+    for (int32_t i = 0; i < nq; ++i) {
+      const int32_t x = q0 + i;
+      while (L.segs[g].start + L.segs[g].len <= x) ++g;
+      const int32_t lim_pos =
+          L.segs[g].type == PK_IMAGE ? L.segs[g].start + L.segs[g].len - 1 : x;
+      const int32_t rel = std::min(lim_pos, k0 + nk - 1) - k0;
+      p->kv_limit[cq[s] + i] = rel < 0 ? -1 : rel;
+      p->visible_pairs += rel < 0 ? 0 : rel + 1;
+    }
   }
 
   // Work items: every 128-row query tile x key/value head x query-head pair.
   std::vector<pk_work_item> items;
   const int32_t group = hq / hkv;
   const int32_t pairs = (group + 1) / 2;
-  for (int32_t s = 0; s < num_seqs; ++s) {
-    const int32_t b = cu[s], e = cu[s + 1];
-    for (int32_t t = b; t < e; ++t) p->visible_pairs += p->kv_limit[t] - b + 1;
-    for (int32_t q0 = b; q0 < e; q0 += pk::kTileQ) {
-      const int32_t rows = std::min(pk::kTileQ, e - q0);
-      const int32_t lim_first = p->kv_limit[q0];
-      const int32_t lim_last = p->kv_limit[q0 + rows - 1];
+  for (int32_t s = 0; s < S; ++s) {
+    const int32_t b = cq[s], e = cq[s + 1];
+    const int32_t k0 = L.k_pos0 ? L.k_pos0[s] : 0;
+    for (int32_t r0 = b; r0 < e; r0 += pk::kTileQ) {
+      const int32_t rows = std::min(pk::kTileQ, e - r0);
+      const int32_t lim_first = p->kv_limit[r0];
+      const int32_t lim_last = p->kv_limit[r0 + rows - 1];
       pk_work_item w{};
-      w.q_start = q0;
+      w.q_start = r0;
       w.q_rows = rows;
-      w.kv_start = b;
-      w.n_kt = (lim_last - b) / pk::kTileK + 1;
-      w.n_full = std::min(w.n_kt, (lim_first - b + 1) / pk::kTileK);
+      // An empty key range (every row masked) still reads one key tile: for
+      // paged keys point it at table entry 0, a validated block.
+      const bool no_keys = ck[s + 1] == ck[s];
+      w.kv_start = p->paged ? (no_keys ? 0 : s * L.blocks_per_seq + k0 / pk::kKeyBlock) : ck[s];
+      // A tile whose rows see no key still visits key tile 0 (all masked),
+      // so every row's output and LSE are written by the same path.
+      w.n_kt = lim_last < 0 ? 1 : lim_last / pk::kTileK + 1;
+      w.n_full = std::min(w.n_kt, lim_first < 0 ? 0 : (lim_first + 1) / pk::kTileK);
       for (int32_t g = 0; g < hkv; ++g) {
         for (int32_t pr = 0; pr < pairs; ++pr) {
           w.hkv = g;
@@ -183,20 +226,86 @@ pk_status pk_plan_create(const int32_t* cu, int32_t num_seqs,
   }
 
   // Device image.
-  pk::PlanImageLayout& L = p->layout;
-  L.items_off = 0;
-  L.cta_off_off = align_up(L.items_off + sizeof(pk_work_item) * n_items, pk::kImageAlign);
-  L.kvlim_off = align_up(L.cta_off_off + sizeof(int32_t) * (grid + 1), pk::kImageAlign);
-  L.bytes = align_up(L.kvlim_off + sizeof(int32_t) * static_cast<size_t>(T), pk::kImageAlign);
-  p->image.assign(L.bytes, 0);
+  pk::PlanImageLayout& IL = p->layout;
+  IL.items_off = 0;
+  IL.cta_off_off = align_up(IL.items_off + sizeof(pk_work_item) * n_items, pk::kImageAlign);
+  IL.kvlim_off = align_up(IL.cta_off_off + sizeof(int32_t) * (grid + 1), pk::kImageAlign);
+  IL.table_off = align_up(IL.kvlim_off + sizeof(int32_t) * static_cast<size_t>(Tq), pk::kImageAlign);
+  IL.bytes = align_up(IL.table_off + sizeof(int32_t) * p->block_table.size(), pk::kImageAlign);
+  p->image.assign(IL.bytes, 0);
   if (n_items)
-    std::memcpy(p->image.data() + L.items_off, p->items.data(), sizeof(pk_work_item) * n_items);
-  std::memcpy(p->image.data() + L.cta_off_off, p->cta_offsets.data(), sizeof(int32_t) * (grid + 1));
-  if (T)
-    std::memcpy(p->image.data() + L.kvlim_off, p->kv_limit.data(), sizeof(int32_t) * T);
+    std::memcpy(p->image.data() + IL.items_off, p->items.data(), sizeof(pk_work_item) * n_items);
+  std::memcpy(p->image.data() + IL.cta_off_off, p->cta_offsets.data(), sizeof(int32_t) * (grid + 1));
+  if (Tq)
+    std::memcpy(p->image.data() + IL.kvlim_off, p->kv_limit.data(), sizeof(int32_t) * Tq);
+  if (!p->block_table.empty())
+    std::memcpy(p->image.data() + IL.table_off, p->block_table.data(),
+                sizeof(int32_t) * p->block_table.size());
 
   *out = p;
   return PK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pk_status_string(pk_status st) {
+  switch (st) {
+    case PK_OK: return "ok";
+    case PK_ERR_INVALID_ARG: return "invalid argument";
+    case PK_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PK_ERR_ALIGNMENT: return "misaligned tensor";
+    case PK_ERR_CUDA: return "CUDA error";
+    case PK_ERR_TIMEOUT: return "device wait timed out";
+    case PK_ERR_DEVICE_CHECK: return "device consistency check failed";
+    case PK_ERR_NOT_UPLOADED: return "plan not uploaded";
+  }
+  return "unknown status";
+}
+
+pk_status pk_plan_create_layout(const pk_layout* layout, int32_t hq, int32_t hkv,
+                                int32_t head_dim, int32_t num_ctas, pk_plan** out) {
+  if (out) *out = nullptr;
+  if (layout == nullptr) return PK_ERR_INVALID_ARG;
+  return build_plan(*layout, hq, hkv, head_dim, num_ctas, out);
+}
+
+pk_status pk_plan_create(const int32_t* cu, int32_t num_seqs, const pk_segment* segs,
+                         int32_t num_segs, int32_t hq, int32_t hkv, int32_t d, int32_t num_ctas,
+                         pk_plan** out) {
+  if (out == nullptr) return PK_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (num_seqs < 0 || num_segs < 0 || cu == nullptr || (num_segs > 0 && segs == nullptr))
+    return PK_ERR_INVALID_ARG;
+  if (cu[0] != 0) return PK_ERR_INVALID_ARG;
+  for (int32_t s = 0; s < num_seqs; ++s)
+    if (cu[s + 1] < cu[s]) return PK_ERR_INVALID_ARG;
+  // Global segments -> per-sequence segments: each must tile its sequence.
+  std::vector<pk_seq_segment> ss;
+  ss.reserve(num_segs);
+  int32_t g = 0;
+  for (int32_t s = 0; s < num_seqs; ++s) {
+    int32_t pos = cu[s];
+    while (pos < cu[s + 1]) {
+      if (g >= num_segs) return PK_ERR_INVALID_ARG;
+      const pk_segment& sg = segs[g];
+      if (sg.start != pos || sg.len <= 0 || sg.len > cu[s + 1] - pos) return PK_ERR_INVALID_ARG;
+      if (sg.type != PK_TEXT && sg.type != PK_IMAGE) return PK_ERR_INVALID_ARG;
+      ss.push_back(pk_seq_segment{s, pos - cu[s], sg.len, sg.type});
+      pos += sg.len;
+      ++g;
+    }
+  }
+  if (g != num_segs) return PK_ERR_INVALID_ARG;
+  pk_layout L{};
+  L.num_seqs = num_seqs;
+  L.cu_seqlens_q = cu;
+  L.cu_seqlens_k = cu;
+  L.segs = ss.data();
+  L.num_segs = static_cast<int32_t>(ss.size());
+  L.num_kv_rows = cu[num_seqs];
+  return build_plan(L, hq, hkv, d, num_ctas, out);
 }
 
 size_t pk_plan_device_bytes(const pk_plan* p) { return p ? p->layout.bytes : 0; }
@@ -232,6 +341,7 @@ pk_status pk_plan_get_info(const pk_plan* p, pk_plan_info* info) {
   info->num_ctas = p->num_ctas;
   info->num_full_tiles = p->num_full_tiles;
   info->num_partial_tiles = p->num_partial_tiles;
+  info->kv_rows = p->Tk;
   info->visible_pairs = p->visible_pairs;
   info->useful_flops = pk_plan_useful_flops(p);
   return PK_OK;

@@ -276,3 +276,26 @@ def test_row_sampled_call_equals_full_call():
     o2, l2 = _run(pack, q, k, v, rows=rows)
     np.testing.assert_array_equal(o2, out[rows])
     np.testing.assert_array_equal(l2, lse[:, rows])
+
+
+@pytest.mark.parametrize("name", ["tiny", "cfg_pair"])
+def test_row_keys_are_mask_row_sums_and_closed_form(name):
+    """Per-row visible keys: a text row at position x of its sequence sees
+    x + 1 keys, an image row sees every key up to its segment's end; they sum
+    to the pinned pair count."""
+    pack = W.CONFIGS[name]()
+    n = oracle.row_keys(pack.cu_seqlens, pack.segments)
+    want = np.zeros(pack.total_tokens, np.int64)
+    cu = pack.cu_seqlens
+    for s, seq in enumerate(pack.seqs):
+        pos = 0
+        for typ, ln in seq:
+            for x in range(pos, pos + ln):
+                want[cu[s] + x] = (pos + ln) if typ == W.IMAGE else x + 1
+            pos += ln
+    np.testing.assert_array_equal(n, want)
+    assert int(n.sum()) == oracle.visible_pairs(cu, pack.segments)
+    if name == "tiny":
+        for s in range(len(cu) - 1):
+            M = oracle.dense_mask(cu, pack.segments, s)
+            np.testing.assert_array_equal(n[cu[s]:cu[s + 1]], M.sum(axis=1))

@@ -74,14 +74,9 @@ def _chunked(pack, q, k, v, chunk):
     one general call per chunk index; returns the stacked parts."""
     cu = pack.cu_seqlens
     S = len(cu) - 1
-    L = np.diff(cu)
-    C = int(math.ceil(max(L) / chunk))
     o_parts, l_parts = [], []
-    for c in range(C):
-        k_pos0 = np.minimum(c * chunk, L).astype(np.int32)
-        nk = np.clip(L - c * chunk, 0, chunk)
-        cu_k = np.concatenate([[0], np.cumsum(nk)]).astype(np.int32)
-        idx = np.concatenate([np.arange(cu[s] + k_pos0[s], cu[s] + k_pos0[s] + nk[s]) for s in range(S)])
+    for cu_k, k_pos0, rows in W.key_chunks(pack, chunk):
+        idx = torch.as_tensor(rows)
         o, l = oracle.attention_general(q, k[idx], v[idx], cu, cu_k, np.zeros(S, np.int32), k_pos0,
                                         W.seq_segments(pack), pack.hq, pack.hkv, pack.d, pack.scale)
         o_parts.append(o)

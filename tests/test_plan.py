@@ -29,7 +29,8 @@ def _packs():
 
 @pytest.mark.parametrize("pack", _packs(), ids=lambda p: p.name)
 def test_kv_limit_is_the_dense_mask_prefix(pack):
-    """Every row of the dense mask is exactly the key prefix [0, kv_limit]."""
+    """Every row of the dense mask is exactly the key prefix [0, kv_limit]
+    (the limit is an index into the row's own key range)."""
     lim = _plan(pack).kv_limit()
     cu = pack.cu_seqlens
     for s in range(len(cu) - 1):
@@ -38,7 +39,7 @@ def test_kv_limit_is_the_dense_mask_prefix(pack):
             continue
         M = oracle.dense_mask(cu, pack.segments, s)
         L = e - b
-        want = np.arange(L)[None, :] <= (lim[b:e] - b)[:, None]
+        want = np.arange(L)[None, :] <= lim[b:e][:, None]
         np.testing.assert_array_equal(M, want)
 
 
@@ -107,7 +108,7 @@ def test_schedule_balance_and_longest_first():
     pack = W.skewed()
     pl = _plan(pack, 152)
     items, offs = pl.items()
-    cost = np.where(items[:, 6] >= 0, 1.0, 0.55) * (items[:, 4] + 1.3 * (items[:, 3] - items[:, 4]) + 3.0)
+    cost = np.where(items[:, 6] >= 0, 2.0, 1.0) * (items[:, 4] + 1.3 * (items[:, 3] - items[:, 4]) + 3.0)
     loads = np.array([cost[offs[c]:offs[c + 1]].sum() for c in range(len(offs) - 1)])
     # greedy LPT bound: max load <= mean + largest item
     assert loads.max() <= loads.mean() + cost.max() + 1e-9

@@ -259,3 +259,23 @@ def paged_layout(pack: Pack, rng: np.random.Generator, block: int = 128, spare: 
                 if t < int(cu[s + 1]):
                     pool_rows[pb * block + r] = t
     return table, pool_rows
+
+
+def key_chunks(pack: Pack, chunk: int):
+    """Split every sequence's keys into chunks of ``chunk`` positions (ring
+    attention's per-step key blocks).  Returns one (cu_seqlens_k, k_pos0,
+    key_rows) per chunk index: key_rows are the global tokens the chunk's
+    contiguous key tensor holds, sequence by sequence."""
+    cu = pack.cu_seqlens
+    S = len(cu) - 1
+    L = np.diff(cu).astype(np.int64)
+    C = int(-(-int(L.max()) // chunk)) if S and L.max() > 0 else 0
+    out = []
+    for c in range(C):
+        k_pos0 = np.minimum(c * chunk, L).astype(np.int32)
+        nk = np.clip(L - c * chunk, 0, chunk)
+        cu_k = np.concatenate([[0], np.cumsum(nk)]).astype(np.int32)
+        rows = np.concatenate([np.arange(cu[s] + k_pos0[s], cu[s] + k_pos0[s] + nk[s])
+                               for s in range(S)]).astype(np.int64)
+        out.append((cu_k, k_pos0, rows))
+    return out
