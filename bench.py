@@ -38,7 +38,8 @@ METRIC = "packed mixed-mask attention useful TFLOP/s & tokens/s; % of bf16 dense
 NOMINAL_BF16_TFLOPS = 2250.0
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
 KERNEL_SOURCES = ["packed_varlen_masked_gb300/csrc/pk_attn.cu",
-                  "packed_varlen_masked_gb300/csrc/tmem_ops.cuh"]
+                  "packed_varlen_masked_gb300/csrc/tmem_ops.cuh",
+                  "packed_varlen_masked_gb300/csrc/sync.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "pk_attn_fwd_d128_mixed_resolution_traffic.md")
 
 
@@ -275,6 +276,36 @@ def replaced_path(torch, pack, q, k, v, ours_out, steps=3):
     return res
 
 
+def merge_bench(pk, torch, stream, pack, out, lse, parts=2, reps=20):
+    """The LSE merge (ring attention's per-step fold) at the workload's full
+    output size: ``parts`` bf16 partial outputs [T, Hq, d] with their LSEs
+    merged into a bf16 output.  HBM-bound; inputs exceed L2."""
+    peaks = load_peaks()
+    T, H, d = out.shape
+    ps = [(out, lse)] + [(out.clone(), (lse - 0.5).contiguous()) for _ in range(parts - 1)]
+    res_o = torch.empty_like(out)
+    res_l = torch.empty_like(lse)
+    for _ in range(3):
+        pk.lse_merge(ps, out=res_o, lse_out=res_l)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    torch.cuda.synchronize()
+    for a, b in evs:
+        a.record(stream)
+        pk.lse_merge(ps, out=res_o, lse_out=res_l)
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    nbytes = (parts + 1) * (T * H * d * out.element_size() + H * T * 4)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del ps, res_o, res_l
+    return {"kernel": "lse_merge_kernel", "parts": parts, "ms": round(ms, 4),
+            "bytes_per_launch": nbytes,
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                         "peak_source": peaks["source"]}}
+
+
 def sweep(pk, torch, stream, dev):
     """Timing-only pass over every workload (device-generated inputs)."""
     res = {}
@@ -319,6 +350,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-replaced", action="store_true",
                     help="skip timing the replaced padded + explicit-mask SDPA path")
+    ap.add_argument("--no-merge", action="store_true",
+                    help="skip timing the LSE merge at the workload's output size")
+    ap.add_argument("--merge-only", action="store_true",
+                    help="time only the LSE merge (for profiling it alone)")
     ap.add_argument("--requests", type=int, default=8,
                     help="requests in the mixed-resolution pack (x2 CFG branches)")
     args = ap.parse_args()
@@ -359,6 +394,10 @@ def main():
     torch.cuda.synchronize()
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} during warm-up")
+    if args.merge_only:
+        if rank == 0:
+            print(json.dumps({"merge": merge_bench(pk, torch, stream, pack, out, lse)}), flush=True)
+        return
 
     # timed region: K launches, an event pair around each launch on the
     # launching stream (per-launch duration for the roofline)
@@ -424,6 +463,9 @@ def main():
     per_workload = None
     if not args.no_sweep and rank == 0:
         per_workload = sweep(pk, torch, stream, dev)
+    merge = None
+    if not args.no_merge and rank == 0:
+        merge = merge_bench(pk, torch, stream, pack, out, lse)
     replaced = None
     if not args.no_replaced and rank == 0:
         pk.attn_fwd(q, k, v, plan, pack.scale, out=out, lse=lse)
@@ -472,6 +514,7 @@ def main():
                                           "num_partial_tiles")},
         "per_workload": per_workload,
         "replaced_path": replaced,
+        "lse_merge": merge,
     }
     print(json.dumps(line), flush=True)
     if dist is not None:

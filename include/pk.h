@@ -220,6 +220,40 @@ pk_status pk_plan_get_items(const pk_plan* plan, pk_work_item* items,
                             int64_t n_items, int32_t* cta_offsets,
                             int64_t n_offsets);
 
+/* Element types of pk_lse_merge's tensors. */
+typedef enum pk_dtype { PK_DTYPE_BF16 = 0, PK_DTYPE_F32 = 1 } pk_dtype;
+
+/* One partial attention result: o [T][H][d] (dtype) and its natural-log LSE
+ * lse [H][T] fp32, both device memory, as written by pk_attn_fwd over one
+ * block of keys. */
+typedef struct pk_merge_part {
+  const void* o;
+  const float* lse;
+  int32_t dtype;
+} pk_merge_part;
+
+/*
+ * Merge partial attentions over disjoint key sets into the attention over
+ * their union ("Parallelism Acceleration Guide", Ring Attention: each ring
+ * step's block result is folded into the running output):
+ *   lse[h,t]   = ln sum_c exp(lse_c[h,t])
+ *   out[t,h,:] = sum_c exp(lse_c[h,t] - lse[h,t]) * o_c[t,h,:]
+ * A part with lse_c = -inf adds nothing (its o_c is not read); a row with no
+ * finite lse_c gets out = 0 and lse = -inf; a NaN lse_c gives NaN.  LSE
+ * inputs must be finite or -inf.
+ *   parts     : host array of num_parts (1..16) descriptors.
+ *   T, H, d   : rows, heads, head dim; d in {8, 16, 32, 64, 128, 256}.
+ *   out       : device [T][H][d] of out_dtype; lse_out device fp32 [H][T].
+ * out may be the o of a part of the same dtype and lse_out the lse of a
+ * part (in-place accumulation); no other overlap is allowed.  o and out
+ * 16-byte aligned, LSEs 4-byte aligned.  Asynchronous on `stream`.
+ * dev_status: nullable device int32 that receives PK_ERR_TIMEOUT if one of
+ * the kernel's bounded waits runs out (as for pk_attn_fwd).
+ */
+pk_status pk_lse_merge(const pk_merge_part* parts, int32_t num_parts, int32_t T, int32_t H,
+                       int32_t d, void* out, int32_t out_dtype, float* lse_out,
+                       pk_stream_t stream, int32_t* dev_status);
+
 /* Upper bound of every device-side wait, in nanoseconds (default 4e9).
  * Process-wide; applies to launches made after the call. */
 void pk_set_wait_timeout_ns(uint64_t ns);

@@ -7,6 +7,7 @@ fails loudly when the compiled library is missing.
 
     plan = pk.plan(cu_seqlens, segments, hq, hkv, head_dim)   # host planner
     out, lse = pk.attn_fwd(q, k, v, plan, scale)               # one launch
+    out, lse = pk.lse_merge([(o1, l1), (o2, l2)])              # key blocks -> union
 
 ``segments`` is a sequence of (start, length, type) triples in token order,
 type 0 = text (causal), 1 = image (sees its whole own segment).  PyTorch
@@ -18,7 +19,7 @@ from ._native import (PK_ERR_ALIGNMENT, PK_ERR_CUDA, PK_ERR_DEVICE_CHECK,  # noq
                       PK_ERR_INVALID_ARG, PK_ERR_NOT_UPLOADED, PK_ERR_TIMEOUT,
                       PK_ERR_UNSUPPORTED, PK_OK, PKError, lib_path, load)
 from .api import (IMAGE, TEXT, Plan, attn_fwd, attn_fwd_host,  # noqa: F401
-                  debug_wait_timeout, plan, plan_layout, set_wait_timeout_ns)
+                  debug_wait_timeout, lse_merge, plan, plan_layout, set_wait_timeout_ns)
 
-__all__ = ["plan", "plan_layout", "Plan", "attn_fwd", "attn_fwd_host", "PKError", "TEXT", "IMAGE",
+__all__ = ["plan", "plan_layout", "Plan", "attn_fwd", "lse_merge", "attn_fwd_host", "PKError", "TEXT", "IMAGE",
            "set_wait_timeout_ns", "debug_wait_timeout", "load", "lib_path"]

@@ -55,6 +55,14 @@ class PlanInfo(ctypes.Structure):
                 ("useful_flops", ctypes.c_double)]
 
 
+class MergePart(ctypes.Structure):
+    _fields_ = [("o", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("dtype", ctypes.c_int32)]
+
+
+PK_DTYPE_BF16 = 0
+PK_DTYPE_F32 = 1
+
+
 class WorkItem(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("q_start", "q_rows", "kv_start", "n_kt", "n_full", "hq0", "hq1", "hkv")]
@@ -82,6 +90,9 @@ SIGNATURES = {
     "pk_plan_get_kv_limit": (ctypes.c_int, [_vp, _i32p, ctypes.c_int64]),
     "pk_plan_get_items": (ctypes.c_int, [_vp, ctypes.POINTER(WorkItem), ctypes.c_int64,
                                          _i32p, ctypes.c_int64]),
+    "pk_lse_merge": (ctypes.c_int, [ctypes.POINTER(MergePart), ctypes.c_int32, ctypes.c_int32,
+                                    ctypes.c_int32, ctypes.c_int32, _vp, ctypes.c_int32, _vp, _vp,
+                                    _vp]),
     "pk_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
     "pk_debug_wait_timeout": (ctypes.c_int, [_vp, ctypes.c_uint64, _vp]),
 }

@@ -8,7 +8,8 @@ from typing import Optional, Sequence, Tuple
 
 import numpy as np
 
-from ._native import Layout, PlanInfo, Segment, SeqSegment, WorkItem, check, load
+from ._native import (PK_DTYPE_BF16, PK_DTYPE_F32, Layout, MergePart, PlanInfo, Segment,
+                      SeqSegment, WorkItem, check, load)
 
 TEXT = 0
 IMAGE = 1
@@ -233,6 +234,61 @@ def attn_fwd_host(q_host, k_host, v_host, plan: Plan, scale: float, dev_buffers:
         float(scale), ctypes.c_void_p(stream),
         ctypes.c_void_p(status.data_ptr() if status is not None else 0)), "pk_attn_fwd_host")
     return out_host, lse_host
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return PK_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return PK_DTYPE_F32
+    raise TypeError("partial outputs must be bfloat16 or float32")
+
+
+def lse_merge(parts, out=None, lse_out=None, out_dtype=None, status=None,
+              check_status: bool = False):
+    """Merge partial attentions over disjoint key sets (pk_lse_merge).
+
+    ``parts``: sequence of (o [T, H, d], lse [H, T] fp32) CUDA tensors, o bf16
+    or fp32.  Returns (out [T, H, d], lse [H, T]); ``out`` / ``lse_out`` may
+    be a part's own tensors (in-place accumulation).  Runs on the current
+    stream; with ``check_status`` it synchronises and raises on a device-side
+    failure."""
+    import torch
+    parts = list(parts)
+    if not parts:
+        raise ValueError("lse_merge needs at least one part")
+    o0, l0 = parts[0]
+    if o0.dim() != 3:
+        raise ValueError("partial outputs must be [T, H, d]")
+    T, H, d = o0.shape
+    arr = (MergePart * len(parts))()
+    for i, (o, l) in enumerate(parts):
+        if not (o.is_cuda and l.is_cuda) or tuple(o.shape) != (T, H, d) or not o.is_contiguous():
+            raise ValueError(f"part {i}: o must be a contiguous CUDA tensor of shape {(T, H, d)}")
+        if l.dtype != torch.float32 or tuple(l.shape) != (H, T) or not l.is_contiguous():
+            raise ValueError(f"part {i}: lse must be a contiguous float32 CUDA tensor [H, T]")
+        arr[i] = MergePart(o.data_ptr(), l.data_ptr(), _dtype_code(o))
+    if out is None:
+        out = torch.empty(T, H, d, dtype=out_dtype or o0.dtype, device=o0.device)
+    elif tuple(out.shape) != (T, H, d) or not out.is_contiguous() or not out.is_cuda:
+        raise ValueError("out must be a contiguous CUDA tensor [T, H, d]")
+    if lse_out is None:
+        lse_out = torch.empty(H, T, dtype=torch.float32, device=o0.device)
+    elif lse_out.dtype != torch.float32 or tuple(lse_out.shape) != (H, T) or not lse_out.is_contiguous():
+        raise ValueError("lse_out must be a contiguous float32 CUDA tensor [H, T]")
+    if check_status and status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=o0.device)
+    stream = torch.cuda.current_stream(o0.device).cuda_stream
+    check(load().pk_lse_merge(arr, len(parts), T, H, d, ctypes.c_void_p(out.data_ptr()),
+                              _dtype_code(out), ctypes.c_void_p(lse_out.data_ptr()),
+                              ctypes.c_void_p(stream),
+                              ctypes.c_void_p(status.data_ptr() if status is not None else 0)),
+          "pk_lse_merge")
+    if check_status:
+        torch.cuda.current_stream(o0.device).synchronize()
+        check(int(status.item()), "pk_lse_merge (device)")
+    return out, lse_out
 
 
 def set_wait_timeout_ns(ns: int) -> None:

@@ -1,8 +1,9 @@
 """Build the in-tree shared library ``_build/libpk.so`` with nvcc for sm_103a.
 
-Two translation units: the host planner (``csrc/pk_plan.cpp``) and the CUDA
-kernels plus launcher (``csrc/pk_attn.cu``).  They compile in parallel and
-are linked against the shared CUDA runtime (the one PyTorch loads too).
+Three translation units: the host planner (``csrc/pk_plan.cpp``), the
+attention kernel plus launcher (``csrc/pk_attn.cu``) and the LSE merge
+(``csrc/pk_merge.cu``).  They compile in parallel and are linked against the
+shared CUDA runtime (the one PyTorch loads too).
 """
 from __future__ import annotations
 
@@ -18,8 +19,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libpk.so")
-SOURCES = ["pk_plan.cpp", "pk_attn.cu"]
+SOURCES = ["pk_plan.cpp", "pk_attn.cu", "pk_merge.cu"]
 HEADERS = [os.path.join(CSRC, "pk_internal.h"), os.path.join(CSRC, "tmem_ops.cuh"),
+           os.path.join(CSRC, "sync.cuh"),
            os.path.join(INCLUDE, "pk.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -25,6 +25,9 @@ struct PlanImageLayout {
   size_t bytes = 0;
 };
 
+// Upper bound of every device-side wait (pk_set_wait_timeout_ns).
+uint64_t wait_limit_ns();
+
 }  // namespace pk
 
 struct pk_plan {

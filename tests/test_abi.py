@@ -66,3 +66,26 @@ def test_upload_rejects_small_or_misaligned_buffers_before_touching_memory():
     assert n > 0 and n % 256 == 0
     assert lib.pk_plan_upload(plan.handle, 4096, n - 1, None) == pk.PK_ERR_INVALID_ARG
     assert lib.pk_plan_upload(plan.handle, 4096 + 16, n, None) == pk.PK_ERR_ALIGNMENT
+
+
+def test_lse_merge_argument_checks_without_a_device():
+    lib = pk.load()
+    MP = _native.MergePart
+    good = (MP * 17)(*[MP(4096 * (i + 1), 8192 * (i + 1), 0) for i in range(17)])
+    f = lib.pk_lse_merge
+    assert f(None, 1, 4, 2, 64, 4096, 0, 4096, None, None) == pk.PK_ERR_INVALID_ARG
+    assert f(good, 0, 4, 2, 64, 4096, 0, 4096, None, None) == pk.PK_ERR_INVALID_ARG
+    assert f(good, 17, 4, 2, 64, 4096, 0, 4096, None, None) == pk.PK_ERR_UNSUPPORTED
+    for d in (0, 12, 96, 512):
+        assert f(good, 2, 4, 2, d, 4096, 0, 4096, None, None) == pk.PK_ERR_UNSUPPORTED
+    assert f(good, 2, 4, 2, 64, 4096, 2, 4096, None, None) == pk.PK_ERR_INVALID_ARG   # out dtype
+    assert f(good, 2, 4, 2, 64, 4096 + 8, 0, 4096, None, None) == pk.PK_ERR_ALIGNMENT
+    assert f(good, 2, 4, 2, 64, 4096, 0, 4096 + 2, None, None) == pk.PK_ERR_ALIGNMENT
+    bad = (MP * 2)(MP(4096, 8192, 0), MP(4096 + 4, 8192, 0))
+    assert f(bad, 2, 4, 2, 64, 4096, 0, 4096, None, None) == pk.PK_ERR_ALIGNMENT
+    bad = (MP * 2)(MP(4096, 8192, 0), MP(4096, 8192, 7))
+    assert f(bad, 2, 4, 2, 64, 4096, 0, 4096, None, None) == pk.PK_ERR_INVALID_ARG
+    bad = (MP * 2)(MP(4096, 8192, 0), MP(0, 8192, 0))
+    assert f(bad, 2, 4, 2, 64, 4096, 0, 4096, None, None) == pk.PK_ERR_INVALID_ARG
+    # zero rows: nothing to launch
+    assert f(good, 2, 0, 2, 64, 4096, 0, 4096, None, None) == pk.PK_OK
