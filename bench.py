@@ -51,21 +51,33 @@ def kernel_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def load_peaks():
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+def _flatten(d, prefix=""):
+    for k, v in d.items():
+        key = f"{prefix}.{k}" if prefix else str(k)
+        if isinstance(v, dict):
+            yield from _flatten(v, key)
+        elif isinstance(v, (int, float)) and not isinstance(v, bool):
+            yield key.lower(), float(v)
+
+
+def load_peaks(path=None):
+    """Roofline denominators: the measured copy bandwidth and bf16 GEMM rate
+    in MEASURED_PEAKS.json (burst and sustained), else the fallback."""
+    path = path or os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         try:
             with open(path) as f:
-                d = json.load(f)
-            tf = d.get("bf16_tflops") or d.get("bf16_tflops_burst")
-            gb = d.get("hbm_gbs")
-            if tf and gb:
-                return {"bf16_tflops": float(tf), "hbm_gbs": float(gb),
-                        "bf16_tflops_sustained": d.get("bf16_tflops_sustained"),
-                        "source": "measured"}
+                flat = dict(_flatten(json.load(f)))
+            burst = [v for k, v in flat.items() if "bf16" in k and "tflop" in k
+                     and "sustain" not in k]
+            sus = [v for k, v in flat.items() if "bf16" in k and "tflop" in k and "sustain" in k]
+            hbm = [v for k, v in flat.items() if ("hbm" in k or "copy" in k) and "gb" in k]
+            if burst and hbm:
+                return {"bf16_tflops": burst[0], "hbm_gbs": hbm[0],
+                        "bf16_tflops_sustained": sus[0] if sus else None, "source": "measured"}
         except Exception:
             pass
-    return dict(FALLBACK_PEAKS, source="fallback")
+    return dict(FALLBACK_PEAKS, bf16_tflops_sustained=1700.0, source="fallback")
 
 
 def load_traffic():
@@ -101,6 +113,12 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
+            # nvidia-smi takes a moment to start: let its first sample arrive
+            # so that the samples cover the whole timed region
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 3.0 and self.proc.poll() is None:
+                time.sleep(0.02)
+            self.lines.clear()
         except Exception:
             self.proc = None
         return self
@@ -142,7 +160,25 @@ def dist_setup(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus and "WORLD_SIZE" in os.environ:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
     return world, rank, local
+
+
+def max_over_ranks(value: float, dist, device) -> float:
+    """The slowest rank's time: every rank's timed region is bracketed by
+    barriers, so the job's step time is the maximum."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, units_per_rank: float, steps: int, total_ms: float) -> float:
+    """Whole-job rate: the units every rank processed over the max time."""
+    return world * units_per_rank * steps / (total_ms * 1e-3)
 
 
 def reference_arm(args, pack, rank, world):
@@ -306,6 +342,44 @@ def merge_bench(pk, torch, stream, pack, out, lse, parts=2, reps=20):
                          "peak_source": peaks["source"]}}
 
 
+def layouts_bench(pk, torch, stream, dev, pack, q, k, v, reps=10):
+    """The workload's image tokens as queries over the whole sequence's keys
+    (text prefix handed over from the autoregressive stage), with contiguous
+    and with paged keys (shuffled 128-row block pool)."""
+    rows, cu_q, q_pos0 = W.prefix_split(pack)
+    cu = pack.cu_seqlens
+    z = np.zeros(len(cu) - 1, np.int32)
+    sg = W.seq_segments(pack)
+    qs = q[torch.as_tensor(rows, device=dev)].contiguous()
+    table, pool_rows = W.paged_layout(pack, np.random.default_rng(0))
+    src = torch.as_tensor(np.maximum(pool_rows, 0), device=dev)
+    kp, vp = k[src].contiguous(), v[src].contiguous()
+    res = {}
+    for name, kk, vv, kw in (("prefix", k, v, {}),
+                             ("prefix_paged", kp, vp,
+                              {"block_table": table, "num_kv_rows": kp.shape[0]})):
+        pl = pk.plan_layout(cu_q, cu, sg, pack.hq, pack.hkv, pack.d, q_pos0=q_pos0, k_pos0=z,
+                            device=dev, **kw)
+        out = torch.empty_like(qs)
+        lse = torch.empty(pack.hq, qs.shape[0], dtype=torch.float32, device=dev)
+        for _ in range(3):
+            pk.attn_fwd(qs, kk, vv, pl, pack.scale, out=out, lse=lse)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            pk.attn_fwd(qs, kk, vv, pl, pack.scale, out=out, lse=lse)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        res[name] = {"ms": round(ms, 4), "useful_tflops": round(pl.useful_flops / ms / 1e9, 1),
+                     "query_tokens": int(qs.shape[0]), "key_rows": int(kk.shape[0])}
+        del pl, out, lse
+    del qs, kp, vp
+    torch.cuda.empty_cache()
+    return res
+
+
 def sweep(pk, torch, stream, dev):
     """Timing-only pass over every workload (device-generated inputs)."""
     res = {}
@@ -341,7 +415,7 @@ def sweep(pk, torch, stream, dev):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mixed_resolution", choices=sorted(W.CONFIGS))
@@ -420,15 +494,12 @@ def main():
     launch_ms = [a.elapsed_time(b) for a, b in evs]
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} in the timed region")
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist, dev)
 
     flops = plan.useful_flops
     ms_step = total_ms / args.steps
-    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
-    tokens_per_s = world * pack.total_tokens * args.steps / (total_ms * 1e-3)
+    value = job_throughput(world, flops, args.steps, total_ms) / 1e12
+    tokens_per_s = job_throughput(world, pack.total_tokens, args.steps, total_ms)
 
     # end to end through the public host-buffer call
     e2e = None
@@ -450,12 +521,8 @@ def main():
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        e_ms = e0.elapsed_time(e1)
-        if dist is not None:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * flops * args.steps / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+        e2e = {"value": job_throughput(world, flops, args.steps, e_ms) / 1e12, "unit": "TFLOP/s",
                "ms_per_step": e_ms / args.steps,
                "h2d_bytes_per_step": int((q.numel() + k.numel() + v.numel()) * 2),
                "d2h_bytes_per_step": int(out.numel() * 2 + lse.numel() * 4)}
@@ -463,6 +530,9 @@ def main():
     per_workload = None
     if not args.no_sweep and rank == 0:
         per_workload = sweep(pk, torch, stream, dev)
+    layouts = None
+    if not args.no_sweep and rank == 0:
+        layouts = layouts_bench(pk, torch, stream, dev, pack, q, k, v)
     merge = None
     if not args.no_merge and rank == 0:
         merge = merge_bench(pk, torch, stream, pack, out, lse)
@@ -503,6 +573,8 @@ def main():
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": traffic,
+                     "frac_of_sustained": (round(achieved / peaks["bf16_tflops_sustained"], 4)
+                                           if peaks.get("bf16_tflops_sustained") else None),
                      "peak_source": peaks["source"] + " (bf16 burst)",
                      "kernel": "pk_attn_fwd_kernel<128>", "launch_ms_mean": round(avg_launch_ms, 4),
                      "launch_ms_min": round(min(launch_ms), 4)},
@@ -514,6 +586,7 @@ def main():
                                           "num_partial_tiles")},
         "per_workload": per_workload,
         "replaced_path": replaced,
+        "layouts": layouts,
         "lse_merge": merge,
     }
     print(json.dumps(line), flush=True)
