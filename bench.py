@@ -39,7 +39,8 @@ NOMINAL_BF16_TFLOPS = 2250.0
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
 KERNEL_SOURCES = ["packed_varlen_masked_gb300/csrc/pk_attn.cu",
                   "packed_varlen_masked_gb300/csrc/tmem_ops.cuh",
-                  "packed_varlen_masked_gb300/csrc/sync.cuh"]
+                  "packed_varlen_masked_gb300/csrc/sync.cuh",
+                  "packed_varlen_masked_gb300/csrc/attn_common.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "pk_attn_fwd_d128_mixed_resolution_traffic.md")
 
 

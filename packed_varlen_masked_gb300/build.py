@@ -21,7 +21,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libpk.so")
 SOURCES = ["pk_plan.cpp", "pk_attn.cu", "pk_merge.cu"]
 HEADERS = [os.path.join(CSRC, "pk_internal.h"), os.path.join(CSRC, "tmem_ops.cuh"),
-           os.path.join(CSRC, "sync.cuh"),
+           os.path.join(CSRC, "sync.cuh"), os.path.join(CSRC, "attn_common.cuh"),
            os.path.join(INCLUDE, "pk.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -1,0 +1,183 @@
+// Device helpers shared by the attention kernels: tcgen05 instruction and
+// shared-memory descriptors, MMA issue, TMA copies with L2 policies, the
+// packed fp32 / bf16 arithmetic of the softmax, and the launch parameters.
+#pragma once
+#include <cuda.h>
+#include <cstdint>
+
+#include "pk_internal.h"
+
+namespace pk {
+namespace dev {
+
+constexpr int kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 64 bf16
+// Growth of a row's maximum (log2 units) tolerated before O and l are
+// rescaled: exponentials run against a stale maximum while it lags by less.
+constexpr float kRescaleLog2 = 16.0f;
+
+
+// Instruction descriptors of tcgen05.mma kind::f16 (dense, f32 accumulate,
+// bf16 A and B): bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16),
+// 10-12 B format (1 = bf16), 15/16 A/B major (0 = K-major, 1 = MN-major),
+// 17-22 N >> 3, 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor (tcgen05 form): start address, leading and
+// stride byte offsets (all >> 4), version 1 at bit 46, 128-byte swizzle (2)
+// at bits 61-63.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+// Same copy with an L2 eviction-priority policy (from createpolicy).
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar, int c0, int c1, int c2,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+// D(tmem) (+)= A(smem desc) * B(smem desc)
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D(tmem) (+)= A(tmem) * B(smem desc)
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// Three-input maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// Packed pair arithmetic: (d0, d1) = (a0, a1) * (b0, b1) + (c0, c1).
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
+                                     float c0, float c1) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+// (d0, d1) += (a0, a1)
+__device__ __forceinline__ void acc2(float& d0, float& d1, float a0, float a1) {
+  asm("{\n\t.reg .b64 ra, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rd, {%0, %1};\n\t"
+      "add.rn.f32x2 rd, rd, ra;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1));
+}
+// {lo -> bits 0-15, hi -> bits 16-31}, round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+struct KernelParams {
+  const pk_work_item* items;
+  const int32_t* cta_offsets;
+  const int32_t* kv_limit;       // per query row: last visible key of its range, -1 none
+  const int32_t* block_table;    // paged keys: physical 128-row block of each key tile; else null
+  uint8_t* out;   // bf16 [T][hq][D]
+  float* lse;     // [hq][T]
+  int32_t* status;
+  int32_t T;
+  int32_t hq;
+  float scale_log2;  // softmax scale * log2(e)
+  uint64_t wait_limit_ns;
+};
+
+// First key/value row of key tile j of a work item: contiguous keys start
+// at kv_start; paged keys take the block of the item's key range from the
+// block table (blocks are one key tile, 128 rows).
+__device__ __forceinline__ int key_tile_row(const KernelParams& p, const pk_work_item& w, int j) {
+  return p.block_table ? p.block_table[w.kv_start + j] * 128 : w.kv_start + j * 128;
+}
+
+// S(tmem) = Q K^T over the head dimension: D/16 MMAs of 128x128x16.  Both
+// tiles are K-major with 128-byte swizzle: row r of a 64-column box sits at
+// r*128 bytes, 8-row groups 1024 bytes apart; the k-th 16-column step starts
+// 32*(k%4) bytes into box k/4.  q_desc / k_desc describe the tiles' first
+// byte; a step only adds its byte offset / 16 to the start-address field.
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
+  constexpr uint32_t idesc = make_idesc(128, 128, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t off = (uint64_t)(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
+    mma_ss(d_tmem, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// O(tmem) (+)= P V: 8 MMAs of 128 x D x 16.  P (bf16 pairs) is read from
+// TMEM, 8 columns per 16 keys.  V is MN-major with 128-byte swizzle: 16 keys
+// span 2048 bytes, and the second 64-column box (D = 128) is 16384 bytes on.
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
+                                         bool accumulate) {
+  constexpr uint32_t idesc = make_idesc(128, D, true);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    mma_ts(d_tmem, p_tmem + (uint32_t)kk * 8u, v_desc + (uint64_t)(kk * (2048 >> 4)), idesc,
+           (accumulate || kk > 0) ? 1u : 0u);
+}
+
+}  // namespace dev
+}  // namespace pk
