@@ -77,6 +77,15 @@ def _load():
         lib.pko_row_keys.argtypes = [i32p, ctypes.c_int32, i32p, ctypes.c_int32,
                                      ctypes.POINTER(ctypes.c_int64)]
         lib.pko_row_keys.restype = ctypes.c_int
+        lib.pko_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        lib.pko_e4m3_to_double.restype = ctypes.c_double
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        lib.pko_attention_e4m3.argtypes = [u8p, ctypes.c_double, u8p, ctypes.c_double, u16p,
+                                           i32p, ctypes.c_int32, i32p, ctypes.c_int32,
+                                           ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                           ctypes.c_double, i32p, ctypes.c_int32, f64p, f64p,
+                                           ctypes.c_int32]
+        lib.pko_attention_e4m3.restype = ctypes.c_int
         lib.pko_attention.argtypes = [u16p, u16p, u16p, i32p, ctypes.c_int32, i32p,
                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                       ctypes.c_int32, ctypes.c_double, i32p,
@@ -159,6 +168,47 @@ def row_keys(cu_seqlens, segments) -> np.ndarray:
     if rc:
         raise ValueError("oracle: invalid descriptors")
     return out[: int(cu[-1])]
+
+
+def e4m3_to_double(code: int) -> float:
+    """Value of an FP8 E4M3 code (OCP 8-bit format, decoded by definition)."""
+    return float(_load().pko_e4m3_to_double(ctypes.c_uint8(int(code))))
+
+
+def _codes(x) -> np.ndarray:
+    """FP8 codes as a contiguous uint8 array (torch float8/uint8 tensor or array)."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            return np.ascontiguousarray(x.contiguous().view(torch.uint8).cpu().numpy())
+    except ImportError:
+        pass
+    return np.ascontiguousarray(np.asarray(x, dtype=np.uint8))
+
+
+def attention_e4m3(q8, q_scale: float, k8, k_scale: float, v, cu_seqlens, segments, hq: int,
+                   hkv: int, d: int, scale: float, rows=None, nthreads: int = 0):
+    """fp64 packed masked attention with E4M3 q and k (codes + one scale each)
+    and bf16 v.  Returns (out [R, hq, d], lse [hq, R]) like ``attention``."""
+    qb, kb, vb = _codes(q8), _codes(k8), _bits(v)
+    cu = _i32(cu_seqlens)
+    sg = _segs_array(segments)
+    T = int(cu[-1])
+    if rows is None:
+        R, rp = T, None
+    else:
+        rr = _i32(rows)
+        R, rp = rr.size, _ptr(rr, ctypes.c_int32)
+    out = np.zeros((R, hq, d), dtype=np.float64)
+    lse = np.zeros((hq, R), dtype=np.float64)
+    rc = _load().pko_attention_e4m3(
+        _ptr(qb, ctypes.c_uint8), float(q_scale), _ptr(kb, ctypes.c_uint8), float(k_scale),
+        _ptr(vb, ctypes.c_uint16), _ptr(cu, ctypes.c_int32), len(cu) - 1,
+        _ptr(sg, ctypes.c_int32), sg.shape[0], hq, hkv, d, float(scale), rp, R,
+        _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double), int(nthreads))
+    if rc:
+        raise ValueError(f"oracle: invalid arguments (code {rc})")
+    return out, lse
 
 
 def attention(q, k, v, cu_seqlens, segments, hq: int, hkv: int, d: int,

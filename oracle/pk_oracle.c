@@ -449,3 +449,104 @@ void pko_lse_merge(const double* o_parts, const double* lse_parts, int32_t C, in
       }
     }
 }
+
+/* ------------------------------------------------------------------------
+ * FP8 queries and keys.  The pages quantise linear layers to FP8 (e.g.
+ * "HunyuanImage-3.0-Instruct ...", FP8 checkpoints; "MiniMax H3-Image on Vera
+ * Rubin", MXFP8 GEMMs); this entry is the attention of the same packed
+ * sequences when q and k arrive as FP8 E4M3 codes with one scale each.
+ *
+ * E4M3 (the OCP 8-bit floating point format): 1 sign bit, 4 exponent bits
+ * with bias 7, 3 mantissa bits; exponent field 0 encodes subnormals
+ * m/8 * 2^-6; there are no infinities, and S.1111.111 is NaN.
+ */
+double pko_e4m3_to_double(uint8_t code) {
+  const int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+  if (e == 15 && m == 7) return NAN;
+  const double mag = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+  return sign ? -mag : mag;
+}
+
+/* One query row over its sequence: q value = e4m3(q8) * q_scale, k value =
+ * e4m3(k8) * k_scale, v bf16; the same score, LSE and output definitions as
+ * the bf16 entry.  A row with no visible key gets o = 0, lse = -inf. */
+static void attend_row_e4m3(const uint8_t* q_row, double q_scale, const uint8_t* k_seq,
+                            double k_scale, const uint16_t* v_seq, const uint8_t* mrow,
+                            int32_t L, int32_t Hq, int32_t Hkv, int32_t d, double scale,
+                            double* out_row, double* lse, int64_t lse_stride, double* s_buf) {
+  const int32_t group = Hq / Hkv;
+  for (int32_t h = 0; h < Hq; ++h) {
+    const int32_t g = h / group;
+    double mx = -INFINITY;
+    for (int32_t j = 0; j < L; ++j) {
+      if (!mrow[j]) continue;
+      double dot = 0.0;
+      for (int32_t c = 0; c < d; ++c)
+        dot += (pko_e4m3_to_double(q_row[(size_t)h * d + c]) * q_scale) *
+               (pko_e4m3_to_double(k_seq[((size_t)j * Hkv + g) * d + c]) * k_scale);
+      s_buf[j] = scale * dot;
+      if (s_buf[j] > mx) mx = s_buf[j];
+    }
+    double* o = out_row + (size_t)h * d;
+    for (int32_t c = 0; c < d; ++c) o[c] = 0.0;
+    if (mx == -INFINITY) {
+      lse[(size_t)h * lse_stride] = -INFINITY;
+      continue;
+    }
+    double z = 0.0;
+    for (int32_t j = 0; j < L; ++j)
+      if (mrow[j]) z += exp(s_buf[j] - mx);
+    const double l = mx + log(z);
+    lse[(size_t)h * lse_stride] = l;
+    for (int32_t j = 0; j < L; ++j) {
+      if (!mrow[j]) continue;
+      const double w = exp(s_buf[j] - l);
+      const uint16_t* vr = v_seq + ((size_t)j * Hkv + g) * d;
+      for (int32_t c = 0; c < d; ++c) o[c] += w * pko_bf16_to_double(vr[c]);
+    }
+  }
+}
+
+/* Packed attention with E4M3 q [T][Hq][d] and k [T][Hkv][d] (codes), their
+ * scales, bf16 v.  rows == NULL: every row, out [T][Hq][d], lse [Hq][T];
+ * else the n_rows listed rows, out [n_rows][Hq][d], lse [Hq][n_rows]. */
+int pko_attention_e4m3(const uint8_t* q8, double q_scale, const uint8_t* k8, double k_scale,
+                       const uint16_t* v, const int32_t* cu, int32_t num_seqs,
+                       const int32_t* segs, int32_t num_segs, int32_t Hq, int32_t Hkv,
+                       int32_t d, double scale, const int32_t* rows, int32_t n_rows,
+                       double* out, double* lse, int32_t nthreads) {
+  int rc = pko_validate(cu, num_seqs, segs, num_segs);
+  if (rc) return rc;
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return 10;
+  const int32_t T = cu[num_seqs];
+  const int32_t n = rows ? n_rows : T;
+  for (int32_t r = 0; rows && r < n_rows; ++r)
+    if (rows[r] < 0 || rows[r] >= T) return 11;
+  int32_t* seg_of = segment_of_tokens(T, segs, num_segs);
+  int32_t Lmax = 1;
+  for (int32_t s = 0; s < num_seqs; ++s)
+    if (cu[s + 1] - cu[s] > Lmax) Lmax = cu[s + 1] - cu[s];
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#endif
+#pragma omp parallel
+  {
+    double* s_buf = (double*)malloc(sizeof(double) * (size_t)Lmax);
+    uint8_t* mrow = (uint8_t*)malloc((size_t)Lmax);
+#pragma omp for schedule(dynamic, 1)
+    for (int32_t r = 0; r < n; ++r) {
+      const int32_t t = rows ? rows[r] : r;
+      int32_t s = 0;
+      while (cu[s + 1] <= t) ++s;
+      const int32_t b = cu[s], L = cu[s + 1] - cu[s];
+      mask_row(b, L, t - b, seg_of, segs, mrow);
+      attend_row_e4m3(q8 + (size_t)t * Hq * d, q_scale, k8 + (size_t)b * Hkv * d, k_scale,
+                      v + (size_t)b * Hkv * d, mrow, L, Hq, Hkv, d, scale,
+                      out + (size_t)r * Hq * d, lse + r, n, s_buf);
+    }
+    free(s_buf);
+    free(mrow);
+  }
+  free(seg_of);
+  return 0;
+}

@@ -279,3 +279,15 @@ def key_chunks(pack: Pack, chunk: int):
                                for s in range(S)]).astype(np.int64)
         out.append((cu_k, k_pos0, rows))
     return out
+
+
+def quantize_e4m3(x):
+    """Per-tensor FP8 E4M3 quantisation of a bf16/fp32 torch tensor: the scale
+    maps the tensor's largest magnitude to 448 (E4M3's largest finite
+    value); returns (codes uint8 tensor, scale float).  Input preparation for
+    the FP8 path; torch's float8_e4m3fn conversion rounds to nearest even."""
+    import torch
+    amax = float(x.float().abs().max())
+    scale = amax / 448.0 if amax > 0 else 1.0
+    codes = (x.float() / scale).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes, scale
