@@ -381,6 +381,32 @@ def layouts_bench(pk, torch, stream, dev, pack, q, k, v, reps=10):
     return res
 
 
+def fp8_bench(pk, torch, stream, dev, pack, q, k, v, reps=10):
+    """The workload with FP8 E4M3 queries and keys (per-tensor scales) and
+    bf16 values."""
+    q8, qs = W.quantize_e4m3(q)
+    k8, ks = W.quantize_e4m3(k)
+    plan = pk.plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty(pack.hq, pack.total_tokens, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        pk.attn_fwd_fp8(q8, qs, k8, ks, v, plan, pack.scale, out=out, lse=lse)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(reps):
+        pk.attn_fwd_fp8(q8, qs, k8, ks, v, plan, pack.scale, out=out, lse=lse)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    res = {"kernel": "pk_attn_fwd_kernel<128, fp8 q/k>", "ms": round(ms, 4),
+           "useful_tflops": round(plan.useful_flops / ms / 1e9, 1),
+           "qk_bytes_saved": int(q.numel() + k.numel())}
+    del q8, k8, out, lse, plan
+    torch.cuda.empty_cache()
+    return res
+
+
 def sweep(pk, torch, stream, dev):
     """Timing-only pass over every workload (device-generated inputs)."""
     res = {}
@@ -531,9 +557,10 @@ def main():
     per_workload = None
     if not args.no_sweep and rank == 0:
         per_workload = sweep(pk, torch, stream, dev)
-    layouts = None
+    layouts = fp8 = None
     if not args.no_sweep and rank == 0:
         layouts = layouts_bench(pk, torch, stream, dev, pack, q, k, v)
+        fp8 = fp8_bench(pk, torch, stream, dev, pack, q, k, v)
     merge = None
     if not args.no_merge and rank == 0:
         merge = merge_bench(pk, torch, stream, pack, out, lse)
@@ -588,6 +615,7 @@ def main():
         "per_workload": per_workload,
         "replaced_path": replaced,
         "layouts": layouts,
+        "fp8_qk": fp8,
         "lse_merge": merge,
     }
     print(json.dumps(line), flush=True)

@@ -188,6 +188,23 @@ pk_status pk_attn_fwd(const pk_plan* plan, const void* q, const void* k,
                       pk_stream_t stream, int32_t* dev_status);
 
 /*
+ * FP8 variant: queries and keys as FP8 E4M3 codes (1 sign, 4 exponent bits
+ * with bias 7, 3 mantissa bits; the OCP 8-bit format), one dequantisation
+ * scale each, values bf16.  The scores are scale * q_scale * k_scale *
+ * (q8 . k8), computed on the tensor cores in FP8 with fp32 accumulation;
+ * softmax, P V, out and lse as for pk_attn_fwd.
+ *   q8 [Tq][hq][128], k8 [Tk][hkv][128] uint8 codes, 16-byte aligned;
+ *   q_scale, k_scale: finite and > 0.
+ * head_dim must be 128 (else PK_ERR_UNSUPPORTED).  The pages quantise their
+ * linear layers to FP8 ("HunyuanImage-3.0-Instruct ...", FP8 checkpoints;
+ * "MiniMax H3-Image on Vera Rubin", MXFP8 GEMMs); this is the attention of
+ * such a model with FP8 queries and keys.
+ */
+pk_status pk_attn_fwd_fp8(const pk_plan* plan, const void* q8, float q_scale, const void* k8,
+                          float k_scale, const void* v, void* out, float* lse, float scale,
+                          pk_stream_t stream, int32_t* dev_status);
+
+/*
  * End-to-end variant for callers holding host buffers: copies q, k, v from
  * host memory into the caller's device buffers, runs pk_attn_fwd, and copies
  * out and lse back into host memory, all on `stream` (asynchronous; pinned

@@ -212,6 +212,49 @@ def attn_fwd(q, k, v, plan: Plan, scale: Optional[float] = None, out=None, lse=N
     return out, lse
 
 
+def attn_fwd_fp8(q8, q_scale: float, k8, k_scale: float, v, plan: Plan,
+                 scale: Optional[float] = None, out=None, lse=None, status=None,
+                 check_status: bool = False):
+    """Attention with FP8 E4M3 queries and keys (pk_attn_fwd_fp8).
+
+    q8 [T, hq, 128] and k8 [Tk, hkv, 128]: CUDA uint8 or float8_e4m3fn
+    tensors of E4M3 codes, dequantised by q_scale / k_scale; v bf16
+    [Tk, hkv, 128].  Returns (out bf16 [T, hq, 128], lse fp32 [hq, T])."""
+    import torch
+    T, hq, hkv, d = plan.total_tokens, plan.hq, plan.hkv, plan.head_dim
+    Tk = plan.kv_rows
+    for name, t, shape in (("q8", q8, (T, hq, d)), ("k8", k8, (Tk, hkv, d))):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.element_size() != 1:
+            raise TypeError(f"{name} must be a CUDA tensor of 1-byte E4M3 codes")
+        if tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous with shape {shape}")
+    _check_tensor(v, "v", (Tk, hkv, d))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty(T, hq, d, dtype=torch.bfloat16, device=v.device)
+    else:
+        _check_tensor(out, "out", (T, hq, d))
+    if lse is None:
+        lse = torch.empty(hq, T, dtype=torch.float32, device=v.device)
+    elif lse.dtype != torch.float32 or tuple(lse.shape) != (hq, T) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 tensor of shape [hq, T]")
+    if check_status and status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=v.device)
+    stream = torch.cuda.current_stream(v.device).cuda_stream
+    check(plan._lib.pk_attn_fwd_fp8(plan.handle, ctypes.c_void_p(q8.data_ptr()), float(q_scale),
+                                    ctypes.c_void_p(k8.data_ptr()), float(k_scale),
+                                    ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+                                    ctypes.c_void_p(lse.data_ptr()), float(scale),
+                                    ctypes.c_void_p(stream),
+                                    ctypes.c_void_p(status.data_ptr() if status is not None else 0)),
+          "pk_attn_fwd_fp8")
+    if check_status:
+        torch.cuda.current_stream(v.device).synchronize()
+        check(int(status.item()), "pk_attn_fwd_fp8 (device)")
+    return out, lse
+
+
 def attn_fwd_host(q_host, k_host, v_host, plan: Plan, scale: float, dev_buffers: dict,
                   out_host, lse_host, status=None):
     """End-to-end call from host buffers (ideally pinned): copies q/k/v to the

@@ -25,6 +25,12 @@ __host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool b_mn_major)
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// kind::f8f6f4 with A and B both FP8 E4M3 (format code 0 in bits 7-9 and
+// 10-12), f32 accumulate, both K-major.
+__host__ __device__ constexpr uint32_t make_idesc_e4m3(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 // Shared-memory matrix descriptor (tcgen05 form): start address, leading and
 // stride byte offsets (all >> 4), version 1 at bit 46, 128-byte swizzle (2)
 // at bits 61-63.
@@ -82,6 +88,15 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D(tmem) (+)= A(smem desc) * B(smem desc), FP8 operands.
+__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -151,18 +166,23 @@ __device__ __forceinline__ int key_tile_row(const KernelParams& p, const pk_work
   return p.block_table ? p.block_table[w.kv_start + j] * 128 : w.kv_start + j * 128;
 }
 
-// S(tmem) = Q K^T over the head dimension: D/16 MMAs of 128x128x16.  Both
-// tiles are K-major with 128-byte swizzle: row r of a 64-column box sits at
-// r*128 bytes, 8-row groups 1024 bytes apart; the k-th 16-column step starts
-// 32*(k%4) bytes into box k/4.  q_desc / k_desc describe the tiles' first
-// byte; a step only adds its byte offset / 16 to the start-address field.
-template <int D>
+// S(tmem) = Q K^T over the head dimension: MMAs of 128x128 and K = 16
+// (bf16) or 32 (FP8) elements, i.e. 32 bytes of every row per step.  Both
+// tiles are K-major with 128-byte swizzle: row r of a box sits at r*128
+// bytes, 8-row groups 1024 bytes apart; the k-th step starts 32*(k%4) bytes
+// into box k/4.  q_desc / k_desc describe the tiles' first byte; a step only
+// adds its byte offset / 16 to the start-address field.
+template <int D, bool F8 = false>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
-  constexpr uint32_t idesc = make_idesc(128, 128, false);
+  constexpr uint32_t idesc = F8 ? make_idesc_e4m3(128, 128) : make_idesc(128, 128, false);
+  constexpr int kSteps = F8 ? D / 32 : D / 16;
 #pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
+  for (int kk = 0; kk < kSteps; ++kk) {
     const uint64_t off = (uint64_t)(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
-    mma_ss(d_tmem, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
+    if (F8)
+      mma_ss_f8(d_tmem, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
+    else
+      mma_ss(d_tmem, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 

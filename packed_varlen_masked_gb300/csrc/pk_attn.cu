@@ -53,23 +53,30 @@ namespace dev {
 
 constexpr int kThreads = 256;
 constexpr uint32_t kTmemCols = 512;
-template <int D>
+// F8: queries and keys are FP8 E4M3 (one byte per element), values bf16.
+template <int D, bool F8 = false>
 struct Cfg {
-  static constexpr int kHalves = D / 64;
-  static constexpr int kTileBytes = 128 * D * 2;
-  // Rings: two query tiles (the next unit's loads during this one), three
-  // key tiles, two value tiles.  Shared memory stays above half an SM, so
-  // exactly one CTA (and one 512-column TMEM allocation) lives on each SM.
-  static constexpr int kKStages = D == 128 ? 3 : 4;
-  static constexpr int kVStages = D == 128 ? 2 : 4;
+  // Query/key tiles: 128 rows in boxes of 128-byte rows (64 bf16 or 128
+  // FP8 elements); value tiles: 128 rows of D bf16 in 64-column boxes.
+  static constexpr int kQKElemsPerBox = F8 ? 128 : 64;
+  static constexpr int kQKBoxes = D / kQKElemsPerBox;
+  static constexpr int kQKTileBytes = 128 * D * (F8 ? 1 : 2);
+  static constexpr int kVHalves = D / 64;
+  static constexpr int kVTileBytes = 128 * D * 2;
+  // Rings: two query tiles (the next unit's loads during this one), and key
+  // and value tiles.  Shared memory stays above half an SM, so exactly one
+  // CTA (and one 512-column TMEM allocation) lives on each SM.
+  static constexpr int kKStages = F8 ? 4 : (D == 128 ? 3 : 4);
+  static constexpr int kVStages = F8 ? 3 : (D == 128 ? 2 : 4);
   // TMEM columns: S double buffer, P double buffer (bf16 pairs), O.
   static constexpr uint32_t kColS0 = 0;    // S(t) in [128*(t%2), +128)
   static constexpr uint32_t kColP0 = 256;  // P(t) in [256 + 64*(t%2), +64)
   static constexpr uint32_t kColO = 384;   // O in [384, 384 + D)
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = 2 * kTileBytes;
-  static constexpr int kOffV = kOffK + kKStages * kTileBytes;
-  static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
+  static constexpr int kOffK = 2 * kQKTileBytes;
+  static constexpr int kOffV = kOffK + kKStages * kQKTileBytes;
+  static constexpr int kOffBar = kOffV + kVStages * kVTileBytes;
+  static_assert(!F8 || D == 128, "FP8 queries/keys need head_dim 128");
   // barrier indices
   static constexpr int kQFull = 0, kQEmpty = 2;  // [2] each
   static constexpr int kKFull = 4, kKEmpty = kKFull + kKStages;
@@ -116,11 +123,11 @@ struct UnitIter {
 // the ring of key tiles.  Keys and values are re-read by the other query
 // heads of the group and by neighbouring query tiles, so they are kept in L2
 // (evict-last); a query tile is read once (evict-first).
-template <int D>
+template <int D, bool F8>
 __device__ void producer_qk_role(const KernelParams& p, const CUtensorMap* tm_q,
                                  const CUtensorMap* tm_k, uint32_t sbase, int beg, int end,
                                  const WaitCtl& wc) {
-  using C = Cfg<D>;
+  using C = Cfg<D, F8>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
   const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
   uint32_t g = 0, u = 0, k_armed = 0, q_armed = 0;
@@ -129,21 +136,22 @@ __device__ void producer_qk_role(const KernelParams& p, const CUtensorMap* tm_q,
     const pk_work_item& w = ui.w;
     const uint32_t qb = u & 1u;
     if (!(ok = mbar_wait(bar(C::kQEmpty + qb), ((u >> 1) & 1u) ^ 1u, wc))) break;
-    mbar_arrive_expect_tx(bar(C::kQFull + qb), C::kTileBytes);
+    mbar_arrive_expect_tx(bar(C::kQFull + qb), C::kQKTileBytes);
     ++q_armed;
 #pragma unroll
-    for (int h = 0; h < C::kHalves; ++h)
-      tma_load_3d_hint(sbase + C::kOffQ + qb * C::kTileBytes + h * kBoxBytes, tm_q,
-                       bar(C::kQFull + qb), h * 64, ui.head(), w.q_start, stream);
+    for (int h = 0; h < C::kQKBoxes; ++h)
+      tma_load_3d_hint(sbase + C::kOffQ + qb * C::kQKTileBytes + h * kBoxBytes, tm_q,
+                       bar(C::kQFull + qb), h * C::kQKElemsPerBox, ui.head(), w.q_start, stream);
     for (int j = 0; j < w.n_kt; ++j, ++g) {
       const uint32_t st = g % C::kKStages, ph = (g / C::kKStages) & 1u;
       if (!(ok = mbar_wait(bar(C::kKEmpty + st), ph ^ 1u, wc))) break;
-      mbar_arrive_expect_tx(bar(C::kKFull + st), C::kTileBytes);
+      mbar_arrive_expect_tx(bar(C::kKFull + st), C::kQKTileBytes);
       ++k_armed;
 #pragma unroll
-      for (int h = 0; h < C::kHalves; ++h)
-        tma_load_3d_hint(sbase + C::kOffK + st * C::kTileBytes + h * kBoxBytes, tm_k,
-                         bar(C::kKFull + st), h * 64, w.hkv, key_tile_row(p, w, j), keep);
+      for (int h = 0; h < C::kQKBoxes; ++h)
+        tma_load_3d_hint(sbase + C::kOffK + st * C::kQKTileBytes + h * kBoxBytes, tm_k,
+                         bar(C::kKFull + st), h * C::kQKElemsPerBox, w.hkv, key_tile_row(p, w, j),
+                         keep);
     }
   }
   if (!ok) {
@@ -163,10 +171,10 @@ __device__ void producer_qk_role(const KernelParams& p, const CUtensorMap* tm_q,
 
 // V producer (one thread of another warp): the ring of value tiles, so that
 // a value tile waiting for its stage never holds back the next key tile.
-template <int D>
+template <int D, bool F8>
 __device__ void producer_v_role(const KernelParams& p, const CUtensorMap* tm_v, uint32_t sbase,
                                 int beg, int end, const WaitCtl& wc) {
-  using C = Cfg<D>;
+  using C = Cfg<D, F8>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
   const uint64_t keep = l2_policy_evict_last();
   uint32_t g = 0, v_armed = 0;
@@ -176,11 +184,11 @@ __device__ void producer_v_role(const KernelParams& p, const CUtensorMap* tm_v, 
     for (int j = 0; j < w.n_kt; ++j, ++g) {
       const uint32_t st = g % C::kVStages, ph = (g / C::kVStages) & 1u;
       if (!(ok = mbar_wait(bar(C::kVEmpty + st), ph ^ 1u, wc))) break;
-      mbar_arrive_expect_tx(bar(C::kVFull + st), C::kTileBytes);
+      mbar_arrive_expect_tx(bar(C::kVFull + st), C::kVTileBytes);
       ++v_armed;
 #pragma unroll
-      for (int h = 0; h < C::kHalves; ++h)
-        tma_load_3d_hint(sbase + C::kOffV + st * C::kTileBytes + h * kBoxBytes, tm_v,
+      for (int h = 0; h < C::kVHalves; ++h)
+        tma_load_3d_hint(sbase + C::kOffV + st * C::kVTileBytes + h * kBoxBytes, tm_v,
                          bar(C::kVFull + st), h * 64, w.hkv, key_tile_row(p, w, j), keep);
     }
   }
@@ -201,14 +209,14 @@ __device__ void producer_v_role(const KernelParams& p, const CUtensorMap* tm_v, 
 // S issuer (warp 1): S(t) needs K(t) loaded and S buffer t%2 released by the
 // softmax of tile t-2, so it runs up to two tiles ahead of the softmax and
 // the tensor pipe computes S(t+2) while the softmax works on tile t.
-template <int D>
+template <int D, bool F8>
 __device__ void mma_s_role(const KernelParams& p, uint32_t sbase, uint32_t tmem, int beg,
                            int end, const WaitCtl& wc) {
-  using C = Cfg<D>;
+  using C = Cfg<D, F8>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
   const uint64_t q_desc0 = sdesc(sbase + C::kOffQ, 16, 1024);
   const uint64_t k_desc0 = sdesc(sbase + C::kOffK, 16, 1024);
-  constexpr uint64_t kTileDesc = (uint64_t)(C::kTileBytes >> 4);
+  constexpr uint64_t kTileDesc = (uint64_t)(C::kQKTileBytes >> 4);
   uint32_t t = 0, u = 0;
   bool ok = true;
   for (UnitIter ui(p.items, beg, end); ui.valid() && ok; ui.next(), ++u) {
@@ -219,7 +227,7 @@ __device__ void mma_s_role(const KernelParams& p, uint32_t sbase, uint32_t tmem,
       if (!(ok = mbar_wait(bar(C::kKFull + kst), (t / C::kKStages) & 1u, wc))) break;
       if (t >= 2 && !(ok = mbar_wait(bar(C::kSFree + b), ((t >> 1) - 1u) & 1u, wc))) break;
       tc_fence_after();
-      issue_qk<D>(tmem + C::kColS0 + b * 128u, q_desc0 + qb * kTileDesc,
+      issue_qk<D, F8>(tmem + C::kColS0 + b * 128u, q_desc0 + qb * kTileDesc,
                   k_desc0 + kst * kTileDesc);
       tc_commit(bar(C::kSFull + b));
       tc_commit(bar(C::kKEmpty + kst));
@@ -233,13 +241,13 @@ __device__ void mma_s_role(const KernelParams& p, uint32_t sbase, uint32_t tmem,
 
 // P V issuer (warp 3): O (+)= P(t) V(t) needs V(t) loaded and P(t) written;
 // a unit's first product overwrites O, after the previous unit's O was read.
-template <int D>
+template <int D, bool F8>
 __device__ void mma_pv_role(const KernelParams& p, uint32_t sbase, uint32_t tmem, int beg,
                             int end, const WaitCtl& wc) {
-  using C = Cfg<D>;
+  using C = Cfg<D, F8>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
   const uint64_t v_desc0 = sdesc(sbase + C::kOffV, kBoxBytes, 1024);
-  constexpr uint64_t kTileDesc = (uint64_t)(C::kTileBytes >> 4);
+  constexpr uint64_t kTileDesc = (uint64_t)(C::kVTileBytes >> 4);
   uint32_t t = 0, u = 0;
   bool ok = true;
   for (UnitIter ui(p.items, beg, end); ui.valid() && ok; ui.next(), ++u) {
@@ -260,10 +268,10 @@ __device__ void mma_pv_role(const KernelParams& p, uint32_t sbase, uint32_t tmem
 }
 
 // Softmax warpgroup (warps 4-7): thread r owns row r of S, P and O in TMEM.
-template <int D>
+template <int D, bool F8>
 __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint32_t tmem, int beg,
                              int end, const WaitCtl& wc) {
-  using C = Cfg<D>;
+  using C = Cfg<D, F8>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;  // TMEM lane quadrant this warp may access
@@ -419,12 +427,12 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint32_t tme
   }
 }
 
-template <int D>
+template <int D, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     pk_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const KernelParams p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, F8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1 KB alignment
@@ -475,19 +483,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtl wc{abort_flag, p.status, p.wait_limit_ns};
 
   if (warp == 0) {
-    if (lane == 0) producer_qk_role<D>(p, &tm_q, &tm_k, sbase, beg, end, wc);
+    if (lane == 0) producer_qk_role<D, F8>(p, &tm_q, &tm_k, sbase, beg, end, wc);
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) mma_s_role<D>(p, sbase, tmem, beg, end, wc);
+    if (lane == 0) mma_s_role<D, F8>(p, sbase, tmem, beg, end, wc);
     __syncwarp();
   } else if (warp == 2) {
-    if (lane == 0) producer_v_role<D>(p, &tm_v, sbase, beg, end, wc);
+    if (lane == 0) producer_v_role<D, F8>(p, &tm_v, sbase, beg, end, wc);
     __syncwarp();
   } else if (warp == 3) {
-    if (lane == 0) mma_pv_role<D>(p, sbase, tmem, beg, end, wc);
+    if (lane == 0) mma_pv_role<D, F8>(p, sbase, tmem, beg, end, wc);
     __syncwarp();
   } else {
-    softmax_role<D>(p, sbase, tmem, beg, end, wc);
+    softmax_role<D, F8>(p, sbase, tmem, beg, end, wc);
   }
 
   tc_fence_before();
@@ -549,14 +557,19 @@ EncodeTiledFn get_encode_fn() {
 
 // [T][H][D] bf16 viewed as a 3-D tensor (D, H, T); boxes of 64 x 1 x 128
 // with 128-byte swizzle; rows past T read as zeros.
-bool make_map(CUtensorMap* m, const void* base, int H, int T, int D) {
+// (d, H, T) view of a [T][H][d] tensor of 2-byte (bf16) or 1-byte (FP8)
+// elements, boxes of 128 bytes x 1 head x 128 rows.
+bool make_map(CUtensorMap* m, const void* base, int H, int T, int D, int elem_bytes = 2) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
+  const cuuint64_t eb = (cuuint64_t)elem_bytes;
   const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
-  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
-  const cuuint32_t box[3] = {64, 1, 128};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * eb, (cuuint64_t)H * D * eb};
+  const cuuint32_t box[3] = {(cuuint32_t)(128 / elem_bytes), 1, 128};
   const cuuint32_t estr[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+  const CUtensorMapDataType dt =
+      elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -585,15 +598,19 @@ pk_status check_device() {
   return verdict[dev] == 1 ? PK_OK : PK_ERR_UNSUPPORTED;
 }
 
-template <int D>
+// scale: the softmax scale of the scores as the MMA computes them (for FP8
+// queries/keys it includes their dequantisation scales).
+template <int D, bool F8 = false>
 pk_status launch(const pk_plan* plan, const void* q, const void* k, const void* v, void* out,
                  float* lse, float scale, cudaStream_t stream, int32_t* dev_status) {
-  using C = pk::dev::Cfg<D>;
+  using C = pk::dev::Cfg<D, F8>;
   CUtensorMap tq, tk, tv;
-  if (!make_map(&tq, q, plan->hq, plan->T, D) || !make_map(&tk, k, plan->hkv, plan->Tk, D) ||
+  const int qk_bytes = F8 ? 1 : 2;
+  if (!make_map(&tq, q, plan->hq, plan->T, D, qk_bytes) ||
+      !make_map(&tk, k, plan->hkv, plan->Tk, D, qk_bytes) ||
       !make_map(&tv, v, plan->hkv, plan->Tk, D))
     return PK_ERR_CUDA;
-  if (cudaFuncSetAttribute(pk::dev::pk_attn_fwd_kernel<D>,
+  if (cudaFuncSetAttribute(pk::dev::pk_attn_fwd_kernel<D, F8>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kSmemBytes) != cudaSuccess) {
     cudaGetLastError();
@@ -613,8 +630,8 @@ pk_status launch(const pk_plan* plan, const void* q, const void* k, const void* 
   kp.hq = plan->hq;
   kp.scale_log2 = scale * 1.4426950408889634f;
   kp.wait_limit_ns = g_wait_limit_ns.load();
-  pk::dev::pk_attn_fwd_kernel<D><<<plan->num_ctas, pk::dev::kThreads, C::kSmemBytes, stream>>>(
-      tq, tk, tv, kp);
+  pk::dev::pk_attn_fwd_kernel<D, F8>
+      <<<plan->num_ctas, pk::dev::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, kp);
   if (cudaGetLastError() != cudaSuccess) return PK_ERR_CUDA;
   return PK_OK;
 }
@@ -649,6 +666,28 @@ pk_status pk_attn_fwd(const pk_plan* plan, const void* q, const void* k, const v
   if (plan->head_dim == 128) return launch<128>(plan, q, k, v, out, lse, scale, s, dev_status);
   if (plan->head_dim == 64) return launch<64>(plan, q, k, v, out, lse, scale, s, dev_status);
   return PK_ERR_UNSUPPORTED;
+}
+
+pk_status pk_attn_fwd_fp8(const pk_plan* plan, const void* q8, float q_scale, const void* k8,
+                          float k_scale, const void* v, void* out, float* lse, float scale,
+                          pk_stream_t stream, int32_t* dev_status) {
+  if (plan == nullptr) return PK_ERR_INVALID_ARG;
+  const float s_all = scale * q_scale * k_scale;
+  if (!(scale > 0.f) || !(q_scale > 0.f) || !(k_scale > 0.f) || !std::isfinite(s_all) ||
+      !(s_all > 0.f))
+    return PK_ERR_INVALID_ARG;
+  if (plan->head_dim != 128) return PK_ERR_UNSUPPORTED;
+  if (plan->T == 0 || plan->items.empty()) return PK_OK;
+  if (plan->dev == nullptr) return PK_ERR_NOT_UPLOADED;
+  if (plan->Tk <= 0) return PK_ERR_INVALID_ARG;
+  if (!q8 || !k8 || !v || !out || !lse) return PK_ERR_INVALID_ARG;
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return PK_ERR_ALIGNMENT;
+  pk_status st = check_device();
+  if (st != PK_OK) return st;
+  return launch<128, true>(plan, q8, k8, v, out, lse, s_all, reinterpret_cast<cudaStream_t>(stream),
+                           dev_status);
 }
 
 pk_status pk_attn_fwd_host(const pk_plan* plan, const void* q_host, const void* k_host,

@@ -89,3 +89,16 @@ def test_lse_merge_argument_checks_without_a_device():
     assert f(bad, 2, 4, 2, 64, 4096, 0, 4096, None, None) == pk.PK_ERR_INVALID_ARG
     # zero rows: nothing to launch
     assert f(good, 2, 0, 2, 64, 4096, 0, 4096, None, None) == pk.PK_OK
+
+
+def test_fp8_entry_argument_checks_without_a_device():
+    lib = pk.load()
+    plan = pk.Plan([0, 300], [(0, 300, 1)], 4, 2, 128, num_ctas=4, upload=False)
+    f = lib.pk_attn_fwd_fp8
+    assert f(None, 16, 1.0, 16, 1.0, 16, 16, 16, 0.1, None, None) == pk.PK_ERR_INVALID_ARG
+    for qs, ks, sc in ((0.0, 1.0, 0.1), (1.0, -1.0, 0.1), (1.0, 1.0, float("nan")),
+                       (1e30, 1e30, 1e30)):
+        assert f(plan.handle, 16, qs, 16, ks, 16, 16, 16, sc, None, None) == pk.PK_ERR_INVALID_ARG
+    assert f(plan.handle, 16, 1.0, 16, 1.0, 16, 16, 16, 0.1, None, None) == pk.PK_ERR_NOT_UPLOADED
+    p64 = pk.Plan([0, 300], [(0, 300, 1)], 4, 2, 64, num_ctas=4, upload=False)
+    assert f(p64.handle, 16, 1.0, 16, 1.0, 16, 16, 16, 0.1, None, None) == pk.PK_ERR_UNSUPPORTED
