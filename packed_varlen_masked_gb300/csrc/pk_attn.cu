@@ -8,6 +8,9 @@
 // heads.  The host planner turns the mask into a per-token key limit and a
 // list of 128-row query tiles, each visiting a prefix of 128-key tiles that
 // are either fully visible (no mask math) or partial (per-element compare).
+// Queries and keys are bf16, or FP8 E4M3 (F8: S = Q K^T on kind::f8f6f4,
+// one dequantisation scale each folded into the softmax scale); values, P
+// and the output are bf16 in both.
 //
 // Kernel organisation (one persistent CTA per SM, 8 warps).  The CTA runs
 // its work items' query heads ("units") one after another; a unit is a
