@@ -219,6 +219,44 @@ pk_status pk_attn_fwd_host(const pk_plan* plan, const void* q_host,
                            float* lse_dev, float scale, pk_stream_t stream,
                            int32_t* dev_status);
 
+/*
+ * Host-buffer pipeline: successive steps whose inputs and outputs live in
+ * host memory (pinned memory makes the copies asynchronous).  Each step's
+ * host -> device copy of q, k, v, its pk_attn_fwd and its device -> host
+ * copy of out and lse run on three streams of the pipeline, ordered by
+ * events, so one step's copies overlap the neighbouring steps' kernels.
+ * Device memory is the caller's: num_slots (1..8) sets of buffers of the
+ * pk_attn_fwd shapes for `plan`, used round robin; a slot is refilled only
+ * after its previous kernel has read it and its previous outputs are out.
+ * The pipeline creates and owns its streams and events, no device memory.
+ */
+typedef struct pk_dev_slot {
+  void* q;
+  void* k;
+  void* v;
+  void* out;
+  float* lse;
+} pk_dev_slot;
+
+typedef struct pk_pipeline pk_pipeline;
+
+/* slots: host array of num_slots descriptors (copied).  The plan must stay
+ * alive and uploaded while the pipeline is used. */
+pk_status pk_pipeline_create(const pk_plan* plan, const pk_dev_slot* slots, int32_t num_slots,
+                             pk_pipeline** out);
+/* Enqueue one step (asynchronous).  The host buffers must stay valid and
+ * unmodified until pk_pipeline_sync returns (or the step's copy-out stream
+ * has passed it). */
+pk_status pk_pipeline_submit(pk_pipeline* pipe, const void* q_host, const void* k_host,
+                             const void* v_host, void* out_host, float* lse_host, float scale,
+                             int32_t* dev_status);
+/* Wait for every submitted step. */
+pk_status pk_pipeline_sync(pk_pipeline* pipe);
+/* The pipeline's streams: 0 copy-in, 1 compute, 2 copy-out (NULL otherwise). */
+pk_stream_t pk_pipeline_stream(const pk_pipeline* pipe, int32_t which);
+/* Waits for outstanding work, then frees the streams and events. */
+void pk_pipeline_destroy(pk_pipeline* pipe);
+
 void pk_plan_destroy(pk_plan* plan);
 
 const char* pk_status_string(pk_status status);

@@ -18,8 +18,10 @@ from __future__ import annotations
 from ._native import (PK_ERR_ALIGNMENT, PK_ERR_CUDA, PK_ERR_DEVICE_CHECK,  # noqa: F401
                       PK_ERR_INVALID_ARG, PK_ERR_NOT_UPLOADED, PK_ERR_TIMEOUT,
                       PK_ERR_UNSUPPORTED, PK_OK, PKError, lib_path, load)
-from .api import (IMAGE, TEXT, Plan, attn_fwd, attn_fwd_fp8, attn_fwd_host,  # noqa: F401
-                  debug_wait_timeout, lse_merge, plan, plan_layout, set_wait_timeout_ns)
+from .api import (IMAGE, TEXT, HostPipeline, Plan, attn_fwd, attn_fwd_fp8,  # noqa: F401
+                  attn_fwd_host, debug_wait_timeout, lse_merge, plan, plan_layout,
+                  set_wait_timeout_ns)
 
-__all__ = ["plan", "plan_layout", "Plan", "attn_fwd", "attn_fwd_fp8", "lse_merge", "attn_fwd_host", "PKError", "TEXT", "IMAGE",
-           "set_wait_timeout_ns", "debug_wait_timeout", "load", "lib_path"]
+__all__ = ["plan", "plan_layout", "Plan", "attn_fwd", "attn_fwd_fp8", "attn_fwd_host",
+           "lse_merge", "HostPipeline", "PKError", "TEXT", "IMAGE", "set_wait_timeout_ns",
+           "debug_wait_timeout", "load", "lib_path"]

@@ -63,6 +63,11 @@ PK_DTYPE_BF16 = 0
 PK_DTYPE_F32 = 1
 
 
+class DevSlot(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p)]
+
+
 class WorkItem(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("q_start", "q_rows", "kv_start", "n_kt", "n_full", "hq0", "hq1", "hkv")]
@@ -86,6 +91,12 @@ SIGNATURES = {
     "pk_attn_fwd_host": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                         _vp, ctypes.c_float, _vp, _vp]),
     "pk_plan_destroy": (None, [_vp]),
+    "pk_pipeline_create": (ctypes.c_int, [_vp, ctypes.POINTER(DevSlot), ctypes.c_int32,
+                                          ctypes.POINTER(_vp)]),
+    "pk_pipeline_submit": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp]),
+    "pk_pipeline_sync": (ctypes.c_int, [_vp]),
+    "pk_pipeline_stream": (_vp, [_vp, ctypes.c_int32]),
+    "pk_pipeline_destroy": (None, [_vp]),
     "pk_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "pk_plan_useful_flops": (ctypes.c_double, [_vp]),
     "pk_plan_get_info": (ctypes.c_int, [_vp, ctypes.POINTER(PlanInfo)]),

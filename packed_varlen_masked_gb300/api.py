@@ -8,8 +8,8 @@ from typing import Optional, Sequence, Tuple
 
 import numpy as np
 
-from ._native import (PK_DTYPE_BF16, PK_DTYPE_F32, Layout, MergePart, PlanInfo, Segment,
-                      SeqSegment, WorkItem, check, load)
+from ._native import (PK_DTYPE_BF16, PK_DTYPE_F32, DevSlot, Layout, MergePart, PlanInfo,
+                      Segment, SeqSegment, WorkItem, check, load)
 
 TEXT = 0
 IMAGE = 1
@@ -332,6 +332,68 @@ def lse_merge(parts, out=None, lse_out=None, out_dtype=None, status=None,
         torch.cuda.current_stream(o0.device).synchronize()
         check(int(status.item()), "pk_lse_merge (device)")
     return out, lse_out
+
+
+class HostPipeline:
+    """Successive steps from host buffers with the copies of one step
+    overlapping the kernels of its neighbours (pk_pipeline_*).
+
+    ``slots`` device buffer sets (dicts of CUDA tensors 'q', 'k', 'v', 'out',
+    'lse' of the pk_attn_fwd shapes; allocated here when omitted) are used
+    round robin.  ``submit`` enqueues one step; ``sync`` waits for all."""
+
+    def __init__(self, plan: Plan, num_slots: int = 2, slots=None, device=None):
+        import torch
+        self._lib = plan._lib
+        self.plan = plan
+        dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        if slots is None:
+            T, Tk, hq, hkv, d = plan.total_tokens, plan.kv_rows, plan.hq, plan.hkv, plan.head_dim
+            e = lambda *sh: torch.empty(*sh, dtype=torch.bfloat16, device=dev)
+            slots = [{"q": e(T, hq, d), "k": e(Tk, hkv, d), "v": e(Tk, hkv, d), "out": e(T, hq, d),
+                      "lse": torch.empty(hq, T, dtype=torch.float32, device=dev)}
+                     for _ in range(num_slots)]
+        self.slots = slots
+        arr = (DevSlot * len(slots))()
+        for i, sl in enumerate(slots):
+            arr[i] = DevSlot(sl["q"].data_ptr(), sl["k"].data_ptr(), sl["v"].data_ptr(),
+                             sl["out"].data_ptr(), sl["lse"].data_ptr())
+        self._h = ctypes.c_void_p()
+        check(self._lib.pk_pipeline_create(plan.handle, arr, len(slots), ctypes.byref(self._h)),
+              "pk_pipeline_create")
+
+    def submit(self, q_host, k_host, v_host, out_host, lse_host, scale: Optional[float] = None,
+               status=None) -> None:
+        if scale is None:
+            scale = 1.0 / math.sqrt(self.plan.head_dim)
+        for name, t in (("q_host", q_host), ("k_host", k_host), ("v_host", v_host),
+                        ("out_host", out_host), ("lse_host", lse_host)):
+            if t.is_cuda or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous host tensor")
+        check(self._lib.pk_pipeline_submit(
+            self._h, ctypes.c_void_p(q_host.data_ptr()), ctypes.c_void_p(k_host.data_ptr()),
+            ctypes.c_void_p(v_host.data_ptr()), ctypes.c_void_p(out_host.data_ptr()),
+            ctypes.c_void_p(lse_host.data_ptr()), float(scale),
+            ctypes.c_void_p(status.data_ptr() if status is not None else 0)), "pk_pipeline_submit")
+
+    def sync(self) -> None:
+        check(self._lib.pk_pipeline_sync(self._h), "pk_pipeline_sync")
+
+    def stream(self, which: int):
+        """torch view of the pipeline's stream: 0 copy-in, 1 compute, 2 copy-out."""
+        import torch
+        return torch.cuda.ExternalStream(self._lib.pk_pipeline_stream(self._h, which))
+
+    def close(self) -> None:
+        if getattr(self, "_h", None) is not None and self._h.value:
+            self._lib.pk_pipeline_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def set_wait_timeout_ns(ns: int) -> None:

@@ -1,8 +1,8 @@
 """Build the in-tree shared library ``_build/libpk.so`` with nvcc for sm_103a.
 
-Three translation units: the host planner (``csrc/pk_plan.cpp``), the
-attention kernel plus launcher (``csrc/pk_attn.cu``) and the LSE merge
-(``csrc/pk_merge.cu``).  They compile in parallel and are linked against the
+Four translation units: the host planner (``csrc/pk_plan.cpp``), the
+attention kernel plus launcher (``csrc/pk_attn.cu``), the LSE merge
+(``csrc/pk_merge.cu``) and the host-buffer pipeline (``csrc/pk_pipeline.cpp``).  They compile in parallel and are linked against the
 shared CUDA runtime (the one PyTorch loads too).
 """
 from __future__ import annotations
@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libpk.so")
-SOURCES = ["pk_plan.cpp", "pk_attn.cu", "pk_merge.cu"]
+SOURCES = ["pk_plan.cpp", "pk_attn.cu", "pk_merge.cu", "pk_pipeline.cpp"]
 HEADERS = [os.path.join(CSRC, "pk_internal.h"), os.path.join(CSRC, "tmem_ops.cuh"),
            os.path.join(CSRC, "sync.cuh"), os.path.join(CSRC, "attn_common.cuh"),
            os.path.join(INCLUDE, "pk.h")]

@@ -102,3 +102,22 @@ def test_fp8_entry_argument_checks_without_a_device():
     assert f(plan.handle, 16, 1.0, 16, 1.0, 16, 16, 16, 0.1, None, None) == pk.PK_ERR_NOT_UPLOADED
     p64 = pk.Plan([0, 300], [(0, 300, 1)], 4, 2, 64, num_ctas=4, upload=False)
     assert f(p64.handle, 16, 1.0, 16, 1.0, 16, 16, 16, 0.1, None, None) == pk.PK_ERR_UNSUPPORTED
+
+
+def test_pipeline_argument_checks_without_a_device():
+    lib = pk.load()
+    out = ctypes.c_void_p()
+    plan = pk.Plan([0, 300], [(0, 300, 1)], 4, 2, 128, num_ctas=4, upload=False)
+    S = _native.DevSlot
+    good = (S * 2)(S(16, 16, 16, 16, 16), S(16, 16, 16, 16, 16))
+    assert lib.pk_pipeline_create(None, good, 2, ctypes.byref(out)) == pk.PK_ERR_INVALID_ARG
+    assert lib.pk_pipeline_create(plan.handle, None, 2, ctypes.byref(out)) == pk.PK_ERR_INVALID_ARG
+    assert lib.pk_pipeline_create(plan.handle, good, 0, ctypes.byref(out)) == pk.PK_ERR_INVALID_ARG
+    assert lib.pk_pipeline_create(plan.handle, good, 9, ctypes.byref(out)) == pk.PK_ERR_INVALID_ARG
+    bad = (S * 1)(S(16, 16, 0, 16, 16))
+    assert lib.pk_pipeline_create(plan.handle, bad, 1, ctypes.byref(out)) == pk.PK_ERR_INVALID_ARG
+    assert out.value is None
+    assert lib.pk_pipeline_submit(None, 16, 16, 16, 16, 16, 0.1, None) == pk.PK_ERR_INVALID_ARG
+    assert lib.pk_pipeline_sync(None) == pk.PK_ERR_INVALID_ARG
+    assert lib.pk_pipeline_stream(None, 0) is None
+    lib.pk_pipeline_destroy(None)
