@@ -7,7 +7,11 @@ fails loudly when the compiled library is missing.
 
     plan = pk.plan(cu_seqlens, segments, hq, hkv, head_dim)   # host planner
     out, lse = pk.attn_fwd(q, k, v, plan, scale)               # one launch
+    out, lse = pk.attn_fwd_fp8(q8, qs, k8, ks, v, plan, scale) # E4M3 queries/keys
     out, lse = pk.lse_merge([(o1, l1), (o2, l2)])              # key blocks -> union
+    plan = pk.plan_layout(cu_q, cu_k, seq_segments, hq, hkv, head_dim,
+                          q_pos0=..., k_pos0=..., block_table=...)  # prefix / paged / chunks
+    pipe = pk.HostPipeline(plan); pipe.submit(qh, kh, vh, oh, lh)   # host buffers
 
 ``segments`` is a sequence of (start, length, type) triples in token order,
 type 0 = text (causal), 1 = image (sees its whole own segment).  PyTorch

@@ -1,5 +1,6 @@
-"""User-facing calls: ``plan`` / ``Plan`` and ``attn_fwd`` (argument
-marshalling around the C ABI; all computation happens in the library)."""
+"""User-facing calls (argument marshalling around the C ABI; all computation
+happens in the library): ``plan`` / ``plan_layout`` / ``Plan``, ``attn_fwd``,
+``attn_fwd_fp8``, ``attn_fwd_host``, ``HostPipeline`` and ``lse_merge``."""
 from __future__ import annotations
 
 import ctypes
@@ -176,8 +177,9 @@ def attn_fwd(q, k, v, plan: Plan, scale: Optional[float] = None, out=None, lse=N
              status=None, check_status: bool = False):
     """Packed mixed-mask attention forward on the current CUDA stream.
 
-    q [T, hq, d], k and v [T, hkv, d] bf16 CUDA tensors.  Returns
-    (out bf16 [T, hq, d], lse fp32 [hq, T]).  With ``check_status`` the call
+    q [T, hq, d], k and v [Tk, hkv, d] bf16 CUDA tensors (Tk = T for a
+    plan from ``plan``; the key rows or pool rows for ``plan_layout``).
+    Returns (out bf16 [T, hq, d], lse fp32 [hq, T]).  With ``check_status`` the call
     synchronises and raises if the kernel reported a device-side failure.
     """
     import torch
