@@ -44,17 +44,32 @@ TEXT = 0
 IMAGE = 1
 
 
+def _fingerprint() -> str:
+    """Host architecture + source bytes: a library built on another machine
+    type or from another source is rebuilt, whatever the file times say."""
+    import hashlib
+    import platform
+    h = hashlib.sha256(platform.machine().encode())
+    with open(_SRC, "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()
+
+
 def build(force: bool = False) -> str:
     """Compile ``pk_oracle.c`` into ``_build/libpk_oracle.so`` with gcc."""
     os.makedirs(_LIB_DIR, exist_ok=True)
-    if (not force and os.path.exists(_LIB)
-            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
-        return _LIB
+    stamp = _LIB + ".stamp"
+    if not force and os.path.exists(_LIB) and os.path.exists(stamp):
+        with open(stamp) as f:
+            if f.read().strip() == _fingerprint():
+                return _LIB
     tmp = _LIB + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
            "-o", tmp, _SRC, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB)
+    with open(stamp, "w") as f:
+        f.write(_fingerprint())
     return _LIB
 
 

@@ -7,7 +7,9 @@ shared CUDA runtime (the one PyTorch loads too).
 """
 from __future__ import annotations
 
+import hashlib
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -36,12 +38,25 @@ def nvcc() -> str:
     return found
 
 
+STAMP = LIB + ".stamp"
+
+
+def _fingerprint() -> str:
+    """Host architecture + the bytes of every source and header: a library
+    built elsewhere (another machine type) or from other sources is stale,
+    whatever the file times say."""
+    h = hashlib.sha256(platform.machine().encode())
+    for p in [os.path.join(CSRC, s) for s in SOURCES] + HEADERS + [__file__]:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def _stale() -> bool:
-    if not os.path.exists(LIB):
+    if not os.path.exists(LIB) or not os.path.exists(STAMP):
         return True
-    t = os.path.getmtime(LIB)
-    deps = [os.path.join(CSRC, s) for s in SOURCES] + HEADERS + [__file__]
-    return any(os.path.getmtime(p) > t for p in deps)
+    with open(STAMP) as f:
+        return f.read().strip() != _fingerprint()
 
 
 def build(force: bool = False, verbose_ptxas: bool = False) -> str:
@@ -59,13 +74,19 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
         subprocess.run(cmd, check=True)
         return obj
 
-    with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(compile_one, SOURCES))
+    objs = [os.path.join(BUILD, src + f".{os.getpid()}.o") for src in SOURCES]
     tmp = LIB + f".tmp{os.getpid()}"
-    subprocess.run([cc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs], check=True)
-    for o in objs:
-        os.remove(o)
-    os.replace(tmp, LIB)
+    try:
+        with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+            list(ex.map(compile_one, SOURCES))
+        subprocess.run([cc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs], check=True)
+        os.replace(tmp, LIB)
+    finally:
+        for o in objs + [tmp]:
+            if os.path.exists(o):
+                os.remove(o)
+    with open(STAMP, "w") as f:
+        f.write(_fingerprint())
     return LIB
 
 

@@ -193,3 +193,24 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     torch.cuda.synchronize()
     assert int(status.item()) == pk.PK_ERR_TIMEOUT
     _full(W.Pack("after-timeout", [[(W.TEXT, 20), (W.IMAGE, 150)]], hq=2, hkv=1, d=64, seed=2))
+
+
+def test_one_64k_token_sequence_sampled():
+    """A single 65,536-token sequence (1,024 text + 64,512 image): 512 key
+    tiles per query tile, the longest rows any workload here has."""
+    pack = W.Pack("64k", [[(W.TEXT, 1024), (W.IMAGE, 64512)]], hq=8, hkv=2, d=128, seed=21)
+    q, k, v = W.make_qkv(pack)
+    rows = np.array([0, 1, 127, 128, 1023, 1024, 1025, 30000, 65407, 65535], np.int32)
+    out_o, lse_o = oracle.attention(q, k, v, pack.cu_seqlens, pack.segments, pack.hq, pack.hkv,
+                                    pack.d, pack.scale, rows=rows)
+    out_g, lse_g = _gpu(pack, q, k, v)
+    _compare(pack, out_g, lse_g, out_o, lse_o, rows=rows)
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(64, 8, 128), (16, 1, 64), (1, 1, 128)])
+def test_head_layouts(hq, hkv, d):
+    """Wide GQA groups (8 and 16 query heads per key/value head) and a single
+    head."""
+    pack = W.Pack(f"heads-{hq}-{hkv}-{d}", [[(W.TEXT, 77), (W.IMAGE, 300)], [(W.IMAGE, 129)]],
+                  hq=hq, hkv=hkv, d=d, seed=hq + hkv + d)
+    _full(pack)
