@@ -182,6 +182,20 @@ def job_throughput(world: int, units_per_rank: float, steps: int, total_ms: floa
     return world * units_per_rank * steps / (total_ms * 1e-3)
 
 
+def workload_config(pack, world: int, useful_flops: float) -> dict:
+    """The bench line's config, identical for both arms: the workload, its
+    per-step useful FLOPs (each arm counts them its own way: the planner
+    here, the oracle's visible keys in the reference arm) and the L2 rule."""
+    T = pack.total_tokens
+    q_mb = T * pack.hq * pack.d * 2 / 1e6
+    kv_mb = 2 * T * pack.hkv * pack.d * 2 / 1e6
+    return dict(pack.describe(), parallelism=f"replicas{world}",
+                l2="inputs larger than L2 (q %.0f MB, k+v %.0f MB)" % (q_mb, kv_mb),
+                useful_flops_per_step=float(useful_flops),
+                padded_dense_mask_flops_per_step=4.0 * pack.d * pack.hq * len(pack.seqs)
+                * pack.max_seqlen ** 2)
+
+
 def reference_arm(args, pack, rank, world):
     """fp64 CPU oracle, as it stands, on bounded row samples of the pack."""
     if rank != 0:
@@ -215,7 +229,7 @@ def reference_arm(args, pack, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total_t / len(times), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": dict(pack.describe(), l2="CPU run"),
+        "config": workload_config(pack, world, 4.0 * pack.d * pack.hq * keys.sum()),
         "tokens_per_s": (n_rows * len(times)) / total_t,
         "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": f"{n_rows} uniformly drawn query rows (all {pack.hq} heads) per step"},
@@ -613,12 +627,7 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": dict(pack.describe(), parallelism=f"replicas{world}",
-                       l2="inputs larger than L2 (q %.0f MB, k+v %.0f MB)" % (
-                           q.numel() * 2 / 1e6, (k.numel() + v.numel()) * 2 / 1e6),
-                       useful_flops_per_step=flops,
-                       padded_dense_mask_flops_per_step=4.0 * pack.d * pack.hq * len(pack.seqs)
-                       * pack.max_seqlen ** 2),
+        "config": workload_config(pack, world, flops),
         "tokens_per_s": round(tokens_per_s),
         "pct_of_nominal_bf16_peak": round(100 * value / world / NOMINAL_BF16_TFLOPS, 2),
         "pct_of_measured_bf16_peak": round(100 * value / world / peaks["bf16_tflops"], 2),
