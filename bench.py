@@ -349,12 +349,29 @@ def merge_bench(pk, torch, stream, pack, out, lse, parts=2, reps=20):
     ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
     nbytes = (parts + 1) * (T * H * d * out.element_size() + H * T * 4)
     gbs = nbytes / (ms * 1e-3) / 1e9
-    del ps, res_o, res_l
+    # a ring step's fold: a bf16 block result into an fp32 running accumulator, in place
+    acc = out.float()
+    acc_l = lse.clone()
+    for _ in range(3):
+        pk.lse_merge([(acc, acc_l), (out, lse)], out=acc, lse_out=acc_l)
+    torch.cuda.synchronize()
+    for a, b in evs:
+        a.record(stream)
+        pk.lse_merge([(acc, acc_l), (out, lse)], out=acc, lse_out=acc_l)
+        b.record(stream)
+    torch.cuda.synchronize()
+    ring_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    ring_bytes = T * H * d * (4 + 2 + 4) + 3 * H * T * 4
+    ring_gbs = ring_bytes / (ring_ms * 1e-3) / 1e9
+    del ps, res_o, res_l, acc, acc_l
     return {"kernel": "lse_merge_kernel", "parts": parts, "ms": round(ms, 4),
             "bytes_per_launch": nbytes,
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
-                         "peak_source": peaks["source"]}}
+                         "peak_source": peaks["source"]},
+            "ring_fold_fp32_acc": {"ms": round(ring_ms, 4), "bytes_per_launch": ring_bytes,
+                                   "achieved_gbs": round(ring_gbs, 1),
+                                   "frac": round(ring_gbs / peaks["hbm_gbs"], 4)}}
 
 
 def layouts_bench(pk, torch, stream, dev, pack, q, k, v, reps=10):

@@ -11,14 +11,14 @@
 // A part whose row saw no key (lse_c = -inf) contributes nothing; a row
 // that no part saw gets out = 0 and lse = -inf.
 //
-// HBM-bound streaming.  The common case (bf16 parts, up to four of them,
+// HBM-bound streaming.  The common case (up to four bf16 or fp32 parts,
 // head dim >= 64) runs a staged kernel: one CTA per SM, one producer warp
 // that moves chunks of consecutive rows of every part into a ring of shared
 // memory stages with bulk asynchronous copies (and the rows' LSEs with
 // 4-byte asynchronous copies) completing on the stage's mbarrier, and twelve
 // consumer warps (three per SM sub-partition, to hide the arithmetic's
 // latencies) that merge a stage and write the result with 16-byte stores.  Up to ~190 KB per SM are in flight, which is what HBM3e needs.
-// Every other case runs a register kernel: a row's d values in 16-byte
+// Every other case (more parts, smaller head dims) runs a register kernel: a row's d values in 16-byte
 // chunks, one per thread, so a warp covers 32 / (d / 8) whole rows.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -48,6 +48,9 @@ struct Params {
   float* lse_out;
   int32_t* status;         // device status word for a timed-out wait, may be null
   uint64_t wait_ns;
+  // staged kernel: stage layout (bytes), set on the host from the parts' types
+  int32_t st_bytes, n_stages, lse_off;
+  int32_t part_off[kMaxParts];
 };
 
 __device__ __forceinline__ void load8(const uint8_t* base, bool f32, int64_t elem, float (&x)[8]) {
@@ -147,23 +150,17 @@ __global__ void __launch_bounds__(kThreads) lse_merge_kernel(const Params p) {
 
 // ---------------------------------------------------------------------------
 // Staged kernel (bf16 parts, NP <= 4, d in {64, 128, 256}).
-// One part's rows per stage: 48 rows at d = 128 (96 at 64, 24 at 256), so
-// the twelve consumer warps each take the same share of a stage.
+// Rows per stage: 48 at d = 128 (96 at 64, 24 at 256), so the twelve
+// consumer warps each take the same share of a stage; a bf16 part's rows
+// are 12 KB of a stage, an fp32 part's 24 KB.
 constexpr int kChunkBytes = 12288;
 constexpr int kBulkConsumerWarps = 12;
 constexpr int kBulkThreads = 32 * (1 + kBulkConsumerWarps);
-constexpr int kMaxChunkRows = kChunkBytes / (2 * 64);  // d >= 64
-
-template <int NP>
-struct BulkCfg {
-  static constexpr int kStageBytes = NP * kChunkBytes + NP * kMaxChunkRows * 4;  // o + lse
-  static constexpr int kStagesFit = (200 * 1024) / kStageBytes;
-  static constexpr int kStages = kStagesFit < 16 ? kStagesFit : 16;
-  static constexpr int kOffBar = kStages * kStageBytes;
-  static constexpr int kOffMisc = kOffBar + 2 * kStages * 8;
-  static constexpr int kSmem = kOffMisc + 16;
-  static_assert(kSmem <= 227 * 1024, "shared memory budget");
-};
+constexpr int kMaxStages = 16;
+constexpr int kStageBudget = 200 * 1024;
+// Shared memory after the stages: full and empty barriers of kMaxStages
+// stages, abort flag, issued count.
+constexpr int kBulkTail = 2 * kMaxStages * 8 + 16;
 
 // 2^x on the SFU (relative error ~2^-22): weights of parts whose LSE lies
 // below the row maximum.
@@ -190,24 +187,25 @@ __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
 
 template <int NP, bool kOutF32>
 __global__ void __launch_bounds__(kBulkThreads, 1) lse_merge_bulk_kernel(const Params p) {
-  using C = BulkCfg<NP>;
   using namespace pk::dev;
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
-  auto stage_o = [&](int s, int c) { return (uint32_t)(s * C::kStageBytes + c * kChunkBytes); };
+  const int n_stages = p.n_stages;
+  const uint32_t st_bytes = (uint32_t)p.st_bytes, off_bar = (uint32_t)(n_stages * p.st_bytes);
+  auto stage_o = [&](int s, int c) { return (uint32_t)s * st_bytes + (uint32_t)p.part_off[c]; };
   auto stage_l = [&](int s, int c) {
-    return (uint32_t)(s * C::kStageBytes + NP * kChunkBytes + c * kMaxChunkRows * 4);
+    return (uint32_t)s * st_bytes + (uint32_t)p.lse_off + (uint32_t)c * (kChunkBytes / 128) * 4u;
   };
-  auto full = [&](int s) { return sbase + C::kOffBar + 8u * (uint32_t)s; };
-  auto empty = [&](int s) { return sbase + C::kOffBar + 8u * (uint32_t)(C::kStages + s); };
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc);
-  uint32_t* issued_count = reinterpret_cast<uint32_t*>(smem + C::kOffMisc + 4);
+  auto full = [&](int s) { return sbase + off_bar + 8u * (uint32_t)s; };
+  auto empty = [&](int s) { return sbase + off_bar + 8u * (uint32_t)(kMaxStages + s); };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + off_bar + 2 * kMaxStages * 8);
+  uint32_t* issued_count = reinterpret_cast<uint32_t*>(smem + off_bar + 2 * kMaxStages * 8 + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rpc = kChunkBytes / (2 * p.d);    // rows per chunk
   const uint32_t rows = (uint32_t)p.rows, H = (uint32_t)p.H;
   const uint32_t nchunks = (rows + rpc - 1) / rpc;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < n_stages; ++s) {
       mbar_init(full(s), 1 + 32);  // expect_tx arrival + every producer lane's LSE copies
       mbar_init(empty(s), kBulkConsumerWarps);
     }
@@ -223,18 +221,25 @@ __global__ void __launch_bounds__(kBulkThreads, 1) lse_merge_bulk_kernel(const P
     // Producer warp: lane 0 moves the outputs, every lane some of the LSEs.
     uint32_t i = 0;
     for (uint32_t k = blockIdx.x; k < nchunks; k += gridDim.x, ++i) {
-      const int s = (int)(i % C::kStages);
-      const uint32_t n = i / C::kStages;
+      const int s = (int)(i % (uint32_t)n_stages);
+      const uint32_t n = i / (uint32_t)n_stages;
       if (n > 0 && !__all_sync(0xffffffffu, mbar_wait(empty(s), (n - 1) & 1u, wc))) break;
       const uint32_t r0 = k * rpc;
       const uint32_t nr = rows - r0 < rpc ? rows - r0 : rpc;
       if (lane == 0) {
-        const uint32_t bytes = nr * (uint32_t)p.d * 2u;
-        mbar_arrive_expect_tx(full(s), bytes * (uint32_t)np);
+        const uint32_t row_elems = nr * (uint32_t)p.d;
+        uint32_t total = 0;
 #pragma unroll
         for (int c = 0; c < NP; ++c)
-          if (c < np)
-            bulk_g2s(sbase + stage_o(s, c), p.o[c] + (size_t)r0 * (size_t)p.d * 2, bytes, full(s));
+          if (c < np) total += row_elems * (p.f32[c] ? 4u : 2u);
+        mbar_arrive_expect_tx(full(s), total);
+#pragma unroll
+        for (int c = 0; c < NP; ++c)
+          if (c < np) {
+            const uint32_t eb = p.f32[c] ? 4u : 2u;
+            bulk_g2s(sbase + stage_o(s, c), p.o[c] + (size_t)r0 * (size_t)p.d * eb,
+                     row_elems * eb, full(s));
+          }
       }
       for (uint32_t r = lane; r < nr; r += 32) {
         const uint32_t row = r0 + r, t = row / H, h = row - t * H;
@@ -258,8 +263,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1) lse_merge_bulk_kernel(const P
     constexpr float kLog2e = 1.4426950408889634f;
     uint32_t i = 0;
     for (uint32_t k = blockIdx.x; k < nchunks; k += gridDim.x, ++i) {
-      const int s = (int)(i % C::kStages);
-      if (!__all_sync(0xffffffffu, mbar_wait(full(s), (i / C::kStages) & 1u, wc))) break;
+      const int s = (int)(i % (uint32_t)n_stages);
+      if (!__all_sync(0xffffffffu, mbar_wait(full(s), (i / (uint32_t)n_stages) & 1u, wc))) break;
       const uint32_t r0 = k * rpc;
       const uint32_t nr = rows - r0 < rpc ? rows - r0 : rpc;
       for (uint32_t rb = (uint32_t)(cw * rpw); rb < nr; rb += (uint32_t)(kBulkConsumerWarps * rpw)) {
@@ -278,19 +283,32 @@ __global__ void __launch_bounds__(kBulkThreads, 1) lse_merge_bulk_kernel(const P
         float acc[16], wsum = 0.f;
 #pragma unroll
         for (int e = 0; e < 16; ++e) acc[e] = 0.f;
-        const uint32_t off0 = (r * (uint32_t)p.d + (uint32_t)chunk * 8u) * 2u;
+        const uint32_t e_off = r * (uint32_t)p.d + (uint32_t)chunk * 8u;  // element offset
 #pragma unroll
         for (int c = 0; c < NP; ++c) {
           w[c] = m > -INFINITY ? ex2_approx((w[c] - m) * kLog2e) : 0.f;
           if (w[c] > 0.f) {
-            const uint8_t* src = smem + stage_o(s, c) + off0;
-            const uint4 u0 = *reinterpret_cast<const uint4*>(src);
-            const uint4 u1 = *reinterpret_cast<const uint4*>(src + half * 2u);
-            const uint32_t b[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+            if (p.f32[c]) {
+              const float4* src = reinterpret_cast<const float4*>(smem + stage_o(s, c) + e_off * 4u);
+              const float4* src2 = reinterpret_cast<const float4*>(smem + stage_o(s, c) + (e_off + half) * 4u);
+              const float4 x[4] = {src[0], src[1], src2[0], src2[1]};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              acc[2 * e] = fmaf(w[c], __uint_as_float(b[e] << 16), acc[2 * e]);
-              acc[2 * e + 1] = fmaf(w[c], __uint_as_float(b[e] & 0xffff0000u), acc[2 * e + 1]);
+              for (int q4 = 0; q4 < 4; ++q4) {
+                acc[4 * q4 + 0] = fmaf(w[c], x[q4].x, acc[4 * q4 + 0]);
+                acc[4 * q4 + 1] = fmaf(w[c], x[q4].y, acc[4 * q4 + 1]);
+                acc[4 * q4 + 2] = fmaf(w[c], x[q4].z, acc[4 * q4 + 2]);
+                acc[4 * q4 + 3] = fmaf(w[c], x[q4].w, acc[4 * q4 + 3]);
+              }
+            } else {
+              const uint8_t* src = smem + stage_o(s, c) + e_off * 2u;
+              const uint4 u0 = *reinterpret_cast<const uint4*>(src);
+              const uint4 u1 = *reinterpret_cast<const uint4*>(src + half * 2u);
+              const uint32_t b[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                acc[2 * e] = fmaf(w[c], __uint_as_float(b[e] << 16), acc[2 * e]);
+                acc[2 * e + 1] = fmaf(w[c], __uint_as_float(b[e] & 0xffff0000u), acc[2 * e + 1]);
+              }
             }
             wsum += w[c];
           }
@@ -323,9 +341,9 @@ __global__ void __launch_bounds__(kBulkThreads, 1) lse_merge_bulk_kernel(const P
   // memory: wait (bounded) for every stage's latest use before exiting.
   if (threadIdx.x == 0 && *abort_flag) {
     const uint32_t n = *issued_count;
-    const uint32_t first = n > (uint32_t)C::kStages ? n - (uint32_t)C::kStages : 0u;
+    const uint32_t first = n > (uint32_t)n_stages ? n - (uint32_t)n_stages : 0u;
     for (uint32_t j = first; j < n; ++j)
-      mbar_wait_drain(full((int)(j % C::kStages)), (j / C::kStages) & 1u, wc);
+      mbar_wait_drain(full((int)(j % (uint32_t)n_stages)), (j / (uint32_t)n_stages) & 1u, wc);
   }
 }
 
@@ -366,18 +384,30 @@ pk_status launch_regs(const Params& p, int64_t rows, int sms, cudaStream_t st) {
   return PK_OK;
 }
 
+// Stage layout from the parts' element types: each part's rows of a chunk
+// (bf16 or fp32) one after another, then every part's LSEs.
 template <int NP, bool kOutF32>
-pk_status launch_bulk(const Params& p, int64_t rows, int sms, cudaStream_t st) {
-  using C = BulkCfg<NP>;
+pk_status launch_bulk(Params p, int64_t rows, int sms, cudaStream_t st) {
+  const int rpc = kChunkBytes / (2 * p.d);
+  int off = 0;
+  for (int c = 0; c < p.num_parts; ++c) {
+    p.part_off[c] = off;
+    off += rpc * p.d * (p.f32[c] ? 4 : 2);
+  }
+  p.lse_off = off;
+  p.st_bytes = (off + p.num_parts * (kChunkBytes / 128) * 4 + 127) & ~127;
+  p.n_stages = kStageBudget / p.st_bytes;
+  if (p.n_stages > kMaxStages) p.n_stages = kMaxStages;
+  if (p.n_stages < 2) return PK_ERR_UNSUPPORTED;
+  const int smem = p.n_stages * p.st_bytes + kBulkTail;
   auto kern = lse_merge_bulk_kernel<NP, kOutF32>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess) {
     cudaGetLastError();
     return PK_ERR_CUDA;
   }
-  const int64_t rpc = kChunkBytes / (2 * p.d);
   const int64_t chunks = (rows + rpc - 1) / rpc;
-  kern<<<(int)(chunks < sms ? chunks : sms), kBulkThreads, C::kSmem, st>>>(p);
+  kern<<<(int)(chunks < sms ? chunks : sms), kBulkThreads, smem, st>>>(p);
   if (cudaGetLastError() != cudaSuccess) return PK_ERR_CUDA;
   return PK_OK;
 }
@@ -398,7 +428,6 @@ extern "C" pk_status pk_lse_merge(const pk_merge_part* parts, int32_t num_parts,
   if (out_dtype != PK_DTYPE_BF16 && out_dtype != PK_DTYPE_F32) return PK_ERR_INVALID_ARG;
   if (!aligned(out, 16) || !aligned(lse_out, 4)) return PK_ERR_ALIGNMENT;
   Params p{};
-  bool bf16 = true;
   for (int c = 0; c < num_parts; ++c) {
     if (parts[c].o == nullptr || parts[c].lse == nullptr) return PK_ERR_INVALID_ARG;
     if (parts[c].dtype != PK_DTYPE_BF16 && parts[c].dtype != PK_DTYPE_F32) return PK_ERR_INVALID_ARG;
@@ -406,7 +435,6 @@ extern "C" pk_status pk_lse_merge(const pk_merge_part* parts, int32_t num_parts,
     p.o[c] = static_cast<const uint8_t*>(parts[c].o);
     p.lse[c] = parts[c].lse;
     p.f32[c] = parts[c].dtype == PK_DTYPE_F32;
-    bf16 = bf16 && !p.f32[c];
   }
   const int64_t rows = (int64_t)T * H;
   if (rows == 0) return PK_OK;
@@ -424,7 +452,7 @@ extern "C" pk_status pk_lse_merge(const pk_merge_part* parts, int32_t num_parts,
   const int sms = sm_count();
   if (sms <= 0) return PK_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (bf16 && d >= 64 && num_parts <= 4) {
+  if (d >= 64 && num_parts <= 4) {
     const bool f = p.out_f32 != 0;
     if (num_parts == 1) return f ? launch_bulk<1, true>(p, rows, sms, st) : launch_bulk<1, false>(p, rows, sms, st);
     if (num_parts == 2) return f ? launch_bulk<2, true>(p, rows, sms, st) : launch_bulk<2, false>(p, rows, sms, st);
