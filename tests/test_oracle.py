@@ -299,3 +299,52 @@ def test_row_keys_are_mask_row_sums_and_closed_form(name):
         for s in range(len(cu) - 1):
             M = oracle.dense_mask(cu, pack.segments, s)
             np.testing.assert_array_equal(n[cu[s]:cu[s + 1]], M.sum(axis=1))
+
+
+def test_brute_force_python_loops_on_a_tiny_pack():
+    """A second, independent implementation: plain Python loops over the
+    mask rule as stated (text causal; an image token also sees its whole own
+    segment; nothing across sequences), fp64 math.exp, on a tiny pack with
+    adjacent image segments and GQA.  The oracle must agree to 1e-12."""
+    import math
+    seqs = [[(W.TEXT, 5), (W.IMAGE, 7), (W.IMAGE, 4), (W.TEXT, 3)], [(W.IMAGE, 6)], [(W.TEXT, 9)]]
+    pack = W.Pack("brute", seqs, hq=4, hkv=2, d=8, seed=77)
+    q, k, v = W.make_qkv(pack)
+    qf, kf, vf = q.double().numpy(), k.double().numpy(), v.double().numpy()
+    T, group = pack.total_tokens, pack.hq // pack.hkv
+    # (sequence, segment index, type, segment start, segment end) per token
+    info = []
+    for s, seq in enumerate(pack.seqs):
+        pos = 0
+        for gi, (typ, n) in enumerate(seq):
+            for _ in range(n):
+                info.append((s, gi, typ, pos, pos + n))
+            pos += n
+    start_of = {}
+    t0 = 0
+    for s, seq in enumerate(pack.seqs):
+        start_of[s] = t0
+        t0 += sum(n for _, n in seq)
+    out = np.zeros((T, pack.hq, pack.d))
+    lse = np.zeros((pack.hq, T))
+    for i in range(T):
+        si, gi, ti, _, _ = info[i]
+        for h in range(pack.hq):
+            g = h // group
+            keys = []
+            for j in range(T):
+                sj, gj, _, _, _ = info[j]
+                if sj != si:
+                    continue
+                if j <= i or (ti == W.IMAGE and gj == gi):
+                    keys.append(j)
+            sc = [pack.scale * sum(qf[i, h, c] * kf[j, g, c] for c in range(pack.d)) for j in keys]
+            mx = max(sc)
+            z = sum(math.exp(x - mx) for x in sc)
+            lse[h, i] = mx + math.log(z)
+            for c in range(pack.d):
+                out[i, h, c] = sum(math.exp(x - lse[h, i]) * vf[j, g, c] for x, j in zip(sc, keys))
+    o, l = oracle.attention(q, k, v, pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d,
+                            pack.scale)
+    np.testing.assert_allclose(o, out, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l, lse, rtol=0, atol=1e-12)
