@@ -56,7 +56,8 @@ typedef enum pk_status {
   PK_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
   PK_ERR_TIMEOUT = 5,       /* device: a bounded wait ran out (in dev_status) */
   PK_ERR_DEVICE_CHECK = 6,  /* device: an internal consistency check failed */
-  PK_ERR_NOT_UPLOADED = 7   /* plan has no device image yet */
+  PK_ERR_NOT_UPLOADED = 7,  /* plan has no device image yet */
+  PK_ERR_OUT_OF_MEMORY = 8  /* a host memory allocation failed */
 } pk_status;
 
 typedef enum pk_seg_type { PK_TEXT = 0, PK_IMAGE = 1 } pk_seg_type;

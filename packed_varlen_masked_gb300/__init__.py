@@ -20,7 +20,7 @@ provides device memory and the current stream.
 from __future__ import annotations
 
 from ._native import (PK_ERR_ALIGNMENT, PK_ERR_CUDA, PK_ERR_DEVICE_CHECK,  # noqa: F401
-                      PK_ERR_INVALID_ARG, PK_ERR_NOT_UPLOADED, PK_ERR_TIMEOUT,
+                      PK_ERR_INVALID_ARG, PK_ERR_NOT_UPLOADED, PK_ERR_OUT_OF_MEMORY, PK_ERR_TIMEOUT,
                       PK_ERR_UNSUPPORTED, PK_OK, PKError, lib_path, load)
 from .api import (IMAGE, TEXT, HostPipeline, Plan, attn_fwd, attn_fwd_fp8,  # noqa: F401
                   attn_fwd_host, debug_wait_timeout, lse_merge, plan, plan_layout,

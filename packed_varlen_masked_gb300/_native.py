@@ -18,6 +18,7 @@ PK_ERR_CUDA = 4
 PK_ERR_TIMEOUT = 5
 PK_ERR_DEVICE_CHECK = 6
 PK_ERR_NOT_UPLOADED = 7
+PK_ERR_OUT_OF_MEMORY = 8
 
 
 class PKError(RuntimeError):

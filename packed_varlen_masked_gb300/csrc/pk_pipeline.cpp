@@ -51,13 +51,18 @@ pk_status pk_pipeline_create(const pk_plan* plan, const pk_dev_slot* slots, int3
     if (!s.q || !s.k || !s.v || !s.out || !s.lse) return PK_ERR_INVALID_ARG;
   }
   pk_pipeline* p = new (std::nothrow) pk_pipeline();
-  if (p == nullptr) return PK_ERR_INVALID_ARG;
-  p->plan = plan;
-  p->slots.assign(slots, slots + num_slots);
-  p->ev_in.assign(num_slots, nullptr);
-  p->ev_comp.assign(num_slots, nullptr);
-  p->ev_out.assign(num_slots, nullptr);
-  p->used.assign(num_slots, false);
+  if (p == nullptr) return PK_ERR_OUT_OF_MEMORY;
+  try {
+    p->plan = plan;
+    p->slots.assign(slots, slots + num_slots);
+    p->ev_in.assign(num_slots, nullptr);
+    p->ev_comp.assign(num_slots, nullptr);
+    p->ev_out.assign(num_slots, nullptr);
+    p->used.assign(num_slots, false);
+  } catch (...) {  // no C++ exception crosses the C boundary
+    delete p;
+    return PK_ERR_OUT_OF_MEMORY;
+  }
   bool ok = cudaStreamCreateWithFlags(&p->s_in, cudaStreamNonBlocking) == cudaSuccess &&
             cudaStreamCreateWithFlags(&p->s_comp, cudaStreamNonBlocking) == cudaSuccess &&
             cudaStreamCreateWithFlags(&p->s_out, cudaStreamNonBlocking) == cudaSuccess;

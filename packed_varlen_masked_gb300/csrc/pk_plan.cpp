@@ -19,6 +19,7 @@
 //   partial  : anything else (per-element compare against kv_limit).
 #include <algorithm>
 #include <cstring>
+#include <memory>
 #include <new>
 #include <numeric>
 #include <queue>
@@ -124,8 +125,9 @@ pk_status build_plan(const pk_layout& L, int32_t hq, int32_t hkv, int32_t d, int
     num_ctas = sms;
   }
 
-  pk_plan* p = new (std::nothrow) pk_plan();
-  if (p == nullptr) return PK_ERR_INVALID_ARG;
+  // Owned here until the plan is complete (the vectors below may throw).
+  std::unique_ptr<pk_plan> owner(new pk_plan());
+  pk_plan* p = owner.get();
   const int32_t S = L.num_seqs;
   const int32_t* cq = L.cu_seqlens_q;
   const int32_t* ck = L.cu_seqlens_k;
@@ -242,38 +244,28 @@ pk_status build_plan(const pk_layout& L, int32_t hq, int32_t hkv, int32_t d, int
     std::memcpy(p->image.data() + IL.table_off, p->block_table.data(),
                 sizeof(int32_t) * p->block_table.size());
 
-  *out = p;
+  *out = owner.release();
   return PK_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-const char* pk_status_string(pk_status st) {
-  switch (st) {
-    case PK_OK: return "ok";
-    case PK_ERR_INVALID_ARG: return "invalid argument";
-    case PK_ERR_UNSUPPORTED: return "unsupported configuration";
-    case PK_ERR_ALIGNMENT: return "misaligned tensor";
-    case PK_ERR_CUDA: return "CUDA error";
-    case PK_ERR_TIMEOUT: return "device wait timed out";
-    case PK_ERR_DEVICE_CHECK: return "device consistency check failed";
-    case PK_ERR_NOT_UPLOADED: return "plan not uploaded";
+// The C entry points never let a C++ exception out: a failed host
+// allocation is PK_ERR_OUT_OF_MEMORY.
+template <typename F>
+pk_status guarded(F&& f) {
+  try {
+    return f();
+  } catch (const std::bad_alloc&) {
+    return PK_ERR_OUT_OF_MEMORY;
+  } catch (...) {
+    return PK_ERR_INVALID_ARG;
   }
-  return "unknown status";
 }
 
-pk_status pk_plan_create_layout(const pk_layout* layout, int32_t hq, int32_t hkv,
-                                int32_t head_dim, int32_t num_ctas, pk_plan** out) {
-  if (out) *out = nullptr;
-  if (layout == nullptr) return PK_ERR_INVALID_ARG;
-  return build_plan(*layout, hq, hkv, head_dim, num_ctas, out);
-}
-
-pk_status pk_plan_create(const int32_t* cu, int32_t num_seqs, const pk_segment* segs,
-                         int32_t num_segs, int32_t hq, int32_t hkv, int32_t d, int32_t num_ctas,
-                         pk_plan** out) {
+// pk_plan_create's work: global (packed-stream) segments to the
+// per-sequence form of the general layout, then the planner.
+pk_status create_from_global_segments(const int32_t* cu, int32_t num_seqs, const pk_segment* segs,
+                                      int32_t num_segs, int32_t hq, int32_t hkv, int32_t d,
+                                      int32_t num_ctas, pk_plan** out) {
   if (out == nullptr) return PK_ERR_INVALID_ARG;
   *out = nullptr;
   if (num_seqs < 0 || num_segs < 0 || cu == nullptr || (num_segs > 0 && segs == nullptr))
@@ -306,6 +298,40 @@ pk_status pk_plan_create(const int32_t* cu, int32_t num_seqs, const pk_segment* 
   L.num_segs = static_cast<int32_t>(ss.size());
   L.num_kv_rows = cu[num_seqs];
   return build_plan(L, hq, hkv, d, num_ctas, out);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pk_status_string(pk_status st) {
+  switch (st) {
+    case PK_OK: return "ok";
+    case PK_ERR_INVALID_ARG: return "invalid argument";
+    case PK_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PK_ERR_ALIGNMENT: return "misaligned tensor";
+    case PK_ERR_CUDA: return "CUDA error";
+    case PK_ERR_TIMEOUT: return "device wait timed out";
+    case PK_ERR_DEVICE_CHECK: return "device consistency check failed";
+    case PK_ERR_NOT_UPLOADED: return "plan not uploaded";
+    case PK_ERR_OUT_OF_MEMORY: return "host memory allocation failed";
+  }
+  return "unknown status";
+}
+
+pk_status pk_plan_create_layout(const pk_layout* layout, int32_t hq, int32_t hkv,
+                                int32_t head_dim, int32_t num_ctas, pk_plan** out) {
+  if (out) *out = nullptr;
+  if (layout == nullptr) return PK_ERR_INVALID_ARG;
+  return guarded([&] { return build_plan(*layout, hq, hkv, head_dim, num_ctas, out); });
+}
+
+pk_status pk_plan_create(const int32_t* cu, int32_t num_seqs, const pk_segment* segs,
+                         int32_t num_segs, int32_t hq, int32_t hkv, int32_t d, int32_t num_ctas,
+                         pk_plan** out) {
+  return guarded([&] {
+    return create_from_global_segments(cu, num_seqs, segs, num_segs, hq, hkv, d, num_ctas, out);
+  });
 }
 
 size_t pk_plan_device_bytes(const pk_plan* p) { return p ? p->layout.bytes : 0; }

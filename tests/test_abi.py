@@ -38,8 +38,8 @@ def test_binding_covers_every_declared_symbol():
 
 def test_status_strings():
     lib = pk.load()
-    for code in range(8):
-        assert lib.pk_status_string(code)
+    for code in range(9):
+        assert lib.pk_status_string(code).decode() != "unknown status"
     assert lib.pk_status_string(pk.PK_ERR_TIMEOUT).decode() == "device wait timed out"
 
 
