@@ -363,6 +363,7 @@ class HostPipeline:
         self._h = ctypes.c_void_p()
         check(self._lib.pk_pipeline_create(plan.handle, arr, len(slots), ctypes.byref(self._h)),
               "pk_pipeline_create")
+        self._inflight = []  # host tensors of submitted steps, kept alive until sync
 
     def submit(self, q_host, k_host, v_host, out_host, lse_host, scale: Optional[float] = None,
                status=None) -> None:
@@ -377,9 +378,11 @@ class HostPipeline:
             ctypes.c_void_p(v_host.data_ptr()), ctypes.c_void_p(out_host.data_ptr()),
             ctypes.c_void_p(lse_host.data_ptr()), float(scale),
             ctypes.c_void_p(status.data_ptr() if status is not None else 0)), "pk_pipeline_submit")
+        self._inflight.append((q_host, k_host, v_host, out_host, lse_host, status))
 
     def sync(self) -> None:
         check(self._lib.pk_pipeline_sync(self._h), "pk_pipeline_sync")
+        self._inflight.clear()
 
     def stream(self, which: int):
         """torch view of the pipeline's stream: 0 copy-in, 1 compute, 2 copy-out."""
@@ -388,8 +391,9 @@ class HostPipeline:
 
     def close(self) -> None:
         if getattr(self, "_h", None) is not None and self._h.value:
-            self._lib.pk_pipeline_destroy(self._h)
+            self._lib.pk_pipeline_destroy(self._h)  # waits for outstanding steps
             self._h = ctypes.c_void_p()
+            self._inflight = []
 
     def __del__(self):
         try:
