@@ -239,26 +239,39 @@ def reference_arm(args, pack, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def cpu_baseline(pack, seconds: float = 12.0):
-    """The oracle as it stands, on a bounded sample of the same workload."""
+def _oracle_rate(pack, seconds: float, seed: int = 1):
+    """Useful TFLOP/s of the oracle on uniformly drawn rows of ``pack``,
+    about ``seconds`` of CPU work; returns (TFLOP/s, seconds, rows)."""
     import oracle
     q, k, v = W.make_qkv(pack)
     cu = pack.cu_seqlens
     keys = oracle.row_keys(cu, pack.segments).astype(np.float64)  # FLOP count per row
-    rng = np.random.default_rng(1)
-    probe = rng.integers(0, pack.total_tokens, size=32).astype(np.int32)
+    rng = np.random.default_rng(seed)
+    probe = rng.integers(0, pack.total_tokens, size=16).astype(np.int32)
     t0 = time.perf_counter()
     oracle.attention(q, k, v, cu, pack.segments, pack.hq, pack.hkv, pack.d, pack.scale, rows=probe)
     dt = time.perf_counter() - t0
-    n_rows = int(max(32, min(20000, 32 * seconds / max(dt, 1e-6))))
+    n_rows = int(max(16, min(20000, 16 * seconds / max(dt, 1e-6))))
     rows = rng.integers(0, pack.total_tokens, size=n_rows).astype(np.int32)
     t0 = time.perf_counter()
     oracle.attention(q, k, v, cu, pack.segments, pack.hq, pack.hkv, pack.d, pack.scale, rows=rows)
     t = time.perf_counter() - t0
-    fl = 4.0 * pack.d * pack.hq * keys[rows].sum()
-    return {"value": fl / t / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+    return 4.0 * pack.d * pack.hq * keys[rows].sum() / t / 1e12, t, n_rows
+
+
+def cpu_baseline(pack, seconds: float = 10.0, per_config_seconds: float = 1.5):
+    """The oracle as it stands, on a bounded sample of the same workload, and
+    on a short sample of every other configuration."""
+    import oracle
+    value, t, n_rows = _oracle_rate(pack, seconds)
+    per = {}
+    for name, fn in W.CONFIGS.items():
+        rate, tc, nc = _oracle_rate(fn(), per_config_seconds)
+        per[name] = {"tflops": rate, "rows": nc, "seconds": round(tc, 2)}
+    return {"value": value, "unit": "TFLOP/s", "cores": oracle.max_threads(),
             "kind": "oracle", "seconds": t,
-            "sample": f"{n_rows} uniformly drawn query rows x {pack.hq} heads of the workload"}
+            "sample": f"{n_rows} uniformly drawn query rows x {pack.hq} heads of the workload",
+            "per_config": per}
 
 
 def replaced_path(torch, pack, q, k, v, ours_out, steps=3):
