@@ -185,19 +185,38 @@ __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-template <int NP, bool kOutF32>
+// Stage layout when every part is bf16 (known at compile time).
+template <int NP>
+struct Bf16Layout {
+  static constexpr int kLseOff = NP * kChunkBytes;
+  static constexpr int kStBytes = (kLseOff + NP * (kChunkBytes / 128) * 4 + 127) & ~127;
+  static constexpr int kStagesFit = kStageBudget / kStBytes;
+  static constexpr int kStages = kStagesFit < kMaxStages ? kStagesFit : kMaxStages;
+  static constexpr int kSmem = kStages * kStBytes + kBulkTail;
+  static_assert(kStages >= 2 && kSmem <= 227 * 1024, "shared memory budget");
+};
+
+// kBf16: every part is bf16, so the stage layout and the element size are
+// compile-time constants; otherwise they come from Params.
+template <int NP, bool kOutF32, bool kBf16>
 __global__ void __launch_bounds__(kBulkThreads, 1) lse_merge_bulk_kernel(const Params p) {
   using namespace pk::dev;
+  using BL = Bf16Layout<NP>;
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
-  const int n_stages = p.n_stages;
-  const uint32_t st_bytes = (uint32_t)p.st_bytes, off_bar = (uint32_t)(n_stages * p.st_bytes);
-  auto stage_o = [&](int s, int c) { return (uint32_t)s * st_bytes + (uint32_t)p.part_off[c]; };
-  auto stage_l = [&](int s, int c) {
-    return (uint32_t)s * st_bytes + (uint32_t)p.lse_off + (uint32_t)c * (kChunkBytes / 128) * 4u;
+  const uint32_t n_stages = kBf16 ? (uint32_t)BL::kStages : (uint32_t)p.n_stages;
+  const uint32_t st_bytes = kBf16 ? (uint32_t)BL::kStBytes : (uint32_t)p.st_bytes;
+  const uint32_t off_bar = n_stages * st_bytes;
+  auto is_f32 = [&](int c) { return kBf16 ? false : p.f32[c] != 0; };
+  auto stage_o = [&](uint32_t s, int c) {
+    return s * st_bytes + (kBf16 ? (uint32_t)(c * kChunkBytes) : (uint32_t)p.part_off[c]);
   };
-  auto full = [&](int s) { return sbase + off_bar + 8u * (uint32_t)s; };
-  auto empty = [&](int s) { return sbase + off_bar + 8u * (uint32_t)(kMaxStages + s); };
+  auto stage_l = [&](uint32_t s, int c) {
+    return s * st_bytes + (kBf16 ? (uint32_t)BL::kLseOff : (uint32_t)p.lse_off) +
+           (uint32_t)c * (kChunkBytes / 128) * 4u;
+  };
+  auto full = [&](uint32_t s) { return sbase + off_bar + 8u * s; };
+  auto empty = [&](uint32_t s) { return sbase + off_bar + 8u * ((uint32_t)kMaxStages + s); };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + off_bar + 2 * kMaxStages * 8);
   uint32_t* issued_count = reinterpret_cast<uint32_t*>(smem + off_bar + 2 * kMaxStages * 8 + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -205,7 +224,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) lse_merge_bulk_kernel(const P
   const uint32_t rows = (uint32_t)p.rows, H = (uint32_t)p.H;
   const uint32_t nchunks = (rows + rpc - 1) / rpc;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < n_stages; ++s) {
+    for (uint32_t s = 0; s < n_stages; ++s) {
       mbar_init(full(s), 1 + 32);  // expect_tx arrival + every producer lane's LSE copies
       mbar_init(empty(s), kBulkConsumerWarps);
     }
@@ -221,8 +240,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1) lse_merge_bulk_kernel(const P
     // Producer warp: lane 0 moves the outputs, every lane some of the LSEs.
     uint32_t i = 0;
     for (uint32_t k = blockIdx.x; k < nchunks; k += gridDim.x, ++i) {
-      const int s = (int)(i % (uint32_t)n_stages);
-      const uint32_t n = i / (uint32_t)n_stages;
+      const uint32_t s = i % n_stages;
+      const uint32_t n = i / n_stages;
       if (n > 0 && !__all_sync(0xffffffffu, mbar_wait(empty(s), (n - 1) & 1u, wc))) break;
       const uint32_t r0 = k * rpc;
       const uint32_t nr = rows - r0 < rpc ? rows - r0 : rpc;
@@ -231,12 +250,12 @@ __global__ void __launch_bounds__(kBulkThreads, 1) lse_merge_bulk_kernel(const P
         uint32_t total = 0;
 #pragma unroll
         for (int c = 0; c < NP; ++c)
-          if (c < np) total += row_elems * (p.f32[c] ? 4u : 2u);
+          if (c < np) total += row_elems * (is_f32(c) ? 4u : 2u);
         mbar_arrive_expect_tx(full(s), total);
 #pragma unroll
         for (int c = 0; c < NP; ++c)
           if (c < np) {
-            const uint32_t eb = p.f32[c] ? 4u : 2u;
+            const uint32_t eb = is_f32(c) ? 4u : 2u;
             bulk_g2s(sbase + stage_o(s, c), p.o[c] + (size_t)r0 * (size_t)p.d * eb,
                      row_elems * eb, full(s));
           }
@@ -263,8 +282,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1) lse_merge_bulk_kernel(const P
     constexpr float kLog2e = 1.4426950408889634f;
     uint32_t i = 0;
     for (uint32_t k = blockIdx.x; k < nchunks; k += gridDim.x, ++i) {
-      const int s = (int)(i % (uint32_t)n_stages);
-      if (!__all_sync(0xffffffffu, mbar_wait(full(s), (i / (uint32_t)n_stages) & 1u, wc))) break;
+      const uint32_t s = i % n_stages;
+      if (!__all_sync(0xffffffffu, mbar_wait(full(s), (i / n_stages) & 1u, wc))) break;
       const uint32_t r0 = k * rpc;
       const uint32_t nr = rows - r0 < rpc ? rows - r0 : rpc;
       for (uint32_t rb = (uint32_t)(cw * rpw); rb < nr; rb += (uint32_t)(kBulkConsumerWarps * rpw)) {
@@ -288,7 +307,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) lse_merge_bulk_kernel(const P
         for (int c = 0; c < NP; ++c) {
           w[c] = m > -INFINITY ? ex2_approx((w[c] - m) * kLog2e) : 0.f;
           if (w[c] > 0.f) {
-            if (p.f32[c]) {
+            if (is_f32(c)) {
               const float4* src = reinterpret_cast<const float4*>(smem + stage_o(s, c) + e_off * 4u);
               const float4* src2 = reinterpret_cast<const float4*>(smem + stage_o(s, c) + (e_off + half) * 4u);
               const float4 x[4] = {src[0], src[1], src2[0], src2[1]};
@@ -341,9 +360,9 @@ __global__ void __launch_bounds__(kBulkThreads, 1) lse_merge_bulk_kernel(const P
   // memory: wait (bounded) for every stage's latest use before exiting.
   if (threadIdx.x == 0 && *abort_flag) {
     const uint32_t n = *issued_count;
-    const uint32_t first = n > (uint32_t)n_stages ? n - (uint32_t)n_stages : 0u;
+    const uint32_t first = n > n_stages ? n - n_stages : 0u;
     for (uint32_t j = first; j < n; ++j)
-      mbar_wait_drain(full((int)(j % (uint32_t)n_stages)), (j / (uint32_t)n_stages) & 1u, wc);
+      mbar_wait_drain(full(j % n_stages), (j / n_stages) & 1u, wc);
   }
 }
 
@@ -386,21 +405,24 @@ pk_status launch_regs(const Params& p, int64_t rows, int sms, cudaStream_t st) {
 
 // Stage layout from the parts' element types: each part's rows of a chunk
 // (bf16 or fp32) one after another, then every part's LSEs.
-template <int NP, bool kOutF32>
+template <int NP, bool kOutF32, bool kBf16>
 pk_status launch_bulk(Params p, int64_t rows, int sms, cudaStream_t st) {
   const int rpc = kChunkBytes / (2 * p.d);
-  int off = 0;
-  for (int c = 0; c < p.num_parts; ++c) {
-    p.part_off[c] = off;
-    off += rpc * p.d * (p.f32[c] ? 4 : 2);
+  int smem = Bf16Layout<NP>::kSmem;
+  if (!kBf16) {
+    int off = 0;
+    for (int c = 0; c < p.num_parts; ++c) {
+      p.part_off[c] = off;
+      off += rpc * p.d * (p.f32[c] ? 4 : 2);
+    }
+    p.lse_off = off;
+    p.st_bytes = (off + p.num_parts * (kChunkBytes / 128) * 4 + 127) & ~127;
+    p.n_stages = kStageBudget / p.st_bytes;
+    if (p.n_stages > kMaxStages) p.n_stages = kMaxStages;
+    if (p.n_stages < 2) return PK_ERR_UNSUPPORTED;
+    smem = p.n_stages * p.st_bytes + kBulkTail;
   }
-  p.lse_off = off;
-  p.st_bytes = (off + p.num_parts * (kChunkBytes / 128) * 4 + 127) & ~127;
-  p.n_stages = kStageBudget / p.st_bytes;
-  if (p.n_stages > kMaxStages) p.n_stages = kMaxStages;
-  if (p.n_stages < 2) return PK_ERR_UNSUPPORTED;
-  const int smem = p.n_stages * p.st_bytes + kBulkTail;
-  auto kern = lse_merge_bulk_kernel<NP, kOutF32>;
+  auto kern = lse_merge_bulk_kernel<NP, kOutF32, kBf16>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess) {
     cudaGetLastError();
@@ -454,9 +476,15 @@ extern "C" pk_status pk_lse_merge(const pk_merge_part* parts, int32_t num_parts,
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (d >= 64 && num_parts <= 4) {
     const bool f = p.out_f32 != 0;
-    if (num_parts == 1) return f ? launch_bulk<1, true>(p, rows, sms, st) : launch_bulk<1, false>(p, rows, sms, st);
-    if (num_parts == 2) return f ? launch_bulk<2, true>(p, rows, sms, st) : launch_bulk<2, false>(p, rows, sms, st);
-    return f ? launch_bulk<4, true>(p, rows, sms, st) : launch_bulk<4, false>(p, rows, sms, st);
+    bool bf16 = true;
+    for (int c = 0; c < num_parts; ++c) bf16 = bf16 && !p.f32[c];
+    if (bf16) {
+      if (num_parts == 1) return f ? launch_bulk<1, true, true>(p, rows, sms, st) : launch_bulk<1, false, true>(p, rows, sms, st);
+      if (num_parts == 2) return f ? launch_bulk<2, true, true>(p, rows, sms, st) : launch_bulk<2, false, true>(p, rows, sms, st);
+      return f ? launch_bulk<4, true, true>(p, rows, sms, st) : launch_bulk<4, false, true>(p, rows, sms, st);
+    }
+    if (num_parts <= 2) return f ? launch_bulk<2, true, false>(p, rows, sms, st) : launch_bulk<2, false, false>(p, rows, sms, st);
+    return f ? launch_bulk<4, true, false>(p, rows, sms, st) : launch_bulk<4, false, false>(p, rows, sms, st);
   }
   if (num_parts <= 2) return launch_regs<2>(p, rows, sms, st);
   if (num_parts <= 4) return launch_regs<4>(p, rows, sms, st);
