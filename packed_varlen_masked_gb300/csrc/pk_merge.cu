@@ -17,9 +17,11 @@
 // memory stages with bulk asynchronous copies (and the rows' LSEs with
 // 4-byte asynchronous copies) completing on the stage's mbarrier, and twelve
 // consumer warps (three per SM sub-partition, to hide the arithmetic's
-// latencies) that merge a stage and write the result with 16-byte stores.  Up to ~190 KB per SM are in flight, which is what HBM3e needs.
-// Every other case (more parts, smaller head dims) runs a register kernel: a row's d values in 16-byte
-// chunks, one per thread, so a warp covers 32 / (d / 8) whole rows.
+// latencies) that merge a stage and write the result with 16-byte stores.
+// Up to ~200 KB per SM are in flight, which is what HBM3e needs.  Every
+// other case (more parts, smaller head dims) runs a register kernel: a row's
+// d values in 16-byte chunks, one per thread, so a warp covers 32 / (d / 8)
+// whole rows.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -149,7 +151,7 @@ __global__ void __launch_bounds__(kThreads) lse_merge_kernel(const Params p) {
 }
 
 // ---------------------------------------------------------------------------
-// Staged kernel (bf16 parts, NP <= 4, d in {64, 128, 256}).
+// Staged kernel (up to 4 parts, bf16 or fp32 each, d in {64, 128, 256}).
 // Rows per stage: 48 at d = 128 (96 at 64, 24 at 256), so the twelve
 // consumer warps each take the same share of a stage; a bf16 part's rows
 // are 12 KB of a stage, an fp32 part's 24 KB.
