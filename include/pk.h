@@ -182,7 +182,9 @@ pk_status pk_plan_upload(pk_plan* plan, void* dev_buf, size_t bytes,
  *               writes PK_ERR_TIMEOUT / PK_ERR_DEVICE_CHECK there (the caller
  *               zeroes it; it is never cleared by the library).
  * Argument and launch errors are returned synchronously.  Requires a device
- * of compute capability 10.3 (GB300).
+ * of compute capability 10.3 (GB300); PK_ERR_UNSUPPORTED also if the
+ * library's kernel was compiled with fewer registers per thread than its
+ * warp roles share out (a build-configuration error, checked once).
  */
 pk_status pk_attn_fwd(const pk_plan* plan, const void* q, const void* k,
                       const void* v, void* out, float* lse, float scale,

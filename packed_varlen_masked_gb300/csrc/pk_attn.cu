@@ -12,7 +12,7 @@
 // one dequantisation scale each folded into the softmax scale); values, P
 // and the output are bf16 in both.
 //
-// Kernel organisation (one persistent CTA per SM, 8 warps).  The CTA runs
+// Kernel organisation (one persistent CTA per SM, 12 warps).  The CTA runs
 // its work items' query heads ("units") one after another; a unit is a
 // 128-row query tile streaming the key/value tiles of its sequence.
 //   warp 0      TMA producer of the query tiles (double buffered) and of a
@@ -27,8 +27,14 @@
 //               issuers in different warps work concurrently.
 //   warps 4-7   softmax: thread r owns row r of S, P and O in TMEM.  Online
 //               softmax in base 2 with a lazily moved running maximum, P
-//               written as bf16 pairs, epilogue O / l -> bf16 and the
-//               natural-log LSE.
+//               written as bf16 pairs; at the end of a unit it hands the
+//               row's (m, l) to the epilogue and goes on to the next unit.
+//   warps 8-11  epilogue: after a unit's last P V, moves O out of TMEM
+//               (freeing it for the next unit), writes O / l as bf16 and
+//               the natural-log LSE.
+// Registers: the one-thread roles give theirs up (setmaxnreg) to the
+// softmax, whose exponential loop keeps a whole 128-column row of scores
+// and its 64 bf16 pairs live, and to the epilogue, which holds a row of O.
 // TMEM columns: S double buffer [0,256), P double buffer [256,384), O
 // [384,384+D).  Because S(t) and P(t) live in different columns and both are
 // double buffered, the S issuer computes S(t+2) as soon as the softmax has
@@ -54,7 +60,16 @@
 namespace pk {
 namespace dev {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
+// Registers per thread after setmaxnreg: warps 0-3, 4-7 and 8-11.  A CTA is
+// launched with kThreads x kRegsLaunch registers (the most __launch_bounds__
+// allows at one CTA per SM); the three shares must fit in that, or the
+// increases would wait forever.  The host checks the compiled count before
+// the first launch.
+constexpr int kRegsMma = 64, kRegsSoftmax = 240, kRegsEpi = 200;
+constexpr int kRegsLaunch = 65536 / kThreads / 8 * 8;  // 168
+static_assert(128 * (kRegsMma + kRegsSoftmax + kRegsEpi) <= kThreads * kRegsLaunch,
+              "register split exceeds the CTA's allocation");
 constexpr uint32_t kTmemCols = 512;
 // F8: queries and keys are FP8 E4M3 (one byte per element), values bf16.
 template <int D, bool F8 = false>
@@ -90,8 +105,11 @@ struct Cfg {
   static constexpr int kPvDone = kPReady + 2;        // [2]
   static constexpr int kOFree = kPvDone + 2;
   static constexpr int kMmaDone = kOFree + 1;  // [2]: one per MMA issuer
-  static constexpr int kNumBars = kMmaDone + 2;
-  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kLmFull = kMmaDone + 2;   // a unit's row (m, l) handed over
+  static constexpr int kLmFree = kLmFull + 1;    // ... and taken by the epilogue
+  static constexpr int kNumBars = kLmFree + 1;
+  static constexpr int kOffLm = kOffBar + kNumBars * 8;  // float2 [128]
+  static constexpr int kOffMisc = kOffLm + 128 * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   static_assert(kSmemBytes > 114 * 1024, "one CTA per SM");
@@ -272,8 +290,8 @@ __device__ void mma_pv_role(const KernelParams& p, uint32_t sbase, uint32_t tmem
 
 // Softmax warpgroup (warps 4-7): thread r owns row r of S, P and O in TMEM.
 template <int D, bool F8>
-__device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint32_t tmem, int beg,
-                             int end, const WaitCtl& wc) {
+__device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint8_t* sgen, uint32_t tmem,
+                             int beg, int end, const WaitCtl& wc) {
   using C = Cfg<D, F8>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -282,10 +300,11 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint32_t tme
   const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
   const uint32_t tO = tmem + lane_base + C::kColO;
   const float sl2 = p.scale_log2;
-  uint32_t g = 0;
+  uint32_t g = 0, u = 0;
   bool ok = true;
   bool s_ready = false;  // S(t) of the next tile already seen complete
-  for (UnitIter ui(p.items, beg, end); ui.valid() && ok; ui.next()) {
+  float2* lm = reinterpret_cast<float2*>(sgen + C::kOffLm);
+  for (UnitIter ui(p.items, beg, end); ui.valid() && ok; ui.next(), ++u) {
     const pk_work_item& w = ui.w;
     const int h = ui.head();
     const bool valid = r < w.q_rows;
@@ -354,41 +373,45 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint32_t tme
       };
       constexpr float kRescaleSum = 65536.0f;  // 2^kRescaleLog2
       if (j == 0) m_used = row_max();
-      // A row that sees no key of its range keeps m_used = -inf and p = 0.
-      exp_pass(m_used == -INFINITY ? 0.0f : -m_used);
-      const float tile_sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-      // One warp vote for: a possible rescale (bit 0), P buffer still busy
-      // (bit 1), next S not yet seen (bit 2).
-      const unsigned votes = __reduce_or_sync(
-          0xffffffffu, (!(tile_sum <= kRescaleSum) ? 1u : 0u) | (p_free ? 0u : 2u) | (s_next ? 0u : 4u));
-      s_ready = (votes & 4u) == 0u;
-      if (votes & 1u) {
+      // The rare rescale path takes a second trip through this one copy of
+      // the exponential loop (a second inlined copy measured slower).
+      unsigned votes;
+      for (int pass = 0;; ++pass) {
+        // A row that sees no key of its range keeps m_used = -inf and p = 0.
+        exp_pass(m_used == -INFINITY ? 0.0f : -m_used);
+        if (pass == 1) break;
+        const float tile_sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+        // One warp vote for: a possible rescale (bit 0), P buffer still busy
+        // (bit 1), next S not yet seen (bit 2).
+        votes = __reduce_or_sync(
+            0xffffffffu, (!(tile_sum <= kRescaleSum) ? 1u : 0u) | (p_free ? 0u : 2u) | (s_next ? 0u : 4u));
+        if (!(votes & 1u)) break;
         // Rare: some row's maximum may have outgrown m_used.
         const float m_tile = row_max();
         const bool need = m_tile > m_used + kRescaleLog2;
-        if (__any_sync(0xffffffffu, need)) {
-          // O must hold P(t-1) V(t-1) before it is rescaled (j > 0 here: the
-          // first tile's maximum is exact).
-          const uint32_t tp = t - 1u;
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kPvDone + (tp & 1u)), (tp >> 1) & 1u, wc));
-          if (!ok) break;
-          tc_fence_after();
-          const float f = need ? ex2(m_used - m_tile) : 1.0f;
-          if (need) {
-            m_used = m_tile;
-            l *= f;
-          }
+        if (!__any_sync(0xffffffffu, need)) break;
+        // O must hold P(t-1) V(t-1) before it is rescaled (j > 0 here: the
+        // first tile's maximum is exact).
+        const uint32_t tp = t - 1u;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kPvDone + (tp & 1u)), (tp >> 1) & 1u, wc));
+        if (!ok) break;
+        tc_fence_after();
+        const float f = need ? ex2(m_used - m_tile) : 1.0f;
+        if (need) {
+          m_used = m_tile;
+          l *= f;
+        }
 #pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t o[32];
-            tmem_ld_x32(tO + (uint32_t)c0, o);
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld_x32(tO + (uint32_t)c0, o);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * f);
-            tmem_st_x32(tO + (uint32_t)c0, o);
-          }
-          exp_pass(m_used == -INFINITY ? 0.0f : -m_used);
+          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * f);
+          tmem_st_x32(tO + (uint32_t)c0, o);
         }
       }
+      if (!ok) break;
+      s_ready = (votes & 4u) == 0u;
       l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
       if (votes & 2u) {
         ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kPvDone + b), (tpp >> 1) & 1u, wc));
@@ -400,32 +423,72 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint32_t tme
       mbar_arrive(bar(C::kPReady + b));
     }
     if (!ok) break;
+    // Hand the unit's row statistics to the epilogue warps, once they have
+    // taken the previous unit's.
+    if (u > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kLmFree), (u - 1u) & 1u, wc));
+      if (!ok) break;
+    }
+    lm[r] = make_float2(m_used, l);
+    mbar_arrive(bar(C::kLmFull));
+    g += (uint32_t)w.n_kt;
+  }
+}
+
+// Epilogue warpgroup (warps 8-11): thread r owns row r of O in TMEM.  Per
+// unit it takes (m, l) from the softmax, waits for the unit's last P V,
+// moves O into registers and frees it for the next unit's first product,
+// then writes O / l as bf16 and the natural-log LSE.
+template <int D, bool F8>
+__device__ void epilogue_role(const KernelParams& p, uint32_t sbase, const uint8_t* sgen,
+                              uint32_t tmem, int beg, int end, const WaitCtl& wc) {
+  using C = Cfg<D, F8>;
+  auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quad = warp & 3;
+  const int r = quad * 32 + lane;
+  const uint32_t tO = tmem + ((uint32_t)(quad * 32) << 16) + C::kColO;
+  const float2* lm = reinterpret_cast<const float2*>(sgen + C::kOffLm);
+  uint32_t g = 0, u = 0;
+  bool ok = true;
+  for (UnitIter ui(p.items, beg, end); ui.valid() && ok; ui.next(), ++u) {
+    const pk_work_item& w = ui.w;
+    const int h = ui.head();
+    const bool valid = r < w.q_rows;
+    if (!(ok = __all_sync(0xffffffffu, mbar_wait_sleep(bar(C::kLmFull), u & 1u, wc)))) break;
+    const float2 ml = lm[r];
+    mbar_arrive(bar(C::kLmFree));
     const uint32_t tl = g + (uint32_t)w.n_kt - 1u;  // the unit's last product
-    ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kPvDone + (tl & 1u)), (tl >> 1) & 1u, wc));
+    ok = __all_sync(0xffffffffu, mbar_wait_sleep(bar(C::kPvDone + (tl & 1u)), (tl >> 1) & 1u, wc));
     if (!ok) break;
     tc_fence_after();
-    const float inv_l = l > 0.f ? 1.0f / l : 0.f;  // a row without keys writes zeros
-    uint8_t* orow = p.out + (((size_t)(w.q_start + r) * (size_t)p.hq + (size_t)h) * D) * 2;
-#pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 32) {
-      uint32_t o[32];
-      tmem_ld_x32(tO + (uint32_t)c0, o);
-      uint32_t bb[16];
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        bb[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv_l, __uint_as_float(o[2 * c + 1]) * inv_l);
-      if (valid) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + (size_t)c0 * 2);
-#pragma unroll
-        for (int v = 0; v < 4; ++v)
-          dst[v] = make_uint4(bb[4 * v], bb[4 * v + 1], bb[4 * v + 2], bb[4 * v + 3]);
-      }
+    uint32_t o[D];
+    if constexpr (D == 128) {
+      tmem_ld_x128(tO, o);
+    } else {
+      uint32_t (&o0)[32] = *reinterpret_cast<uint32_t (*)[32]>(&o[0]);
+      uint32_t (&o1)[32] = *reinterpret_cast<uint32_t (*)[32]>(&o[32]);
+      tmem_ld_x32(tO, o0);
+      tmem_ld_x32(tO + 32u, o1);
     }
     tc_fence_before();
     mbar_arrive(bar(C::kOFree));
-    if (valid)
+    const float l = ml.y;
+    const float inv_l = l > 0.f ? 1.0f / l : 0.f;  // a row without keys writes zeros
+    if (valid) {
+      uint8_t* orow = p.out + (((size_t)(w.q_start + r) * (size_t)p.hq + (size_t)h) * D) * 2;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 8) {
+        uint4 v4;
+        v4.x = pack_bf16x2(__uint_as_float(o[c0 + 0]) * inv_l, __uint_as_float(o[c0 + 1]) * inv_l);
+        v4.y = pack_bf16x2(__uint_as_float(o[c0 + 2]) * inv_l, __uint_as_float(o[c0 + 3]) * inv_l);
+        v4.z = pack_bf16x2(__uint_as_float(o[c0 + 4]) * inv_l, __uint_as_float(o[c0 + 5]) * inv_l);
+        v4.w = pack_bf16x2(__uint_as_float(o[c0 + 6]) * inv_l, __uint_as_float(o[c0 + 7]) * inv_l);
+        *reinterpret_cast<uint4*>(orow + (size_t)c0 * 2) = v4;
+      }
       p.lse[(size_t)h * (size_t)p.T + (size_t)(w.q_start + r)] =
-          l > 0.f ? (m_used + __log2f(l)) * 0.69314718055994530942f : -INFINITY;
+          l > 0.f ? (ml.x + __log2f(l)) * 0.69314718055994530942f : -INFINITY;
+    }
     g += (uint32_t)w.n_kt;
   }
 }
@@ -465,6 +528,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(C::kOFree), 128);
     mbar_init(bar(C::kMmaDone + 0), 1);
     mbar_init(bar(C::kMmaDone + 1), 1);
+    mbar_init(bar(C::kLmFull), 128);
+    mbar_init(bar(C::kLmFree), 128);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     tma_prefetch_desc(&tm_q);
@@ -485,20 +550,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int beg = p.cta_offsets[blockIdx.x], end = p.cta_offsets[blockIdx.x + 1];
   const WaitCtl wc{abort_flag, p.status, p.wait_limit_ns};
 
-  if (warp == 0) {
-    if (lane == 0) producer_qk_role<D, F8>(p, &tm_q, &tm_k, sbase, beg, end, wc);
+  if (warp < 4) {
+    // Producers and MMA issuers: one thread each, few registers.
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsMma));
+    if (warp == 0) {
+      if (lane == 0) producer_qk_role<D, F8>(p, &tm_q, &tm_k, sbase, beg, end, wc);
+    } else if (warp == 1) {
+      if (lane == 0) mma_s_role<D, F8>(p, sbase, tmem, beg, end, wc);
+    } else if (warp == 2) {
+      if (lane == 0) producer_v_role<D, F8>(p, &tm_v, sbase, beg, end, wc);
+    } else {
+      if (lane == 0) mma_pv_role<D, F8>(p, sbase, tmem, beg, end, wc);
+    }
     __syncwarp();
-  } else if (warp == 1) {
-    if (lane == 0) mma_s_role<D, F8>(p, sbase, tmem, beg, end, wc);
-    __syncwarp();
-  } else if (warp == 2) {
-    if (lane == 0) producer_v_role<D, F8>(p, &tm_v, sbase, beg, end, wc);
-    __syncwarp();
-  } else if (warp == 3) {
-    if (lane == 0) mma_pv_role<D, F8>(p, sbase, tmem, beg, end, wc);
-    __syncwarp();
+  } else if (warp < 8) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    softmax_role<D, F8>(p, sbase, sgen, tmem, beg, end, wc);
   } else {
-    softmax_role<D, F8>(p, sbase, tmem, beg, end, wc);
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
+    epilogue_role<D, F8>(p, sbase, sgen, tmem, beg, end, wc);
   }
 
   tc_fence_before();
@@ -619,6 +689,20 @@ pk_status launch(const pk_plan* plan, const void* q, const void* k, const void* 
     cudaGetLastError();
     return PK_ERR_CUDA;
   }
+  // The warpgroups' register split draws on the CTA's launch allocation: a
+  // build whose kernel was compiled with fewer registers per thread must
+  // not launch (its setmaxnreg increases could never be granted).
+  static std::atomic<int> regs_state{0};  // 0 unknown, 1 fits, 2 does not
+  if (regs_state.load() == 0) {
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, pk::dev::pk_attn_fwd_kernel<D, F8>) != cudaSuccess) {
+      cudaGetLastError();
+      return PK_ERR_CUDA;
+    }
+    regs_state.store(fa.numRegs >= pk::dev::kRegsLaunch && fa.maxThreadsPerBlock >= pk::dev::kThreads
+                         ? 1 : 2);
+  }
+  if (regs_state.load() != 1) return PK_ERR_UNSUPPORTED;
   const uint8_t* img = static_cast<const uint8_t*>(plan->dev);
   pk::dev::KernelParams kp;
   kp.items = reinterpret_cast<const pk_work_item*>(img + plan->layout.items_off);

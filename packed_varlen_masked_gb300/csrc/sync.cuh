@@ -37,6 +37,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// try_wait that may suspend the thread for up to `ns` nanoseconds while the
+// phase is incomplete (it resumes as soon as the phase completes).
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -62,7 +75,9 @@ struct WaitCtl {
 
 // Slow path of a bounded wait: poll until the phase completes, the CTA has
 // aborted, or the time limit passes (then record the timeout and abort).
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, WaitCtl c,
+// Inlined: an out-of-line call inside the softmax loop constrains its
+// register allocation, which measured about 1% slower.
+static __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, WaitCtl c,
                                             bool honour_abort) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t n = 1;; ++n) {
@@ -85,6 +100,23 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, const WaitCtl& c) {
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, c, false);
+}
+
+// Bounded wait for a waiter with nothing else to do (the epilogue warps
+// between units): each try suspends the thread for up to 2 us, so the
+// waiting warps take no issue slots from the softmax warps on the same SM
+// sub-partitions.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, const WaitCtl& c) {
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_hint(bar, parity, 2000u)) return true;
+    if (*c.abort_flag) return false;
+    if (globaltimer_ns() - t0 > c.limit_ns) {
+      *c.abort_flag = 1;
+      if (c.status) atomicCAS(c.status, 0, (int32_t)PK_ERR_TIMEOUT);
+      return false;
+    }
+  }
 }
 
 }  // namespace dev
