@@ -668,6 +668,7 @@ def main():
                                            if peaks.get("bf16_tflops_sustained") else None),
                      "peak_source": peaks["source"] + " (bf16 burst)",
                      "kernel": "pk_attn_fwd_kernel<128>", "launch_ms_mean": round(avg_launch_ms, 4),
+                     "launch_ms_median": round(statistics.median(launch_ms), 4),
                      "launch_ms_min": round(min(launch_ms), 4)},
         "cpu_baseline": cpu,
         "e2e": e2e,

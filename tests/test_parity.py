@@ -122,6 +122,22 @@ def test_full_size_configs_sampled(name, budget):
     _compare(pack, out_g, lse_g, out_o, lse_o, rows=rows)
 
 
+@pytest.mark.parametrize("name,budget", [("mixed_resolution", 1536), ("highres_edit", 512),
+                                         ("skewed", 1536)])
+def test_full_size_boundary_tiles(name, budget):
+    """Full-size packs, every row of the query tiles where the mask changes
+    shape (segment starts and ends, ragged sequence tails): the rows whose
+    key tiles are partial."""
+    pack = W.CONFIGS[name]()
+    q, k, v = W.make_qkv(pack)
+    rows = W.boundary_tile_rows(pack, budget)
+    assert len(rows) >= 256
+    out_o, lse_o = oracle.attention(q, k, v, pack.cu_seqlens, pack.segments, pack.hq,
+                                    pack.hkv, pack.d, pack.scale, rows=rows)
+    out_g, lse_g = _gpu(pack, q, k, v)
+    _compare(pack, out_g, lse_g, out_o, lse_o, rows=rows)
+
+
 def test_growing_maximum_rescales_output():
     """Scores that grow key tile after key tile force the running maximum to
     move by more than the lazy-rescale threshold many times."""

@@ -204,6 +204,34 @@ def sample_rows(pack: Pack, budget: int, seed: int = 1, tile: int = 128) -> np.n
     return rows[:budget]
 
 
+def boundary_tile_rows(pack: Pack, budget: int, tile: int = 128) -> np.ndarray:
+    """Every row of the 128-row query tiles where the mask changes shape: the
+    tile holding each segment's first and last row and each sequence's last
+    (ragged) tile, taken sequence by sequence (shortest first, so that every
+    kind of sequence is represented) until ``budget`` rows."""
+    cu = pack.cu_seqlens
+    tiles = []
+    for s in range(len(cu) - 1):
+        b, e = int(cu[s]), int(cu[s + 1])
+        if e == b:
+            continue
+        starts = {b + ((e - 1 - b) // tile) * tile}
+        for st, n, _ in pack.segments:
+            st, n = int(st), int(n)
+            if b <= st < e:
+                starts.add(b + ((st - b) // tile) * tile)
+                starts.add(b + ((st + n - 1 - b) // tile) * tile)
+        tiles.append((e - b, sorted((t0, min(t0 + tile, e)) for t0 in starts)))
+    tiles.sort(key=lambda x: x[0])
+    rows: List[int] = []
+    for _, ts in tiles:
+        for t0, t1 in ts:
+            if len(rows) + (t1 - t0) > budget:
+                return np.unique(np.asarray(rows, dtype=np.int32))
+            rows.extend(range(t0, t1))
+    return np.unique(np.asarray(rows, dtype=np.int32))
+
+
 def seq_segments(pack: Pack) -> np.ndarray:
     """[G, 4] int32 (seq, start, len, type): segments in each sequence's own
     position space."""
