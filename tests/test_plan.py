@@ -145,3 +145,28 @@ def test_invalid_descriptors(cu, segs, hq, hkv, d, code):
     with pytest.raises(PKError) as ei:
         pk.Plan(cu, segs, hq, hkv, d, num_ctas=4, upload=False)
     assert ei.value.status == code
+
+
+def test_boundary_tile_rows_are_whole_mask_boundary_tiles():
+    """The full-size parity sample of mask-boundary tiles: whole 128-row
+    query tiles, each holding a segment's first or last row or a sequence's
+    last row, and the tiles in which a row's key limit changes shape."""
+    for name in ["mixed_resolution", "skewed", "cfg_pair"]:
+        pack = W.CONFIGS[name]()
+        rows = W.boundary_tile_rows(pack, 1536)
+        cu = pack.cu_seqlens
+        assert 0 < len(rows) <= 1536 and np.all(np.diff(rows) > 0)
+        seq = np.searchsorted(cu, rows, side="right") - 1
+        edges = set()
+        for s in range(len(cu) - 1):
+            edges.add(int(cu[s + 1]) - 1)
+        for st, n, _ in pack.segments:
+            edges.update((int(st), int(st + n - 1)))
+        tiles = {}
+        for r, s in zip(rows.tolist(), seq.tolist()):
+            t0 = int(cu[s]) + (r - int(cu[s])) // 128 * 128
+            tiles.setdefault((s, t0), []).append(r)
+        for (s, t0), rs in tiles.items():
+            t1 = min(t0 + 128, int(cu[s + 1]))
+            assert rs == list(range(t0, t1)), "a sampled tile is whole"
+            assert any(t0 <= e < t1 for e in edges), "it holds a segment or sequence edge"
