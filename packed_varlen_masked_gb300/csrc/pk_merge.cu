@@ -187,10 +187,18 @@ __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// Stage layout when every part is bf16 (known at compile time).
-template <int NP>
-struct Bf16Layout {
-  static constexpr int kLseOff = NP * kChunkBytes;
+// Stage layout when the parts' element types are known at compile time:
+// bit c of kMask set means part c is fp32 (its rows of a chunk take twice
+// the bytes of bf16 rows); the parts' rows one after another, then the LSEs.
+template <int NP, int kMask>
+struct StageLayout {
+  __host__ __device__ static constexpr int part_bytes(int c) { return ((kMask >> c) & 1) ? 2 * kChunkBytes : kChunkBytes; }
+  __host__ __device__ static constexpr int part_off(int c) {
+    int o = 0;
+    for (int i = 0; i < c; ++i) o += part_bytes(i);
+    return o;
+  }
+  static constexpr int kLseOff = part_off(NP);
   static constexpr int kStBytes = (kLseOff + NP * (kChunkBytes / 128) * 4 + 127) & ~127;
   static constexpr int kStagesFit = kStageBudget / kStBytes;
   static constexpr int kStages = kStagesFit < kMaxStages ? kStagesFit : kMaxStages;
@@ -198,23 +206,25 @@ struct Bf16Layout {
   static_assert(kStages >= 2 && kSmem <= 227 * 1024, "shared memory budget");
 };
 
-// kBf16: every part is bf16, so the stage layout and the element size are
-// compile-time constants; otherwise they come from Params.
-template <int NP, bool kOutF32, bool kBf16>
+// kMask >= 0: the parts' element types (bit c: part c is fp32) are known at
+// compile time, and so are the stage layout and every element size;
+// kMask < 0: they come from Params.
+template <int NP, bool kOutF32, int kMask>
 __global__ void __launch_bounds__(kBulkThreads, 1) lse_merge_bulk_kernel(const Params p) {
   using namespace pk::dev;
-  using BL = Bf16Layout<NP>;
+  constexpr bool kFixed = kMask >= 0;
+  using BL = StageLayout<NP, kFixed ? kMask : 0>;
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t n_stages = kBf16 ? (uint32_t)BL::kStages : (uint32_t)p.n_stages;
-  const uint32_t st_bytes = kBf16 ? (uint32_t)BL::kStBytes : (uint32_t)p.st_bytes;
+  const uint32_t n_stages = kFixed ? (uint32_t)BL::kStages : (uint32_t)p.n_stages;
+  const uint32_t st_bytes = kFixed ? (uint32_t)BL::kStBytes : (uint32_t)p.st_bytes;
   const uint32_t off_bar = n_stages * st_bytes;
-  auto is_f32 = [&](int c) { return kBf16 ? false : p.f32[c] != 0; };
+  auto is_f32 = [&](int c) { return kFixed ? ((kMask >> c) & 1) != 0 : p.f32[c] != 0; };
   auto stage_o = [&](uint32_t s, int c) {
-    return s * st_bytes + (kBf16 ? (uint32_t)(c * kChunkBytes) : (uint32_t)p.part_off[c]);
+    return s * st_bytes + (kFixed ? (uint32_t)BL::part_off(c) : (uint32_t)p.part_off[c]);
   };
   auto stage_l = [&](uint32_t s, int c) {
-    return s * st_bytes + (kBf16 ? (uint32_t)BL::kLseOff : (uint32_t)p.lse_off) +
+    return s * st_bytes + (kFixed ? (uint32_t)BL::kLseOff : (uint32_t)p.lse_off) +
            (uint32_t)c * (kChunkBytes / 128) * 4u;
   };
   auto full = [&](uint32_t s) { return sbase + off_bar + 8u * s; };
@@ -407,11 +417,11 @@ pk_status launch_regs(const Params& p, int64_t rows, int sms, cudaStream_t st) {
 
 // Stage layout from the parts' element types: each part's rows of a chunk
 // (bf16 or fp32) one after another, then every part's LSEs.
-template <int NP, bool kOutF32, bool kBf16>
+template <int NP, bool kOutF32, int kMask>
 pk_status launch_bulk(Params p, int64_t rows, int sms, cudaStream_t st) {
   const int rpc = kChunkBytes / (2 * p.d);
-  int smem = Bf16Layout<NP>::kSmem;
-  if (!kBf16) {
+  int smem = StageLayout<NP, kMask >= 0 ? kMask : 0>::kSmem;
+  if (kMask < 0) {
     int off = 0;
     for (int c = 0; c < p.num_parts; ++c) {
       p.part_off[c] = off;
@@ -424,7 +434,7 @@ pk_status launch_bulk(Params p, int64_t rows, int sms, cudaStream_t st) {
     if (p.n_stages < 2) return PK_ERR_UNSUPPORTED;
     smem = p.n_stages * p.st_bytes + kBulkTail;
   }
-  auto kern = lse_merge_bulk_kernel<NP, kOutF32, kBf16>;
+  auto kern = lse_merge_bulk_kernel<NP, kOutF32, kMask>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess) {
     cudaGetLastError();
@@ -481,12 +491,14 @@ extern "C" pk_status pk_lse_merge(const pk_merge_part* parts, int32_t num_parts,
     bool bf16 = true;
     for (int c = 0; c < num_parts; ++c) bf16 = bf16 && !p.f32[c];
     if (bf16) {
-      if (num_parts == 1) return f ? launch_bulk<1, true, true>(p, rows, sms, st) : launch_bulk<1, false, true>(p, rows, sms, st);
-      if (num_parts == 2) return f ? launch_bulk<2, true, true>(p, rows, sms, st) : launch_bulk<2, false, true>(p, rows, sms, st);
-      return f ? launch_bulk<4, true, true>(p, rows, sms, st) : launch_bulk<4, false, true>(p, rows, sms, st);
+      if (num_parts == 1) return f ? launch_bulk<1, true, 0>(p, rows, sms, st) : launch_bulk<1, false, 0>(p, rows, sms, st);
+      if (num_parts == 2) return f ? launch_bulk<2, true, 0>(p, rows, sms, st) : launch_bulk<2, false, 0>(p, rows, sms, st);
+      return f ? launch_bulk<4, true, 0>(p, rows, sms, st) : launch_bulk<4, false, 0>(p, rows, sms, st);
     }
-    if (num_parts <= 2) return f ? launch_bulk<2, true, false>(p, rows, sms, st) : launch_bulk<2, false, false>(p, rows, sms, st);
-    return f ? launch_bulk<4, true, false>(p, rows, sms, st) : launch_bulk<4, false, false>(p, rows, sms, st);
+    // A ring step: a running fp32 accumulator folded with one bf16 block.
+    if (num_parts == 2 && p.f32[0] && !p.f32[1] && f) return launch_bulk<2, true, 1>(p, rows, sms, st);
+    if (num_parts <= 2) return f ? launch_bulk<2, true, -1>(p, rows, sms, st) : launch_bulk<2, false, -1>(p, rows, sms, st);
+    return f ? launch_bulk<4, true, -1>(p, rows, sms, st) : launch_bulk<4, false, -1>(p, rows, sms, st);
   }
   if (num_parts <= 2) return launch_regs<2>(p, rows, sms, st);
   if (num_parts <= 4) return launch_regs<4>(p, rows, sms, st);
