@@ -651,7 +651,7 @@ bool make_map(CUtensorMap* m, const void* base, int H, int T, int D, int elem_by
 // Device capability check, cached per device ordinal.
 pk_status check_device() {
   static std::mutex mu;
-  static int verdict[64];  // 0 unknown, 1 ok, 2 unsupported
+  static int cap_state[64];  // 0 unknown, 1 ok, 2 unsupported
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
@@ -659,16 +659,16 @@ pk_status check_device() {
   }
   if (dev < 0 || dev >= 64) return PK_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lk(mu);
-  if (verdict[dev] == 0) {
+  if (cap_state[dev] == 0) {
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
       cudaGetLastError();
       return PK_ERR_CUDA;
     }
-    verdict[dev] = (major == 10 && minor == 3) ? 1 : 2;
+    cap_state[dev] = (major == 10 && minor == 3) ? 1 : 2;
   }
-  return verdict[dev] == 1 ? PK_OK : PK_ERR_UNSUPPORTED;
+  return cap_state[dev] == 1 ? PK_OK : PK_ERR_UNSUPPORTED;
 }
 
 // scale: the softmax scale of the scores as the MMA computes them (for FP8
