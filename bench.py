@@ -451,6 +451,31 @@ def fp8_bench(pk, torch, stream, dev, pack, q, k, v, reps=10):
     return res
 
 
+def precise_bench(pk, torch, stream, dev, pack, q, k, v, reps=10):
+    """The workload through pk_attn_fwd_precise (O divided by the sum of the
+    bf16 probabilities the tensor cores take), and the default path timed
+    beside it in the same way."""
+    plan = pk.plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty(pack.hq, pack.total_tokens, dtype=torch.float32, device=dev)
+    res = {}
+    for key, precise in (("default", False), ("precise", True)):
+        for _ in range(3):
+            pk.attn_fwd(q, k, v, plan, pack.scale, out=out, lse=lse, precise=precise)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            pk.attn_fwd(q, k, v, plan, pack.scale, out=out, lse=lse, precise=precise)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        res[key] = {"ms": round(ms, 4), "useful_tflops": round(plan.useful_flops / ms / 1e9, 1)}
+    del out, lse, plan
+    torch.cuda.empty_cache()
+    return res
+
+
 def sweep(pk, torch, stream, dev):
     """Timing-only pass over every workload (device-generated inputs)."""
     res = {}
@@ -625,10 +650,11 @@ def main():
     per_workload = None
     if not args.no_sweep and rank == 0:
         per_workload = sweep(pk, torch, stream, dev)
-    layouts = fp8 = None
+    layouts = fp8 = precise = None
     if not args.no_sweep and rank == 0:
         layouts = layouts_bench(pk, torch, stream, dev, pack, q, k, v)
         fp8 = fp8_bench(pk, torch, stream, dev, pack, q, k, v)
+        precise = precise_bench(pk, torch, stream, dev, pack, q, k, v)
     merge = None
     if not args.no_merge and rank == 0:
         merge = merge_bench(pk, torch, stream, pack, out, lse)
@@ -680,6 +706,7 @@ def main():
         "replaced_path": replaced,
         "layouts": layouts,
         "fp8_qk": fp8,
+        "precise_norm": precise,
         "lse_merge": merge,
     }
     print(json.dumps(line), flush=True)

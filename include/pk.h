@@ -191,6 +191,20 @@ pk_status pk_attn_fwd(const pk_plan* plan, const void* q, const void* k,
                       pk_stream_t stream, int32_t* dev_status);
 
 /*
+ * The same attention with precise normalisation: O is divided by the sum of
+ * the bf16 probabilities the P·V tensor-core product takes (read back from
+ * tensor memory tile by tile), so the weights applied to V sum to one
+ * exactly; the LSE still comes from the fp32 sum of the unrounded ones.
+ * This halves the output error on rows that a few keys dominate (the q ×4
+ * workload's sharpest rows: 4.9e-3 against 1.07e-2 above the output's half
+ * ulp) and costs ~20% of the throughput.  Arguments, layouts, errors and
+ * asynchrony as for pk_attn_fwd.
+ */
+pk_status pk_attn_fwd_precise(const pk_plan* plan, const void* q, const void* k,
+                              const void* v, void* out, float* lse, float scale,
+                              pk_stream_t stream, int32_t* dev_status);
+
+/*
  * FP8 variant: queries and keys as FP8 E4M3 codes (1 sign, 4 exponent bits
  * with bias 7, 3 mantissa bits; the OCP 8-bit format), one dequantisation
  * scale each, values bf16.  The scores are scale * q_scale * k_scale *

@@ -87,6 +87,7 @@ SIGNATURES = {
     "pk_plan_device_bytes": (ctypes.c_size_t, [_vp]),
     "pk_plan_upload": (ctypes.c_int, [_vp, _vp, ctypes.c_size_t, _vp]),
     "pk_attn_fwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),
+    "pk_attn_fwd_precise": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),
     "pk_attn_fwd_fp8": (ctypes.c_int, [_vp, _vp, ctypes.c_float, _vp, ctypes.c_float, _vp, _vp,
                                        _vp, ctypes.c_float, _vp, _vp]),
     "pk_attn_fwd_host": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,

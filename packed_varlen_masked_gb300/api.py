@@ -174,13 +174,15 @@ def _check_tensor(t, name, shape):
 
 
 def attn_fwd(q, k, v, plan: Plan, scale: Optional[float] = None, out=None, lse=None,
-             status=None, check_status: bool = False):
+             status=None, check_status: bool = False, precise: bool = False):
     """Packed mixed-mask attention forward on the current CUDA stream.
 
     q [T, hq, d], k and v [Tk, hkv, d] bf16 CUDA tensors (Tk = T for a
     plan from ``plan``; the key rows or pool rows for ``plan_layout``).
     Returns (out bf16 [T, hq, d], lse fp32 [hq, T]).  With ``check_status`` the call
     synchronises and raises if the kernel reported a device-side failure.
+    ``precise`` selects pk_attn_fwd_precise (O divided by the sum of the
+    bf16 probabilities the tensor cores take; ~20% slower).
     """
     import torch
     T, hq, hkv, d = plan.total_tokens, plan.hq, plan.hkv, plan.head_dim
@@ -202,12 +204,13 @@ def attn_fwd(q, k, v, plan: Plan, scale: Optional[float] = None, out=None, lse=N
         status = torch.zeros(1, dtype=torch.int32, device=q.device)
     stream = torch.cuda.current_stream(q.device).cuda_stream
     lib = plan._lib
-    check(lib.pk_attn_fwd(plan.handle, ctypes.c_void_p(q.data_ptr()),
+    fn = lib.pk_attn_fwd_precise if precise else lib.pk_attn_fwd
+    check(fn(plan.handle, ctypes.c_void_p(q.data_ptr()),
                           ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()),
                           ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(lse.data_ptr()),
                           float(scale), ctypes.c_void_p(stream),
                           ctypes.c_void_p(status.data_ptr() if status is not None else 0)),
-          "pk_attn_fwd")
+          "pk_attn_fwd_precise" if precise else "pk_attn_fwd")
     if check_status:
         torch.cuda.current_stream(q.device).synchronize()
         check(int(status.item()), "pk_attn_fwd (device)")

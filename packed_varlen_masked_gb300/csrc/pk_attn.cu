@@ -107,9 +107,14 @@ struct Cfg {
   static constexpr int kMmaDone = kOFree + 1;  // [2]: one per MMA issuer
   static constexpr int kLmFull = kMmaDone + 2;   // a unit's row (m, l) handed over
   static constexpr int kLmFree = kLmFull + 1;    // ... and taken by the epilogue
-  static constexpr int kNumBars = kLmFree + 1;
+  // Precise normalisation only: the epilogue has summed P(t) [2], and the
+  // softmax's posts of a rare rescale factor for the epilogue's sum.
+  static constexpr int kPRead = kLmFree + 1;
+  static constexpr int kNumBars = kPRead + 2;
   static constexpr int kOffLm = kOffBar + kNumBars * 8;  // float2 [128]
-  static constexpr int kOffMisc = kOffLm + 128 * 8;
+  static constexpr int kOffF = kOffLm + 128 * 8;         // float [128]: a tile's rescale factor
+  static constexpr int kOffFlag = kOffF + 128 * 4;       // u32 [4][2]: factor posted, per warp and tile parity
+  static constexpr int kOffMisc = kOffFlag + 32;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   static_assert(kSmemBytes > 114 * 1024, "one CTA per SM");
@@ -289,7 +294,10 @@ __device__ void mma_pv_role(const KernelParams& p, uint32_t sbase, uint32_t tmem
 }
 
 // Softmax warpgroup (warps 4-7): thread r owns row r of S, P and O in TMEM.
-template <int D, bool F8>
+// PN (precise normalisation): the epilogue also reads every P(t) back, so
+// P buffer b is free only once it has, and a rare rescale's factor is
+// posted to it.
+template <int D, bool F8, bool PN>
 __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint8_t* sgen, uint32_t tmem,
                              int beg, int end, const WaitCtl& wc) {
   using C = Cfg<D, F8>;
@@ -332,7 +340,8 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint8_t* sge
       // P buffer b last held P(t-2); test early whether its product has
       // been read, so the barrier latency hides under the exponentials.
       const uint32_t tpp = t - 2u;
-      const bool p_free = t < 2 || mbar_test_wait(bar(C::kPvDone + b), (tpp >> 1) & 1u);
+      const bool p_free = t < 2 || (mbar_test_wait(bar(C::kPvDone + b), (tpp >> 1) & 1u) &&
+                                    (!PN || mbar_test_wait(bar(C::kPRead + b), (tpp >> 1) & 1u)));
       // Likewise whether S(t+1) has landed (S(t+3) cannot complete before
       // this softmax frees S(t+1)'s buffer, so a yes stays valid).
       const bool s_next = mbar_test_wait(bar(C::kSFull + (b ^ 1u)), ((t + 1u) >> 1) & 1u);
@@ -409,12 +418,24 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint8_t* sge
           for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * f);
           tmem_st_x32(tO + (uint32_t)c0, o);
         }
+        if constexpr (PN) {
+          // The epilogue's sum of the bf16 P takes the same factor: once it
+          // has summed P(t-1) (and so taken any earlier factor), post this
+          // tile's.
+          const uint32_t tq = t - 1u;
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kPRead + (tq & 1u)), (tq >> 1) & 1u, wc));
+          if (!ok) break;
+          reinterpret_cast<float*>(sgen + C::kOffF)[r] = f;
+          if (lane == 0)
+            reinterpret_cast<volatile uint32_t*>(sgen + C::kOffFlag)[quad * 2 + (int)(t & 1u)] = 1u;
+        }
       }
       if (!ok) break;
       s_ready = (votes & 4u) == 0u;
       l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
       if (votes & 2u) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kPvDone + b), (tpp >> 1) & 1u, wc));
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kPvDone + b), (tpp >> 1) & 1u, wc) &&
+                                         (!PN || mbar_wait(bar(C::kPRead + b), (tpp >> 1) & 1u, wc)));
         if (!ok) break;
       }
       tc_fence_after();
@@ -438,9 +459,12 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint8_t* sge
 // Epilogue warpgroup (warps 8-11): thread r owns row r of O in TMEM.  Per
 // unit it takes (m, l) from the softmax, waits for the unit's last P V,
 // moves O into registers and frees it for the next unit's first product,
-// then writes O / l as bf16 and the natural-log LSE.
-template <int D, bool F8>
-__device__ void epilogue_role(const KernelParams& p, uint32_t sbase, const uint8_t* sgen,
+// then writes O / l as bf16 and the natural-log LSE.  PN: O is divided
+// instead by the sum of the bf16 P the P V product took, which this warp
+// group reads back from TMEM tile by tile (so the weights applied to V sum
+// to one); l still gives the LSE.
+template <int D, bool F8, bool PN>
+__device__ void epilogue_role(const KernelParams& p, uint32_t sbase, uint8_t* sgen,
                               uint32_t tmem, int beg, int end, const WaitCtl& wc) {
   using C = Cfg<D, F8>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
@@ -455,6 +479,40 @@ __device__ void epilogue_role(const KernelParams& p, uint32_t sbase, const uint8
     const pk_work_item& w = ui.w;
     const int h = ui.head();
     const bool valid = r < w.q_rows;
+    float lp = 0.f;  // PN: sum of the unit's bf16 P
+    if constexpr (PN) {
+      const uint32_t tP0 = tmem + ((uint32_t)(quad * 32) << 16) + C::kColP0;
+      volatile uint32_t* flags = reinterpret_cast<volatile uint32_t*>(sgen + C::kOffFlag);
+      for (int j = 0; j < w.n_kt && ok; ++j) {
+        const uint32_t t = g + (uint32_t)j, b = t & 1u;
+        ok = __all_sync(0xffffffffu, mbar_wait_sleep(bar(C::kPReady + b), (t >> 1) & 1u, wc));
+        if (!ok) break;
+        tc_fence_after();
+        if (flags[quad * 2 + (int)b] != 0u) {  // rare: the softmax rescaled at this tile
+          lp *= reinterpret_cast<const float*>(sgen + C::kOffF)[r];
+          __syncwarp();
+          if (lane == 0) flags[quad * 2 + (int)b] = 0u;
+        }
+        float a[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a[i] = 0.f;
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          uint32_t pv[32];
+          tmem_ld_x32(tP0 + b * 64u + (uint32_t)c0, pv);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int k = c & 3;
+            acc2(a[2 * k], a[2 * k + 1], __uint_as_float(pv[c] << 16),
+                 __uint_as_float(pv[c] & 0xffff0000u));
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bar(C::kPRead + b));
+        lp += ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+      }
+      if (!ok) break;
+    }
     if (!(ok = __all_sync(0xffffffffu, mbar_wait_sleep(bar(C::kLmFull), u & 1u, wc)))) break;
     const float2 ml = lm[r];
     mbar_arrive(bar(C::kLmFree));
@@ -474,7 +532,8 @@ __device__ void epilogue_role(const KernelParams& p, uint32_t sbase, const uint8
     tc_fence_before();
     mbar_arrive(bar(C::kOFree));
     const float l = ml.y;
-    const float inv_l = l > 0.f ? 1.0f / l : 0.f;  // a row without keys writes zeros
+    const float ln = PN ? lp : l;
+    const float inv_l = ln > 0.f ? 1.0f / ln : 0.f;  // a row without keys writes zeros
     if (valid) {
       uint8_t* orow = p.out + (((size_t)(w.q_start + r) * (size_t)p.hq + (size_t)h) * D) * 2;
 #pragma unroll
@@ -493,7 +552,7 @@ __device__ void epilogue_role(const KernelParams& p, uint32_t sbase, const uint8
   }
 }
 
-template <int D, bool F8>
+template <int D, bool F8, bool PN>
 __global__ void __launch_bounds__(kThreads, 1)
     pk_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -530,6 +589,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(C::kMmaDone + 1), 1);
     mbar_init(bar(C::kLmFull), 128);
     mbar_init(bar(C::kLmFree), 128);
+    mbar_init(bar(C::kPRead + 0), 128);
+    mbar_init(bar(C::kPRead + 1), 128);
+    for (int i = 0; i < 8; ++i) reinterpret_cast<volatile uint32_t*>(sgen + C::kOffFlag)[i] = 0u;
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     tma_prefetch_desc(&tm_q);
@@ -565,10 +627,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp < 8) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
-    softmax_role<D, F8>(p, sbase, sgen, tmem, beg, end, wc);
+    softmax_role<D, F8, PN>(p, sbase, sgen, tmem, beg, end, wc);
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
-    epilogue_role<D, F8>(p, sbase, sgen, tmem, beg, end, wc);
+    epilogue_role<D, F8, PN>(p, sbase, sgen, tmem, beg, end, wc);
   }
 
   tc_fence_before();
@@ -673,7 +735,7 @@ pk_status check_device() {
 
 // scale: the softmax scale of the scores as the MMA computes them (for FP8
 // queries/keys it includes their dequantisation scales).
-template <int D, bool F8 = false>
+template <int D, bool F8 = false, bool PN = false>
 pk_status launch(const pk_plan* plan, const void* q, const void* k, const void* v, void* out,
                  float* lse, float scale, cudaStream_t stream, int32_t* dev_status) {
   using C = pk::dev::Cfg<D, F8>;
@@ -683,7 +745,7 @@ pk_status launch(const pk_plan* plan, const void* q, const void* k, const void* 
       !make_map(&tk, k, plan->hkv, plan->Tk, D, qk_bytes) ||
       !make_map(&tv, v, plan->hkv, plan->Tk, D))
     return PK_ERR_CUDA;
-  if (cudaFuncSetAttribute(pk::dev::pk_attn_fwd_kernel<D, F8>,
+  if (cudaFuncSetAttribute(pk::dev::pk_attn_fwd_kernel<D, F8, PN>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kSmemBytes) != cudaSuccess) {
     cudaGetLastError();
@@ -695,7 +757,7 @@ pk_status launch(const pk_plan* plan, const void* q, const void* k, const void* 
   static std::atomic<int> regs_state{0};  // 0 unknown, 1 fits, 2 does not
   if (regs_state.load() == 0) {
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, pk::dev::pk_attn_fwd_kernel<D, F8>) != cudaSuccess) {
+    if (cudaFuncGetAttributes(&fa, pk::dev::pk_attn_fwd_kernel<D, F8, PN>) != cudaSuccess) {
       cudaGetLastError();
       return PK_ERR_CUDA;
     }
@@ -717,7 +779,7 @@ pk_status launch(const pk_plan* plan, const void* q, const void* k, const void* 
   kp.hq = plan->hq;
   kp.scale_log2 = scale * 1.4426950408889634f;
   kp.wait_limit_ns = g_wait_limit_ns.load();
-  pk::dev::pk_attn_fwd_kernel<D, F8>
+  pk::dev::pk_attn_fwd_kernel<D, F8, PN>
       <<<plan->num_ctas, pk::dev::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, kp);
   if (cudaGetLastError() != cudaSuccess) return PK_ERR_CUDA;
   return PK_OK;
@@ -735,9 +797,15 @@ extern "C" {
 
 void pk_set_wait_timeout_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : 1); }
 
-pk_status pk_attn_fwd(const pk_plan* plan, const void* q, const void* k, const void* v,
-                      void* out, float* lse, float scale, pk_stream_t stream,
-                      int32_t* dev_status) {
+}  // extern "C"
+
+namespace {
+
+// Argument checks and dispatch shared by the bf16 entry points.
+template <bool PN>
+pk_status attn_fwd_bf16(const pk_plan* plan, const void* q, const void* k, const void* v,
+                        void* out, float* lse, float scale, pk_stream_t stream,
+                        int32_t* dev_status) {
   if (plan == nullptr) return PK_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return PK_ERR_INVALID_ARG;
   if (plan->T == 0 || plan->items.empty()) return PK_OK;
@@ -750,9 +818,25 @@ pk_status pk_attn_fwd(const pk_plan* plan, const void* q, const void* k, const v
   pk_status st = check_device();
   if (st != PK_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (plan->head_dim == 128) return launch<128>(plan, q, k, v, out, lse, scale, s, dev_status);
-  if (plan->head_dim == 64) return launch<64>(plan, q, k, v, out, lse, scale, s, dev_status);
+  if (plan->head_dim == 128) return launch<128, false, PN>(plan, q, k, v, out, lse, scale, s, dev_status);
+  if (plan->head_dim == 64) return launch<64, false, PN>(plan, q, k, v, out, lse, scale, s, dev_status);
   return PK_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+extern "C" {
+
+pk_status pk_attn_fwd(const pk_plan* plan, const void* q, const void* k, const void* v,
+                      void* out, float* lse, float scale, pk_stream_t stream,
+                      int32_t* dev_status) {
+  return attn_fwd_bf16<false>(plan, q, k, v, out, lse, scale, stream, dev_status);
+}
+
+pk_status pk_attn_fwd_precise(const pk_plan* plan, const void* q, const void* k, const void* v,
+                              void* out, float* lse, float scale, pk_stream_t stream,
+                              int32_t* dev_status) {
+  return attn_fwd_bf16<true>(plan, q, k, v, out, lse, scale, stream, dev_status);
 }
 
 pk_status pk_attn_fwd_fp8(const pk_plan* plan, const void* q8, float q_scale, const void* k8,
