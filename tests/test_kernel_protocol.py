@@ -21,11 +21,11 @@ class _Bar:
         self.c += 1
 
 
-def _run(units, kst, vst, seed, rare, handover_wait=True):
+def _run(units, kst, vst, seed, rare, handover_wait=True, precise=False):
     rng = random.Random(seed)
     B = {}
     for i in range(2):
-        for nm in ("QFull", "QEmpty", "SFull", "SFree", "PReady", "PvDone"):
+        for nm in ("QFull", "QEmpty", "SFull", "SFree", "PReady", "PvDone", "PRead"):
             B[f"{nm}{i}"] = _Bar(f"{nm}{i}")
     for i in range(kst):
         B[f"KFull{i}"], B[f"KEmpty{i}"] = _Bar("KFull"), _Bar("KEmpty")
@@ -34,6 +34,7 @@ def _run(units, kst, vst, seed, rare, handover_wait=True):
     for nm in ("OFree", "LmFull", "LmFree"):
         B[nm] = _Bar(nm)
     pipe = []
+    posted = {0: None, 1: None}  # precise path: the tile whose rescale factor waits, per parity
 
     def W(n, par, k):  # wait for phase k of n (parity par)
         return ("wait", n, par, k)
@@ -96,8 +97,14 @@ def _run(units, kst, vst, seed, rare, handover_wait=True):
                 yield A(f"SFree{b}")
                 if j > 0 and rng.random() < rare:  # rescale O after P(t-1) V(t-1)
                     yield W(f"PvDone{(t - 1) & 1}", ((t - 1) >> 1) & 1, (t - 1) >> 1)
-                if t >= 2:  # P buffer b free: P(t-2) V(t-2) done
+                    if precise:  # post the factor once the epilogue has summed P(t-1)
+                        yield W(f"PRead{(t - 1) & 1}", ((t - 1) >> 1) & 1, (t - 1) >> 1)
+                        assert posted[b] is None, "a posted factor was overwritten"
+                        posted[b] = t
+                if t >= 2:  # P buffer b free: P(t-2) V(t-2) done (and, precise, summed)
                     yield W(f"PvDone{b}", ((t >> 1) - 1) & 1, (t >> 1) - 1)
+                    if precise:
+                        yield W(f"PRead{b}", ((t >> 1) - 1) & 1, (t >> 1) - 1)
                 yield A(f"PReady{b}")
                 t += 1
             if u > 0:
@@ -107,6 +114,14 @@ def _run(units, kst, vst, seed, rare, handover_wait=True):
     def epilogue():
         t = 0
         for u, n in enumerate(units):
+            if precise:  # sum every tile's P as it is handed to the P V product
+                for j in range(n):
+                    b = (t + j) & 1
+                    yield W(f"PReady{b}", ((t + j) >> 1) & 1, (t + j) >> 1)
+                    if posted[b] is not None:
+                        assert posted[b] == t + j, "the epilogue took another tile's factor"
+                        posted[b] = None
+                    yield A(f"PRead{b}")
             t += n
             tl = t - 1
             if handover_wait:
@@ -155,12 +170,13 @@ def _run(units, kst, vst, seed, rare, handover_wait=True):
         assert progressed or pipe, f"deadlock: { {k: cur[k] for k in roles if k not in done} }"
 
 
+@pytest.mark.parametrize("precise", [False, True], ids=["default", "precise"])
 @pytest.mark.parametrize("kst,vst", [(3, 2), (4, 4), (4, 3)])  # bf16 d=128, d=64, FP8
-def test_kernel_barrier_protocol(kst, vst):
+def test_kernel_barrier_protocol(kst, vst, precise):
     for seed in range(150):
         rng = random.Random(1000 * kst + 10 * vst + seed)
         units = [rng.choice([1, 1, 2, 3, 4, 5, 9, 17]) for _ in range(rng.randint(1, 16))]
-        _run(units, kst, vst, seed, rare=rng.choice([0.0, 0.1, 1.0]))
+        _run(units, kst, vst, seed, rare=rng.choice([0.0, 0.1, 1.0]), precise=precise)
 
 
 def test_model_catches_a_skipped_phase():
