@@ -1,8 +1,10 @@
 """Benchmark: packed mixed-mask attention, useful TFLOP/s on one GB300.
 
-One step = one pk_attn_fwd launch over the whole pack (all heads, all
-sequences) with inputs already resident in HBM; the plan is built once,
-outside the timed region (it is reused by every layer and denoising step).
+One step = one pk_attn_fwd over the whole pack (all heads, all sequences)
+with inputs already resident in HBM: its two kernels, the conversion of the
+values to fp16 and the attention, timed apart through the two calls that make
+it up.  The plan is built once, outside the timed region (it is reused by
+every layer and denoising step).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -407,19 +409,20 @@ def layouts_bench(pk, torch, stream, dev, pack, q, k, v, reps=10):
                             device=dev, **kw)
         out = torch.empty_like(qs)
         lse = torch.empty(pack.hq, qs.shape[0], dtype=torch.float32, device=dev)
+        ws = torch.empty(pl.workspace_bytes, dtype=torch.uint8, device=dev)
         for _ in range(3):
-            pk.attn_fwd(qs, kk, vv, pl, pack.scale, out=out, lse=lse)
+            pk.attn_fwd(qs, kk, vv, pl, pack.scale, out=out, lse=lse, workspace=ws)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         e0.record(stream)
         for _ in range(reps):
-            pk.attn_fwd(qs, kk, vv, pl, pack.scale, out=out, lse=lse)
+            pk.attn_fwd(qs, kk, vv, pl, pack.scale, out=out, lse=lse, workspace=ws)
         e1.record(stream)
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / reps
         res[name] = {"ms": round(ms, 4), "useful_tflops": round(pl.useful_flops / ms / 1e9, 1),
                      "query_tokens": int(qs.shape[0]), "key_rows": int(kk.shape[0])}
-        del pl, out, lse
+        del pl, out, lse, ws
     del qs, kp, vp
     torch.cuda.empty_cache()
     return res
@@ -433,45 +436,21 @@ def fp8_bench(pk, torch, stream, dev, pack, q, k, v, reps=10):
     plan = pk.plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d, device=dev)
     out = torch.empty_like(q)
     lse = torch.empty(pack.hq, pack.total_tokens, dtype=torch.float32, device=dev)
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
     for _ in range(3):
-        pk.attn_fwd_fp8(q8, qs, k8, ks, v, plan, pack.scale, out=out, lse=lse)
+        pk.attn_fwd_fp8(q8, qs, k8, ks, v, plan, pack.scale, out=out, lse=lse, workspace=ws)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     e0.record(stream)
     for _ in range(reps):
-        pk.attn_fwd_fp8(q8, qs, k8, ks, v, plan, pack.scale, out=out, lse=lse)
+        pk.attn_fwd_fp8(q8, qs, k8, ks, v, plan, pack.scale, out=out, lse=lse, workspace=ws)
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / reps
     res = {"kernel": "pk_attn_fwd_kernel<128, fp8 q/k>", "ms": round(ms, 4),
            "useful_tflops": round(plan.useful_flops / ms / 1e9, 1),
            "qk_bytes_saved": int(q.numel() + k.numel())}
-    del q8, k8, out, lse, plan
-    torch.cuda.empty_cache()
-    return res
-
-
-def precise_bench(pk, torch, stream, dev, pack, q, k, v, reps=10):
-    """The workload through pk_attn_fwd_precise (O divided by the sum of the
-    bf16 probabilities the tensor cores take), and the default path timed
-    beside it in the same way."""
-    plan = pk.plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d, device=dev)
-    out = torch.empty_like(q)
-    lse = torch.empty(pack.hq, pack.total_tokens, dtype=torch.float32, device=dev)
-    res = {}
-    for key, precise in (("default", False), ("precise", True)):
-        for _ in range(3):
-            pk.attn_fwd(q, k, v, plan, pack.scale, out=out, lse=lse, precise=precise)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        e0.record(stream)
-        for _ in range(reps):
-            pk.attn_fwd(q, k, v, plan, pack.scale, out=out, lse=lse, precise=precise)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / reps
-        res[key] = {"ms": round(ms, 4), "useful_tflops": round(plan.useful_flops / ms / 1e9, 1)}
-    del out, lse, plan
+    del q8, k8, out, lse, plan, ws
     torch.cuda.empty_cache()
     return res
 
@@ -489,21 +468,22 @@ def sweep(pk, torch, stream, dev):
         plan = pk.plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d, device=dev)
         out = torch.empty_like(q)
         lse = torch.empty(pack.hq, T, dtype=torch.float32, device=dev)
+        ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
         for _ in range(3):
-            pk.attn_fwd(q, k, v, plan, pack.scale, out=out, lse=lse)
+            pk.attn_fwd(q, k, v, plan, pack.scale, out=out, lse=lse, workspace=ws)
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
         n = 10
         torch.cuda.synchronize()
         ev[0].record(stream)
         for _ in range(n):
-            pk.attn_fwd(q, k, v, plan, pack.scale, out=out, lse=lse)
+            pk.attn_fwd(q, k, v, plan, pack.scale, out=out, lse=lse, workspace=ws)
         ev[1].record(stream)
         torch.cuda.synchronize()
         ms = ev[0].elapsed_time(ev[1]) / n
         fl = plan.useful_flops
         res[name] = {"ms": round(ms, 4), "useful_tflops": round(fl / ms / 1e9, 1),
                      "tokens_per_s": round(T / ms * 1e3), "total_tokens": T}
-        del q, k, v, out, lse, plan
+        del q, k, v, out, lse, plan, ws
         torch.cuda.empty_cache()
     return res
 
@@ -556,11 +536,16 @@ def main():
     plan = pk.plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d, device=dev)
     out = torch.empty_like(q)
     lse = torch.empty(pack.hq, pack.total_tokens, dtype=torch.float32, device=dev)
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
+    def step():
+        pk.convert_values(v, plan, workspace=ws, status=status)
+        pk.attn_fwd_converted(q, k, ws, plan, pack.scale, out=out, lse=lse, status=status)
+
     for _ in range(args.warmup):
-        pk.attn_fwd(q, k, v, plan, pack.scale, out=out, lse=lse, status=status)
+        step()
     torch.cuda.synchronize()
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} during warm-up")
@@ -569,9 +554,9 @@ def main():
             print(json.dumps({"merge": merge_bench(pk, torch, stream, pack, out, lse)}), flush=True)
         return
 
-    # timed region: K launches, an event pair around each launch on the
-    # launching stream (per-launch duration for the roofline)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    # timed region: K steps, events before, between and after each step's two
+    # launches on the launching stream (per-launch durations for the rooflines)
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3))
            for _ in range(args.steps)]
     t_all = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     with ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
@@ -581,13 +566,16 @@ def main():
         t_all[0].record(stream)
         for i in range(args.steps):
             evs[i][0].record(stream)
-            pk.attn_fwd(q, k, v, plan, pack.scale, out=out, lse=lse, status=status)
+            pk.convert_values(v, plan, workspace=ws, status=status)
             evs[i][1].record(stream)
+            pk.attn_fwd_converted(q, k, ws, plan, pack.scale, out=out, lse=lse, status=status)
+            evs[i][2].record(stream)
         t_all[1].record(stream)
         torch.cuda.synchronize()
         barrier()
     total_ms = t_all[0].elapsed_time(t_all[1])
-    launch_ms = [a.elapsed_time(b) for a, b in evs]
+    conv_ms = [a.elapsed_time(b) for a, b, _ in evs]
+    launch_ms = [b.elapsed_time(c) for _, b, c in evs]
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} in the timed region")
     total_ms = max_over_ranks(total_ms, dist, dev)
@@ -608,7 +596,9 @@ def main():
         qh, kh, vh = pin(q), pin(k), pin(v)
         oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-        bufs = {"q": q, "k": k, "v": v, "out": out, "lse": lse}
+        # the call's own device staging (its v is converted to fp16 in place)
+        bufs = {"q": torch.empty_like(q), "k": torch.empty_like(k), "v": torch.empty_like(v),
+                "out": torch.empty_like(out), "lse": torch.empty_like(lse)}
         for _ in range(args.warmup):
             pk.attn_fwd_host(qh, kh, vh, plan, pack.scale, bufs, oh, lh)
         torch.cuda.synchronize()
@@ -639,6 +629,7 @@ def main():
         barrier()
         e_ms = max_over_ranks(p0.elapsed_time(p1), dist, dev)
         pipe.close()
+        del bufs
         e2e = {"value": job_throughput(world, flops, args.steps, e_ms) / 1e12, "unit": "TFLOP/s",
                "ms_per_step": e_ms / args.steps,
                "h2d_bytes_per_step": int((q.numel() + k.numel() + v.numel()) * 2),
@@ -650,17 +641,16 @@ def main():
     per_workload = None
     if not args.no_sweep and rank == 0:
         per_workload = sweep(pk, torch, stream, dev)
-    layouts = fp8 = precise = None
+    layouts = fp8 = None
     if not args.no_sweep and rank == 0:
         layouts = layouts_bench(pk, torch, stream, dev, pack, q, k, v)
         fp8 = fp8_bench(pk, torch, stream, dev, pack, q, k, v)
-        precise = precise_bench(pk, torch, stream, dev, pack, q, k, v)
     merge = None
     if not args.no_merge and rank == 0:
         merge = merge_bench(pk, torch, stream, pack, out, lse)
     replaced = None
     if not args.no_replaced and rank == 0:
-        pk.attn_fwd(q, k, v, plan, pack.scale, out=out, lse=lse)
+        step()
         torch.cuda.synchronize()
         replaced = replaced_path(torch, pack, q, k, v, out)
         replaced["speedup_of_packed"] = round(replaced["ms"] / ms_step, 2)
@@ -673,6 +663,9 @@ def main():
     peaks = load_peaks()
     avg_launch_ms = statistics.mean(launch_ms)
     achieved = flops / (avg_launch_ms * 1e-3) / 1e12
+    avg_conv_ms = statistics.mean(conv_ms)
+    conv_bytes = 2 * plan.workspace_bytes  # read bf16 v, write fp16 v
+    conv_gbs = conv_bytes / (avg_conv_ms * 1e-3) / 1e9
     traffic = load_traffic()
     info = plan.info
     cpu = None
@@ -682,7 +675,7 @@ def main():
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic",
+        "pv_dtype": "fp16", "data": "synthetic",
         "config": workload_config(pack, world, flops),
         "tokens_per_s": round(tokens_per_s),
         "pct_of_nominal_bf16_peak": round(100 * value / world / NOMINAL_BF16_TFLOPS, 2),
@@ -696,9 +689,14 @@ def main():
                      "kernel": "pk_attn_fwd_kernel<128>", "launch_ms_mean": round(avg_launch_ms, 4),
                      "launch_ms_median": round(statistics.median(launch_ms), 4),
                      "launch_ms_min": round(min(launch_ms), 4)},
+        "value_conversion": {"kernel": "pk_v_to_f16_kernel", "bound": "hbm",
+                             "ms_mean": round(avg_conv_ms, 4), "bytes_per_launch": conv_bytes,
+                             "achieved": round(conv_gbs, 1), "peak": peaks["hbm_gbs"],
+                             "unit": "GB/s", "frac": round(conv_gbs / peaks["hbm_gbs"], 4),
+                             "share_of_step": round(avg_conv_ms / ms_step, 4)},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": 2 * args.steps,
         "clocks": clk.summary(),
         "plan": {k2: info[k2] for k2 in ("num_items", "num_ctas", "num_full_tiles",
                                           "num_partial_tiles")},
@@ -706,7 +704,6 @@ def main():
         "replaced_path": replaced,
         "layouts": layouts,
         "fp8_qk": fp8,
-        "precise_norm": precise,
         "lse_merge": merge,
     }
     print(json.dumps(line), flush=True)

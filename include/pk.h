@@ -32,8 +32,11 @@
  * Ownership: the library never allocates device memory.  A plan owns host
  * memory only; its device image lives in a caller-allocated buffer of
  * pk_plan_device_bytes() bytes that must outlive every launch using it.
+ * Each launch also takes a caller-allocated workspace of
+ * pk_attn_workspace_bytes() bytes (an fp16 copy of the values, see
+ * pk_attn_fwd).
  * Thread safety: a plan is read-only after pk_plan_upload; concurrent
- * launches on one plan are safe.
+ * launches on one plan are safe when each has its own workspace.
  */
 #ifndef PK_H_
 #define PK_H_
@@ -57,7 +60,8 @@ typedef enum pk_status {
   PK_ERR_TIMEOUT = 5,       /* device: a bounded wait ran out (in dev_status) */
   PK_ERR_DEVICE_CHECK = 6,  /* device: an internal consistency check failed */
   PK_ERR_NOT_UPLOADED = 7,  /* plan has no device image yet */
-  PK_ERR_OUT_OF_MEMORY = 8  /* a host memory allocation failed */
+  PK_ERR_OUT_OF_MEMORY = 8, /* a host memory allocation failed */
+  PK_ERR_RANGE = 9          /* device: a value of magnitude >= 2^16 (outside fp16) */
 } pk_status;
 
 typedef enum pk_seg_type { PK_TEXT = 0, PK_IMAGE = 1 } pk_seg_type;
@@ -173,14 +177,32 @@ size_t pk_plan_device_bytes(const pk_plan* plan);
 pk_status pk_plan_upload(pk_plan* plan, void* dev_buf, size_t bytes,
                          pk_stream_t stream);
 
+/* Bytes of the workspace a launch with `plan` needs: Tk * hkv * head_dim * 2
+ * (the fp16 copy of the value rows). */
+size_t pk_attn_workspace_bytes(const pk_plan* plan);
+
 /*
- * Launch the attention forward on `stream` (asynchronous).
+ * Launch the attention forward on `stream` (asynchronous): two kernels, the
+ * conversion of the value rows the plan reads from bf16 to fp16 into the
+ * workspace, then the attention.
  *   q, k, v   : device bf16 tensors as described above.
  *   out, lse  : device outputs as described above.
  *   scale     : softmax scale, finite and > 0 (usually 1/sqrt(head_dim)).
- *   dev_status: nullable device int32; on a device-side failure the kernel
- *               writes PK_ERR_TIMEOUT / PK_ERR_DEVICE_CHECK there (the caller
- *               zeroes it; it is never cleared by the library).
+ *   workspace : caller-owned device memory of at least
+ *               pk_attn_workspace_bytes(plan) bytes, 16-byte aligned; it
+ *               receives the fp16 values at the rows of v, and must not be
+ *               used by another launch until this one is done.  It may be v
+ *               itself when the caller no longer needs v: the conversion is
+ *               then in place and leaves fp16 values in v.
+ *   dev_status: nullable device int32; on a device-side failure the kernels
+ *               write PK_ERR_TIMEOUT / PK_ERR_DEVICE_CHECK there, and
+ *               PK_ERR_RANGE when a value's magnitude is 2^16 or more (the
+ *               caller zeroes it; it is never cleared by the library).
+ * P enters the P V product in fp16 (11 significant bits), with v converted
+ * to fp16 to match: exact for 2^-14 <= |v| < 2^16, rounded to fp16
+ * subnormals below (absolute error at most 2^-25), saturated to 65504 (and
+ * PK_ERR_RANGE reported) at 2^16 and above.  O is divided by the fp32 sum of
+ * the unrounded probabilities, which also gives the LSE.
  * Argument and launch errors are returned synchronously.  Requires a device
  * of compute capability 10.3 (GB300); PK_ERR_UNSUPPORTED also if the
  * library's kernel was compiled with fewer registers per thread than its
@@ -188,28 +210,32 @@ pk_status pk_plan_upload(pk_plan* plan, void* dev_buf, size_t bytes,
  */
 pk_status pk_attn_fwd(const pk_plan* plan, const void* q, const void* k,
                       const void* v, void* out, float* lse, float scale,
+                      void* workspace, size_t workspace_bytes,
                       pk_stream_t stream, int32_t* dev_status);
 
 /*
- * The same attention with precise normalisation: O is divided by the sum of
- * the bf16 probabilities the P·V tensor-core product takes (read back from
- * tensor memory tile by tile), so the weights applied to V sum to one
- * exactly; the LSE still comes from the fp32 sum of the unrounded ones.
- * This halves the output error on rows that a few keys dominate (the q ×4
- * workload's sharpest rows: 4.9e-3 against 1.07e-2 above the output's half
- * ulp) and costs ~20% of the throughput.  Arguments, layouts, errors and
- * asynchrony as for pk_attn_fwd.
+ * The two launches of pk_attn_fwd as separate calls, for callers that reuse
+ * converted values (for example the text prefix's values handed over from
+ * the autoregressive stage, unchanged across denoising steps) or time the
+ * kernels apart.  pk_attn_convert_values writes the fp16 copy of the value
+ * rows the plan reads into `workspace` (arguments, in-place use and
+ * PK_ERR_RANGE as for pk_attn_fwd); pk_attn_fwd_converted runs the attention
+ * on such a copy, v16 (pk_attn_workspace_bytes(plan) bytes, 16-byte
+ * aligned), which it only reads.  Both asynchronous on `stream`.
  */
-pk_status pk_attn_fwd_precise(const pk_plan* plan, const void* q, const void* k,
-                              const void* v, void* out, float* lse, float scale,
-                              pk_stream_t stream, int32_t* dev_status);
+pk_status pk_attn_convert_values(const pk_plan* plan, const void* v, void* workspace,
+                                 size_t workspace_bytes, pk_stream_t stream,
+                                 int32_t* dev_status);
+pk_status pk_attn_fwd_converted(const pk_plan* plan, const void* q, const void* k,
+                                const void* v16, void* out, float* lse, float scale,
+                                pk_stream_t stream, int32_t* dev_status);
 
 /*
  * FP8 variant: queries and keys as FP8 E4M3 codes (1 sign, 4 exponent bits
  * with bias 7, 3 mantissa bits; the OCP 8-bit format), one dequantisation
  * scale each, values bf16.  The scores are scale * q_scale * k_scale *
  * (q8 . k8), computed on the tensor cores in FP8 with fp32 accumulation;
- * softmax, P V, out and lse as for pk_attn_fwd.
+ * softmax, P V, workspace, out and lse as for pk_attn_fwd.
  *   q8 [Tq][hq][128], k8 [Tk][hkv][128] uint8 codes, 16-byte aligned;
  *   q_scale, k_scale: finite and > 0.
  * head_dim must be 128 (else PK_ERR_UNSUPPORTED).  The pages quantise their
@@ -219,15 +245,17 @@ pk_status pk_attn_fwd_precise(const pk_plan* plan, const void* q, const void* k,
  */
 pk_status pk_attn_fwd_fp8(const pk_plan* plan, const void* q8, float q_scale, const void* k8,
                           float k_scale, const void* v, void* out, float* lse, float scale,
-                          pk_stream_t stream, int32_t* dev_status);
+                          void* workspace, size_t workspace_bytes, pk_stream_t stream,
+                          int32_t* dev_status);
 
 /*
  * End-to-end variant for callers holding host buffers: copies q, k, v from
  * host memory into the caller's device buffers, runs pk_attn_fwd, and copies
  * out and lse back into host memory, all on `stream` (asynchronous; pinned
  * host memory makes the copies truly asynchronous).  Device buffers are the
- * caller's (same shapes as pk_attn_fwd); host buffers must stay valid until
- * the stream reaches the end of this call's work.
+ * caller's (same shapes as pk_attn_fwd); v_dev also serves as the workspace
+ * (its values are converted to fp16 in place).  Host buffers must stay
+ * valid until the stream reaches the end of this call's work.
  */
 pk_status pk_attn_fwd_host(const pk_plan* plan, const void* q_host,
                            const void* k_host, const void* v_host,
@@ -243,7 +271,8 @@ pk_status pk_attn_fwd_host(const pk_plan* plan, const void* q_host,
  * copy of out and lse run on three streams of the pipeline, ordered by
  * events, so one step's copies overlap the neighbouring steps' kernels.
  * Device memory is the caller's: num_slots (1..8) sets of buffers of the
- * pk_attn_fwd shapes for `plan`, used round robin; a slot is refilled only
+ * pk_attn_fwd shapes for `plan`, used round robin (a slot's v is its
+ * launch's workspace, converted to fp16 in place); a slot is refilled only
  * after its previous kernel has read it and its previous outputs are out.
  * The pipeline creates and owns its streams and events, no device memory.
  */

@@ -19,6 +19,7 @@ PK_ERR_TIMEOUT = 5
 PK_ERR_DEVICE_CHECK = 6
 PK_ERR_NOT_UPLOADED = 7
 PK_ERR_OUT_OF_MEMORY = 8
+PK_ERR_RANGE = 9
 
 
 class PKError(RuntimeError):
@@ -86,10 +87,14 @@ SIGNATURES = {
                                              ctypes.POINTER(_vp)]),
     "pk_plan_device_bytes": (ctypes.c_size_t, [_vp]),
     "pk_plan_upload": (ctypes.c_int, [_vp, _vp, ctypes.c_size_t, _vp]),
-    "pk_attn_fwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),
-    "pk_attn_fwd_precise": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]),
+    "pk_attn_workspace_bytes": (ctypes.c_size_t, [_vp]),
+    "pk_attn_fwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp,
+                                   ctypes.c_size_t, _vp, _vp]),
+    "pk_attn_convert_values": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_size_t, _vp, _vp]),
+    "pk_attn_fwd_converted": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp,
+                                             _vp]),
     "pk_attn_fwd_fp8": (ctypes.c_int, [_vp, _vp, ctypes.c_float, _vp, ctypes.c_float, _vp, _vp,
-                                       _vp, ctypes.c_float, _vp, _vp]),
+                                       _vp, ctypes.c_float, _vp, ctypes.c_size_t, _vp, _vp]),
     "pk_attn_fwd_host": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                         _vp, ctypes.c_float, _vp, _vp]),
     "pk_plan_destroy": (None, [_vp]),

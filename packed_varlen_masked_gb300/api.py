@@ -107,6 +107,11 @@ class Plan:
     def useful_flops(self) -> float:
         return float(self._lib.pk_plan_useful_flops(self._h))
 
+    @property
+    def workspace_bytes(self) -> int:
+        """Bytes of the per-launch workspace (the fp16 copy of the values)."""
+        return int(self._lib.pk_attn_workspace_bytes(self._h))
+
     def kv_limit(self) -> np.ndarray:
         out = np.zeros(max(self.total_tokens, 1), dtype=np.int32)
         check(self._lib.pk_plan_get_kv_limit(self._h, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
@@ -173,16 +178,33 @@ def _check_tensor(t, name, shape):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _workspace(plan: "Plan", workspace, device):
+    """The launch's workspace: the caller's tensor (checked), else a fresh
+    one from PyTorch's caching allocator on the current stream."""
+    import torch
+    nbytes = plan.workspace_bytes
+    if workspace is None:
+        return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+    if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda or \
+            not workspace.is_contiguous():
+        raise TypeError("workspace must be a contiguous CUDA tensor")
+    if workspace.numel() * workspace.element_size() < nbytes:
+        raise ValueError(f"workspace holds {workspace.numel() * workspace.element_size()} bytes, "
+                         f"the plan needs {nbytes}")
+    return workspace
+
+
 def attn_fwd(q, k, v, plan: Plan, scale: Optional[float] = None, out=None, lse=None,
-             status=None, check_status: bool = False, precise: bool = False):
+             status=None, check_status: bool = False, workspace=None):
     """Packed mixed-mask attention forward on the current CUDA stream.
 
     q [T, hq, d], k and v [Tk, hkv, d] bf16 CUDA tensors (Tk = T for a
     plan from ``plan``; the key rows or pool rows for ``plan_layout``).
-    Returns (out bf16 [T, hq, d], lse fp32 [hq, T]).  With ``check_status`` the call
-    synchronises and raises if the kernel reported a device-side failure.
-    ``precise`` selects pk_attn_fwd_precise (O divided by the sum of the
-    bf16 probabilities the tensor cores take; ~20% slower).
+    Returns (out bf16 [T, hq, d], lse fp32 [hq, T]).  ``workspace``: a CUDA
+    tensor of at least ``plan.workspace_bytes`` bytes for the fp16 copy of
+    the values (allocated here when omitted; passing ``v`` converts v in
+    place).  With ``check_status`` the call synchronises and raises if the
+    kernels reported a device-side failure.
     """
     import torch
     T, hq, hkv, d = plan.total_tokens, plan.hq, plan.hkv, plan.head_dim
@@ -200,31 +222,78 @@ def attn_fwd(q, k, v, plan: Plan, scale: Optional[float] = None, out=None, lse=N
         lse = torch.empty(hq, T, dtype=torch.float32, device=q.device)
     elif lse.dtype != torch.float32 or tuple(lse.shape) != (hq, T) or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous float32 tensor of shape [hq, T]")
+    ws = _workspace(plan, workspace, q.device)
     if check_status and status is None:
         status = torch.zeros(1, dtype=torch.int32, device=q.device)
     stream = torch.cuda.current_stream(q.device).cuda_stream
-    lib = plan._lib
-    fn = lib.pk_attn_fwd_precise if precise else lib.pk_attn_fwd
-    check(fn(plan.handle, ctypes.c_void_p(q.data_ptr()),
-                          ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()),
-                          ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(lse.data_ptr()),
-                          float(scale), ctypes.c_void_p(stream),
-                          ctypes.c_void_p(status.data_ptr() if status is not None else 0)),
-          "pk_attn_fwd_precise" if precise else "pk_attn_fwd")
+    check(plan._lib.pk_attn_fwd(plan.handle, ctypes.c_void_p(q.data_ptr()),
+                                ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()),
+                                ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(lse.data_ptr()),
+                                float(scale), ctypes.c_void_p(ws.data_ptr()),
+                                ws.numel() * ws.element_size(), ctypes.c_void_p(stream),
+                                ctypes.c_void_p(status.data_ptr() if status is not None else 0)),
+          "pk_attn_fwd")
     if check_status:
         torch.cuda.current_stream(q.device).synchronize()
         check(int(status.item()), "pk_attn_fwd (device)")
     return out, lse
 
 
+def convert_values(v, plan: Plan, workspace=None, status=None):
+    """pk_attn_convert_values: the fp16 copy of the value rows ``plan`` reads,
+    into ``workspace`` (allocated when omitted; ``v`` itself converts in
+    place).  Returns the workspace, for ``attn_fwd_converted``."""
+    import torch
+    _check_tensor(v, "v", (plan.kv_rows, plan.hkv, plan.head_dim))
+    ws = _workspace(plan, workspace, v.device)
+    stream = torch.cuda.current_stream(v.device).cuda_stream
+    check(plan._lib.pk_attn_convert_values(
+        plan.handle, ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(ws.data_ptr()),
+        ws.numel() * ws.element_size(), ctypes.c_void_p(stream),
+        ctypes.c_void_p(status.data_ptr() if status is not None else 0)), "pk_attn_convert_values")
+    return ws
+
+
+def attn_fwd_converted(q, k, v16, plan: Plan, scale: Optional[float] = None, out=None, lse=None,
+                       status=None, check_status: bool = False):
+    """pk_attn_fwd_converted: the attention on values ``convert_values``
+    prepared (``v16``: its workspace, only read)."""
+    import torch
+    T, hq, hkv, d = plan.total_tokens, plan.hq, plan.hkv, plan.head_dim
+    _check_tensor(q, "q", (T, hq, d))
+    _check_tensor(k, "k", (plan.kv_rows, hkv, d))
+    if not isinstance(v16, torch.Tensor) or not v16.is_cuda or \
+            v16.numel() * v16.element_size() < plan.workspace_bytes:
+        raise ValueError("v16 must be a CUDA tensor of at least plan.workspace_bytes bytes")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = torch.empty_like(q) if out is None else out
+    if lse is None:
+        lse = torch.empty(hq, T, dtype=torch.float32, device=q.device)
+    _check_tensor(out, "out", (T, hq, d))
+    if check_status and status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=q.device)
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    check(plan._lib.pk_attn_fwd_converted(
+        plan.handle, ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+        ctypes.c_void_p(v16.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+        ctypes.c_void_p(lse.data_ptr()), float(scale), ctypes.c_void_p(stream),
+        ctypes.c_void_p(status.data_ptr() if status is not None else 0)), "pk_attn_fwd_converted")
+    if check_status:
+        torch.cuda.current_stream(q.device).synchronize()
+        check(int(status.item()), "pk_attn_fwd_converted (device)")
+    return out, lse
+
+
 def attn_fwd_fp8(q8, q_scale: float, k8, k_scale: float, v, plan: Plan,
                  scale: Optional[float] = None, out=None, lse=None, status=None,
-                 check_status: bool = False):
+                 check_status: bool = False, workspace=None):
     """Attention with FP8 E4M3 queries and keys (pk_attn_fwd_fp8).
 
     q8 [T, hq, 128] and k8 [Tk, hkv, 128]: CUDA uint8 or float8_e4m3fn
     tensors of E4M3 codes, dequantised by q_scale / k_scale; v bf16
-    [Tk, hkv, 128].  Returns (out bf16 [T, hq, 128], lse fp32 [hq, T])."""
+    [Tk, hkv, 128].  Returns (out bf16 [T, hq, 128], lse fp32 [hq, T]).
+    ``workspace`` as for ``attn_fwd``."""
     import torch
     T, hq, hkv, d = plan.total_tokens, plan.hq, plan.hkv, plan.head_dim
     Tk = plan.kv_rows
@@ -244,6 +313,7 @@ def attn_fwd_fp8(q8, q_scale: float, k8, k_scale: float, v, plan: Plan,
         lse = torch.empty(hq, T, dtype=torch.float32, device=v.device)
     elif lse.dtype != torch.float32 or tuple(lse.shape) != (hq, T) or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous float32 tensor of shape [hq, T]")
+    ws = _workspace(plan, workspace, v.device)
     if check_status and status is None:
         status = torch.zeros(1, dtype=torch.int32, device=v.device)
     stream = torch.cuda.current_stream(v.device).cuda_stream
@@ -251,6 +321,7 @@ def attn_fwd_fp8(q8, q_scale: float, k8, k_scale: float, v, plan: Plan,
                                     ctypes.c_void_p(k8.data_ptr()), float(k_scale),
                                     ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()),
                                     ctypes.c_void_p(lse.data_ptr()), float(scale),
+                                    ctypes.c_void_p(ws.data_ptr()), ws.numel() * ws.element_size(),
                                     ctypes.c_void_p(stream),
                                     ctypes.c_void_p(status.data_ptr() if status is not None else 0)),
           "pk_attn_fwd_fp8")
@@ -265,7 +336,8 @@ def attn_fwd_host(q_host, k_host, v_host, plan: Plan, scale: float, dev_buffers:
     """End-to-end call from host buffers (ideally pinned): copies q/k/v to the
     caller's device buffers, runs the attention and copies out/lse back, all
     on the current stream.  ``dev_buffers`` holds CUDA tensors 'q', 'k', 'v',
-    'out', 'lse' of the pk_attn_fwd shapes."""
+    'out', 'lse' of the pk_attn_fwd shapes ('v' also serves as the workspace:
+    its values are converted to fp16 in place)."""
     import torch
     for name, t in (("q_host", q_host), ("k_host", k_host), ("v_host", v_host),
                     ("out_host", out_host), ("lse_host", lse_host)):
@@ -345,7 +417,8 @@ class HostPipeline:
 
     ``slots`` device buffer sets (dicts of CUDA tensors 'q', 'k', 'v', 'out',
     'lse' of the pk_attn_fwd shapes; allocated here when omitted) are used
-    round robin.  ``submit`` enqueues one step; ``sync`` waits for all."""
+    round robin; a slot's 'v' is its launch's workspace (converted to fp16
+    in place).  ``submit`` enqueues one step; ``sync`` waits for all."""
 
     def __init__(self, plan: Plan, num_slots: int = 2, slots=None, device=None):
         import torch

@@ -12,8 +12,9 @@ namespace dev {
 
 constexpr int kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 64 bf16
 // Growth of a row's maximum (log2 units) tolerated before O and l are
-// rescaled: exponentials run against a stale maximum while it lags by less.
-constexpr float kRescaleLog2 = 16.0f;
+// rescaled: exponentials run against a stale maximum while it lags by less,
+// so p <= 2^15, within fp16's largest finite value (65504).
+constexpr float kRescaleLog2 = 15.0f;
 
 
 // Instruction descriptors of tcgen05.mma kind::f16 (dense, f32 accumulate,
@@ -23,6 +24,12 @@ constexpr float kRescaleLog2 = 16.0f;
 __host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// The same for fp16 A and B (format code 0 in bits 7-9 and 10-12).
+__host__ __device__ constexpr uint32_t make_idesc_f16(int M, int N, bool b_mn_major) {
+  return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
 }
 
 // kind::f8f6f4 with A and B both FP8 E4M3 (format code 0 in bits 7-9 and
@@ -144,6 +151,21 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// The same packing into fp16 (finite inputs up to 65504 stay finite).
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// A bf16 pair to an fp16 pair (round to nearest even, saturating at 65504),
+// keeping the running maximum magnitude for the range check.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x, float& amax) {
+  const float lo = __uint_as_float(x << 16), hi = __uint_as_float(x & 0xffff0000u);
+  amax = max3(amax, fabsf(lo), fabsf(hi));
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 
 struct KernelParams {
   const pk_work_item* items;
@@ -186,13 +208,13 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint6
   }
 }
 
-// O(tmem) (+)= P V: 8 MMAs of 128 x D x 16.  P (bf16 pairs) is read from
-// TMEM, 8 columns per 16 keys.  V is MN-major with 128-byte swizzle: 16 keys
+// O(tmem) (+)= P V: 8 MMAs of 128 x D x 16, fp16 operands.  P (fp16 pairs)
+// is read from TMEM, 8 columns per 16 keys.  V is MN-major with 128-byte swizzle: 16 keys
 // span 2048 bytes, and the second 64-column box (D = 128) is 16384 bytes on.
 template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
                                          bool accumulate) {
-  constexpr uint32_t idesc = make_idesc(128, D, true);
+  constexpr uint32_t idesc = make_idesc_f16(128, D, true);
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk)
     mma_ts(d_tmem, p_tmem + (uint32_t)kk * 8u, v_desc + (uint64_t)(kk * (2048 >> 4)), idesc,

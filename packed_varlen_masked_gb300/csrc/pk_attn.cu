@@ -47,6 +47,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -75,7 +76,7 @@ constexpr uint32_t kTmemCols = 512;
 template <int D, bool F8 = false>
 struct Cfg {
   // Query/key tiles: 128 rows in boxes of 128-byte rows (64 bf16 or 128
-  // FP8 elements); value tiles: 128 rows of D bf16 in 64-column boxes.
+  // FP8 elements); value tiles: 128 rows of D fp16 in 64-column boxes.
   static constexpr int kQKElemsPerBox = F8 ? 128 : 64;
   static constexpr int kQKBoxes = D / kQKElemsPerBox;
   static constexpr int kQKTileBytes = 128 * D * (F8 ? 1 : 2);
@@ -86,7 +87,7 @@ struct Cfg {
   // CTA (and one 512-column TMEM allocation) lives on each SM.
   static constexpr int kKStages = F8 ? 4 : (D == 128 ? 3 : 4);
   static constexpr int kVStages = F8 ? 3 : (D == 128 ? 2 : 4);
-  // TMEM columns: S double buffer, P double buffer (bf16 pairs), O.
+  // TMEM columns: S double buffer, P double buffer (16-bit pairs), O.
   static constexpr uint32_t kColS0 = 0;    // S(t) in [128*(t%2), +128)
   static constexpr uint32_t kColP0 = 256;  // P(t) in [256 + 64*(t%2), +64)
   static constexpr uint32_t kColO = 384;   // O in [384, 384 + D)
@@ -107,14 +108,9 @@ struct Cfg {
   static constexpr int kMmaDone = kOFree + 1;  // [2]: one per MMA issuer
   static constexpr int kLmFull = kMmaDone + 2;   // a unit's row (m, l) handed over
   static constexpr int kLmFree = kLmFull + 1;    // ... and taken by the epilogue
-  // Precise normalisation only: the epilogue has summed P(t) [2], and the
-  // softmax's posts of a rare rescale factor for the epilogue's sum.
-  static constexpr int kPRead = kLmFree + 1;
-  static constexpr int kNumBars = kPRead + 2;
-  static constexpr int kOffLm = kOffBar + kNumBars * 8;  // float2 [128]
-  static constexpr int kOffF = kOffLm + 128 * 8;         // float [128]: a tile's rescale factor
-  static constexpr int kOffFlag = kOffF + 128 * 4;       // u32 [4][2]: factor posted, per warp and tile parity
-  static constexpr int kOffMisc = kOffFlag + 32;
+  static constexpr int kNumBars = kLmFree + 1;
+  static constexpr int kOffLm = (kOffBar + kNumBars * 8 + 15) / 16 * 16;  // float2 [128]
+  static constexpr int kOffMisc = kOffLm + 128 * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
   static_assert(kSmemBytes > 114 * 1024, "one CTA per SM");
@@ -294,10 +290,7 @@ __device__ void mma_pv_role(const KernelParams& p, uint32_t sbase, uint32_t tmem
 }
 
 // Softmax warpgroup (warps 4-7): thread r owns row r of S, P and O in TMEM.
-// PN (precise normalisation): the epilogue also reads every P(t) back, so
-// P buffer b is free only once it has, and a rare rescale's factor is
-// posted to it.
-template <int D, bool F8, bool PN>
+template <int D, bool F8>
 __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint8_t* sgen, uint32_t tmem,
                              int beg, int end, const WaitCtl& wc) {
   using C = Cfg<D, F8>;
@@ -314,7 +307,6 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint8_t* sge
   float2* lm = reinterpret_cast<float2*>(sgen + C::kOffLm);
   for (UnitIter ui(p.items, beg, end); ui.valid() && ok; ui.next(), ++u) {
     const pk_work_item& w = ui.w;
-    const int h = ui.head();
     const bool valid = r < w.q_rows;
     const int lim = p.kv_limit[w.q_start + (valid ? r : w.q_rows - 1)];
     float m_used = -INFINITY, l = 0.f;
@@ -340,20 +332,19 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint8_t* sge
       // P buffer b last held P(t-2); test early whether its product has
       // been read, so the barrier latency hides under the exponentials.
       const uint32_t tpp = t - 2u;
-      const bool p_free = t < 2 || (mbar_test_wait(bar(C::kPvDone + b), (tpp >> 1) & 1u) &&
-                                    (!PN || mbar_test_wait(bar(C::kPRead + b), (tpp >> 1) & 1u)));
+      const bool p_free = t < 2 || mbar_test_wait(bar(C::kPvDone + b), (tpp >> 1) & 1u);
       // Likewise whether S(t+1) has landed (S(t+3) cannot complete before
       // this softmax frees S(t+1)'s buffer, so a yes stays valid).
       const bool s_next = mbar_test_wait(bar(C::kSFull + (b ^ 1u)), ((t + 1u) >> 1) & 1u);
-      // p = 2^(s*scale*log2e - m) as bf16 pairs for the tensor cores, the
+      // p = 2^(s*scale*log2e - m) as fp16 pairs for the tensor cores, the
       // row sum l in fp32.  After a unit's first tile, the exponentials use
       // the running maximum m_used as it stands.  Every p is non-negative, so
       // none can pass 2^kRescaleLog2 unless the tile's sum does: only then is
       // the tile maximum computed, and if it passes m_used + kRescaleLog2
       // the row takes it, rescales O and l, and recomputes the tile from the
-      // scores still in registers.  P (bf16), O and l (fp32) keep their
-      // relative precision at any scale, so the only limit on the threshold
-      // is range: O <= L * 2^16 * max|v|.
+      // scores still in registers.  P, O and l keep their relative
+      // precision at any scale, so the only limits on the threshold are
+      // range: p <= 2^15 fits fp16 P, and O <= L * 2^15 * max|v|.
       uint32_t pp[64];
       float acc[8];
       auto exp_pass = [&](float neg) {
@@ -364,7 +355,7 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint8_t* sge
           float a0, a1;
           fma2(a0, a1, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]), sl2, sl2, neg, neg);
           const float p0 = ex2(a0), p1 = ex2(a1);
-          pp[c >> 1] = pack_bf16x2(p0, p1);
+          pp[c >> 1] = pack_f16x2(p0, p1);
           const int q = (c >> 1) & 3;
           acc2(acc[2 * q], acc[2 * q + 1], p0, p1);
         }
@@ -380,7 +371,7 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint8_t* sge
             mc[i] = max3(mc[i], __uint_as_float(sr[b0 + 2 * i]), __uint_as_float(sr[b0 + 2 * i + 1]));
         return max3(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7])) * sl2;
       };
-      constexpr float kRescaleSum = 65536.0f;  // 2^kRescaleLog2
+      constexpr float kRescaleSum = 32768.0f;  // 2^kRescaleLog2
       if (j == 0) m_used = row_max();
       // The rare rescale path takes a second trip through this one copy of
       // the exponential loop (a second inlined copy measured slower).
@@ -418,24 +409,12 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint8_t* sge
           for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * f);
           tmem_st_x32(tO + (uint32_t)c0, o);
         }
-        if constexpr (PN) {
-          // The epilogue's sum of the bf16 P takes the same factor: once it
-          // has summed P(t-1) (and so taken any earlier factor), post this
-          // tile's.
-          const uint32_t tq = t - 1u;
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kPRead + (tq & 1u)), (tq >> 1) & 1u, wc));
-          if (!ok) break;
-          reinterpret_cast<float*>(sgen + C::kOffF)[r] = f;
-          if (lane == 0)
-            reinterpret_cast<volatile uint32_t*>(sgen + C::kOffFlag)[quad * 2 + (int)(t & 1u)] = 1u;
-        }
       }
       if (!ok) break;
       s_ready = (votes & 4u) == 0u;
       l += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
       if (votes & 2u) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kPvDone + b), (tpp >> 1) & 1u, wc) &&
-                                         (!PN || mbar_wait(bar(C::kPRead + b), (tpp >> 1) & 1u, wc)));
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::kPvDone + b), (tpp >> 1) & 1u, wc));
         if (!ok) break;
       }
       tc_fence_after();
@@ -459,11 +438,8 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint8_t* sge
 // Epilogue warpgroup (warps 8-11): thread r owns row r of O in TMEM.  Per
 // unit it takes (m, l) from the softmax, waits for the unit's last P V,
 // moves O into registers and frees it for the next unit's first product,
-// then writes O / l as bf16 and the natural-log LSE.  PN: O is divided
-// instead by the sum of the bf16 P the P V product took, which this warp
-// group reads back from TMEM tile by tile (so the weights applied to V sum
-// to one); l still gives the LSE.
-template <int D, bool F8, bool PN>
+// then writes O / l as bf16 and the natural-log LSE.
+template <int D, bool F8>
 __device__ void epilogue_role(const KernelParams& p, uint32_t sbase, uint8_t* sgen,
                               uint32_t tmem, int beg, int end, const WaitCtl& wc) {
   using C = Cfg<D, F8>;
@@ -478,41 +454,6 @@ __device__ void epilogue_role(const KernelParams& p, uint32_t sbase, uint8_t* sg
   for (UnitIter ui(p.items, beg, end); ui.valid() && ok; ui.next(), ++u) {
     const pk_work_item& w = ui.w;
     const int h = ui.head();
-    const bool valid = r < w.q_rows;
-    float lp = 0.f;  // PN: sum of the unit's bf16 P
-    if constexpr (PN) {
-      const uint32_t tP0 = tmem + ((uint32_t)(quad * 32) << 16) + C::kColP0;
-      volatile uint32_t* flags = reinterpret_cast<volatile uint32_t*>(sgen + C::kOffFlag);
-      for (int j = 0; j < w.n_kt && ok; ++j) {
-        const uint32_t t = g + (uint32_t)j, b = t & 1u;
-        ok = __all_sync(0xffffffffu, mbar_wait_sleep(bar(C::kPReady + b), (t >> 1) & 1u, wc));
-        if (!ok) break;
-        tc_fence_after();
-        if (flags[quad * 2 + (int)b] != 0u) {  // rare: the softmax rescaled at this tile
-          lp *= reinterpret_cast<const float*>(sgen + C::kOffF)[r];
-          __syncwarp();
-          if (lane == 0) flags[quad * 2 + (int)b] = 0u;
-        }
-        float a[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) a[i] = 0.f;
-#pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 32) {
-          uint32_t pv[32];
-          tmem_ld_x32(tP0 + b * 64u + (uint32_t)c0, pv);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int k = c & 3;
-            acc2(a[2 * k], a[2 * k + 1], __uint_as_float(pv[c] << 16),
-                 __uint_as_float(pv[c] & 0xffff0000u));
-          }
-        }
-        tc_fence_before();
-        mbar_arrive(bar(C::kPRead + b));
-        lp += ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
-      }
-      if (!ok) break;
-    }
     if (!(ok = __all_sync(0xffffffffu, mbar_wait_sleep(bar(C::kLmFull), u & 1u, wc)))) break;
     const float2 ml = lm[r];
     mbar_arrive(bar(C::kLmFree));
@@ -532,9 +473,8 @@ __device__ void epilogue_role(const KernelParams& p, uint32_t sbase, uint8_t* sg
     tc_fence_before();
     mbar_arrive(bar(C::kOFree));
     const float l = ml.y;
-    const float ln = PN ? lp : l;
-    const float inv_l = ln > 0.f ? 1.0f / ln : 0.f;  // a row without keys writes zeros
-    if (valid) {
+    const float inv_l = l > 0.f ? 1.0f / l : 0.f;  // a row without keys writes zeros
+    if (r < w.q_rows) {
       uint8_t* orow = p.out + (((size_t)(w.q_start + r) * (size_t)p.hq + (size_t)h) * D) * 2;
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 8) {
@@ -552,7 +492,57 @@ __device__ void epilogue_role(const KernelParams& p, uint32_t sbase, uint8_t* sg
   }
 }
 
-template <int D, bool F8, bool PN>
+// Values bf16 -> fp16, before the attention launch, into the caller's
+// workspace (rows at the same offsets as in v; v16 may be v itself).  P
+// enters the P V product as fp16 (11 significant bits, against bf16's 8), and
+// the product takes both operands in one format.  bf16 values in [2^-14,
+// 2^16) convert exactly; smaller ones round to fp16 subnormals (absolute
+// error <= 2^-25); magnitudes of 2^16 and beyond saturate to 65504 and the
+// launch reports PK_ERR_RANGE.  The work is a list of 128-row blocks:
+// `blocks` holds (block, rows holding keys) pairs, the block's other rows
+// zeroed (they are read only as masked keys, where 0 * P must stay 0 even if
+// the pool holds garbage there); with `blocks` null, blocks 0, 1, ... of
+// rows [0, rows).  Every thread moves 16 bytes per step, four steps in
+// flight.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 x, float& amax) {
+  uint4 y;
+  y.x = bf16x2_to_f16x2(x.x, amax);
+  y.y = bf16x2_to_f16x2(x.y, amax);
+  y.z = bf16x2_to_f16x2(x.z, amax);
+  y.w = bf16x2_to_f16x2(x.w, amax);
+  return y;
+}
+
+__global__ void __launch_bounds__(512) pk_v_to_f16_kernel(const uint4* v, uint4* v16,
+                                                          const int32_t* __restrict__ blocks,
+                                                          int32_t num_blocks, int32_t rows,
+                                                          int32_t pieces_per_row,
+                                                          int32_t* status) {
+  constexpr int kStep = 512;
+  float amax = 0.f;
+  for (int32_t i = blockIdx.x; i < num_blocks; i += gridDim.x) {
+    const int32_t blk = blocks ? blocks[2 * i] : i;
+    const int32_t nvalid = blocks ? blocks[2 * i + 1] : min(128, rows - blk * 128);
+    const size_t base = (size_t)blk * 128 * pieces_per_row;
+    const int32_t n = nvalid * pieces_per_row;
+    int32_t k = threadIdx.x;
+    for (; k + 3 * kStep < n; k += 4 * kStep) {
+      uint4 x[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) x[c] = v[base + k + c * kStep];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) v16[base + k + c * kStep] = bf16x8_to_f16x8(x[c], amax);
+    }
+    for (; k < n; k += kStep) v16[base + k] = bf16x8_to_f16x8(v[base + k], amax);
+    if (blocks) {
+      const int32_t n_all = 128 * pieces_per_row;
+      for (k = n + threadIdx.x; k < n_all; k += kStep) v16[base + k] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  if (!(amax < 65520.0f) && status) atomicCAS(status, 0, (int32_t)PK_ERR_RANGE);
+}
+
+template <int D, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     pk_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -589,9 +579,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(C::kMmaDone + 1), 1);
     mbar_init(bar(C::kLmFull), 128);
     mbar_init(bar(C::kLmFree), 128);
-    mbar_init(bar(C::kPRead + 0), 128);
-    mbar_init(bar(C::kPRead + 1), 128);
-    for (int i = 0; i < 8; ++i) reinterpret_cast<volatile uint32_t*>(sgen + C::kOffFlag)[i] = 0u;
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     tma_prefetch_desc(&tm_q);
@@ -627,10 +614,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp < 8) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
-    softmax_role<D, F8, PN>(p, sbase, sgen, tmem, beg, end, wc);
+    softmax_role<D, F8>(p, sbase, sgen, tmem, beg, end, wc);
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
-    epilogue_role<D, F8, PN>(p, sbase, sgen, tmem, beg, end, wc);
+    epilogue_role<D, F8>(p, sbase, sgen, tmem, beg, end, wc);
   }
 
   tc_fence_before();
@@ -690,30 +677,28 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// [T][H][D] bf16 viewed as a 3-D tensor (D, H, T); boxes of 64 x 1 x 128
-// with 128-byte swizzle; rows past T read as zeros.
-// (d, H, T) view of a [T][H][d] tensor of 2-byte (bf16) or 1-byte (FP8)
-// elements, boxes of 128 bytes x 1 head x 128 rows.
-bool make_map(CUtensorMap* m, const void* base, int H, int T, int D, int elem_bytes = 2) {
+// (d, H, T) view of a [T][H][d] tensor of 2-byte (bf16, fp16) or 1-byte
+// (FP8) elements, boxes of 128 bytes x 1 head x 128 rows with 128-byte
+// swizzle; rows past T read as zeros.
+bool make_map(CUtensorMap* m, const void* base, int H, int T, int D, CUtensorMapDataType dt) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
-  const cuuint64_t eb = (cuuint64_t)elem_bytes;
+  const cuuint64_t eb = dt == CU_TENSOR_MAP_DATA_TYPE_UINT8 ? 1 : 2;
   const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
   const cuuint64_t strides[2] = {(cuuint64_t)D * eb, (cuuint64_t)H * D * eb};
-  const cuuint32_t box[3] = {(cuuint32_t)(128 / elem_bytes), 1, 128};
+  const cuuint32_t box[3] = {(cuuint32_t)(128 / eb), 1, 128};
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUtensorMapDataType dt =
-      elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Device capability check, cached per device ordinal.
-pk_status check_device() {
+// Device capability check and SM count, cached per device ordinal.
+pk_status check_device(int* sm_count = nullptr) {
   static std::mutex mu;
   static int cap_state[64];  // 0 unknown, 1 ok, 2 unsupported
+  static int sms[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
@@ -722,30 +707,70 @@ pk_status check_device() {
   if (dev < 0 || dev >= 64) return PK_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lk(mu);
   if (cap_state[dev] == 0) {
-    int major = 0, minor = 0;
+    int major = 0, minor = 0, n = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
       cudaGetLastError();
       return PK_ERR_CUDA;
     }
+    sms[dev] = n;
     cap_state[dev] = (major == 10 && minor == 3) ? 1 : 2;
   }
+  if (sm_count) *sm_count = sms[dev];
   return cap_state[dev] == 1 ? PK_OK : PK_ERR_UNSUPPORTED;
+}
+
+// The value rows the plan's kernel reads, bf16 -> fp16 into v16 (which may
+// be v itself: the conversion is elementwise, in place).  Contiguous keys:
+// rows [0, v_conv_rows) converted, rows no sequence owns zeroed (a key tile
+// overhanging the last sequence reads them, masked, and 0 * P must stay 0).
+// Paged keys: the pool blocks the block table lists, rows past each block's
+// keys zeroed.
+pk_status convert_values(const pk_plan* plan, const void* v, void* v16, int sm_count,
+                         cudaStream_t stream, int32_t* dev_status) {
+  const size_t row_bytes = (size_t)plan->hkv * plan->head_dim * 2;
+  const int32_t pieces_per_row = (int32_t)(row_bytes / 16);
+  const int32_t* list = nullptr;
+  int32_t nblocks = 0, rows = plan->Tk;
+  if (plan->paged) {
+    list = reinterpret_cast<const int32_t*>(static_cast<const uint8_t*>(plan->dev) +
+                                            plan->layout.vblk_off);
+    nblocks = (int32_t)(plan->v_blocks.size() / 2);
+  } else {
+    rows = plan->v_conv_rows;
+    nblocks = (rows + 127) / 128;
+    if (plan->Tk > rows &&
+        cudaMemsetAsync(static_cast<uint8_t*>(v16) + (size_t)rows * row_bytes, 0,
+                        (size_t)(plan->Tk - rows) * row_bytes, stream) != cudaSuccess) {
+      cudaGetLastError();
+      return PK_ERR_CUDA;
+    }
+  }
+  if (nblocks == 0) return PK_OK;
+  const int grid = std::min(nblocks, 4 * std::max(sm_count, 1));
+  pk::dev::pk_v_to_f16_kernel<<<grid, 512, 0, stream>>>(static_cast<const uint4*>(v),
+                                                         static_cast<uint4*>(v16), list, nblocks,
+                                                         rows, pieces_per_row, dev_status);
+  if (cudaGetLastError() != cudaSuccess) return PK_ERR_CUDA;
+  return PK_OK;
 }
 
 // scale: the softmax scale of the scores as the MMA computes them (for FP8
 // queries/keys it includes their dequantisation scales).
-template <int D, bool F8 = false, bool PN = false>
-pk_status launch(const pk_plan* plan, const void* q, const void* k, const void* v, void* out,
+// v16: the fp16 values (the workspace convert_values has filled).
+template <int D, bool F8>
+pk_status launch(const pk_plan* plan, const void* q, const void* k, const void* v16, void* out,
                  float* lse, float scale, cudaStream_t stream, int32_t* dev_status) {
   using C = pk::dev::Cfg<D, F8>;
   CUtensorMap tq, tk, tv;
-  const int qk_bytes = F8 ? 1 : 2;
-  if (!make_map(&tq, q, plan->hq, plan->T, D, qk_bytes) ||
-      !make_map(&tk, k, plan->hkv, plan->Tk, D, qk_bytes) ||
-      !make_map(&tv, v, plan->hkv, plan->Tk, D))
+  const CUtensorMapDataType qk_dt =
+      F8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!make_map(&tq, q, plan->hq, plan->T, D, qk_dt) ||
+      !make_map(&tk, k, plan->hkv, plan->Tk, D, qk_dt) ||
+      !make_map(&tv, v16, plan->hkv, plan->Tk, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
     return PK_ERR_CUDA;
-  if (cudaFuncSetAttribute(pk::dev::pk_attn_fwd_kernel<D, F8, PN>,
+  if (cudaFuncSetAttribute(pk::dev::pk_attn_fwd_kernel<D, F8>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kSmemBytes) != cudaSuccess) {
     cudaGetLastError();
@@ -757,7 +782,7 @@ pk_status launch(const pk_plan* plan, const void* q, const void* k, const void* 
   static std::atomic<int> regs_state{0};  // 0 unknown, 1 fits, 2 does not
   if (regs_state.load() == 0) {
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, pk::dev::pk_attn_fwd_kernel<D, F8, PN>) != cudaSuccess) {
+    if (cudaFuncGetAttributes(&fa, pk::dev::pk_attn_fwd_kernel<D, F8>) != cudaSuccess) {
       cudaGetLastError();
       return PK_ERR_CUDA;
     }
@@ -779,7 +804,7 @@ pk_status launch(const pk_plan* plan, const void* q, const void* k, const void* 
   kp.hq = plan->hq;
   kp.scale_log2 = scale * 1.4426950408889634f;
   kp.wait_limit_ns = g_wait_limit_ns.load();
-  pk::dev::pk_attn_fwd_kernel<D, F8, PN>
+  pk::dev::pk_attn_fwd_kernel<D, F8>
       <<<plan->num_ctas, pk::dev::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, kp);
   if (cudaGetLastError() != cudaSuccess) return PK_ERR_CUDA;
   return PK_OK;
@@ -801,64 +826,110 @@ void pk_set_wait_timeout_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : 1); }
 
 namespace {
 
-// Argument checks and dispatch shared by the bf16 entry points.
-template <bool PN>
-pk_status attn_fwd_bf16(const pk_plan* plan, const void* q, const void* k, const void* v,
-                        void* out, float* lse, float scale, pk_stream_t stream,
-                        int32_t* dev_status) {
+// Argument checks shared by the entry points.  check_plan: PK_OK with
+// *nothing = true when the plan has no work.
+pk_status check_plan(const pk_plan* plan, bool* nothing) {
+  *nothing = false;
   if (plan == nullptr) return PK_ERR_INVALID_ARG;
-  if (!(scale > 0.f) || !std::isfinite(scale)) return PK_ERR_INVALID_ARG;
-  if (plan->T == 0 || plan->items.empty()) return PK_OK;
+  if (plan->T == 0 || plan->items.empty()) {
+    *nothing = true;
+    return PK_OK;
+  }
   if (plan->dev == nullptr) return PK_ERR_NOT_UPLOADED;
   if (plan->Tk <= 0) return PK_ERR_INVALID_ARG;  // queries need a key/value tensor to map
-  if (!q || !k || !v || !out || !lse) return PK_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
-      (reinterpret_cast<uintptr_t>(lse) & 3u))
+  return PK_OK;
+}
+
+// A value tensor and a workspace (the fp16 copy) of the plan's size.
+pk_status check_values(const pk_plan* plan, const void* v, const void* workspace,
+                       size_t workspace_bytes) {
+  if (!v || !workspace) return PK_ERR_INVALID_ARG;
+  if (workspace_bytes < pk_attn_workspace_bytes(plan)) return PK_ERR_INVALID_ARG;
+  if (!aligned16(v) || !aligned16(workspace)) return PK_ERR_ALIGNMENT;
+  return PK_OK;
+}
+
+// Queries, keys, the outputs and the scale.
+pk_status check_attn(const void* q, const void* k, const void* out, const float* lse, float scale) {
+  if (!(scale > 0.f) || !std::isfinite(scale)) return PK_ERR_INVALID_ARG;
+  if (!q || !k || !out || !lse) return PK_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(out) || (reinterpret_cast<uintptr_t>(lse) & 3u))
     return PK_ERR_ALIGNMENT;
-  pk_status st = check_device();
-  if (st != PK_OK) return st;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (plan->head_dim == 128) return launch<128, false, PN>(plan, q, k, v, out, lse, scale, s, dev_status);
-  if (plan->head_dim == 64) return launch<64, false, PN>(plan, q, k, v, out, lse, scale, s, dev_status);
-  return PK_ERR_UNSUPPORTED;
+  return PK_OK;
 }
 
 }  // namespace
 
 extern "C" {
 
-pk_status pk_attn_fwd(const pk_plan* plan, const void* q, const void* k, const void* v,
-                      void* out, float* lse, float scale, pk_stream_t stream,
-                      int32_t* dev_status) {
-  return attn_fwd_bf16<false>(plan, q, k, v, out, lse, scale, stream, dev_status);
+pk_status pk_attn_convert_values(const pk_plan* plan, const void* v, void* workspace,
+                                 size_t workspace_bytes, pk_stream_t stream,
+                                 int32_t* dev_status) {
+  bool nothing = false;
+  pk_status st = check_plan(plan, &nothing);
+  if (st != PK_OK || nothing) return st;
+  if ((st = check_values(plan, v, workspace, workspace_bytes)) != PK_OK) return st;
+  int sms = 0;
+  if ((st = check_device(&sms)) != PK_OK) return st;
+  return convert_values(plan, v, workspace, sms, reinterpret_cast<cudaStream_t>(stream),
+                        dev_status);
 }
 
-pk_status pk_attn_fwd_precise(const pk_plan* plan, const void* q, const void* k, const void* v,
-                              void* out, float* lse, float scale, pk_stream_t stream,
-                              int32_t* dev_status) {
-  return attn_fwd_bf16<true>(plan, q, k, v, out, lse, scale, stream, dev_status);
+pk_status pk_attn_fwd_converted(const pk_plan* plan, const void* q, const void* k,
+                                const void* v16, void* out, float* lse, float scale,
+                                pk_stream_t stream, int32_t* dev_status) {
+  if (plan == nullptr || !(scale > 0.f) || !std::isfinite(scale)) return PK_ERR_INVALID_ARG;
+  bool nothing = false;
+  pk_status st = check_plan(plan, &nothing);
+  if (st != PK_OK || nothing) return st;
+  if ((st = check_attn(q, k, out, lse, scale)) != PK_OK ||
+      (st = check_values(plan, v16, v16, pk_attn_workspace_bytes(plan))) != PK_OK)
+    return st;
+  if ((st = check_device()) != PK_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (plan->head_dim == 128) return launch<128, false>(plan, q, k, v16, out, lse, scale, s, dev_status);
+  if (plan->head_dim == 64) return launch<64, false>(plan, q, k, v16, out, lse, scale, s, dev_status);
+  return PK_ERR_UNSUPPORTED;
+}
+
+pk_status pk_attn_fwd(const pk_plan* plan, const void* q, const void* k, const void* v,
+                      void* out, float* lse, float scale, void* workspace, size_t workspace_bytes,
+                      pk_stream_t stream, int32_t* dev_status) {
+  if (plan == nullptr || !(scale > 0.f) || !std::isfinite(scale)) return PK_ERR_INVALID_ARG;
+  bool nothing = false;
+  pk_status st = check_plan(plan, &nothing);
+  if (st != PK_OK || nothing) return st;
+  if ((st = check_attn(q, k, out, lse, scale)) != PK_OK ||
+      (st = check_values(plan, v, workspace, workspace_bytes)) != PK_OK)
+    return st;
+  if ((st = pk_attn_convert_values(plan, v, workspace, workspace_bytes, stream, dev_status)) !=
+      PK_OK)
+    return st;
+  return pk_attn_fwd_converted(plan, q, k, workspace, out, lse, scale, stream, dev_status);
 }
 
 pk_status pk_attn_fwd_fp8(const pk_plan* plan, const void* q8, float q_scale, const void* k8,
                           float k_scale, const void* v, void* out, float* lse, float scale,
-                          pk_stream_t stream, int32_t* dev_status) {
+                          void* workspace, size_t workspace_bytes, pk_stream_t stream,
+                          int32_t* dev_status) {
   if (plan == nullptr) return PK_ERR_INVALID_ARG;
   const float s_all = scale * q_scale * k_scale;
   if (!(scale > 0.f) || !(q_scale > 0.f) || !(k_scale > 0.f) || !std::isfinite(s_all) ||
       !(s_all > 0.f))
     return PK_ERR_INVALID_ARG;
   if (plan->head_dim != 128) return PK_ERR_UNSUPPORTED;
-  if (plan->T == 0 || plan->items.empty()) return PK_OK;
-  if (plan->dev == nullptr) return PK_ERR_NOT_UPLOADED;
-  if (plan->Tk <= 0) return PK_ERR_INVALID_ARG;
-  if (!q8 || !k8 || !v || !out || !lse) return PK_ERR_INVALID_ARG;
-  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v) || !aligned16(out) ||
-      (reinterpret_cast<uintptr_t>(lse) & 3u))
-    return PK_ERR_ALIGNMENT;
-  pk_status st = check_device();
-  if (st != PK_OK) return st;
-  return launch<128, true>(plan, q8, k8, v, out, lse, s_all, reinterpret_cast<cudaStream_t>(stream),
-                           dev_status);
+  bool nothing = false;
+  pk_status st = check_plan(plan, &nothing);
+  if (st != PK_OK || nothing) return st;
+  if ((st = check_attn(q8, k8, out, lse, s_all)) != PK_OK ||
+      (st = check_values(plan, v, workspace, workspace_bytes)) != PK_OK)
+    return st;
+  if ((st = pk_attn_convert_values(plan, v, workspace, workspace_bytes, stream, dev_status)) !=
+      PK_OK)
+    return st;
+  if ((st = check_device()) != PK_OK) return st;
+  return launch<128, true>(plan, q8, k8, workspace, out, lse, s_all,
+                           reinterpret_cast<cudaStream_t>(stream), dev_status);
 }
 
 pk_status pk_attn_fwd_host(const pk_plan* plan, const void* q_host, const void* k_host,
@@ -879,8 +950,9 @@ pk_status pk_attn_fwd_host(const pk_plan* plan, const void* q_host, const void* 
     cudaGetLastError();
     return PK_ERR_CUDA;
   }
-  pk_status st = pk_attn_fwd(plan, q_dev, k_dev, v_dev, out_dev, lse_dev, scale, stream,
-                             dev_status);
+  // v_dev is library staging: the values are converted to fp16 in place.
+  pk_status st = pk_attn_fwd(plan, q_dev, k_dev, v_dev, out_dev, lse_dev, scale, v_dev, kvb,
+                             stream, dev_status);
   if (st != PK_OK) return st;
   if (cudaMemcpyAsync(out_host, out_dev, qb, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
       cudaMemcpyAsync(lse_host, lse_dev, lb, cudaMemcpyDeviceToHost, s) != cudaSuccess) {

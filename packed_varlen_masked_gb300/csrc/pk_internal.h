@@ -22,6 +22,7 @@ struct PlanImageLayout {
   size_t cta_off_off = 0;  // int32[num_ctas + 1]
   size_t kvlim_off = 0;    // int32[Tq]: last visible key index of the row's key range, -1 none
   size_t table_off = 0;    // int32[num_seqs * blocks_per_seq] when keys are paged
+  size_t vblk_off = 0;     // int32[v_blocks.size()]: (pool block, valid rows) the kernel reads
   size_t bytes = 0;
 };
 
@@ -42,6 +43,12 @@ struct pk_plan {
   int32_t num_full_tiles = 0, num_partial_tiles = 0;
   int64_t visible_pairs = 0;
   std::vector<int32_t> kv_limit;           // [Tq] last visible key of the row's key range, -1 none
+  // Value rows the attention kernel reads, for their conversion to fp16:
+  // contiguous keys, rows [0, v_conv_rows) (rows [v_conv_rows, Tk) no
+  // sequence owns are zeroed in the copy); paged keys, (pool block, rows of
+  // it holding keys) pairs, the block's other rows zeroed in the copy.
+  int32_t v_conv_rows = 0;
+  std::vector<int32_t> v_blocks;
   std::vector<pk_work_item> items;         // CTA-ordered
   std::vector<int32_t> cta_offsets;        // [num_ctas + 1]
   pk::PlanImageLayout layout;

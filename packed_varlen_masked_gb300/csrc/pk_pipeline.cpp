@@ -106,7 +106,8 @@ pk_status pk_pipeline_submit(pk_pipeline* p, const void* q_host, const void* k_h
     cudaGetLastError();
     return PK_ERR_CUDA;
   }
-  pk_status st = pk_attn_fwd(plan, s.q, s.k, s.v, s.out, s.lse, scale,
+  // The slot's v is this launch's workspace: its values become fp16 in place.
+  pk_status st = pk_attn_fwd(plan, s.q, s.k, s.v, s.out, s.lse, scale, s.v, kvb,
                              reinterpret_cast<pk_stream_t>(p->s_comp), dev_status);
   if (st != PK_OK) return st;
   if (cudaEventRecord(p->ev_comp[i], p->s_comp) != cudaSuccess ||

@@ -163,6 +163,37 @@ pk_status build_plan(const pk_layout& L, int32_t hq, int32_t hkv, int32_t d, int
     }
   }
 
+  // Value rows the kernel reads (converted to fp16 before each launch).  For
+  // paged keys: each referenced pool block with the rows of it that hold
+  // keys (the rest of the block is read only as masked keys, and zeroed in
+  // the copy); a tile of rows without keys reads table entry 0's block.
+  if (p->paged) {
+    std::vector<int32_t> valid(static_cast<size_t>(L.num_kv_rows / pk::kKeyBlock), -1);
+    bool keyless_rows = false;
+    for (int32_t s = 0; s < S; ++s) {
+      const int32_t nk = ck[s + 1] - ck[s];
+      if (nk == 0) {
+        keyless_rows = keyless_rows || cq[s + 1] > cq[s];
+        continue;
+      }
+      const int32_t k0 = L.k_pos0 ? L.k_pos0[s] : 0;
+      const int32_t b0 = k0 / pk::kKeyBlock, nb = (nk + pk::kKeyBlock - 1) / pk::kKeyBlock;
+      for (int32_t bb = b0; bb < b0 + nb; ++bb) {
+        const int32_t pb = L.block_table[(size_t)s * L.blocks_per_seq + bb];
+        const int32_t rows = std::min(pk::kKeyBlock, k0 + nk - bb * pk::kKeyBlock);
+        valid[pb] = std::max(valid[pb], rows);
+      }
+    }
+    if (keyless_rows) valid[L.block_table[0]] = std::max(valid[L.block_table[0]], 0);
+    for (size_t i = 0; i < valid.size(); ++i)
+      if (valid[i] >= 0) {
+        p->v_blocks.push_back(static_cast<int32_t>(i));
+        p->v_blocks.push_back(valid[i]);
+      }
+  } else {
+    p->v_conv_rows = ck[S];
+  }
+
   // Work items: every 128-row query tile x key/value head x query-head pair.
   std::vector<pk_work_item> items;
   const int32_t group = hq / hkv;
@@ -233,7 +264,8 @@ pk_status build_plan(const pk_layout& L, int32_t hq, int32_t hkv, int32_t d, int
   IL.cta_off_off = align_up(IL.items_off + sizeof(pk_work_item) * n_items, pk::kImageAlign);
   IL.kvlim_off = align_up(IL.cta_off_off + sizeof(int32_t) * (grid + 1), pk::kImageAlign);
   IL.table_off = align_up(IL.kvlim_off + sizeof(int32_t) * static_cast<size_t>(Tq), pk::kImageAlign);
-  IL.bytes = align_up(IL.table_off + sizeof(int32_t) * p->block_table.size(), pk::kImageAlign);
+  IL.vblk_off = align_up(IL.table_off + sizeof(int32_t) * p->block_table.size(), pk::kImageAlign);
+  IL.bytes = align_up(IL.vblk_off + sizeof(int32_t) * p->v_blocks.size(), pk::kImageAlign);
   p->image.assign(IL.bytes, 0);
   if (n_items)
     std::memcpy(p->image.data() + IL.items_off, p->items.data(), sizeof(pk_work_item) * n_items);
@@ -243,6 +275,9 @@ pk_status build_plan(const pk_layout& L, int32_t hq, int32_t hkv, int32_t d, int
   if (!p->block_table.empty())
     std::memcpy(p->image.data() + IL.table_off, p->block_table.data(),
                 sizeof(int32_t) * p->block_table.size());
+  if (!p->v_blocks.empty())
+    std::memcpy(p->image.data() + IL.vblk_off, p->v_blocks.data(),
+                sizeof(int32_t) * p->v_blocks.size());
 
   *out = owner.release();
   return PK_OK;
@@ -315,6 +350,7 @@ const char* pk_status_string(pk_status st) {
     case PK_ERR_DEVICE_CHECK: return "device consistency check failed";
     case PK_ERR_NOT_UPLOADED: return "plan not uploaded";
     case PK_ERR_OUT_OF_MEMORY: return "host memory allocation failed";
+    case PK_ERR_RANGE: return "a value of magnitude >= 2^16 is outside the fp16 P V product's range";
   }
   return "unknown status";
 }
@@ -335,6 +371,10 @@ pk_status pk_plan_create(const int32_t* cu, int32_t num_seqs, const pk_segment* 
 }
 
 size_t pk_plan_device_bytes(const pk_plan* p) { return p ? p->layout.bytes : 0; }
+
+size_t pk_attn_workspace_bytes(const pk_plan* p) {
+  return p ? static_cast<size_t>(p->Tk) * p->hkv * p->head_dim * 2 : 0;
+}
 
 pk_status pk_plan_upload(pk_plan* p, void* dev_buf, size_t bytes, pk_stream_t stream) {
   if (p == nullptr || dev_buf == nullptr) return PK_ERR_INVALID_ARG;

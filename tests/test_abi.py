@@ -22,7 +22,8 @@ def _declared_functions():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     for required in ["pk_plan_create", "pk_plan_upload", "pk_attn_fwd", "pk_plan_destroy",
-                     "pk_plan_device_bytes", "pk_status_string", "pk_plan_useful_flops"]:
+                     "pk_plan_device_bytes", "pk_status_string", "pk_plan_useful_flops",
+                     "pk_attn_workspace_bytes"]:
         assert required in names
 
 
@@ -38,7 +39,7 @@ def test_binding_covers_every_declared_symbol():
 
 def test_status_strings():
     lib = pk.load()
-    for code in range(9):
+    for code in range(10):
         assert lib.pk_status_string(code).decode() != "unknown status"
     assert lib.pk_status_string(pk.PK_ERR_TIMEOUT).decode() == "device wait timed out"
 
@@ -48,15 +49,28 @@ def test_null_and_bad_arguments_are_rejected_without_a_device():
     out = ctypes.c_void_p()
     assert lib.pk_plan_create(None, 1, None, 0, 4, 4, 64, 4, ctypes.byref(out)) == pk.PK_ERR_INVALID_ARG
     assert lib.pk_plan_device_bytes(None) == 0
-    assert lib.pk_attn_fwd(None, None, None, None, None, None, 0.125, None, None) == pk.PK_ERR_INVALID_ARG
+    assert lib.pk_attn_fwd(None, None, None, None, None, None, 0.125, None, 0, None, None) \
+        == pk.PK_ERR_INVALID_ARG
     plan = pk.Plan([0, 3], [(0, 3, 0)], 2, 2, 64, num_ctas=2, upload=False)
     # scale must be finite and positive
     for bad in (0.0, -1.0, float("nan"), float("inf")):
-        assert lib.pk_attn_fwd(plan.handle, None, None, None, None, None, bad, None, None) \
-            == pk.PK_ERR_INVALID_ARG
+        assert lib.pk_attn_fwd(plan.handle, None, None, None, None, None, bad, None, 0, None,
+                               None) == pk.PK_ERR_INVALID_ARG
     # not uploaded yet
-    assert lib.pk_attn_fwd(plan.handle, 16, 16, 16, 16, 16, 0.125, None, None) == pk.PK_ERR_NOT_UPLOADED
+    assert lib.pk_attn_fwd(plan.handle, 16, 16, 16, 16, 16, 0.125, 16, 1 << 20, None, None) \
+        == pk.PK_ERR_NOT_UPLOADED
     assert lib.pk_plan_upload(plan.handle, None, 0, None) == pk.PK_ERR_INVALID_ARG
+
+
+def test_workspace_bytes_is_the_fp16_copy_of_the_value_rows():
+    lib = pk.load()
+    assert lib.pk_attn_workspace_bytes(None) == 0
+    plan = pk.Plan([0, 300, 1000], [(0, 300, 1), (300, 700, 0)], 8, 2, 128, num_ctas=4,
+                   upload=False)
+    assert plan.workspace_bytes == 1000 * 2 * 128 * 2
+    lay = pk.plan_layout([0, 5], [0, 300], [(0, 0, 300, 1)], 4, 1, 64, k_pos0=[0],
+                         block_table=[[3, 0, 1]], num_kv_rows=512, num_ctas=2, upload=False)
+    assert lay.workspace_bytes == 512 * 1 * 64 * 2  # the whole pool
 
 
 def test_upload_rejects_small_or_misaligned_buffers_before_touching_memory():
@@ -95,13 +109,14 @@ def test_fp8_entry_argument_checks_without_a_device():
     lib = pk.load()
     plan = pk.Plan([0, 300], [(0, 300, 1)], 4, 2, 128, num_ctas=4, upload=False)
     f = lib.pk_attn_fwd_fp8
-    assert f(None, 16, 1.0, 16, 1.0, 16, 16, 16, 0.1, None, None) == pk.PK_ERR_INVALID_ARG
+    W = (16, 1 << 20)  # workspace pointer and bytes
+    assert f(None, 16, 1.0, 16, 1.0, 16, 16, 16, 0.1, *W, None, None) == pk.PK_ERR_INVALID_ARG
     for qs, ks, sc in ((0.0, 1.0, 0.1), (1.0, -1.0, 0.1), (1.0, 1.0, float("nan")),
                        (1e30, 1e30, 1e30)):
-        assert f(plan.handle, 16, qs, 16, ks, 16, 16, 16, sc, None, None) == pk.PK_ERR_INVALID_ARG
-    assert f(plan.handle, 16, 1.0, 16, 1.0, 16, 16, 16, 0.1, None, None) == pk.PK_ERR_NOT_UPLOADED
+        assert f(plan.handle, 16, qs, 16, ks, 16, 16, 16, sc, *W, None, None) == pk.PK_ERR_INVALID_ARG
+    assert f(plan.handle, 16, 1.0, 16, 1.0, 16, 16, 16, 0.1, *W, None, None) == pk.PK_ERR_NOT_UPLOADED
     p64 = pk.Plan([0, 300], [(0, 300, 1)], 4, 2, 64, num_ctas=4, upload=False)
-    assert f(p64.handle, 16, 1.0, 16, 1.0, 16, 16, 16, 0.1, None, None) == pk.PK_ERR_UNSUPPORTED
+    assert f(p64.handle, 16, 1.0, 16, 1.0, 16, 16, 16, 0.1, *W, None, None) == pk.PK_ERR_UNSUPPORTED
 
 
 def test_pipeline_argument_checks_without_a_device():

@@ -3,11 +3,13 @@
 Each warp role of the kernel (query/key producer, value producer, S issuer,
 P V issuer, softmax, epilogue) is a generator of the same waits and arrivals,
 with the same parities, as its device code; the tensor pipe completes queued
-MMA commits in order after random delays.  Over random unit sequences and
-random interleavings the model checks that no role deadlocks, that every
-parity wait passes only once the awaited phase has completed, and that no
-wait ever faces a barrier two phases ahead (where a parity check would read
-the wrong phase)."""
+MMA commits in order after random delays.  With the fp16 P V product the
+epilogue also converts every landed value tile, polling (non-blocking tests)
+for whichever of its jobs is ready: the model lets it take any ready one.
+Over random unit sequences and random interleavings the model checks that no
+role deadlocks, that every parity wait or test passes only once the awaited
+phase has completed, and that no wait ever faces a barrier two phases ahead
+(where a parity check would read the wrong phase)."""
 import random
 
 import pytest
@@ -21,20 +23,23 @@ class _Bar:
         self.c += 1
 
 
-def _run(units, kst, vst, seed, rare, handover_wait=True, precise=False):
+def _run(units, kst, vst, seed, rare, handover_wait=True, convert=False):
     rng = random.Random(seed)
     B = {}
     for i in range(2):
-        for nm in ("QFull", "QEmpty", "SFull", "SFree", "PReady", "PvDone", "PRead"):
+        for nm in ("QFull", "QEmpty", "SFull", "SFree", "PReady", "PvDone"):
             B[f"{nm}{i}"] = _Bar(f"{nm}{i}")
     for i in range(kst):
         B[f"KFull{i}"], B[f"KEmpty{i}"] = _Bar("KFull"), _Bar("KEmpty")
     for i in range(vst):
         B[f"VFull{i}"], B[f"VEmpty{i}"] = _Bar("VFull"), _Bar("VEmpty")
+        B[f"VConv{i}"] = _Bar("VConv")
     for nm in ("OFree", "LmFull", "LmFree"):
         B[nm] = _Bar(nm)
     pipe = []
-    posted = {0: None, 1: None}  # precise path: the tile whose rescale factor waits, per parity
+
+    def pv_done(t):  # the P-V-done barrier of tile t (two, alternating) and its phase
+        return (f"PvDone{t & 1}", (t >> 1) & 1, t >> 1)
 
     def W(n, par, k):  # wait for phase k of n (parity par)
         return ("wait", n, par, k)
@@ -81,11 +86,11 @@ def _run(units, kst, vst, seed, rare, handover_wait=True, precise=False):
         for u, n in enumerate(units):
             for j in range(n):
                 v, b = t % vst, t & 1
-                yield W(f"VFull{v}", (t // vst) & 1, t // vst)
+                yield W(f"{'VConv' if convert else 'VFull'}{v}", (t // vst) & 1, t // vst)
                 yield W(f"PReady{b}", (t >> 1) & 1, t >> 1)
                 if j == 0:
                     yield W("OFree", (u & 1) ^ 1, u - 1)
-                yield ("mma", [f"PvDone{b}", f"VEmpty{v}"])
+                yield ("mma", [pv_done(t)[0], f"VEmpty{v}"])
                 t += 1
 
     def softmax():
@@ -96,15 +101,9 @@ def _run(units, kst, vst, seed, rare, handover_wait=True, precise=False):
                 yield W(f"SFull{b}", (t >> 1) & 1, t >> 1)
                 yield A(f"SFree{b}")
                 if j > 0 and rng.random() < rare:  # rescale O after P(t-1) V(t-1)
-                    yield W(f"PvDone{(t - 1) & 1}", ((t - 1) >> 1) & 1, (t - 1) >> 1)
-                    if precise:  # post the factor once the epilogue has summed P(t-1)
-                        yield W(f"PRead{(t - 1) & 1}", ((t - 1) >> 1) & 1, (t - 1) >> 1)
-                        assert posted[b] is None, "a posted factor was overwritten"
-                        posted[b] = t
-                if t >= 2:  # P buffer b free: P(t-2) V(t-2) done (and, precise, summed)
-                    yield W(f"PvDone{b}", ((t >> 1) - 1) & 1, (t >> 1) - 1)
-                    if precise:
-                        yield W(f"PRead{b}", ((t >> 1) - 1) & 1, (t >> 1) - 1)
+                    yield W(*pv_done(t - 1))
+                if t >= 2:  # P buffer b free: P(t-2) V(t-2) done
+                    yield W(*pv_done(t - 2))
                 yield A(f"PReady{b}")
                 t += 1
             if u > 0:
@@ -114,24 +113,44 @@ def _run(units, kst, vst, seed, rare, handover_wait=True, precise=False):
     def epilogue():
         t = 0
         for u, n in enumerate(units):
-            if precise:  # sum every tile's P as it is handed to the P V product
-                for j in range(n):
-                    b = (t + j) & 1
-                    yield W(f"PReady{b}", ((t + j) >> 1) & 1, (t + j) >> 1)
-                    if posted[b] is not None:
-                        assert posted[b] == t + j, "the epilogue took another tile's factor"
-                        posted[b] = None
-                    yield A(f"PRead{b}")
             t += n
             tl = t - 1
             if handover_wait:
                 yield W("LmFull", u & 1, u)
             yield A("LmFree")
-            yield W(f"PvDone{tl & 1}", (tl >> 1) & 1, tl >> 1)
+            yield W(*pv_done(tl))
             yield A("OFree")
 
+    def epilogue_convert():
+        # poll whichever job is ready: convert the next landed value tile, or
+        # take the pending unit's (m, l), or write it once its last product is done
+        total = sum(units)
+        tv, go, u, ostage = 0, 0, 0, 0
+        while u < len(units) or tv < total:
+            opts = []
+            if tv < total:
+                opts.append((f"VFull{tv % vst}", (tv // vst) & 1, tv // vst, "conv"))
+            if u < len(units):
+                tl = go + units[u] - 1
+                if ostage == 0:
+                    opts.append(("LmFull", u & 1, u, "lm"))
+                else:
+                    opts.append((*pv_done(tl), "out"))
+            tag = yield ("poll", opts)
+            if tag == "conv":
+                yield A(f"VConv{tv % vst}")
+                tv += 1
+            elif tag == "lm":
+                yield A("LmFree")
+                ostage = 1
+            else:
+                yield A("OFree")
+                go += units[u]
+                u += 1
+                ostage = 0
+
     roles = {"qk": producer_qk(), "v": producer_v(), "s": mma_s(), "pv": mma_pv(),
-             "softmax": softmax(), "epilogue": epilogue()}
+             "softmax": softmax(), "epilogue": epilogue_convert() if convert else epilogue()}
     cur = dict.fromkeys(roles)
     done = set()
     while len(done) < len(roles):
@@ -159,6 +178,22 @@ def _run(units, kst, vst, seed, rare, handover_wait=True, precise=False):
             elif op[0] == "mma":
                 pipe.append(op[1])
                 cur[k], progressed = None, True
+            elif op[0] == "poll":
+                ready = []
+                for nm, par, kk, tag in op[1]:
+                    c = B[nm].c
+                    if (c & 1) != par:
+                        assert c >= kk + 1, f"{k}: test of {nm} phase {kk} passed early ({c} completed)"
+                        ready.append(tag)
+                    else:
+                        assert c <= kk, f"{k}: test of {nm} phase {kk} faces phase {c} (aliased)"
+                if ready:
+                    try:
+                        cur[k] = roles[k].send(rng.choice(ready))
+                    except StopIteration:
+                        done.add(k)
+                        cur[k] = None
+                    progressed = True
             else:
                 _, nm, par, kk = op
                 c = B[nm].c
@@ -170,13 +205,13 @@ def _run(units, kst, vst, seed, rare, handover_wait=True, precise=False):
         assert progressed or pipe, f"deadlock: { {k: cur[k] for k in roles if k not in done} }"
 
 
-@pytest.mark.parametrize("precise", [False, True], ids=["default", "precise"])
+@pytest.mark.parametrize("mode", ["bf16_pv", "f16_pv"])
 @pytest.mark.parametrize("kst,vst", [(3, 2), (4, 4), (4, 3)])  # bf16 d=128, d=64, FP8
-def test_kernel_barrier_protocol(kst, vst, precise):
+def test_kernel_barrier_protocol(kst, vst, mode):
     for seed in range(150):
         rng = random.Random(1000 * kst + 10 * vst + seed)
         units = [rng.choice([1, 1, 2, 3, 4, 5, 9, 17]) for _ in range(rng.randint(1, 16))]
-        _run(units, kst, vst, seed, rare=rng.choice([0.0, 0.1, 1.0]), precise=precise)
+        _run(units, kst, vst, seed, rare=rng.choice([0.0, 0.1, 1.0]), convert=mode == "f16_pv")
 
 
 def test_model_catches_a_skipped_phase():

@@ -9,25 +9,13 @@ import torch
 import oracle
 import packed_varlen_masked_gb300 as pk
 import workloads as W
+from parity_tol import check
 
 pytestmark = pytest.mark.gpu
 
 
-def _half_ulp_bf16(x):
-    a = np.maximum(np.abs(x), np.finfo(np.float32).tiny)
-    return 0.5 * np.exp2(np.floor(np.log2(a)) - 7)
-
-
-def _check(out_g, lse_g, out_o, lse_o):
-    empty = np.isneginf(lse_o)
-    assert (np.isneginf(lse_g) == empty).all()
-    assert (out_g[np.broadcast_to(empty.T[..., None], out_g.shape)] == 0).all()
-    if out_o.size:
-        assert (np.abs(out_g - out_o) <= 1e-2 + _half_ulp_bf16(out_o)).all(), \
-            float(np.abs(out_g - out_o).max())
-        f = ~empty
-        if f.any():
-            assert np.abs(lse_g[f] - lse_o[f]).max() <= 1e-3
+def _check(out_g, lse_g, out_o, lse_o, case="random"):
+    check(case, out_g, lse_g, out_o, lse_o)
 
 
 def _packs():
@@ -56,7 +44,7 @@ def test_random_pack_all_layouts(pack):
                                     pack.scale)
     plan = pk.plan(cu, pack.segments, pack.hq, pack.hkv, pack.d)
     o, l = pk.attn_fwd(q.cuda(), k.cuda(), v.cuda(), plan, pack.scale, check_status=True)
-    _check(o.float().cpu().numpy(), l.cpu().numpy(), out_o, lse_o)
+    _check(o.float().cpu().numpy(), l.cpu().numpy(), out_o, lse_o, pack.name)
     # cached prefix with paged keys: rows of the full result
     rows, cu_q, q_pos0 = W.prefix_split(pack)
     if len(rows):
@@ -67,7 +55,8 @@ def test_random_pack_all_layouts(pack):
                             block_table=table, num_kv_rows=kp.shape[0])
         o, l = pk.attn_fwd(q[torch.as_tensor(rows)].contiguous().cuda(), kp.cuda(), vp.cuda(), pl,
                            pack.scale, check_status=True)
-        _check(o.float().cpu().numpy(), l.cpu().numpy(), out_o[rows], lse_o[:, rows])
+        _check(o.float().cpu().numpy(), l.cpu().numpy(), out_o[rows], lse_o[:, rows],
+               pack.name + "/prefix-paged")
     # key chunks against the oracle's general entry
     for cu_k, k_pos0, krows in W.key_chunks(pack, int(np.random.default_rng(pack.seed).choice([64, 128, 200]))):
         idx = torch.as_tensor(krows)
@@ -78,4 +67,4 @@ def test_random_pack_all_layouts(pack):
                                           pack.d, pack.scale)
         pl = pk.plan_layout(cu, cu_k, sg, pack.hq, pack.hkv, pack.d, q_pos0=z, k_pos0=k_pos0)
         o, l = pk.attn_fwd(q.cuda(), kc.cuda(), vc.cuda(), pl, pack.scale, check_status=True)
-        _check(o.float().cpu().numpy(), l.cpu().numpy(), oo, lo)
+        _check(o.float().cpu().numpy(), l.cpu().numpy(), oo, lo, pack.name + "/key-chunk")
