@@ -61,7 +61,8 @@ typedef enum pk_status {
   PK_ERR_DEVICE_CHECK = 6,  /* device: an internal consistency check failed */
   PK_ERR_NOT_UPLOADED = 7,  /* plan has no device image yet */
   PK_ERR_OUT_OF_MEMORY = 8, /* a host memory allocation failed */
-  PK_ERR_RANGE = 9          /* device: a value of magnitude >= 2^16 (outside fp16) */
+  PK_ERR_RANGE = 9,         /* device: a value of magnitude >= 2^16 (outside fp16) */
+  PK_ERR_TOO_LARGE = 10     /* the plan needs more than pk_attn_fwd_noalloc's static scratch */
 } pk_status;
 
 typedef enum pk_seg_type { PK_TEXT = 0, PK_IMAGE = 1 } pk_seg_type;
@@ -229,6 +230,31 @@ pk_status pk_attn_convert_values(const pk_plan* plan, const void* v, void* works
 pk_status pk_attn_fwd_converted(const pk_plan* plan, const void* q, const void* k,
                                 const void* v16, void* out, float* lse, float scale,
                                 pk_stream_t stream, int32_t* dev_status);
+
+/*
+ * pk_attn_fwd for callers that cannot allocate device memory where they make
+ * the call: code embedded in a host framework that owns all device memory
+ * through its own pool and forbids other allocations, or a latency-critical
+ * loop that must not make a call that can synchronise the device
+ * (cudaMalloc and cudaFree can).  It takes no workspace: the fp16 copy of the
+ * values lives in a static device array of the library, 64 MiB (67108864
+ * bytes), which every device that loads the library holds until the process
+ * exits.  The pages have no counterpart; it is an addition of this library.
+ *   Arguments, layouts, results and dev_status as for pk_attn_fwd.
+ *   PK_ERR_TOO_LARGE, before any device work, when pk_attn_workspace_bytes(plan)
+ *   exceeds 64 MiB (for example 32768 key rows x 8 heads x 128 dims).
+ * Every call shares the one array and leaves its contents behind; each call
+ * rewrites (or zeroes) every part of it that its kernels read, so nothing
+ * depends on an earlier call.  Calls that overlap on the GPU (launched on
+ * different streams without ordering) race on the array: order them.  The
+ * entry point's first call on a device takes the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  It allocates no memory (no cudaMalloc,
+ * cudaFree or allocating library routine).
+ */
+pk_status pk_attn_fwd_noalloc(const pk_plan* plan, const void* q, const void* k,
+                              const void* v, void* out, float* lse, float scale,
+                              pk_stream_t stream, int32_t* dev_status);
 
 /*
  * FP8 variant: queries and keys as FP8 E4M3 codes (1 sign, 4 exponent bits

@@ -21,7 +21,7 @@ from __future__ import annotations
 
 from ._native import (PK_ERR_ALIGNMENT, PK_ERR_CUDA, PK_ERR_DEVICE_CHECK,  # noqa: F401
                       PK_ERR_INVALID_ARG, PK_ERR_NOT_UPLOADED, PK_ERR_OUT_OF_MEMORY, PK_ERR_RANGE,
-                      PK_ERR_TIMEOUT,
+                      PK_ERR_TIMEOUT, PK_ERR_TOO_LARGE,
                       PK_ERR_UNSUPPORTED, PK_OK, PKError, lib_path, load)
 from .api import (IMAGE, TEXT, HostPipeline, Plan, attn_fwd, attn_fwd_converted,  # noqa: F401
                   attn_fwd_fp8, attn_fwd_host, convert_values, debug_wait_timeout, lse_merge,

@@ -20,6 +20,7 @@ PK_ERR_DEVICE_CHECK = 6
 PK_ERR_NOT_UPLOADED = 7
 PK_ERR_OUT_OF_MEMORY = 8
 PK_ERR_RANGE = 9
+PK_ERR_TOO_LARGE = 10
 
 
 class PKError(RuntimeError):
@@ -93,6 +94,8 @@ SIGNATURES = {
     "pk_attn_convert_values": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_size_t, _vp, _vp]),
     "pk_attn_fwd_converted": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp,
                                              _vp]),
+    "pk_attn_fwd_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp,
+                                           _vp]),
     "pk_attn_fwd_fp8": (ctypes.c_int, [_vp, _vp, ctypes.c_float, _vp, ctypes.c_float, _vp, _vp,
                                        _vp, ctypes.c_float, _vp, ctypes.c_size_t, _vp, _vp]),
     "pk_attn_fwd_host": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,

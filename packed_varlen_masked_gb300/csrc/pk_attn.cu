@@ -908,6 +908,59 @@ pk_status pk_attn_fwd(const pk_plan* plan, const void* q, const void* k, const v
   return pk_attn_fwd_converted(plan, q, k, workspace, out, lse, scale, stream, dev_status);
 }
 
+}  // extern "C"
+
+// Scratch of pk_attn_fwd_noalloc: a file-scope device array, so that callers
+// who cannot allocate device memory still have room for the fp16 copy of the
+// values.  Every device that loads the library holds it until the process
+// exits.  In host code its name is only a stand-in: the device address comes
+// from cudaGetSymbolAddress, taken once per device (with that device current)
+// and cached.
+static constexpr size_t kStaticScratchBytes = size_t(64) << 20;
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+namespace {
+
+void* static_scratch_address() {
+  static std::mutex mu;
+  static void* addr[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (addr[dev] == nullptr) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_static_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    addr[dev] = a;
+  }
+  return addr[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+pk_status pk_attn_fwd_noalloc(const pk_plan* plan, const void* q, const void* k, const void* v,
+                              void* out, float* lse, float scale, pk_stream_t stream,
+                              int32_t* dev_status) {
+  if (plan == nullptr) return PK_ERR_INVALID_ARG;
+  if (pk_attn_workspace_bytes(plan) > kStaticScratchBytes) return PK_ERR_TOO_LARGE;
+  bool nothing = false;
+  pk_status st = check_plan(plan, &nothing);
+  if (st != PK_OK || nothing) return st;
+  if ((st = check_device()) != PK_OK) return st;
+  void* scratch = static_scratch_address();
+  if (scratch == nullptr) return PK_ERR_CUDA;
+  return pk_attn_fwd(plan, q, k, v, out, lse, scale, scratch, kStaticScratchBytes, stream,
+                     dev_status);
+}
+
 pk_status pk_attn_fwd_fp8(const pk_plan* plan, const void* q8, float q_scale, const void* k8,
                           float k_scale, const void* v, void* out, float* lse, float scale,
                           void* workspace, size_t workspace_bytes, pk_stream_t stream,

@@ -351,6 +351,8 @@ const char* pk_status_string(pk_status st) {
     case PK_ERR_NOT_UPLOADED: return "plan not uploaded";
     case PK_ERR_OUT_OF_MEMORY: return "host memory allocation failed";
     case PK_ERR_RANGE: return "a value of magnitude >= 2^16 is outside the fp16 P V product's range";
+    case PK_ERR_TOO_LARGE:
+      return "the plan's values need more than the 64 MiB static scratch of pk_attn_fwd_noalloc";
   }
   return "unknown status";
 }
