@@ -39,10 +39,14 @@ import workloads as W  # noqa: E402
 METRIC = "packed mixed-mask attention useful TFLOP/s & tokens/s; % of bf16 dense peak"
 NOMINAL_BF16_TFLOPS = 2250.0
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+# The attention kernel's sources and the planner whose schedule sets its
+# DRAM traffic: the committed traffic figure is valid only for these bytes.
 KERNEL_SOURCES = ["packed_varlen_masked_gb300/csrc/pk_attn.cu",
                   "packed_varlen_masked_gb300/csrc/tmem_ops.cuh",
                   "packed_varlen_masked_gb300/csrc/sync.cuh",
-                  "packed_varlen_masked_gb300/csrc/attn_common.cuh"]
+                  "packed_varlen_masked_gb300/csrc/attn_common.cuh",
+                  "packed_varlen_masked_gb300/csrc/pk_plan.cpp",
+                  "packed_varlen_masked_gb300/csrc/pk_internal.h"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "pk_attn_fwd_d128_mixed_resolution_traffic.md")
 
 

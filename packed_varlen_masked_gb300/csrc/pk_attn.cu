@@ -176,18 +176,18 @@ __device__ void producer_qk_role(const KernelParams& p, const CUtensorMap* tm_q,
                          keep);
     }
   }
-  if (!ok) {
-    // Aborted: let every copy already issued land before the CTA may exit.
-    // The last kKStages armings of the ring (and the last two of Q) are the
-    // only ones that can be open, each the most recent arming of its stage.
-    for (uint32_t k = 1; k <= (uint32_t)C::kKStages && k <= k_armed; ++k) {
-      const uint32_t i = k_armed - k;
-      mbar_wait_drain(bar(C::kKFull + i % C::kKStages), (i / C::kKStages) & 1u, wc);
-    }
-    for (uint32_t k = 1; k <= 2u && k <= q_armed; ++k) {
-      const uint32_t i = q_armed - k;
-      mbar_wait_drain(bar(C::kQFull + (i & 1u)), (i >> 1) & 1u, wc);
-    }
+  // Every copy issued must land before the CTA may exit.  After a normal run
+  // the consumers have waited for them all and these waits pass at once;
+  // after an abort (this thread's or a consumer's) they may be in flight.
+  // The last kKStages armings of the ring (and the last two of Q) are the
+  // only ones that can be open, each the most recent arming of its stage.
+  for (uint32_t k = 1; k <= (uint32_t)C::kKStages && k <= k_armed; ++k) {
+    const uint32_t i = k_armed - k;
+    mbar_wait_drain(bar(C::kKFull + i % C::kKStages), (i / C::kKStages) & 1u, wc);
+  }
+  for (uint32_t k = 1; k <= 2u && k <= q_armed; ++k) {
+    const uint32_t i = q_armed - k;
+    mbar_wait_drain(bar(C::kQFull + (i & 1u)), (i >> 1) & 1u, wc);
   }
 }
 
@@ -214,11 +214,9 @@ __device__ void producer_v_role(const KernelParams& p, const CUtensorMap* tm_v, 
                          bar(C::kVFull + st), h * 64, w.hkv, key_tile_row(p, w, j), keep);
     }
   }
-  if (!ok) {
-    for (uint32_t k = 1; k <= (uint32_t)C::kVStages && k <= v_armed; ++k) {
-      const uint32_t i = v_armed - k;
-      mbar_wait_drain(bar(C::kVFull + i % C::kVStages), (i / C::kVStages) & 1u, wc);
-    }
+  for (uint32_t k = 1; k <= (uint32_t)C::kVStages && k <= v_armed; ++k) {  // as above
+    const uint32_t i = v_armed - k;
+    mbar_wait_drain(bar(C::kVFull + i % C::kVStages), (i / C::kVStages) & 1u, wc);
   }
 }
 

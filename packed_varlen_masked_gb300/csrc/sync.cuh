@@ -73,6 +73,12 @@ struct WaitCtl {
   uint64_t limit_ns;
 };
 
+// Bound of the drain waits on the abort path.  A drain waits for copies and
+// MMAs the CTA has already issued (to validated addresses), which always
+// complete, so its bound is fixed and generous: the user's wait limit, which
+// may be set to a few nanoseconds to force the abort path, does not apply.
+constexpr uint64_t kDrainLimitNs = 5000000000ull;
+
 // Slow path of a bounded wait: poll until the phase completes, the CTA has
 // aborted, or the time limit passes (then record the timeout and abort).
 // Inlined: an out-of-line call inside the softmax loop constrains its
@@ -80,11 +86,12 @@ struct WaitCtl {
 static __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, WaitCtl c,
                                             bool honour_abort) {
   const uint64_t t0 = globaltimer_ns();
+  const uint64_t limit = honour_abort ? c.limit_ns : kDrainLimitNs;
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((n & 15u) == 0) {
       if (honour_abort && *c.abort_flag) return false;
-      if (globaltimer_ns() - t0 > c.limit_ns) {
+      if (globaltimer_ns() - t0 > limit) {
         *c.abort_flag = 1;
         if (c.status) atomicCAS(c.status, 0, (int32_t)PK_ERR_TIMEOUT);
         return false;
@@ -96,7 +103,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, c, true);
 }
-// Drain wait used on the abort path: ignores the abort flag, still bounded.
+// Drain wait, used on the abort path and for the MMA issuers' final commit:
+// ignores the abort flag, bounded by kDrainLimitNs.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, const WaitCtl& c) {
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, c, false);

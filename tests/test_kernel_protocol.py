@@ -2,14 +2,21 @@
 
 Each warp role of the kernel (query/key producer, value producer, S issuer,
 P V issuer, softmax, epilogue) is a generator of the same waits and arrivals,
-with the same parities, as its device code; the tensor pipe completes queued
-MMA commits in order after random delays.  With the fp16 P V product the
-epilogue also converts every landed value tile, polling (non-blocking tests)
-for whichever of its jobs is ready: the model lets it take any ready one.
-Over random unit sequences and random interleavings the model checks that no
-role deadlocks, that every parity wait or test passes only once the awaited
-phase has completed, and that no wait ever faces a barrier two phases ahead
-(where a parity check would read the wrong phase)."""
+with the same parities, as its device code.  TMA copies complete their
+barrier after random delays, in any order; the tensor pipe completes queued
+MMA commits in order after random delays.  Over random unit sequences and
+random interleavings the model checks that no role deadlocks, that every
+parity wait passes only once the awaited phase has completed, and that no
+wait ever faces a barrier two phases ahead (where a parity check would read
+the wrong phase).
+
+The abort path is modelled too: at a random moment a wait runs out of time
+and raises the CTA's abort flag.  From then on a wait whose phase has not
+completed gives up (as the kernel's bounded waits do), each role leaves its
+loop, the producers drain the copies they issued and the MMA issuers commit
+and drain their products (drain waits ignore the flag).  When every role has
+left, no copy and no MMA may still be in flight: the kernel frees the tensor
+memory and the CTA exits at that point."""
 import random
 
 import pytest
@@ -23,91 +30,144 @@ class _Bar:
         self.c += 1
 
 
-def _run(units, kst, vst, seed, rare, handover_wait=True, convert=False):
+def _run(units, kst, vst, seed, rare, handover_wait=True, abort_at=None):
+    """abort_at: None, or the probability per scheduler round that the abort
+    flag is raised (a wait timing out)."""
     rng = random.Random(seed)
     B = {}
     for i in range(2):
-        for nm in ("QFull", "QEmpty", "SFull", "SFree", "PReady", "PvDone"):
+        for nm in ("QFull", "QEmpty", "SFull", "SFree", "PReady", "PvDone", "MmaDone"):
             B[f"{nm}{i}"] = _Bar(f"{nm}{i}")
     for i in range(kst):
         B[f"KFull{i}"], B[f"KEmpty{i}"] = _Bar("KFull"), _Bar("KEmpty")
     for i in range(vst):
         B[f"VFull{i}"], B[f"VEmpty{i}"] = _Bar("VFull"), _Bar("VEmpty")
-        B[f"VConv{i}"] = _Bar("VConv")
     for nm in ("OFree", "LmFull", "LmFree"):
         B[nm] = _Bar(nm)
-    pipe = []
+    pipe = []      # MMA commits, completed in order
+    copies = []    # TMA copies in flight, completed in any order
+    state = {"abort": False}
 
     def pv_done(t):  # the P-V-done barrier of tile t (two, alternating) and its phase
         return (f"PvDone{t & 1}", (t >> 1) & 1, t >> 1)
 
-    def W(n, par, k):  # wait for phase k of n (parity par)
+    def W(n, par, k):  # bounded wait for phase k of n (parity par); gives up on abort
         return ("wait", n, par, k)
+
+    def D(n, par, k):  # drain wait: ignores the abort flag
+        return ("drain", n, par, k)
 
     def A(n):
         return ("arrive", n)
 
     def producer_qk():
-        g = 0
+        g = k_armed = q_armed = 0
+        ok = True
         for u, n in enumerate(units):
             qb = u & 1
-            yield W(f"QEmpty{qb}", ((u >> 1) & 1) ^ 1, (u >> 1) - 1)
-            yield A(f"QFull{qb}")
+            ok = yield W(f"QEmpty{qb}", ((u >> 1) & 1) ^ 1, (u >> 1) - 1)
+            if not ok:
+                break
+            yield ("tma", f"QFull{qb}")
+            q_armed += 1
             for _ in range(n):
                 st = g % kst
-                yield W(f"KEmpty{st}", ((g // kst) & 1) ^ 1, g // kst - 1)
-                yield A(f"KFull{st}")
+                ok = yield W(f"KEmpty{st}", ((g // kst) & 1) ^ 1, g // kst - 1)
+                if not ok:
+                    break
+                yield ("tma", f"KFull{st}")
+                k_armed += 1
                 g += 1
+            if not ok:
+                break
+        # let every copy issued land (the latest arming of each stage); after a
+        # normal run the consumers have already waited for them all
+        for k in range(1, min(kst, k_armed) + 1):
+            i = k_armed - k
+            yield D(f"KFull{i % kst}", (i // kst) & 1, i // kst)
+        for k in range(1, min(2, q_armed) + 1):
+            i = q_armed - k
+            yield D(f"QFull{i & 1}", (i >> 1) & 1, i >> 1)
 
     def producer_v():
-        g = 0
+        g = v_armed = 0
+        ok = True
         for n in units:
             for _ in range(n):
                 st = g % vst
-                yield W(f"VEmpty{st}", ((g // vst) & 1) ^ 1, g // vst - 1)
-                yield A(f"VFull{st}")
+                ok = yield W(f"VEmpty{st}", ((g // vst) & 1) ^ 1, g // vst - 1)
+                if not ok:
+                    break
+                yield ("tma", f"VFull{st}")
+                v_armed += 1
                 g += 1
+            if not ok:
+                break
+        for k in range(1, min(vst, v_armed) + 1):
+            i = v_armed - k
+            yield D(f"VFull{i % vst}", (i // vst) & 1, i // vst)
 
     def mma_s():
         t = 0
+        ok = True
         for u, n in enumerate(units):
             qb = u & 1
-            yield W(f"QFull{qb}", (u >> 1) & 1, u >> 1)
+            ok = yield W(f"QFull{qb}", (u >> 1) & 1, u >> 1)
+            if not ok:
+                break
             for j in range(n):
                 k, b = t % kst, t & 1
-                yield W(f"KFull{k}", (t // kst) & 1, t // kst)
-                if t >= 2:
-                    yield W(f"SFree{b}", ((t >> 1) - 1) & 1, (t >> 1) - 1)
+                ok = yield W(f"KFull{k}", (t // kst) & 1, t // kst)
+                if ok and t >= 2:
+                    ok = yield W(f"SFree{b}", ((t >> 1) - 1) & 1, (t >> 1) - 1)
+                if not ok:
+                    break
                 yield ("mma", [f"SFull{b}", f"KEmpty{k}"] + ([f"QEmpty{qb}"] if j + 1 == n else []))
                 t += 1
+            if not ok:
+                break
+        yield ("mma", ["MmaDone0"])  # every MMA of this thread done before TMEM is freed
+        yield D("MmaDone0", 0, 0)
 
     def mma_pv():
         t = 0
+        ok = True
         for u, n in enumerate(units):
             for j in range(n):
                 v, b = t % vst, t & 1
-                yield W(f"{'VConv' if convert else 'VFull'}{v}", (t // vst) & 1, t // vst)
-                yield W(f"PReady{b}", (t >> 1) & 1, t >> 1)
-                if j == 0:
-                    yield W("OFree", (u & 1) ^ 1, u - 1)
+                ok = yield W(f"VFull{v}", (t // vst) & 1, t // vst)
+                if ok:
+                    ok = yield W(f"PReady{b}", (t >> 1) & 1, t >> 1)
+                if ok and j == 0:
+                    ok = yield W("OFree", (u & 1) ^ 1, u - 1)
+                if not ok:
+                    break
                 yield ("mma", [pv_done(t)[0], f"VEmpty{v}"])
                 t += 1
+            if not ok:
+                break
+        yield ("mma", ["MmaDone1"])
+        yield D("MmaDone1", 0, 0)
 
     def softmax():
         t = 0
         for u, n in enumerate(units):
             for j in range(n):
                 b = t & 1
-                yield W(f"SFull{b}", (t >> 1) & 1, t >> 1)
+                if not (yield W(f"SFull{b}", (t >> 1) & 1, t >> 1)):
+                    return
                 yield A(f"SFree{b}")
                 if j > 0 and rng.random() < rare:  # rescale O after P(t-1) V(t-1)
-                    yield W(*pv_done(t - 1))
+                    if not (yield W(*pv_done(t - 1))):
+                        return
                 if t >= 2:  # P buffer b free: P(t-2) V(t-2) done
-                    yield W(*pv_done(t - 2))
+                    if not (yield W(*pv_done(t - 2))):
+                        return
                 yield A(f"PReady{b}")
                 t += 1
             if u > 0:
-                yield W("LmFree", (u - 1) & 1, u - 1)
+                if not (yield W("LmFree", (u - 1) & 1, u - 1)):
+                    return
             yield A("LmFull")
 
     def epilogue():
@@ -116,102 +176,125 @@ def _run(units, kst, vst, seed, rare, handover_wait=True, convert=False):
             t += n
             tl = t - 1
             if handover_wait:
-                yield W("LmFull", u & 1, u)
+                if not (yield W("LmFull", u & 1, u)):
+                    return
             yield A("LmFree")
-            yield W(*pv_done(tl))
+            if not (yield W(*pv_done(tl))):
+                return
             yield A("OFree")
 
-    def epilogue_convert():
-        # poll whichever job is ready: convert the next landed value tile, or
-        # take the pending unit's (m, l), or write it once its last product is done
-        total = sum(units)
-        tv, go, u, ostage = 0, 0, 0, 0
-        while u < len(units) or tv < total:
-            opts = []
-            if tv < total:
-                opts.append((f"VFull{tv % vst}", (tv // vst) & 1, tv // vst, "conv"))
-            if u < len(units):
-                tl = go + units[u] - 1
-                if ostage == 0:
-                    opts.append(("LmFull", u & 1, u, "lm"))
-                else:
-                    opts.append((*pv_done(tl), "out"))
-            tag = yield ("poll", opts)
-            if tag == "conv":
-                yield A(f"VConv{tv % vst}")
-                tv += 1
-            elif tag == "lm":
-                yield A("LmFree")
-                ostage = 1
-            else:
-                yield A("OFree")
-                go += units[u]
-                u += 1
-                ostage = 0
-
     roles = {"qk": producer_qk(), "v": producer_v(), "s": mma_s(), "pv": mma_pv(),
-             "softmax": softmax(), "epilogue": epilogue_convert() if convert else epilogue()}
-    cur = dict.fromkeys(roles)
+             "softmax": softmax(), "epilogue": epilogue()}
+    cur = {k: None for k in roles}
     done = set()
+
+    def advance(k, value):
+        try:
+            cur[k] = roles[k].send(value) if value is not None else next(roles[k])
+        except StopIteration:
+            cur[k] = None
+            done.add(k)
+
+    for k in roles:
+        advance(k, None)
+    rounds = 0
     while len(done) < len(roles):
+        rounds += 1
+        assert rounds < 200000, "model did not finish"
         progressed = False
+        if abort_at is not None and not state["abort"] and rng.random() < abort_at:
+            state["abort"] = True
+            progressed = True
         if pipe and rng.random() < 0.5:
             for nm in pipe.pop(0):
                 B[nm].arrive()
             progressed = True
-        order = list(roles)
+        if copies and rng.random() < 0.5:
+            B[copies.pop(rng.randrange(len(copies)))].arrive()
+            progressed = True
+        order = [k for k in roles if k not in done]
         rng.shuffle(order)
         for k in order:
-            if k in done:
-                continue
-            if cur[k] is None:
-                try:
-                    cur[k] = next(roles[k])
-                except StopIteration:
-                    done.add(k)
-                    progressed = True
-                    continue
             op = cur[k]
             if op[0] == "arrive":
                 B[op[1]].arrive()
-                cur[k], progressed = None, True
+                advance(k, True)
+                progressed = True
             elif op[0] == "mma":
                 pipe.append(op[1])
-                cur[k], progressed = None, True
-            elif op[0] == "poll":
-                ready = []
-                for nm, par, kk, tag in op[1]:
-                    c = B[nm].c
-                    if (c & 1) != par:
-                        assert c >= kk + 1, f"{k}: test of {nm} phase {kk} passed early ({c} completed)"
-                        ready.append(tag)
-                    else:
-                        assert c <= kk, f"{k}: test of {nm} phase {kk} faces phase {c} (aliased)"
-                if ready:
-                    try:
-                        cur[k] = roles[k].send(rng.choice(ready))
-                    except StopIteration:
-                        done.add(k)
-                        cur[k] = None
-                    progressed = True
+                advance(k, True)
+                progressed = True
+            elif op[0] == "tma":
+                copies.append(op[1])
+                advance(k, True)
+                progressed = True
             else:
-                _, nm, par, kk = op
+                kind, nm, par, kk = op
                 c = B[nm].c
                 if (c & 1) != par:  # what try_wait.parity reports as complete
                     assert c >= kk + 1, f"{k}: wait on {nm} phase {kk} passed early ({c} completed)"
-                    cur[k], progressed = None, True
+                    advance(k, True)
+                    progressed = True
                 else:
                     assert c <= kk, f"{k}: wait on {nm} phase {kk} faces phase {c} (aliased)"
-        assert progressed or pipe, f"deadlock: { {k: cur[k] for k in roles if k not in done} }"
+                    if kind == "wait" and state["abort"]:
+                        advance(k, False)  # the bounded wait gives up
+                        progressed = True
+        assert progressed or pipe or copies, \
+            f"deadlock: { {k: cur[k] for k in roles if k not in done} }"
+    # every role has left: the CTA frees TMEM and exits now
+    assert not pipe, f"MMAs still in flight at exit: {pipe}"
+    assert not copies, f"copies still in flight at exit: {copies}"
+    return state["abort"]
 
 
-@pytest.mark.parametrize("mode", ["bf16_pv", "f16_pv"])
 @pytest.mark.parametrize("kst,vst", [(3, 2), (4, 4), (4, 3)])  # bf16 d=128, d=64, FP8
-def test_kernel_barrier_protocol(kst, vst, mode):
+def test_kernel_barrier_protocol(kst, vst):
     for seed in range(150):
         rng = random.Random(1000 * kst + 10 * vst + seed)
         units = [rng.choice([1, 1, 2, 3, 4, 5, 9, 17]) for _ in range(rng.randint(1, 16))]
-        _run(units, kst, vst, seed, rare=rng.choice([0.0, 0.1, 1.0]), convert=mode == "f16_pv")
+        _run(units, kst, vst, seed, rare=rng.choice([0.0, 0.1, 1.0]))
+
+
+@pytest.mark.parametrize("kst,vst", [(3, 2), (4, 4), (4, 3)])
+def test_abort_path_drains_every_copy_and_mma(kst, vst):
+    """Timeouts raised at random moments: every role leaves, and nothing is
+    in flight when TMEM is freed."""
+    aborted = 0
+    for seed in range(300):
+        rng = random.Random(7 + 1000 * kst + 10 * vst + seed)
+        units = [rng.choice([1, 2, 3, 5, 9, 17]) for _ in range(rng.randint(1, 12))]
+        aborted += _run(units, kst, vst, seed, rare=rng.choice([0.0, 0.1, 1.0]),
+                        abort_at=rng.choice([0.001, 0.01, 0.1, 0.5]))
+    assert aborted >= 150
+
+
+def test_model_catches_a_missing_drain():
+    """Plant a mistake in the model (the producers skip their drain): the
+    check that nothing is in flight at exit must catch it."""
+    caught = 0
+    for seed in range(60):
+        rng = random.Random(seed)
+        units = [rng.choice([2, 3, 5, 9]) for _ in range(rng.randint(2, 8))]
+        try:
+            _run_no_drain(units, 3, 2, seed, 0.1, abort_at=0.2)
+        except AssertionError as e:
+            assert "in flight" in str(e)
+            caught += 1
+    assert caught >= 10
+
+
+def _run_no_drain(*args, **kw):
+    """_run with the producers' drain waits removed (a planted mistake)."""
+    import inspect
+    import textwrap
+    text = textwrap.dedent(inspect.getsource(_run))
+    text = text.replace("yield D(f\"KFull", "pass  # yield D(f\"KFull").replace(
+        "yield D(f\"QFull", "pass  # yield D(f\"QFull").replace(
+        "yield D(f\"VFull", "pass  # yield D(f\"VFull").replace("def _run(", "def _planted(")
+    ns = dict(globals())
+    exec(compile(text, "<planted>", "exec"), ns)
+    return ns["_planted"](*args, **kw)
 
 
 def test_model_catches_a_skipped_phase():

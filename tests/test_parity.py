@@ -188,6 +188,34 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     _full(W.Pack("after-timeout", [[(W.TEXT, 20), (W.IMAGE, 150)]], hq=2, hkv=1, d=64, seed=2))
 
 
+def test_short_wait_limit_aborts_real_launches_and_the_context_survives():
+    """Wait limits of a few microseconds or less make the attention kernel's
+    own waits run out: the launch must report PK_ERR_TIMEOUT, leave through
+    its abort path (drains bounded independently of the limit) and keep the
+    context usable; with the default limit restored the next launch is
+    exact again."""
+    pack = W.mixed_resolution(seed=5, requests=2)
+    q, k, v = W.make_qkv(pack, device="cuda")
+    plan = pk.plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d)
+    seen = []
+    try:
+        for limit in (2000, 300, 1):
+            pk.set_wait_timeout_ns(limit)
+            status = torch.zeros(1, dtype=torch.int32, device="cuda")
+            pk.attn_fwd(q, k, v, plan, pack.scale, status=status)
+            torch.cuda.synchronize()
+            seen.append(int(status.item()))
+    finally:
+        pk.set_wait_timeout_ns(4_000_000_000)
+    assert set(seen) <= {pk.PK_OK, pk.PK_ERR_TIMEOUT}, seen
+    assert pk.PK_ERR_TIMEOUT in seen, seen
+    rows = W.sample_rows(pack, 128)
+    out_o, lse_o = oracle.attention(q.cpu(), k.cpu(), v.cpu(), pack.cu_seqlens, pack.segments,
+                                    pack.hq, pack.hkv, pack.d, pack.scale, rows=rows)
+    out_g, lse_g = _gpu(pack, q, k, v, plan)
+    _compare(pack, out_g, lse_g, out_o, lse_o, rows=rows, tag="/after-abort")
+
+
 def test_one_64k_token_sequence_sampled():
     """A single 65,536-token sequence (1,024 text + 64,512 image): 512 key
     tiles per query tile, the longest rows any workload here has."""
