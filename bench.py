@@ -188,14 +188,14 @@ def job_throughput(world: int, units_per_rank: float, steps: int, total_ms: floa
     return world * units_per_rank * steps / (total_ms * 1e-3)
 
 
-def workload_config(pack, world: int, useful_flops: float) -> dict:
+def workload_config(pack, world: int, useful_flops: float, split: bool = False) -> dict:
     """The bench line's config, identical for both arms: the workload, its
     per-step useful FLOPs (each arm counts them its own way: the planner
     here, the oracle's visible keys in the reference arm) and the L2 rule."""
     T = pack.total_tokens
     q_mb = T * pack.hq * pack.d * 2 / 1e6
     kv_mb = 2 * T * pack.hkv * pack.d * 2 / 1e6
-    return dict(pack.describe(), parallelism=f"replicas{world}",
+    return dict(pack.describe(), parallelism=f"split{world}" if split else f"replicas{world}",
                 l2="inputs larger than L2 (q %.0f MB, k+v %.0f MB)" % (q_mb, kv_mb),
                 useful_flops_per_step=float(useful_flops),
                 padded_dense_mask_flops_per_step=4.0 * pack.d * pack.hq * len(pack.seqs)
@@ -508,6 +508,10 @@ def main():
                     help="skip timing the LSE merge at the workload's output size")
     ap.add_argument("--merge-only", action="store_true",
                     help="time only the LSE merge (for profiling it alone)")
+    ap.add_argument("--split", action="store_true",
+                    help="under torchrun, split the one pack across the ranks (pk_plan_shard: "
+                         "whole (sequence, kv head) units per rank, no exchange; strong scaling) "
+                         "instead of running one replica per rank")
     ap.add_argument("--requests", type=int, default=8,
                     help="requests in the mixed-resolution pack (x2 CFG branches)")
     args = ap.parse_args()
@@ -538,6 +542,10 @@ def main():
     q, k, v = W.make_qkv(pack)
     q, k, v = q.to(dev), k.to(dev), v.to(dev)
     plan = pk.plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d, device=dev)
+    split = args.split and world > 1
+    full_plan = plan
+    if split:  # this rank's share of the one pack, on the full tensors
+        plan = full_plan.shard(rank, world, device=dev)
     out = torch.empty_like(q)
     lse = torch.empty(pack.hq, pack.total_tokens, dtype=torch.float32, device=dev)
     ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
@@ -584,10 +592,13 @@ def main():
         raise RuntimeError(f"device status {int(status.item())} in the timed region")
     total_ms = max_over_ranks(total_ms, dist, dev)
 
-    flops = plan.useful_flops
+    flops = plan.useful_flops  # this rank's launches
     ms_step = total_ms / args.steps
-    value = job_throughput(world, flops, args.steps, total_ms) / 1e12
-    tokens_per_s = job_throughput(world, pack.total_tokens, args.steps, total_ms)
+    # the job's units per step: one pack split across the ranks, or one
+    # replica per rank
+    job_ranks, job_flops = (1, full_plan.useful_flops) if split else (world, flops)
+    value = job_throughput(job_ranks, job_flops, args.steps, total_ms) / 1e12
+    tokens_per_s = job_throughput(job_ranks, pack.total_tokens, args.steps, total_ms)
 
     # end to end through the public host-buffer API: every step copies its
     # inputs from pinned host memory and its outputs back.  HostPipeline runs
@@ -634,13 +645,13 @@ def main():
         e_ms = max_over_ranks(p0.elapsed_time(p1), dist, dev)
         pipe.close()
         del bufs
-        e2e = {"value": job_throughput(world, flops, args.steps, e_ms) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": job_throughput(job_ranks, job_flops, args.steps, e_ms) / 1e12, "unit": "TFLOP/s",
                "ms_per_step": e_ms / args.steps,
                "h2d_bytes_per_step": int((q.numel() + k.numel() + v.numel()) * 2),
                "d2h_bytes_per_step": int(out.numel() * 2 + lse.numel() * 4),
                "api": "HostPipeline (3 device slots; copy-in, compute, copy-out streams)",
                "serial_ms_per_step": serial_ms / args.steps,
-               "serial_value": job_throughput(world, flops, args.steps, serial_ms) / 1e12}
+               "serial_value": job_throughput(job_ranks, job_flops, args.steps, serial_ms) / 1e12}
 
     per_workload = None
     if not args.no_sweep and rank == 0:
@@ -678,9 +689,9 @@ def main():
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "pv_dtype": "fp16", "data": "synthetic",
-        "config": workload_config(pack, world, flops),
+        "higher_is_better": True, "scaling": "strong" if split else "weak", "vs_baseline": None,
+        "dtype": "bf16", "pv_dtype": "fp16", "data": "synthetic",
+        "config": workload_config(pack, world, full_plan.useful_flops, split),
         "tokens_per_s": round(tokens_per_s),
         "pct_of_nominal_bf16_peak": round(100 * value / world / NOMINAL_BF16_TFLOPS, 2),
         "pct_of_measured_bf16_peak": round(100 * value / world / peaks["bf16_tflops"], 2),

@@ -125,8 +125,10 @@ typedef struct pk_plan_info {
   int32_t num_full_tiles;   /* (item, k-tile) visits with no mask math */
   int32_t num_partial_tiles;/* (item, k-tile) visits with per-element mask */
   int32_t kv_rows;          /* Tk: rows of the key/value tensors */
-  int64_t visible_pairs;    /* per query head */
-  double useful_flops;      /* 4 * d * hq * visible_pairs */
+  int64_t visible_pairs;    /* per query head, over the whole pack */
+  double useful_flops;      /* 4 * d per visible pair and query head of the
+                               plan's items (4 * d * hq * visible_pairs
+                               unless the plan is a shard) */
 } pk_plan_info;
 
 /* Device work item, 32 bytes, as stored in the plan image (exposed for
@@ -167,6 +169,23 @@ pk_status pk_plan_create(const int32_t* cu_seqlens, int32_t num_seqs,
  * 128-row blocks. */
 pk_status pk_plan_create_layout(const pk_layout* layout, int32_t hq, int32_t hkv,
                                 int32_t head_dim, int32_t num_ctas, pk_plan** out);
+
+/*
+ * One rank's share of a plan, for running one pack on several GPUs without
+ * an exchange (the pages' CFG-parallel and head-split schemes,
+ * "Parallelism Acceleration Guide").  The plan's work units, one (sequence,
+ * key/value head) pair each, go to ranks longest first, each to the
+ * least-loaded rank; every rank computes the same assignment, so the shares
+ * of ranks 0..num_ranks-1 partition the plan's work items exactly.  The
+ * shard keeps its units' items, scheduled over num_ctas CTAs (0 = the
+ * current device's SM count).  It is launched like any plan, on the full
+ * q, k, v tensors, and writes out and lse only for its units' rows and
+ * query heads; the union of the ranks' outputs is the full plan's output.
+ * pk_plan_useful_flops and pk_plan_get_info's num_items and tile counts
+ * describe the shard's own work.  *out owns a new plan (pk_plan_destroy).
+ */
+pk_status pk_plan_shard(const pk_plan* full, int32_t rank, int32_t num_ranks, int32_t num_ctas,
+                        pk_plan** out);
 
 /* Bytes of the device image of the plan (work list, per-CTA offsets, the
  * per-row key limit and, for paged keys, the block table). */
@@ -333,7 +352,9 @@ void pk_plan_destroy(pk_plan* plan);
 
 const char* pk_status_string(pk_status status);
 
-/* 4 * head_dim * hq * (visible (query, key) pairs per head). */
+/* 4 * head_dim per visible (query, key) pair and query head of the plan's
+ * work items: 4 * head_dim * hq * (visible pairs per head) for a whole pack,
+ * the shard's part for pk_plan_shard. */
 double pk_plan_useful_flops(const pk_plan* plan);
 
 pk_status pk_plan_get_info(const pk_plan* plan, pk_plan_info* info);

@@ -86,6 +86,8 @@ SIGNATURES = {
     "pk_plan_create_layout": (ctypes.c_int, [ctypes.POINTER(Layout), ctypes.c_int32,
                                              ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                              ctypes.POINTER(_vp)]),
+    "pk_plan_shard": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                     ctypes.POINTER(_vp)]),
     "pk_plan_device_bytes": (ctypes.c_size_t, [_vp]),
     "pk_plan_upload": (ctypes.c_int, [_vp, _vp, ctypes.c_size_t, _vp]),
     "pk_attn_workspace_bytes": (ctypes.c_size_t, [_vp]),

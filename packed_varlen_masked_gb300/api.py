@@ -34,12 +34,16 @@ class Plan:
     """
 
     def __init__(self, cu_seqlens, segments, hq: int, hkv: int, head_dim: int,
-                 num_ctas: int = 0, device=None, upload: bool = True, _layout=None):
+                 num_ctas: int = 0, device=None, upload: bool = True, _layout=None, _shard=None):
         self._lib = load()
         self._h = ctypes.c_void_p()
         self.hq, self.hkv, self.head_dim = int(hq), int(hkv), int(head_dim)
         self._buf = None
-        if _layout is not None:
+        if _shard is not None:
+            full, rank, world = _shard
+            check(self._lib.pk_plan_shard(full.handle, int(rank), int(world), int(num_ctas),
+                                          ctypes.byref(self._h)), "pk_plan_shard")
+        elif _layout is not None:
             lay, keep = _layout
             check(self._lib.pk_plan_create_layout(ctypes.byref(lay), self.hq, self.hkv,
                                                   self.head_dim, int(num_ctas),
@@ -59,6 +63,15 @@ class Plan:
         self.kv_rows = int(info["kv_rows"])
         if upload:
             self.upload(device)
+
+    def shard(self, rank: int, num_ranks: int, num_ctas: int = 0, device=None,
+              upload: bool = True) -> "Plan":
+        """Rank ``rank``'s share of this plan (pk_plan_shard): whole
+        (sequence, key/value head) units, longest first to the least-loaded
+        rank; launched on the full tensors, it writes only its units' rows
+        and heads."""
+        return Plan(None, None, self.hq, self.hkv, self.head_dim, num_ctas=num_ctas,
+                    device=device, upload=upload, _shard=(self, rank, num_ranks))
 
     # -- lifetime -----------------------------------------------------------
     def close(self) -> None:

@@ -41,7 +41,10 @@ struct pk_plan {
   int32_t hq = 0, hkv = 0, head_dim = 0;
   int32_t num_ctas = 0;
   int32_t num_full_tiles = 0, num_partial_tiles = 0;
-  int64_t visible_pairs = 0;
+  int64_t visible_pairs = 0;    // per query head, over the whole pack
+  double useful_flops = 0.0;    // 4 d per visible pair and query head of this plan's items
+  std::vector<int32_t> cu_q;    // [num_seqs + 1] query rows of each sequence
+  int32_t shard_rank = 0, shard_ranks = 1;  // pk_plan_shard: this plan's share
   std::vector<int32_t> kv_limit;           // [Tq] last visible key of the row's key range, -1 none
   // Value rows the attention kernel reads, for their conversion to fp16:
   // contiguous keys, rows [0, v_conv_rows) (rows [v_conv_rows, Tk) no

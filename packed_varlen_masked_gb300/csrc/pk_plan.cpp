@@ -106,15 +106,10 @@ pk_status validate_layout(const pk_layout& L, int32_t hq, int32_t hkv, int32_t d
   return PK_OK;
 }
 
-pk_status build_plan(const pk_layout& L, int32_t hq, int32_t hkv, int32_t d, int32_t num_ctas,
-                     pk_plan** out) {
-  if (out == nullptr) return PK_ERR_INVALID_ARG;
-  *out = nullptr;
-  std::vector<int32_t> seg_first, seq_len;
-  pk_status st = validate_layout(L, hq, hkv, d, seg_first, seq_len);
-  if (st != PK_OK) return st;
-  if (num_ctas < 0) return PK_ERR_INVALID_ARG;
-  if (num_ctas == 0) {
+// num_ctas 0: the current device's SM count.
+pk_status resolve_num_ctas(int32_t* num_ctas) {
+  if (*num_ctas < 0) return PK_ERR_INVALID_ARG;
+  if (*num_ctas == 0) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -122,8 +117,86 @@ pk_status build_plan(const pk_layout& L, int32_t hq, int32_t hkv, int32_t d, int
       cudaGetLastError();
       return PK_ERR_CUDA;
     }
-    num_ctas = sms;
+    *num_ctas = sms;
   }
+  return PK_OK;
+}
+
+// Longest-processing-time-first schedule of `items` over `num_ctas` CTAs,
+// then the plan's device image.
+void schedule_and_image(pk_plan* p, std::vector<pk_work_item> items, int32_t num_ctas) {
+  const int32_t Tq = p->T;
+  // The plan's own work: tiles visited and useful FLOPs (4 d per visible
+  // (query, key) pair and query head of its items).
+  p->num_full_tiles = p->num_partial_tiles = 0;
+  double pairs_x_heads = 0.0;
+  for (const pk_work_item& w : items) {
+    p->num_full_tiles += w.n_full;
+    p->num_partial_tiles += w.n_kt - w.n_full;
+    int64_t pairs = 0;
+    for (int32_t r = 0; r < w.q_rows; ++r) pairs += p->kv_limit[w.q_start + r] + 1;
+    pairs_x_heads += static_cast<double>(pairs) * (w.hq1 >= 0 ? 2 : 1);
+  }
+  p->useful_flops = 4.0 * p->head_dim * pairs_x_heads;
+  // Longest-processing-time-first: sort by cost (ties keep pack order so
+  // items streaming the same keys/values start side by side), then give each
+  // item to the least-loaded CTA.
+  const int32_t n_items = static_cast<int32_t>(items.size());
+  const int32_t grid = std::min<int32_t>(num_ctas, n_items);
+  p->num_ctas = grid;
+  std::vector<int32_t> order(n_items);
+  std::iota(order.begin(), order.end(), 0);
+  std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b2) {
+    return item_cost(items[a]) > item_cost(items[b2]);
+  });
+  std::vector<std::vector<int32_t>> per_cta(grid);
+  using Load = std::pair<double, int32_t>;
+  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+  for (int32_t c = 0; c < grid; ++c) heap.push({0.0, c});
+  for (int32_t idx : order) {
+    Load l = heap.top();
+    heap.pop();
+    per_cta[l.second].push_back(idx);
+    l.first += item_cost(items[idx]);
+    heap.push(l);
+  }
+  p->cta_offsets.assign(grid + 1, 0);
+  p->items.reserve(n_items);
+  for (int32_t c = 0; c < grid; ++c) {
+    for (int32_t idx : per_cta[c]) p->items.push_back(items[idx]);
+    p->cta_offsets[c + 1] = static_cast<int32_t>(p->items.size());
+  }
+
+  // Device image.
+  pk::PlanImageLayout& IL = p->layout;
+  IL.items_off = 0;
+  IL.cta_off_off = align_up(IL.items_off + sizeof(pk_work_item) * n_items, pk::kImageAlign);
+  IL.kvlim_off = align_up(IL.cta_off_off + sizeof(int32_t) * (grid + 1), pk::kImageAlign);
+  IL.table_off = align_up(IL.kvlim_off + sizeof(int32_t) * static_cast<size_t>(Tq), pk::kImageAlign);
+  IL.vblk_off = align_up(IL.table_off + sizeof(int32_t) * p->block_table.size(), pk::kImageAlign);
+  IL.bytes = align_up(IL.vblk_off + sizeof(int32_t) * p->v_blocks.size(), pk::kImageAlign);
+  p->image.assign(IL.bytes, 0);
+  if (n_items)
+    std::memcpy(p->image.data() + IL.items_off, p->items.data(), sizeof(pk_work_item) * n_items);
+  std::memcpy(p->image.data() + IL.cta_off_off, p->cta_offsets.data(), sizeof(int32_t) * (grid + 1));
+  if (Tq)
+    std::memcpy(p->image.data() + IL.kvlim_off, p->kv_limit.data(), sizeof(int32_t) * Tq);
+  if (!p->block_table.empty())
+    std::memcpy(p->image.data() + IL.table_off, p->block_table.data(),
+                sizeof(int32_t) * p->block_table.size());
+  if (!p->v_blocks.empty())
+    std::memcpy(p->image.data() + IL.vblk_off, p->v_blocks.data(),
+                sizeof(int32_t) * p->v_blocks.size());
+}
+
+pk_status build_plan(const pk_layout& L, int32_t hq, int32_t hkv, int32_t d, int32_t num_ctas,
+                     pk_plan** out) {
+  if (out == nullptr) return PK_ERR_INVALID_ARG;
+  *out = nullptr;
+  std::vector<int32_t> seg_first, seq_len;
+  pk_status st = validate_layout(L, hq, hkv, d, seg_first, seq_len);
+  if (st != PK_OK) return st;
+  if ((st = resolve_num_ctas(&num_ctas)) != PK_OK) return st;
 
   // Owned here until the plan is complete (the vectors below may throw).
   std::unique_ptr<pk_plan> owner(new pk_plan());
@@ -222,63 +295,82 @@ pk_status build_plan(const pk_layout& L, int32_t hq, int32_t hkv, int32_t d, int
           w.hq0 = g * group + 2 * pr;
           w.hq1 = (2 * pr + 1 < group) ? w.hq0 + 1 : -1;
           items.push_back(w);
-          p->num_full_tiles += w.n_full;
-          p->num_partial_tiles += w.n_kt - w.n_full;
         }
       }
     }
   }
 
-  // Longest-processing-time-first: sort by cost (ties keep pack order so
-  // items streaming the same keys/values start side by side), then give each
-  // item to the least-loaded CTA.
-  const int32_t n_items = static_cast<int32_t>(items.size());
-  const int32_t grid = std::min<int32_t>(num_ctas, n_items);
-  p->num_ctas = grid;
-  std::vector<int32_t> order(n_items);
+  p->cu_q.assign(cq, cq + S + 1);
+  schedule_and_image(p, std::move(items), num_ctas);
+  *out = owner.release();
+  return PK_OK;
+}
+
+// One rank's share of a plan: the plan's work units, a (sequence, key/value
+// head) pair each (all query tiles and query heads of one sequence that read
+// one key/value head), go to ranks longest first, each to the least-loaded
+// rank (the items' cost model), which every rank computes identically; the
+// rank keeps its units' items and schedules them over its own CTAs.  The
+// host data the kernel reads (key limits, block table, value rows) is the
+// full plan's, so the rank's kernel runs on the full tensors and writes only
+// its rows and heads of out and lse.
+pk_status build_shard(const pk_plan* full, int32_t rank, int32_t num_ranks, int32_t num_ctas,
+                      pk_plan** out) {
+  if (out == nullptr) return PK_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (full == nullptr || num_ranks < 1 || rank < 0 || rank >= num_ranks) return PK_ERR_INVALID_ARG;
+  pk_status st = resolve_num_ctas(&num_ctas);
+  if (st != PK_OK) return st;
+  // units in (sequence, key/value head) order
+  const int64_t n_units = static_cast<int64_t>(full->num_seqs) * full->hkv;
+  std::vector<double> cost(n_units, 0.0);
+  std::vector<int64_t> unit_of(full->items.size());
+  for (size_t i = 0; i < full->items.size(); ++i) {
+    const pk_work_item& w = full->items[i];
+    const int32_t s =
+        static_cast<int32_t>(std::upper_bound(full->cu_q.begin(), full->cu_q.end(), w.q_start) -
+                             full->cu_q.begin()) - 1;
+    unit_of[i] = static_cast<int64_t>(s) * full->hkv + w.hkv;
+    cost[unit_of[i]] += item_cost(w);
+  }
+  std::vector<int64_t> order(n_units);
   std::iota(order.begin(), order.end(), 0);
-  std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b2) {
-    return item_cost(items[a]) > item_cost(items[b2]);
-  });
-  std::vector<std::vector<int32_t>> per_cta(grid);
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int64_t a, int64_t b) { return cost[a] > cost[b]; });
+  std::vector<int32_t> owner_of(n_units, -1);
   using Load = std::pair<double, int32_t>;
   std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
-  for (int32_t c = 0; c < grid; ++c) heap.push({0.0, c});
-  for (int32_t idx : order) {
+  for (int32_t r = 0; r < num_ranks; ++r) heap.push({0.0, r});
+  for (int64_t u : order) {
+    if (cost[u] == 0.0) continue;  // no items
     Load l = heap.top();
     heap.pop();
-    per_cta[l.second].push_back(idx);
-    l.first += item_cost(items[idx]);
+    owner_of[u] = l.second;
+    l.first += cost[u];
     heap.push(l);
   }
-  p->cta_offsets.assign(grid + 1, 0);
-  p->items.reserve(n_items);
-  for (int32_t c = 0; c < grid; ++c) {
-    for (int32_t idx : per_cta[c]) p->items.push_back(items[idx]);
-    p->cta_offsets[c + 1] = static_cast<int32_t>(p->items.size());
-  }
-
-  // Device image.
-  pk::PlanImageLayout& IL = p->layout;
-  IL.items_off = 0;
-  IL.cta_off_off = align_up(IL.items_off + sizeof(pk_work_item) * n_items, pk::kImageAlign);
-  IL.kvlim_off = align_up(IL.cta_off_off + sizeof(int32_t) * (grid + 1), pk::kImageAlign);
-  IL.table_off = align_up(IL.kvlim_off + sizeof(int32_t) * static_cast<size_t>(Tq), pk::kImageAlign);
-  IL.vblk_off = align_up(IL.table_off + sizeof(int32_t) * p->block_table.size(), pk::kImageAlign);
-  IL.bytes = align_up(IL.vblk_off + sizeof(int32_t) * p->v_blocks.size(), pk::kImageAlign);
-  p->image.assign(IL.bytes, 0);
-  if (n_items)
-    std::memcpy(p->image.data() + IL.items_off, p->items.data(), sizeof(pk_work_item) * n_items);
-  std::memcpy(p->image.data() + IL.cta_off_off, p->cta_offsets.data(), sizeof(int32_t) * (grid + 1));
-  if (Tq)
-    std::memcpy(p->image.data() + IL.kvlim_off, p->kv_limit.data(), sizeof(int32_t) * Tq);
-  if (!p->block_table.empty())
-    std::memcpy(p->image.data() + IL.table_off, p->block_table.data(),
-                sizeof(int32_t) * p->block_table.size());
-  if (!p->v_blocks.empty())
-    std::memcpy(p->image.data() + IL.vblk_off, p->v_blocks.data(),
-                sizeof(int32_t) * p->v_blocks.size());
-
+  std::unique_ptr<pk_plan> owner(new pk_plan());
+  pk_plan* p = owner.get();
+  p->T = full->T;
+  p->Tk = full->Tk;
+  p->paged = full->paged;
+  p->blocks_per_seq = full->blocks_per_seq;
+  p->block_table = full->block_table;
+  p->num_seqs = full->num_seqs;
+  p->hq = full->hq;
+  p->hkv = full->hkv;
+  p->head_dim = full->head_dim;
+  p->visible_pairs = full->visible_pairs;
+  p->kv_limit = full->kv_limit;
+  p->v_conv_rows = full->v_conv_rows;
+  p->v_blocks = full->v_blocks;
+  p->cu_q = full->cu_q;
+  p->shard_rank = rank;
+  p->shard_ranks = num_ranks;
+  std::vector<pk_work_item> items;
+  for (size_t i = 0; i < full->items.size(); ++i)
+    if (owner_of[unit_of[i]] == rank) items.push_back(full->items[i]);
+  schedule_and_image(p, std::move(items), num_ctas);
   *out = owner.release();
   return PK_OK;
 }
@@ -372,6 +464,12 @@ pk_status pk_plan_create(const int32_t* cu, int32_t num_seqs, const pk_segment* 
   });
 }
 
+pk_status pk_plan_shard(const pk_plan* full, int32_t rank, int32_t num_ranks, int32_t num_ctas,
+                        pk_plan** out) {
+  if (out) *out = nullptr;
+  return guarded([&] { return build_shard(full, rank, num_ranks, num_ctas, out); });
+}
+
 size_t pk_plan_device_bytes(const pk_plan* p) { return p ? p->layout.bytes : 0; }
 
 size_t pk_attn_workspace_bytes(const pk_plan* p) {
@@ -393,9 +491,7 @@ pk_status pk_plan_upload(pk_plan* p, void* dev_buf, size_t bytes, pk_stream_t st
 
 void pk_plan_destroy(pk_plan* p) { delete p; }
 
-double pk_plan_useful_flops(const pk_plan* p) {
-  return p ? 4.0 * p->head_dim * p->hq * static_cast<double>(p->visible_pairs) : 0.0;
-}
+double pk_plan_useful_flops(const pk_plan* p) { return p ? p->useful_flops : 0.0; }
 
 pk_status pk_plan_get_info(const pk_plan* p, pk_plan_info* info) {
   if (p == nullptr || info == nullptr) return PK_ERR_INVALID_ARG;

@@ -2,8 +2,9 @@
 CPU: packs are independent problems, so every rank runs its own replica
 (weak scaling, no collective on the data path); the job's step time is the
 slowest rank's, and the job's rate counts the units of every rank.  Also:
-every rank plans the same pack identically, and only rank 0 runs the CPU
-reference arm."""
+every rank plans the same pack identically, only rank 0 runs the CPU
+reference arm, and when one pack is split across the ranks (pk_plan_shard)
+the shares each rank computes on its own partition the pack's work."""
 import io
 import os
 import socket
@@ -100,3 +101,59 @@ def test_peaks_file_is_read_with_burst_sustained_and_copy_figures(tmp_path):
     assert p == {"bf16_tflops": 1878.4, "hbm_gbs": 6692.8, "bf16_tflops_sustained": 1724.6,
                  "source": "measured"}
     assert bench.load_peaks(str(tmp_path / "missing.json"))["source"] == "fallback"
+
+
+def _shard_rank_main(rank, world, port, out_dir):
+    sys.path.insert(0, ROOT)
+    import torch
+    import torch.distributed as dist
+    import packed_varlen_masked_gb300 as pk
+    import workloads as W
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
+                            world_size=world)
+    try:
+        pack = W.mixed_resolution()
+        full = pk.Plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d, num_ctas=152,
+                       upload=False)
+        mine = full.shard(rank, world, num_ctas=152, upload=False)  # computed on this rank alone
+        items, _ = mine.items()
+        n = torch.tensor([len(items)], dtype=torch.int64)
+        counts = [torch.zeros(1, dtype=torch.int64) for _ in range(world)]
+        dist.all_gather(counts, n)
+        width = int(max(c.item() for c in counts))
+        padded = torch.full((width, 8), -9, dtype=torch.int64)
+        padded[:len(items)] = torch.as_tensor(items.astype(np.int64))
+        gathered = [torch.zeros(width, 8, dtype=torch.int64) for _ in range(world)]
+        dist.all_gather(gathered, padded)
+        flops = torch.tensor([mine.useful_flops], dtype=torch.float64)
+        dist.all_reduce(flops)
+        if rank == 0:
+            f_items, _ = full.items()
+            got = np.concatenate([g[:int(c.item())].numpy() for g, c in zip(gathered, counts)])
+            np.save(os.path.join(out_dir, "shard_items.npy"), got)
+            np.save(os.path.join(out_dir, "full_items.npy"), f_items.astype(np.int64))
+            np.save(os.path.join(out_dir, "flops.npy"), np.array([float(flops.item()),
+                                                                   full.useful_flops]))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_split_one_pack_into_a_partition(tmp_path):
+    world = 2
+    ctx = mp.get_context("spawn")
+    port = _free_port()
+    procs = [ctx.Process(target=_shard_rank_main, args=(r, world, port, str(tmp_path)))
+             for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=180)
+    for p in procs:
+        if p.is_alive():
+            p.kill()
+        assert p.exitcode == 0, p.exitcode
+    got = np.load(tmp_path / "shard_items.npy")
+    full = np.load(tmp_path / "full_items.npy")
+    assert sorted(map(tuple, got.tolist())) == sorted(map(tuple, full.tolist()))
+    fl = np.load(tmp_path / "flops.npy")
+    assert fl[0] == pytest.approx(fl[1], rel=1e-12)

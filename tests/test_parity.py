@@ -216,6 +216,33 @@ def test_short_wait_limit_aborts_real_launches_and_the_context_survives():
     _compare(pack, out_g, lse_g, out_o, lse_o, rows=rows, tag="/after-abort")
 
 
+@pytest.mark.parametrize("world", [2, 3])
+def test_pack_split_across_ranks_assembles_to_the_single_launch(world):
+    """The shares of pk_plan_shard, run one after another on this GPU (they
+    do not wait on one another), each write only their units' rows and
+    heads; put together they equal the one-launch result bit for bit."""
+    pack = W.mixed_resolution(seed=7, requests=2)
+    q, k, v = W.make_qkv(pack, device="cuda")
+    full = pk.plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d)
+    ref_o, ref_l = pk.attn_fwd(q, k, v, full, pack.scale, check_status=True)
+    owner = torch.full((pack.total_tokens, pack.hq), -1, dtype=torch.int32, device="cuda")
+    asm_o = torch.zeros_like(ref_o)
+    asm_l = torch.zeros_like(ref_l)
+    for r in range(world):
+        sh = full.shard(r, world)
+        o = torch.full_like(ref_o, float("nan"))
+        l = torch.full_like(ref_l, float("nan"))
+        pk.attn_fwd(q, k, v, sh, pack.scale, out=o, lse=l, check_status=True)
+        written = ~torch.isnan(l).T  # [T, hq]
+        assert bool((owner[written] == -1).all()), "a row/head written by two ranks"
+        assert bool((~torch.isnan(o)).all(-1).eq(written).all())
+        owner[written] = r
+        asm_o[written] = o[written]
+        asm_l.T[written] = l.T[written]
+    assert bool((owner >= 0).all())
+    assert torch.equal(asm_o, ref_o) and torch.equal(asm_l, ref_l)
+
+
 def test_one_64k_token_sequence_sampled():
     """A single 65,536-token sequence (1,024 text + 64,512 image): 512 key
     tiles per query tile, the longest rows any workload here has."""
