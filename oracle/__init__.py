@@ -101,6 +101,12 @@ def _load():
                                            ctypes.c_double, i32p, ctypes.c_int32, f64p, f64p,
                                            ctypes.c_int32]
         lib.pko_attention_e4m3.restype = ctypes.c_int
+        lib.pko_attention_e4m3_v8.argtypes = [u8p, ctypes.c_double, u8p, ctypes.c_double, u8p,
+                                              ctypes.c_double, i32p, ctypes.c_int32, i32p,
+                                              ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                              ctypes.c_int32, ctypes.c_double, i32p,
+                                              ctypes.c_int32, f64p, f64p, ctypes.c_int32]
+        lib.pko_attention_e4m3_v8.restype = ctypes.c_int
         lib.pko_attention.argtypes = [u16p, u16p, u16p, i32p, ctypes.c_int32, i32p,
                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                       ctypes.c_int32, ctypes.c_double, i32p,
@@ -219,6 +225,32 @@ def attention_e4m3(q8, q_scale: float, k8, k_scale: float, v, cu_seqlens, segmen
     rc = _load().pko_attention_e4m3(
         _ptr(qb, ctypes.c_uint8), float(q_scale), _ptr(kb, ctypes.c_uint8), float(k_scale),
         _ptr(vb, ctypes.c_uint16), _ptr(cu, ctypes.c_int32), len(cu) - 1,
+        _ptr(sg, ctypes.c_int32), sg.shape[0], hq, hkv, d, float(scale), rp, R,
+        _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double), int(nthreads))
+    if rc:
+        raise ValueError(f"oracle: invalid arguments (code {rc})")
+    return out, lse
+
+
+def attention_e4m3_v8(q8, q_scale: float, k8, k_scale: float, v8, v_scale: float, cu_seqlens,
+                      segments, hq: int, hkv: int, d: int, scale: float, rows=None,
+                      nthreads: int = 0):
+    """fp64 packed masked attention with E4M3 q, k and v (codes + one scale
+    each).  Returns (out [R, hq, d], lse [hq, R]) like ``attention``."""
+    qb, kb, vb = _codes(q8), _codes(k8), _codes(v8)
+    cu = _i32(cu_seqlens)
+    sg = _segs_array(segments)
+    T = int(cu[-1])
+    if rows is None:
+        R, rp = T, None
+    else:
+        rr = _i32(rows)
+        R, rp = rr.size, _ptr(rr, ctypes.c_int32)
+    out = np.zeros((R, hq, d), dtype=np.float64)
+    lse = np.zeros((hq, R), dtype=np.float64)
+    rc = _load().pko_attention_e4m3_v8(
+        _ptr(qb, ctypes.c_uint8), float(q_scale), _ptr(kb, ctypes.c_uint8), float(k_scale),
+        _ptr(vb, ctypes.c_uint8), float(v_scale), _ptr(cu, ctypes.c_int32), len(cu) - 1,
         _ptr(sg, ctypes.c_int32), sg.shape[0], hq, hkv, d, float(scale), rp, R,
         _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double), int(nthreads))
     if rc:

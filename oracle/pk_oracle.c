@@ -468,10 +468,12 @@ double pko_e4m3_to_double(uint8_t code) {
 }
 
 /* One query row over its sequence: q value = e4m3(q8) * q_scale, k value =
- * e4m3(k8) * k_scale, v bf16; the same score, LSE and output definitions as
- * the bf16 entry.  A row with no visible key gets o = 0, lse = -inf. */
+ * e4m3(k8) * k_scale, v bf16 (v8_seq NULL) or e4m3(v8) * v_scale; the same
+ * score, LSE and output definitions as the bf16 entry.  A row with no
+ * visible key gets o = 0, lse = -inf. */
 static void attend_row_e4m3(const uint8_t* q_row, double q_scale, const uint8_t* k_seq,
-                            double k_scale, const uint16_t* v_seq, const uint8_t* mrow,
+                            double k_scale, const uint16_t* v_seq, const uint8_t* v8_seq,
+                            double v_scale, const uint8_t* mrow,
                             int32_t L, int32_t Hq, int32_t Hkv, int32_t d, double scale,
                             double* out_row, double* lse, int64_t lse_stride, double* s_buf) {
   const int32_t group = Hq / Hkv;
@@ -501,20 +503,25 @@ static void attend_row_e4m3(const uint8_t* q_row, double q_scale, const uint8_t*
     for (int32_t j = 0; j < L; ++j) {
       if (!mrow[j]) continue;
       const double w = exp(s_buf[j] - l);
-      const uint16_t* vr = v_seq + ((size_t)j * Hkv + g) * d;
-      for (int32_t c = 0; c < d; ++c) o[c] += w * pko_bf16_to_double(vr[c]);
+      const size_t vo = ((size_t)j * Hkv + g) * d;
+      if (v8_seq)
+        for (int32_t c = 0; c < d; ++c) o[c] += w * (pko_e4m3_to_double(v8_seq[vo + c]) * v_scale);
+      else
+        for (int32_t c = 0; c < d; ++c) o[c] += w * pko_bf16_to_double(v_seq[vo + c]);
     }
   }
 }
 
-/* Packed attention with E4M3 q [T][Hq][d] and k [T][Hkv][d] (codes), their
- * scales, bf16 v.  rows == NULL: every row, out [T][Hq][d], lse [Hq][T];
- * else the n_rows listed rows, out [n_rows][Hq][d], lse [Hq][n_rows]. */
-int pko_attention_e4m3(const uint8_t* q8, double q_scale, const uint8_t* k8, double k_scale,
-                       const uint16_t* v, const int32_t* cu, int32_t num_seqs,
-                       const int32_t* segs, int32_t num_segs, int32_t Hq, int32_t Hkv,
-                       int32_t d, double scale, const int32_t* rows, int32_t n_rows,
-                       double* out, double* lse, int32_t nthreads) {
+/* Packed attention with E4M3 q [T][Hq][d] and k [T][Hkv][d] (codes) and
+ * their scales; v bf16 (v8 NULL) or E4M3 codes v8 [T][Hkv][d] with v_scale.
+ * rows == NULL: every row, out [T][Hq][d], lse [Hq][T]; else the n_rows
+ * listed rows, out [n_rows][Hq][d], lse [Hq][n_rows]. */
+static int attention_e4m3(const uint8_t* q8, double q_scale, const uint8_t* k8, double k_scale,
+                          const uint16_t* v, const uint8_t* v8, double v_scale,
+                          const int32_t* cu, int32_t num_seqs,
+                          const int32_t* segs, int32_t num_segs, int32_t Hq, int32_t Hkv,
+                          int32_t d, double scale, const int32_t* rows, int32_t n_rows,
+                          double* out, double* lse, int32_t nthreads) {
   int rc = pko_validate(cu, num_seqs, segs, num_segs);
   if (rc) return rc;
   if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || d <= 0) return 10;
@@ -541,7 +548,8 @@ int pko_attention_e4m3(const uint8_t* q8, double q_scale, const uint8_t* k8, dou
       const int32_t b = cu[s], L = cu[s + 1] - cu[s];
       mask_row(b, L, t - b, seg_of, segs, mrow);
       attend_row_e4m3(q8 + (size_t)t * Hq * d, q_scale, k8 + (size_t)b * Hkv * d, k_scale,
-                      v + (size_t)b * Hkv * d, mrow, L, Hq, Hkv, d, scale,
+                      v8 ? NULL : v + (size_t)b * Hkv * d, v8 ? v8 + (size_t)b * Hkv * d : NULL,
+                      v_scale, mrow, L, Hq, Hkv, d, scale,
                       out + (size_t)r * Hq * d, lse + r, n, s_buf);
     }
     free(s_buf);
@@ -549,4 +557,24 @@ int pko_attention_e4m3(const uint8_t* q8, double q_scale, const uint8_t* k8, dou
   }
   free(seg_of);
   return 0;
+}
+
+int pko_attention_e4m3(const uint8_t* q8, double q_scale, const uint8_t* k8, double k_scale,
+                       const uint16_t* v, const int32_t* cu, int32_t num_seqs,
+                       const int32_t* segs, int32_t num_segs, int32_t Hq, int32_t Hkv,
+                       int32_t d, double scale, const int32_t* rows, int32_t n_rows,
+                       double* out, double* lse, int32_t nthreads) {
+  return attention_e4m3(q8, q_scale, k8, k_scale, v, NULL, 1.0, cu, num_seqs, segs, num_segs,
+                        Hq, Hkv, d, scale, rows, n_rows, out, lse, nthreads);
+}
+
+/* The same with E4M3 values too: v8 [T][Hkv][d] codes, value e4m3(v8) * v_scale. */
+int pko_attention_e4m3_v8(const uint8_t* q8, double q_scale, const uint8_t* k8, double k_scale,
+                          const uint8_t* v8, double v_scale, const int32_t* cu, int32_t num_seqs,
+                          const int32_t* segs, int32_t num_segs, int32_t Hq, int32_t Hkv,
+                          int32_t d, double scale, const int32_t* rows, int32_t n_rows,
+                          double* out, double* lse, int32_t nthreads) {
+  if (v8 == NULL) return 10;
+  return attention_e4m3(q8, q_scale, k8, k_scale, NULL, v8, v_scale, cu, num_seqs, segs,
+                        num_segs, Hq, Hkv, d, scale, rows, n_rows, out, lse, nthreads);
 }

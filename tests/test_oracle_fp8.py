@@ -67,3 +67,28 @@ def test_quantizer_uses_the_full_e4m3_range():
     deq = codes.view(torch.float8_e4m3fn).float() * s
     assert float(deq.abs().max()) == pytest.approx(float(x.float().abs().max()), rel=1e-6)
     assert float((deq - x.float()).abs().max()) <= float(x.float().abs().max()) * 2.0 ** -4
+
+
+def test_e4m3_value_attention_equals_bf16_attention_on_the_decoded_values():
+    """E4M3 values too (codes and a power-of-two scale, exact in bf16): the
+    all-E4M3 entry must reproduce the pinned bf16 oracle on the decoded
+    q, k and v, and the value scale must act as a plain factor."""
+    pack = _pack()
+    q, k, v = W.make_qkv(pack)
+    q8, _ = W.quantize_e4m3(q)
+    k8, _ = W.quantize_e4m3(k)
+    v8, _ = W.quantize_e4m3(v)
+    qs, ks, vs = 2.0 ** -5, 2.0 ** -4, 2.0 ** -3
+    dec = lambda c, s: (c.view(torch.float8_e4m3fn).float() * s).to(torch.bfloat16)
+    qd, kd, vd = dec(q8, qs), dec(k8, ks), dec(v8, vs)
+    assert torch.equal(vd.float(), v8.view(torch.float8_e4m3fn).float() * vs)  # exact
+    o8, l8 = oracle.attention_e4m3_v8(q8, qs, k8, ks, v8, vs, pack.cu_seqlens, pack.segments,
+                                      pack.hq, pack.hkv, pack.d, pack.scale)
+    o, l = oracle.attention(qd, kd, vd, pack.cu_seqlens, pack.segments, pack.hq, pack.hkv,
+                            pack.d, pack.scale)
+    np.testing.assert_allclose(o8, o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l8, l, rtol=0, atol=1e-12)
+    o2, l2 = oracle.attention_e4m3_v8(q8, qs, k8, ks, v8, 2 * vs, pack.cu_seqlens, pack.segments,
+                                      pack.hq, pack.hkv, pack.d, pack.scale)
+    np.testing.assert_allclose(o2, 2 * o8, rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(l2, l8)
