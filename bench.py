@@ -459,6 +459,39 @@ def fp8_bench(pk, torch, stream, dev, pack, q, k, v, reps=10):
     return res
 
 
+def fp8_pv_bench(pk, torch, stream, dev, pack, q, k, v, reps=10):
+    """The workload with FP8 E4M3 queries, keys and values and E4M3 softmax
+    weights (one launch: the value transpose, then the attention)."""
+    q8, qs = W.quantize_e4m3(q)
+    k8, ks = W.quantize_e4m3(k)
+    v8, vs = W.quantize_e4m3(v)
+    plan = pk.plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty(pack.hq, pack.total_tokens, dtype=torch.float32, device=dev)
+    ws = torch.empty(plan.workspace_bytes_fp8_pv, dtype=torch.uint8, device=dev)
+
+    def call():
+        pk.attn_fwd_fp8_pv(q8, qs, k8, ks, v8, vs, plan, pack.scale, out=out, lse=lse,
+                           workspace=ws)
+    for _ in range(3):
+        call()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(reps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    res = {"kernels": ["pk_v8_transpose_kernel", "pk_attn_fwd_kernel<128, fp8 q/k/v/p>"],
+           "ms": round(ms, 4), "useful_tflops": round(plan.useful_flops / ms / 1e9, 1),
+           "parity": "output error above the 1e-2 bound (E4M3 softmax weights); lse within "
+                     "1e-3: recorded by the GPU tests"}
+    del q8, k8, v8, out, lse, plan, ws
+    torch.cuda.empty_cache()
+    return res
+
+
 def sweep(pk, torch, stream, dev):
     """Timing-only pass over every workload (device-generated inputs)."""
     res = {}
@@ -656,10 +689,11 @@ def main():
     per_workload = None
     if not args.no_sweep and rank == 0:
         per_workload = sweep(pk, torch, stream, dev)
-    layouts = fp8 = None
+    layouts = fp8 = fp8_pv = None
     if not args.no_sweep and rank == 0:
         layouts = layouts_bench(pk, torch, stream, dev, pack, q, k, v)
         fp8 = fp8_bench(pk, torch, stream, dev, pack, q, k, v)
+        fp8_pv = fp8_pv_bench(pk, torch, stream, dev, pack, q, k, v)
     merge = None
     if not args.no_merge and rank == 0:
         merge = merge_bench(pk, torch, stream, pack, out, lse)
@@ -719,6 +753,7 @@ def main():
         "replaced_path": replaced,
         "layouts": layouts,
         "fp8_qk": fp8,
+        "fp8_qkvp": fp8_pv,
         "lse_merge": merge,
     }
     print(json.dumps(line), flush=True)

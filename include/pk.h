@@ -201,6 +201,12 @@ pk_status pk_plan_upload(pk_plan* plan, void* dev_buf, size_t bytes,
  * (the fp16 copy of the value rows). */
 size_t pk_attn_workspace_bytes(const pk_plan* plan);
 
+/* Bytes of the workspace pk_attn_fwd_fp8_pv needs with `plan`: the
+ * transposed E4M3 copy of the value rows, hkv * head_dim bytes per row, each
+ * sequence's key rows rounded up to a multiple of 16 (contiguous keys) or
+ * the pool's rows rounded up to 16 (paged keys).  0 for a null plan. */
+size_t pk_attn_workspace_bytes_fp8_pv(const pk_plan* plan);
+
 /*
  * Launch the attention forward on `stream` (asynchronous): two kernels, the
  * conversion of the value rows the plan reads from bf16 to fp16 into the
@@ -292,6 +298,31 @@ pk_status pk_attn_fwd_fp8(const pk_plan* plan, const void* q8, float q_scale, co
                           float k_scale, const void* v, void* out, float* lse, float scale,
                           void* workspace, size_t workspace_bytes, pk_stream_t stream,
                           int32_t* dev_status);
+
+/*
+ * All-FP8 variant: queries, keys and values as FP8 E4M3 codes, one
+ * dequantisation scale each.  Scores as in pk_attn_fwd_fp8; the softmax
+ * weights p (in (0, 256], relative to a running row maximum) are rounded to
+ * E4M3 and the product P V runs on the tensor cores in FP8 with fp32
+ * accumulation; out = v_scale * (P v8) / l with l the fp32 sum of the
+ * unrounded weights, lse as for pk_attn_fwd.  The E4M3 weights carry 3
+ * mantissa bits, so out is less accurate than pk_attn_fwd_fp8's (the tests
+ * record the measured error); lse is unaffected.
+ *   q8 [Tq][hq][128], k8 and v8 [Tk][hkv][128] uint8 codes, 16-byte aligned;
+ *   q_scale, k_scale, v_scale: finite and > 0.
+ *   workspace: >= pk_attn_workspace_bytes_fp8_pv(plan) bytes, 16-byte
+ *   aligned; a kernel before the attention writes the transposed copy of
+ *   v8 into it (keys along rows, rows 16-key aligned per sequence), which
+ *   the FP8 P V product reads.
+ * head_dim must be 128 (else PK_ERR_UNSUPPORTED).  Otherwise as
+ * pk_attn_fwd_fp8 (dev_status, out and lse, errors).  The pages run
+ * attention at FP8 on the linear layers' side only; E4M3 values and
+ * weights are an addition of this library.
+ */
+pk_status pk_attn_fwd_fp8_pv(const pk_plan* plan, const void* q8, float q_scale, const void* k8,
+                             float k_scale, const void* v8, float v_scale, void* out, float* lse,
+                             float scale, void* workspace, size_t workspace_bytes,
+                             pk_stream_t stream, int32_t* dev_status);
 
 /*
  * End-to-end variant for callers holding host buffers: copies q, k, v from

@@ -8,6 +8,7 @@ fails loudly when the compiled library is missing.
     plan = pk.plan(cu_seqlens, segments, hq, hkv, head_dim)   # host planner
     out, lse = pk.attn_fwd(q, k, v, plan, scale)               # fp16 values, attention
     out, lse = pk.attn_fwd_fp8(q8, qs, k8, ks, v, plan, scale) # E4M3 queries/keys
+    out, lse = pk.attn_fwd_fp8_pv(q8, qs, k8, ks, v8, vs, plan) # E4M3 values and P too
     out, lse = pk.lse_merge([(o1, l1), (o2, l2)])              # key blocks -> union
     plan = pk.plan_layout(cu_q, cu_k, seq_segments, hq, hkv, head_dim,
                           q_pos0=..., k_pos0=..., block_table=...)  # prefix / paged / chunks
@@ -24,10 +25,10 @@ from ._native import (PK_ERR_ALIGNMENT, PK_ERR_CUDA, PK_ERR_DEVICE_CHECK,  # noq
                       PK_ERR_TIMEOUT, PK_ERR_TOO_LARGE,
                       PK_ERR_UNSUPPORTED, PK_OK, PKError, lib_path, load)
 from .api import (IMAGE, TEXT, HostPipeline, Plan, attn_fwd, attn_fwd_converted,  # noqa: F401
-                  attn_fwd_fp8, attn_fwd_host, convert_values, debug_wait_timeout, lse_merge,
+                  attn_fwd_fp8, attn_fwd_fp8_pv, attn_fwd_host, convert_values, debug_wait_timeout, lse_merge,
                   plan, plan_layout, set_wait_timeout_ns)
 
 __all__ = ["plan", "plan_layout", "Plan", "attn_fwd", "convert_values", "attn_fwd_converted",
-           "attn_fwd_fp8", "attn_fwd_host",
+           "attn_fwd_fp8", "attn_fwd_fp8_pv", "attn_fwd_host",
            "lse_merge", "HostPipeline", "PKError", "TEXT", "IMAGE", "set_wait_timeout_ns",
            "debug_wait_timeout", "load", "lib_path"]

@@ -91,6 +91,7 @@ SIGNATURES = {
     "pk_plan_device_bytes": (ctypes.c_size_t, [_vp]),
     "pk_plan_upload": (ctypes.c_int, [_vp, _vp, ctypes.c_size_t, _vp]),
     "pk_attn_workspace_bytes": (ctypes.c_size_t, [_vp]),
+    "pk_attn_workspace_bytes_fp8_pv": (ctypes.c_size_t, [_vp]),
     "pk_attn_fwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp,
                                    ctypes.c_size_t, _vp, _vp]),
     "pk_attn_convert_values": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_size_t, _vp, _vp]),
@@ -100,6 +101,9 @@ SIGNATURES = {
                                            _vp]),
     "pk_attn_fwd_fp8": (ctypes.c_int, [_vp, _vp, ctypes.c_float, _vp, ctypes.c_float, _vp, _vp,
                                        _vp, ctypes.c_float, _vp, ctypes.c_size_t, _vp, _vp]),
+    "pk_attn_fwd_fp8_pv": (ctypes.c_int, [_vp, _vp, ctypes.c_float, _vp, ctypes.c_float, _vp,
+                                          ctypes.c_float, _vp, _vp, ctypes.c_float, _vp,
+                                          ctypes.c_size_t, _vp, _vp]),
     "pk_attn_fwd_host": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                         _vp, ctypes.c_float, _vp, _vp]),
     "pk_plan_destroy": (None, [_vp]),

@@ -125,6 +125,11 @@ class Plan:
         """Bytes of the per-launch workspace (the fp16 copy of the values)."""
         return int(self._lib.pk_attn_workspace_bytes(self._h))
 
+    @property
+    def workspace_bytes_fp8_pv(self) -> int:
+        """Bytes of attn_fwd_fp8_pv's workspace (the transposed E4M3 values)."""
+        return int(self._lib.pk_attn_workspace_bytes_fp8_pv(self._h))
+
     def kv_limit(self) -> np.ndarray:
         out = np.zeros(max(self.total_tokens, 1), dtype=np.int32)
         check(self._lib.pk_plan_get_kv_limit(self._h, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
@@ -191,11 +196,12 @@ def _check_tensor(t, name, shape):
         raise ValueError(f"{name} must be contiguous")
 
 
-def _workspace(plan: "Plan", workspace, device):
+def _workspace(plan: "Plan", workspace, device, nbytes: Optional[int] = None):
     """The launch's workspace: the caller's tensor (checked), else a fresh
     one from PyTorch's caching allocator on the current stream."""
     import torch
-    nbytes = plan.workspace_bytes
+    if nbytes is None:
+        nbytes = plan.workspace_bytes
     if workspace is None:
         return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
     if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda or \
@@ -341,6 +347,53 @@ def attn_fwd_fp8(q8, q_scale: float, k8, k_scale: float, v, plan: Plan,
     if check_status:
         torch.cuda.current_stream(v.device).synchronize()
         check(int(status.item()), "pk_attn_fwd_fp8 (device)")
+    return out, lse
+
+
+def attn_fwd_fp8_pv(q8, q_scale: float, k8, k_scale: float, v8, v_scale: float, plan: Plan,
+                    scale: Optional[float] = None, out=None, lse=None, status=None,
+                    check_status: bool = False, workspace=None):
+    """Attention with FP8 E4M3 queries, keys and values, the softmax weights
+    rounded to E4M3 for an FP8 P V product (pk_attn_fwd_fp8_pv).
+
+    q8 [T, hq, 128], k8 and v8 [Tk, hkv, 128]: CUDA uint8 or float8_e4m3fn
+    tensors of E4M3 codes, dequantised by q_scale / k_scale / v_scale.
+    Returns (out bf16 [T, hq, 128], lse fp32 [hq, T]).  ``workspace``: at
+    least ``plan.workspace_bytes_fp8_pv`` bytes, else one is taken from
+    PyTorch's allocator."""
+    import torch
+    T, hq, hkv, d = plan.total_tokens, plan.hq, plan.hkv, plan.head_dim
+    Tk = plan.kv_rows
+    for name, t, shape in (("q8", q8, (T, hq, d)), ("k8", k8, (Tk, hkv, d)),
+                           ("v8", v8, (Tk, hkv, d))):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.element_size() != 1:
+            raise TypeError(f"{name} must be a CUDA tensor of 1-byte E4M3 codes")
+        if tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous with shape {shape}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty(T, hq, d, dtype=torch.bfloat16, device=v8.device)
+    else:
+        _check_tensor(out, "out", (T, hq, d))
+    if lse is None:
+        lse = torch.empty(hq, T, dtype=torch.float32, device=v8.device)
+    elif lse.dtype != torch.float32 or tuple(lse.shape) != (hq, T) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 tensor of shape [hq, T]")
+    ws = _workspace(plan, workspace, v8.device, plan.workspace_bytes_fp8_pv)
+    if check_status and status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=v8.device)
+    stream = torch.cuda.current_stream(v8.device).cuda_stream
+    check(plan._lib.pk_attn_fwd_fp8_pv(
+        plan.handle, ctypes.c_void_p(q8.data_ptr()), float(q_scale),
+        ctypes.c_void_p(k8.data_ptr()), float(k_scale), ctypes.c_void_p(v8.data_ptr()),
+        float(v_scale), ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(lse.data_ptr()),
+        float(scale), ctypes.c_void_p(ws.data_ptr()), ws.numel() * ws.element_size(),
+        ctypes.c_void_p(stream), ctypes.c_void_p(status.data_ptr() if status is not None else 0)),
+        "pk_attn_fwd_fp8_pv")
+    if check_status:
+        torch.cuda.current_stream(v8.device).synchronize()
+        check(int(status.item()), "pk_attn_fwd_fp8_pv (device)")
     return out, lse
 
 

@@ -107,6 +107,15 @@ __device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D(tmem) (+)= A(tmem) * B(smem desc), FP8 operands.
+__device__ __forceinline__ void mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // D(tmem) (+)= A(tmem) * B(smem desc)
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
@@ -157,6 +166,14 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// Four floats as E4M3 codes (round to nearest even, saturating at 448),
+// x0 in bits 0-7 ... x3 in bits 24-31.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float x0, float x1, float x2, float x3) {
+  uint16_t lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(x1), "f"(x0));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(x3), "f"(x2));
+  return (uint32_t)lo | ((uint32_t)hi << 16);
+}
 // A bf16 pair to an fp16 pair (round to nearest even, saturating at 65504),
 // keeping the running maximum magnitude for the range check.
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x, float& amax) {
@@ -172,12 +189,15 @@ struct KernelParams {
   const int32_t* cta_offsets;
   const int32_t* kv_limit;       // per query row: last visible key of its range, -1 none
   const int32_t* block_table;    // paged keys: physical 128-row block of each key tile; else null
+  const int32_t* v8_row;         // E4M3 values, contiguous keys: per item, the row of its first
+                                 // key tile in the transposed copy (a multiple of 16); else null
   uint8_t* out;   // bf16 [T][hq][D]
   float* lse;     // [hq][T]
   int32_t* status;
   int32_t T;
   int32_t hq;
   float scale_log2;  // softmax scale * log2(e)
+  float v_scale;     // dequantisation scale of E4M3 values (1 otherwise)
   uint64_t wait_limit_ns;
 };
 
@@ -219,6 +239,20 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
   for (int kk = 0; kk < 8; ++kk)
     mma_ts(d_tmem, p_tmem + (uint32_t)kk * 8u, v_desc + (uint64_t)(kk * (2048 >> 4)), idesc,
            (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// O(tmem) (+)= P V with E4M3 P and values: 4 MMAs of 128 x D x 32 on
+// kind::f8f6f4.  P is read from TMEM, four keys per column (8 columns per
+// 32 keys); the value tile is K-major with 128-byte swizzle (one 128-byte
+// row of keys per head-dimension index), the k-th step 32 bytes along it.
+template <int D>
+__device__ __forceinline__ void issue_pv_f8(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
+                                            bool accumulate) {
+  constexpr uint32_t idesc = make_idesc_e4m3(128, D);
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk)
+    mma_ts_f8(d_tmem, p_tmem + (uint32_t)kk * 8u, v_desc + (uint64_t)((kk * 32) >> 4), idesc,
+              (accumulate || kk > 0) ? 1u : 0u);
 }
 
 }  // namespace dev

@@ -73,20 +73,22 @@ static_assert(128 * (kRegsMma + kRegsSoftmax + kRegsEpi) <= kThreads * kRegsLaun
               "register split exceeds the CTA's allocation");
 constexpr uint32_t kTmemCols = 512;
 // F8: queries and keys are FP8 E4M3 (one byte per element), values bf16.
-template <int D, bool F8 = false>
+template <int D, bool F8 = false, bool V8 = false>
 struct Cfg {
   // Query/key tiles: 128 rows in boxes of 128-byte rows (64 bf16 or 128
   // FP8 elements); value tiles: 128 rows of D fp16 in 64-column boxes.
   static constexpr int kQKElemsPerBox = F8 ? 128 : 64;
   static constexpr int kQKBoxes = D / kQKElemsPerBox;
   static constexpr int kQKTileBytes = 128 * D * (F8 ? 1 : 2);
-  static constexpr int kVHalves = D / 64;
-  static constexpr int kVTileBytes = 128 * D * 2;
+  // V8: E4M3 values, transposed (one 128-byte row of keys per head-dimension
+  // index), one box per tile; else fp16 values in 64-column boxes.
+  static constexpr int kVBoxes = V8 ? 1 : D / 64;
+  static constexpr int kVTileBytes = 128 * D * (V8 ? 1 : 2);
   // Rings: two query tiles (the next unit's loads during this one), and key
   // and value tiles.  Shared memory stays above half an SM, so exactly one
   // CTA (and one 512-column TMEM allocation) lives on each SM.
   static constexpr int kKStages = F8 ? 4 : (D == 128 ? 3 : 4);
-  static constexpr int kVStages = F8 ? 3 : (D == 128 ? 2 : 4);
+  static constexpr int kVStages = V8 ? 4 : (F8 ? 3 : (D == 128 ? 2 : 4));
   // TMEM columns: S double buffer, P double buffer (16-bit pairs), O.
   static constexpr uint32_t kColS0 = 0;    // S(t) in [128*(t%2), +128)
   static constexpr uint32_t kColP0 = 256;  // P(t) in [256 + 64*(t%2), +64)
@@ -96,6 +98,7 @@ struct Cfg {
   static constexpr int kOffV = kOffK + kKStages * kQKTileBytes;
   static constexpr int kOffBar = kOffV + kVStages * kVTileBytes;
   static_assert(!F8 || D == 128, "FP8 queries/keys need head_dim 128");
+  static_assert(!V8 || F8, "E4M3 values come with E4M3 queries and keys");
   // barrier indices
   static constexpr int kQFull = 0, kQEmpty = 2;  // [2] each
   static constexpr int kKFull = 4, kKEmpty = kKFull + kKStages;
@@ -145,11 +148,11 @@ struct UnitIter {
 // the ring of key tiles.  Keys and values are re-read by the other query
 // heads of the group and by neighbouring query tiles, so they are kept in L2
 // (evict-last); a query tile is read once (evict-first).
-template <int D, bool F8>
+template <int D, bool F8, bool V8>
 __device__ void producer_qk_role(const KernelParams& p, const CUtensorMap* tm_q,
                                  const CUtensorMap* tm_k, uint32_t sbase, int beg, int end,
                                  const WaitCtl& wc) {
-  using C = Cfg<D, F8>;
+  using C = Cfg<D, F8, V8>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
   const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
   uint32_t g = 0, u = 0, k_armed = 0, q_armed = 0;
@@ -193,10 +196,10 @@ __device__ void producer_qk_role(const KernelParams& p, const CUtensorMap* tm_q,
 
 // V producer (one thread of another warp): the ring of value tiles, so that
 // a value tile waiting for its stage never holds back the next key tile.
-template <int D, bool F8>
+template <int D, bool F8, bool V8>
 __device__ void producer_v_role(const KernelParams& p, const CUtensorMap* tm_v, uint32_t sbase,
                                 int beg, int end, const WaitCtl& wc) {
-  using C = Cfg<D, F8>;
+  using C = Cfg<D, F8, V8>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
   const uint64_t keep = l2_policy_evict_last();
   uint32_t g = 0, v_armed = 0;
@@ -208,10 +211,16 @@ __device__ void producer_v_role(const KernelParams& p, const CUtensorMap* tm_v, 
       if (!(ok = mbar_wait(bar(C::kVEmpty + st), ph ^ 1u, wc))) break;
       mbar_arrive_expect_tx(bar(C::kVFull + st), C::kVTileBytes);
       ++v_armed;
+      if constexpr (V8) {  // (key, head-dimension index, head) view of the transposed copy
+        const int row = p.v8_row ? p.v8_row[ui.it] + j * 128 : key_tile_row(p, w, j);
+        tma_load_3d_hint(sbase + C::kOffV + st * C::kVTileBytes, tm_v, bar(C::kVFull + st), row,
+                         0, w.hkv, keep);
+      } else {
 #pragma unroll
-      for (int h = 0; h < C::kVHalves; ++h)
-        tma_load_3d_hint(sbase + C::kOffV + st * C::kVTileBytes + h * kBoxBytes, tm_v,
-                         bar(C::kVFull + st), h * 64, w.hkv, key_tile_row(p, w, j), keep);
+        for (int h = 0; h < C::kVBoxes; ++h)
+          tma_load_3d_hint(sbase + C::kOffV + st * C::kVTileBytes + h * kBoxBytes, tm_v,
+                           bar(C::kVFull + st), h * 64, w.hkv, key_tile_row(p, w, j), keep);
+      }
     }
   }
   for (uint32_t k = 1; k <= (uint32_t)C::kVStages && k <= v_armed; ++k) {  // as above
@@ -229,10 +238,10 @@ __device__ void producer_v_role(const KernelParams& p, const CUtensorMap* tm_v, 
 // S issuer (warp 1): S(t) needs K(t) loaded and S buffer t%2 released by the
 // softmax of tile t-2, so it runs up to two tiles ahead of the softmax and
 // the tensor pipe computes S(t+2) while the softmax works on tile t.
-template <int D, bool F8>
+template <int D, bool F8, bool V8>
 __device__ void mma_s_role(const KernelParams& p, uint32_t sbase, uint32_t tmem, int beg,
                            int end, const WaitCtl& wc) {
-  using C = Cfg<D, F8>;
+  using C = Cfg<D, F8, V8>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
   const uint64_t q_desc0 = sdesc(sbase + C::kOffQ, 16, 1024);
   const uint64_t k_desc0 = sdesc(sbase + C::kOffK, 16, 1024);
@@ -261,12 +270,14 @@ __device__ void mma_s_role(const KernelParams& p, uint32_t sbase, uint32_t tmem,
 
 // P V issuer (warp 3): O (+)= P(t) V(t) needs V(t) loaded and P(t) written;
 // a unit's first product overwrites O, after the previous unit's O was read.
-template <int D, bool F8>
+template <int D, bool F8, bool V8>
 __device__ void mma_pv_role(const KernelParams& p, uint32_t sbase, uint32_t tmem, int beg,
                             int end, const WaitCtl& wc) {
-  using C = Cfg<D, F8>;
+  using C = Cfg<D, F8, V8>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
-  const uint64_t v_desc0 = sdesc(sbase + C::kOffV, kBoxBytes, 1024);
+  // fp16 values: MN-major, 64-column boxes kBoxBytes apart; E4M3 values:
+  // K-major (transposed copy)
+  const uint64_t v_desc0 = sdesc(sbase + C::kOffV, V8 ? 16u : (uint32_t)kBoxBytes, 1024);
   constexpr uint64_t kTileDesc = (uint64_t)(C::kVTileBytes >> 4);
   uint32_t t = 0, u = 0;
   bool ok = true;
@@ -278,7 +289,11 @@ __device__ void mma_pv_role(const KernelParams& p, uint32_t sbase, uint32_t tmem
       if (!(ok = mbar_wait(bar(C::kPReady + b), (t >> 1) & 1u, wc))) break;
       if (j == 0 && !(ok = mbar_wait(bar(C::kOFree), (u & 1u) ^ 1u, wc))) break;
       tc_fence_after();
-      issue_pv<D>(tmem + C::kColO, tmem + C::kColP0 + b * 64u, v_desc0 + vst * kTileDesc, j > 0);
+      if constexpr (V8)
+        issue_pv_f8<D>(tmem + C::kColO, tmem + C::kColP0 + b * 64u, v_desc0 + vst * kTileDesc,
+                       j > 0);
+      else
+        issue_pv<D>(tmem + C::kColO, tmem + C::kColP0 + b * 64u, v_desc0 + vst * kTileDesc, j > 0);
       tc_commit(bar(C::kPvDone + b));
       tc_commit(bar(C::kVEmpty + vst));
     }
@@ -288,10 +303,10 @@ __device__ void mma_pv_role(const KernelParams& p, uint32_t sbase, uint32_t tmem
 }
 
 // Softmax warpgroup (warps 4-7): thread r owns row r of S, P and O in TMEM.
-template <int D, bool F8>
+template <int D, bool F8, bool V8>
 __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint8_t* sgen, uint32_t tmem,
                              int beg, int end, const WaitCtl& wc) {
-  using C = Cfg<D, F8>;
+  using C = Cfg<D, F8, V8>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;  // TMEM lane quadrant this warp may access
@@ -343,19 +358,34 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint8_t* sge
       // scores still in registers.  P, O and l keep their relative
       // precision at any scale, so the only limits on the threshold are
       // range: p <= 2^15 fits fp16 P, and O <= L * 2^15 * max|v|.
-      uint32_t pp[64];
+      // V8: P as E4M3 codes, four keys per TMEM column (32 columns).
+      uint32_t pp[V8 ? 32 : 64];
       float acc[8];
       auto exp_pass = [&](float neg) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+        if constexpr (V8) {
 #pragma unroll
-        for (int c = 0; c < 128; c += 2) {
-          float a0, a1;
-          fma2(a0, a1, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]), sl2, sl2, neg, neg);
-          const float p0 = ex2(a0), p1 = ex2(a1);
-          pp[c >> 1] = pack_f16x2(p0, p1);
-          const int q = (c >> 1) & 3;
-          acc2(acc[2 * q], acc[2 * q + 1], p0, p1);
+          for (int c = 0; c < 128; c += 4) {
+            float a0, a1, a2, a3;
+            fma2(a0, a1, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]), sl2, sl2, neg, neg);
+            fma2(a2, a3, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]), sl2, sl2, neg, neg);
+            const float p0 = ex2(a0), p1 = ex2(a1), p2 = ex2(a2), p3 = ex2(a3);
+            pp[c >> 2] = pack_e4m3x4(p0, p1, p2, p3);
+            const int q = (c >> 2) & 1;
+            acc2(acc[4 * q], acc[4 * q + 1], p0, p1);
+            acc2(acc[4 * q + 2], acc[4 * q + 3], p2, p3);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 128; c += 2) {
+            float a0, a1;
+            fma2(a0, a1, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]), sl2, sl2, neg, neg);
+            const float p0 = ex2(a0), p1 = ex2(a1);
+            pp[c >> 1] = pack_f16x2(p0, p1);
+            const int q = (c >> 1) & 3;
+            acc2(acc[2 * q], acc[2 * q + 1], p0, p1);
+          }
         }
       };
       auto row_max = [&]() {
@@ -369,7 +399,9 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint8_t* sge
             mc[i] = max3(mc[i], __uint_as_float(sr[b0 + 2 * i]), __uint_as_float(sr[b0 + 2 * i + 1]));
         return max3(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7])) * sl2;
       };
-      constexpr float kRescaleSum = 32768.0f;  // 2^kRescaleLog2
+      // E4M3 P (largest finite 448) lets the maximum lag by 8 at most.
+      constexpr float kLag = V8 ? 8.0f : kRescaleLog2;
+      constexpr float kRescaleSum = V8 ? 256.0f : 32768.0f;  // 2^kLag
       if (j == 0) m_used = row_max();
       // The rare rescale path takes a second trip through this one copy of
       // the exponential loop (a second inlined copy measured slower).
@@ -386,7 +418,7 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint8_t* sge
         if (!(votes & 1u)) break;
         // Rare: some row's maximum may have outgrown m_used.
         const float m_tile = row_max();
-        const bool need = m_tile > m_used + kRescaleLog2;
+        const bool need = m_tile > m_used + kLag;
         if (!__any_sync(0xffffffffu, need)) break;
         // O must hold P(t-1) V(t-1) before it is rescaled (j > 0 here: the
         // first tile's maximum is exact).
@@ -416,7 +448,10 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint8_t* sge
         if (!ok) break;
       }
       tc_fence_after();
-      tmem_st_x64(tP, pp);
+      if constexpr (V8)
+        tmem_st_x32(tP, pp);
+      else
+        tmem_st_x64(tP, pp);
       tc_fence_before();
       mbar_arrive(bar(C::kPReady + b));
     }
@@ -437,10 +472,10 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint8_t* sge
 // unit it takes (m, l) from the softmax, waits for the unit's last P V,
 // moves O into registers and frees it for the next unit's first product,
 // then writes O / l as bf16 and the natural-log LSE.
-template <int D, bool F8>
+template <int D, bool F8, bool V8>
 __device__ void epilogue_role(const KernelParams& p, uint32_t sbase, uint8_t* sgen,
                               uint32_t tmem, int beg, int end, const WaitCtl& wc) {
-  using C = Cfg<D, F8>;
+  using C = Cfg<D, F8, V8>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;
@@ -471,7 +506,8 @@ __device__ void epilogue_role(const KernelParams& p, uint32_t sbase, uint8_t* sg
     tc_fence_before();
     mbar_arrive(bar(C::kOFree));
     const float l = ml.y;
-    const float inv_l = l > 0.f ? 1.0f / l : 0.f;  // a row without keys writes zeros
+    // a row without keys writes zeros; E4M3 values carry their scale
+    const float inv_l = l > 0.f ? p.v_scale / l : 0.f;
     if (r < w.q_rows) {
       uint8_t* orow = p.out + (((size_t)(w.q_start + r) * (size_t)p.hq + (size_t)h) * D) * 2;
 #pragma unroll
@@ -540,12 +576,60 @@ __global__ void __launch_bounds__(512) pk_v_to_f16_kernel(const uint4* v, uint4*
   if (!(amax < 65520.0f) && status) atomicCAS(status, 0, (int32_t)PK_ERR_RANGE);
 }
 
-template <int D, bool F8>
+// E4M3 values [Tk][H][D] -> the transposed copy [H][D][rows_t] bytes that
+// the all-E4M3 P V product reads K-major (one row of keys per head-dimension
+// index).  Work items are (chunk, head) pairs; a chunk (source row, copy
+// row, rows holding keys n, rows written m; n <= m <= 128, the copy row and
+// m multiples of 16) moves source rows [src, src + n) to copy rows
+// [dst, dst + n) and writes zeros to copy rows [dst + n, dst + m).  Each
+// item goes through a shared-memory tile: 16-byte loads along the head
+// dimension, 16-byte stores along the keys.
+__global__ void __launch_bounds__(256) pk_v8_transpose_kernel(const uint8_t* v8, uint8_t* vt,
+                                                              const int32_t* __restrict__ chunks,
+                                                              int32_t num_chunks, int32_t H,
+                                                              int32_t D, int32_t rows_t) {
+  __shared__ uint32_t tile[128][33];  // [key][head-dim word] (D <= 128), padded
+  for (int32_t i = blockIdx.x; i < num_chunks * H; i += gridDim.x) {
+    const int32_t ci = i / H, h = i - ci * H;
+    const int32_t src = chunks[4 * ci], dst = chunks[4 * ci + 1];
+    const int32_t n = chunks[4 * ci + 2], m = chunks[4 * ci + 3];
+    const int32_t pieces = D / 16;  // 16-byte pieces per key
+    for (int32_t e = threadIdx.x; e < 128 * pieces; e += 256) {
+      const int32_t k = e / pieces, c = e - k * pieces;
+      uint4 x = make_uint4(0u, 0u, 0u, 0u);
+      if (k < n)
+        x = *reinterpret_cast<const uint4*>(v8 + ((size_t)(src + k) * H + h) * D + (size_t)c * 16);
+      tile[k][4 * c + 0] = x.x;
+      tile[k][4 * c + 1] = x.y;
+      tile[k][4 * c + 2] = x.z;
+      tile[k][4 * c + 3] = x.w;
+    }
+    __syncthreads();
+    for (int32_t e = threadIdx.x; e < D * 8; e += 256) {  // (head-dim index, 16 keys)
+      const int32_t dd = e >> 3, k0 = (e & 7) * 16;
+      if (k0 >= m) continue;
+      uint32_t w[4];
+#pragma unroll
+      for (int32_t q = 0; q < 4; ++q) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int32_t b = 0; b < 4; ++b)
+          word |= ((tile[k0 + 4 * q + b][dd >> 2] >> (8 * (dd & 3))) & 0xffu) << (8 * b);
+        w[q] = word;
+      }
+      *reinterpret_cast<uint4*>(vt + ((size_t)h * D + dd) * rows_t + dst + k0) =
+          make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __syncthreads();
+  }
+}
+
+template <int D, bool F8, bool V8>
 __global__ void __launch_bounds__(kThreads, 1)
     pk_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const KernelParams p) {
-  using C = Cfg<D, F8>;
+  using C = Cfg<D, F8, V8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1 KB alignment
@@ -601,21 +685,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Producers and MMA issuers: one thread each, few registers.
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsMma));
     if (warp == 0) {
-      if (lane == 0) producer_qk_role<D, F8>(p, &tm_q, &tm_k, sbase, beg, end, wc);
+      if (lane == 0) producer_qk_role<D, F8, V8>(p, &tm_q, &tm_k, sbase, beg, end, wc);
     } else if (warp == 1) {
-      if (lane == 0) mma_s_role<D, F8>(p, sbase, tmem, beg, end, wc);
+      if (lane == 0) mma_s_role<D, F8, V8>(p, sbase, tmem, beg, end, wc);
     } else if (warp == 2) {
-      if (lane == 0) producer_v_role<D, F8>(p, &tm_v, sbase, beg, end, wc);
+      if (lane == 0) producer_v_role<D, F8, V8>(p, &tm_v, sbase, beg, end, wc);
     } else {
-      if (lane == 0) mma_pv_role<D, F8>(p, sbase, tmem, beg, end, wc);
+      if (lane == 0) mma_pv_role<D, F8, V8>(p, sbase, tmem, beg, end, wc);
     }
     __syncwarp();
   } else if (warp < 8) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
-    softmax_role<D, F8>(p, sbase, sgen, tmem, beg, end, wc);
+    softmax_role<D, F8, V8>(p, sbase, sgen, tmem, beg, end, wc);
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
-    epilogue_role<D, F8>(p, sbase, sgen, tmem, beg, end, wc);
+    epilogue_role<D, F8, V8>(p, sbase, sgen, tmem, beg, end, wc);
   }
 
   tc_fence_before();
@@ -692,6 +776,22 @@ bool make_map(CUtensorMap* m, const void* base, int H, int T, int D, CUtensorMap
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// (key, head-dimension index, head) view of the transposed E4M3 value copy
+// [H][D][rows_t] bytes: boxes of 128 keys (128 bytes) x D x 1 head with
+// 128-byte swizzle; keys past rows_t read as zeros.
+bool make_map_v8t(CUtensorMap* m, const void* base, int H, int rows_t, int D) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)rows_t, (cuuint64_t)D, (cuuint64_t)H};
+  const cuuint64_t strides[2] = {(cuuint64_t)rows_t, (cuuint64_t)D * rows_t};
+  const cuuint32_t box[3] = {128, (cuuint32_t)D, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Device capability check and SM count, cached per device ordinal.
 pk_status check_device(int* sm_count = nullptr) {
   static std::mutex mu;
@@ -756,19 +856,38 @@ pk_status convert_values(const pk_plan* plan, const void* v, void* v16, int sm_c
 
 // scale: the softmax scale of the scores as the MMA computes them (for FP8
 // queries/keys it includes their dequantisation scales).
-// v16: the fp16 values (the workspace convert_values has filled).
-template <int D, bool F8>
+// The transposed E4M3 copy of the value rows the plan reads (see
+// pk_v8_transpose_kernel and the plan's chunk list), into vt.
+pk_status transpose_values(const pk_plan* plan, const void* v8, void* vt, int sm_count,
+                           cudaStream_t stream) {
+  const int32_t nchunks = (int32_t)(plan->v8_chunks.size() / 4);
+  if (nchunks == 0) return PK_OK;
+  const int32_t* list = reinterpret_cast<const int32_t*>(static_cast<const uint8_t*>(plan->dev) +
+                                                         plan->layout.v8chunk_off);
+  const int grid = std::min(nchunks * plan->hkv, 8 * std::max(sm_count, 1));
+  pk::dev::pk_v8_transpose_kernel<<<grid, 256, 0, stream>>>(
+      static_cast<const uint8_t*>(v8), static_cast<uint8_t*>(vt), list, nchunks, plan->hkv,
+      plan->head_dim, plan->v8_rows);
+  if (cudaGetLastError() != cudaSuccess) return PK_ERR_CUDA;
+  return PK_OK;
+}
+
+// v16: the fp16 values (the workspace convert_values has filled), or with V8
+// the transposed E4M3 copy (transpose_values).
+template <int D, bool F8, bool V8>
 pk_status launch(const pk_plan* plan, const void* q, const void* k, const void* v16, void* out,
-                 float* lse, float scale, cudaStream_t stream, int32_t* dev_status) {
-  using C = pk::dev::Cfg<D, F8>;
+                 float* lse, float scale, cudaStream_t stream, int32_t* dev_status,
+                 float v_scale = 1.0f) {
+  using C = pk::dev::Cfg<D, F8, V8>;
   CUtensorMap tq, tk, tv;
   const CUtensorMapDataType qk_dt =
       F8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if (!make_map(&tq, q, plan->hq, plan->T, D, qk_dt) ||
       !make_map(&tk, k, plan->hkv, plan->Tk, D, qk_dt) ||
-      !make_map(&tv, v16, plan->hkv, plan->Tk, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
+      !(V8 ? make_map_v8t(&tv, v16, plan->hkv, plan->v8_rows, D)
+           : make_map(&tv, v16, plan->hkv, plan->Tk, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)))
     return PK_ERR_CUDA;
-  if (cudaFuncSetAttribute(pk::dev::pk_attn_fwd_kernel<D, F8>,
+  if (cudaFuncSetAttribute(pk::dev::pk_attn_fwd_kernel<D, F8, V8>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kSmemBytes) != cudaSuccess) {
     cudaGetLastError();
@@ -780,7 +899,7 @@ pk_status launch(const pk_plan* plan, const void* q, const void* k, const void* 
   static std::atomic<int> regs_state{0};  // 0 unknown, 1 fits, 2 does not
   if (regs_state.load() == 0) {
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, pk::dev::pk_attn_fwd_kernel<D, F8>) != cudaSuccess) {
+    if (cudaFuncGetAttributes(&fa, pk::dev::pk_attn_fwd_kernel<D, F8, V8>) != cudaSuccess) {
       cudaGetLastError();
       return PK_ERR_CUDA;
     }
@@ -795,14 +914,17 @@ pk_status launch(const pk_plan* plan, const void* q, const void* k, const void* 
   kp.kv_limit = reinterpret_cast<const int32_t*>(img + plan->layout.kvlim_off);
   kp.block_table =
       plan->paged ? reinterpret_cast<const int32_t*>(img + plan->layout.table_off) : nullptr;
+  kp.v8_row = V8 && !plan->paged
+                  ? reinterpret_cast<const int32_t*>(img + plan->layout.v8row_off) : nullptr;
   kp.out = static_cast<uint8_t*>(out);
   kp.lse = lse;
   kp.status = dev_status;
   kp.T = plan->T;
   kp.hq = plan->hq;
   kp.scale_log2 = scale * 1.4426950408889634f;
+  kp.v_scale = v_scale;
   kp.wait_limit_ns = g_wait_limit_ns.load();
-  pk::dev::pk_attn_fwd_kernel<D, F8>
+  pk::dev::pk_attn_fwd_kernel<D, F8, V8>
       <<<plan->num_ctas, pk::dev::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, kp);
   if (cudaGetLastError() != cudaSuccess) return PK_ERR_CUDA;
   return PK_OK;
@@ -840,9 +962,11 @@ pk_status check_plan(const pk_plan* plan, bool* nothing) {
 
 // A value tensor and a workspace (the fp16 copy) of the plan's size.
 pk_status check_values(const pk_plan* plan, const void* v, const void* workspace,
-                       size_t workspace_bytes) {
+                       size_t workspace_bytes, bool e4m3_transposed = false) {
   if (!v || !workspace) return PK_ERR_INVALID_ARG;
-  if (workspace_bytes < pk_attn_workspace_bytes(plan)) return PK_ERR_INVALID_ARG;
+  if (workspace_bytes < (e4m3_transposed ? pk_attn_workspace_bytes_fp8_pv(plan)
+                                         : pk_attn_workspace_bytes(plan)))
+    return PK_ERR_INVALID_ARG;
   if (!aligned16(v) || !aligned16(workspace)) return PK_ERR_ALIGNMENT;
   return PK_OK;
 }
@@ -885,8 +1009,8 @@ pk_status pk_attn_fwd_converted(const pk_plan* plan, const void* q, const void* 
     return st;
   if ((st = check_device()) != PK_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (plan->head_dim == 128) return launch<128, false>(plan, q, k, v16, out, lse, scale, s, dev_status);
-  if (plan->head_dim == 64) return launch<64, false>(plan, q, k, v16, out, lse, scale, s, dev_status);
+  if (plan->head_dim == 128) return launch<128, false, false>(plan, q, k, v16, out, lse, scale, s, dev_status);
+  if (plan->head_dim == 64) return launch<64, false, false>(plan, q, k, v16, out, lse, scale, s, dev_status);
   return PK_ERR_UNSUPPORTED;
 }
 
@@ -979,8 +1103,31 @@ pk_status pk_attn_fwd_fp8(const pk_plan* plan, const void* q8, float q_scale, co
       PK_OK)
     return st;
   if ((st = check_device()) != PK_OK) return st;
-  return launch<128, true>(plan, q8, k8, workspace, out, lse, s_all,
+  return launch<128, true, false>(plan, q8, k8, workspace, out, lse, s_all,
                            reinterpret_cast<cudaStream_t>(stream), dev_status);
+}
+
+pk_status pk_attn_fwd_fp8_pv(const pk_plan* plan, const void* q8, float q_scale, const void* k8,
+                             float k_scale, const void* v8, float v_scale, void* out, float* lse,
+                             float scale, void* workspace, size_t workspace_bytes,
+                             pk_stream_t stream, int32_t* dev_status) {
+  if (plan == nullptr) return PK_ERR_INVALID_ARG;
+  const float s_all = scale * q_scale * k_scale;
+  if (!(scale > 0.f) || !(q_scale > 0.f) || !(k_scale > 0.f) || !std::isfinite(s_all) ||
+      !(s_all > 0.f) || !(v_scale > 0.f) || !std::isfinite(v_scale))
+    return PK_ERR_INVALID_ARG;
+  if (plan->head_dim != 128) return PK_ERR_UNSUPPORTED;
+  bool nothing = false;
+  pk_status st = check_plan(plan, &nothing);
+  if (st != PK_OK || nothing) return st;
+  if ((st = check_attn(q8, k8, out, lse, s_all)) != PK_OK ||
+      (st = check_values(plan, v8, workspace, workspace_bytes, true)) != PK_OK)
+    return st;
+  int sms = 0;
+  if ((st = check_device(&sms)) != PK_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = transpose_values(plan, v8, workspace, sms, s)) != PK_OK) return st;
+  return launch<128, true, true>(plan, q8, k8, workspace, out, lse, s_all, s, dev_status, v_scale);
 }
 
 pk_status pk_attn_fwd_host(const pk_plan* plan, const void* q_host, const void* k_host,

@@ -23,6 +23,9 @@ struct PlanImageLayout {
   size_t kvlim_off = 0;    // int32[Tq]: last visible key index of the row's key range, -1 none
   size_t table_off = 0;    // int32[num_seqs * blocks_per_seq] when keys are paged
   size_t vblk_off = 0;     // int32[v_blocks.size()]: (pool block, valid rows) the kernel reads
+  size_t v8chunk_off = 0;  // int32[v8_chunks.size()]: the E4M3 value transpose's chunks
+  size_t v8row_off = 0;    // int32[num_items] (contiguous keys): row of an item's first
+                           // key tile in the transposed E4M3 value copy
   size_t bytes = 0;
 };
 
@@ -52,6 +55,17 @@ struct pk_plan {
   // it holding keys) pairs, the block's other rows zeroed in the copy.
   int32_t v_conv_rows = 0;
   std::vector<int32_t> v_blocks;
+  // The transposed E4M3 value copy (pk_attn_fwd_fp8_pv), [hkv][d][v8_rows]
+  // bytes: (source row, copy row, rows holding keys, rows written) chunks of
+  // at most 128 rows.  Contiguous keys: sequence s's keys start at copy row
+  // v8_seq_row[s], its key count rounded up to 16 rows after the previous
+  // sequence's (a tensor copy may only start on a 16-byte boundary), written
+  // with zeros past the keys.  Paged keys: pool rows as they are, every
+  // referenced block written whole.
+  int32_t v8_rows = 0;
+  std::vector<int32_t> v8_chunks;
+  std::vector<int32_t> ck;          // contiguous keys: [num_seqs + 1] key row starts
+  std::vector<int32_t> v8_seq_row;  // contiguous keys: [num_seqs]
   std::vector<pk_work_item> items;         // CTA-ordered
   std::vector<int32_t> cta_offsets;        // [num_ctas + 1]
   pk::PlanImageLayout layout;

@@ -174,7 +174,21 @@ void schedule_and_image(pk_plan* p, std::vector<pk_work_item> items, int32_t num
   IL.kvlim_off = align_up(IL.cta_off_off + sizeof(int32_t) * (grid + 1), pk::kImageAlign);
   IL.table_off = align_up(IL.kvlim_off + sizeof(int32_t) * static_cast<size_t>(Tq), pk::kImageAlign);
   IL.vblk_off = align_up(IL.table_off + sizeof(int32_t) * p->block_table.size(), pk::kImageAlign);
-  IL.bytes = align_up(IL.vblk_off + sizeof(int32_t) * p->v_blocks.size(), pk::kImageAlign);
+  IL.v8chunk_off = align_up(IL.vblk_off + sizeof(int32_t) * p->v_blocks.size(), pk::kImageAlign);
+  IL.v8row_off = align_up(IL.v8chunk_off + sizeof(int32_t) * p->v8_chunks.size(), pk::kImageAlign);
+  // Contiguous keys: an item's key tiles sit in the E4M3 value copy at the
+  // copy row of its sequence (the last sequence whose keys start at the
+  // item's first key row: the non-empty one among equal starts).
+  std::vector<int32_t> v8_row;
+  if (!p->paged) {
+    v8_row.resize(n_items);
+    for (int32_t i = 0; i < n_items; ++i) {
+      const int32_t s = static_cast<int32_t>(
+          std::upper_bound(p->ck.begin(), p->ck.end(), p->items[i].kv_start) - p->ck.begin()) - 1;
+      v8_row[i] = (s >= 0 && s < p->num_seqs) ? p->v8_seq_row[s] : 0;
+    }
+  }
+  IL.bytes = align_up(IL.v8row_off + sizeof(int32_t) * v8_row.size(), pk::kImageAlign);
   p->image.assign(IL.bytes, 0);
   if (n_items)
     std::memcpy(p->image.data() + IL.items_off, p->items.data(), sizeof(pk_work_item) * n_items);
@@ -187,6 +201,11 @@ void schedule_and_image(pk_plan* p, std::vector<pk_work_item> items, int32_t num
   if (!p->v_blocks.empty())
     std::memcpy(p->image.data() + IL.vblk_off, p->v_blocks.data(),
                 sizeof(int32_t) * p->v_blocks.size());
+  if (!p->v8_chunks.empty())
+    std::memcpy(p->image.data() + IL.v8chunk_off, p->v8_chunks.data(),
+                sizeof(int32_t) * p->v8_chunks.size());
+  if (!v8_row.empty())
+    std::memcpy(p->image.data() + IL.v8row_off, v8_row.data(), sizeof(int32_t) * v8_row.size());
 }
 
 pk_status build_plan(const pk_layout& L, int32_t hq, int32_t hkv, int32_t d, int32_t num_ctas,
@@ -262,9 +281,29 @@ pk_status build_plan(const pk_layout& L, int32_t hq, int32_t hkv, int32_t d, int
       if (valid[i] >= 0) {
         p->v_blocks.push_back(static_cast<int32_t>(i));
         p->v_blocks.push_back(valid[i]);
+        const int32_t row = static_cast<int32_t>(i) * pk::kKeyBlock;
+        p->v8_chunks.insert(p->v8_chunks.end(), {row, row, valid[i], pk::kKeyBlock});
       }
+    p->v8_rows = (p->Tk + 15) / 16 * 16;
   } else {
     p->v_conv_rows = ck[S];
+    p->ck.assign(ck, ck + S + 1);
+    p->v8_seq_row.assign(S, 0);
+    int32_t row = 0;
+    for (int32_t s = 0; s < S; ++s) {
+      const int32_t nk = ck[s + 1] - ck[s];
+      p->v8_seq_row[s] = row;
+      for (int32_t c = 0; c < nk; c += pk::kKeyBlock) {
+        const int32_t n = std::min(pk::kKeyBlock, nk - c);
+        p->v8_chunks.insert(p->v8_chunks.end(), {ck[s] + c, row + c, n, (n + 15) / 16 * 16});
+      }
+      row += (nk + 15) / 16 * 16;
+    }
+    if (row == 0) {  // no keys at all: one tile of zeros for the masked reads
+      p->v8_chunks.insert(p->v8_chunks.end(), {0, 0, 0, pk::kKeyBlock});
+      row = pk::kKeyBlock;
+    }
+    p->v8_rows = row;
   }
 
   // Work items: every 128-row query tile x key/value head x query-head pair,
@@ -369,6 +408,10 @@ pk_status build_shard(const pk_plan* full, int32_t rank, int32_t num_ranks, int3
   p->kv_limit = full->kv_limit;
   p->v_conv_rows = full->v_conv_rows;
   p->v_blocks = full->v_blocks;
+  p->v8_rows = full->v8_rows;
+  p->v8_chunks = full->v8_chunks;
+  p->ck = full->ck;
+  p->v8_seq_row = full->v8_seq_row;
   p->cu_q = full->cu_q;
   p->shard_rank = rank;
   p->shard_ranks = num_ranks;
@@ -479,6 +522,10 @@ size_t pk_plan_device_bytes(const pk_plan* p) { return p ? p->layout.bytes : 0; 
 
 size_t pk_attn_workspace_bytes(const pk_plan* p) {
   return p ? static_cast<size_t>(p->Tk) * p->hkv * p->head_dim * 2 : 0;
+}
+
+size_t pk_attn_workspace_bytes_fp8_pv(const pk_plan* p) {
+  return p ? static_cast<size_t>(p->v8_rows) * p->hkv * p->head_dim : 0;
 }
 
 pk_status pk_plan_upload(pk_plan* p, void* dev_buf, size_t bytes, pk_stream_t stream) {

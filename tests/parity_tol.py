@@ -32,8 +32,11 @@ def out_allowance(out_oracle):
     return np.where(np.abs(out_oracle) >= 4.0, OUT_TOL + half_ulp_bf16(out_oracle), OUT_TOL)
 
 
-def check(case, out_g, lse_g, out_o, lse_o):
-    """Assert the rule on (rows of) one launch's outputs and record the errors."""
+def check(case, out_g, lse_g, out_o, lse_o, out_bound=None):
+    """Assert the rule on (rows of) one launch's outputs and record the errors.
+    ``out_bound``: a path whose arithmetic cannot meet the output rule (E4M3
+    softmax weights) is held to this looser bound instead, its errors recorded
+    all the same; the LSE rule and the empty-row rule stay."""
     empty = np.isneginf(lse_o)
     assert (np.isneginf(lse_g) == empty).all(), "rows without keys must give lse = -inf"
     assert (out_g[np.broadcast_to(empty.T[..., None], out_g.shape)] == 0).all()
@@ -51,6 +54,6 @@ def check(case, out_g, lse_g, out_o, lse_o):
                    float(np.abs(out_o).max())))
     print(f"{case}: max|dout|={e_out:.3e} (|o|<4: {e_small:.3e}) max|dlse|={e_lse:.3e} "
           f"max|o|={np.abs(out_o).max():.3f}")
-    bad = err > out_allowance(out_o)
+    bad = err > (out_allowance(out_o) if out_bound is None else out_bound)
     assert not bad.any(), (case, e_out, float(err[bad].max()))
     assert e_lse <= LSE_TOL, (case, e_lse)

@@ -73,6 +73,41 @@ def test_workspace_bytes_is_the_fp16_copy_of_the_value_rows():
     assert lay.workspace_bytes == 512 * 1 * 64 * 2  # the whole pool
 
 
+def test_fp8_pv_workspace_is_the_transposed_copy_with_16_row_sequences():
+    lib = pk.load()
+    assert lib.pk_attn_workspace_bytes_fp8_pv(None) == 0
+    # contiguous keys: every sequence's key rows rounded up to 16
+    plan = pk.Plan([0, 300, 300, 1000, 1001], [(0, 300, 1), (300, 700, 0), (1000, 1, 0)], 8, 2,
+                   128, num_ctas=4, upload=False)
+    assert plan.workspace_bytes_fp8_pv == (304 + 704 + 16) * 2 * 128
+    # paged keys: the pool's rows
+    lay = pk.plan_layout([0, 5], [0, 300], [(0, 0, 300, 1)], 4, 1, 128, k_pos0=[0],
+                         block_table=[[3, 0, 1]], num_kv_rows=512, num_ctas=2, upload=False)
+    assert lay.workspace_bytes_fp8_pv == 512 * 1 * 128
+    # no key at all: one zeroed tile for the masked reads
+    nokeys = pk.plan_layout([0, 5], [0, 0], [(0, 0, 8, 0)], 4, 1, 128, q_pos0=[3], k_pos0=[0],
+                            num_kv_rows=16, num_ctas=2, upload=False)
+    assert nokeys.workspace_bytes_fp8_pv == 128 * 1 * 128
+
+
+def test_fp8_pv_entry_argument_checks_without_a_device():
+    lib = pk.load()
+    plan = pk.Plan([0, 300], [(0, 300, 1)], 4, 2, 128, num_ctas=4, upload=False)
+    f = lib.pk_attn_fwd_fp8_pv
+    W = (16, 1 << 20)
+    assert f(None, 16, 1.0, 16, 1.0, 16, 1.0, 16, 16, 0.1, *W, None, None) == pk.PK_ERR_INVALID_ARG
+    for qs, ks, vs, sc in ((0.0, 1.0, 1.0, 0.1), (1.0, 1.0, -1.0, 0.1),
+                           (1.0, 1.0, float("inf"), 0.1), (1.0, 1.0, float("nan"), 0.1),
+                           (1.0, 1.0, 1.0, 0.0)):
+        assert f(plan.handle, 16, qs, 16, ks, 16, vs, 16, 16, sc, *W, None, None) \
+            == pk.PK_ERR_INVALID_ARG
+    assert f(plan.handle, 16, 1.0, 16, 1.0, 16, 1.0, 16, 16, 0.1, *W, None, None) \
+        == pk.PK_ERR_NOT_UPLOADED
+    p64 = pk.Plan([0, 300], [(0, 300, 1)], 4, 2, 64, num_ctas=4, upload=False)
+    assert f(p64.handle, 16, 1.0, 16, 1.0, 16, 1.0, 16, 16, 0.1, *W, None, None) \
+        == pk.PK_ERR_UNSUPPORTED
+
+
 def test_upload_rejects_small_or_misaligned_buffers_before_touching_memory():
     lib = pk.load()
     plan = pk.Plan([0, 300], [(0, 300, 1)], 4, 2, 128, num_ctas=4, upload=False)
