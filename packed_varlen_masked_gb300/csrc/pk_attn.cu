@@ -72,6 +72,8 @@ constexpr int kRegsLaunch = 65536 / kThreads / 8 * 8;  // 168
 static_assert(128 * (kRegsMma + kRegsSoftmax + kRegsEpi) <= kThreads * kRegsLaunch,
               "register split exceeds the CTA's allocation");
 constexpr uint32_t kTmemCols = 512;
+// Lanes that write one output row together in the epilogue (16-byte chunks).
+constexpr int kStoreGroup = 8;
 // F8: queries and keys are FP8 E4M3 (one byte per element), values bf16.
 template <int D, bool F8 = false, bool V8 = false>
 struct Cfg {
@@ -508,20 +510,59 @@ __device__ void epilogue_role(const KernelParams& p, uint32_t sbase, uint8_t* sg
     const float l = ml.y;
     // a row without keys writes zeros; E4M3 values carry their scale
     const float inv_l = l > 0.f ? p.v_scale / l : 0.f;
-    if (r < w.q_rows) {
-      uint8_t* orow = p.out + (((size_t)(w.q_start + r) * (size_t)p.hq + (size_t)h) * D) * 2;
+    // The thread's row as bf16: N = D/8 chunks of 16 bytes (4 words each).
+    constexpr int N = D / 8;
+    constexpr int G = kStoreGroup < N ? kStoreGroup : N;
+    uint32_t pk[D / 2];
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 8) {
-        uint4 v4;
-        v4.x = pack_bf16x2(__uint_as_float(o[c0 + 0]) * inv_l, __uint_as_float(o[c0 + 1]) * inv_l);
-        v4.y = pack_bf16x2(__uint_as_float(o[c0 + 2]) * inv_l, __uint_as_float(o[c0 + 3]) * inv_l);
-        v4.z = pack_bf16x2(__uint_as_float(o[c0 + 4]) * inv_l, __uint_as_float(o[c0 + 5]) * inv_l);
-        v4.w = pack_bf16x2(__uint_as_float(o[c0 + 6]) * inv_l, __uint_as_float(o[c0 + 7]) * inv_l);
-        *reinterpret_cast<uint4*>(orow + (size_t)c0 * 2) = v4;
+    for (int c = 0; c < D / 2; ++c) {
+      float x0, x1;
+      mul2(x0, x1, __uint_as_float(o[2 * c]), __uint_as_float(o[2 * c + 1]), inv_l, inv_l);
+      pk[c] = pack_bf16x2(x0, x1);
+    }
+    // Transpose G x G blocks of chunks within each group of G lanes (rows):
+    // stage m swaps bit m of (lane, chunk) for every chunk (a chunk whose
+    // bits differ moves to lane l ^ m, slot s ^ m), so afterwards lane l
+    // holds, in slot B*G + k, chunk B*G + l of its group's row k.
+    const int lid = lane & (G - 1);
+#pragma unroll
+    for (int m = 1; m < G; m <<= 1) {
+      const bool hi = (lid & m) != 0;
+#pragma unroll
+      for (int s0 = 0; s0 < N; ++s0) {
+        if (s0 & m) continue;
+        const int s1 = s0 | m;
+#pragma unroll
+        for (int wd = 0; wd < 4; ++wd) {
+          const uint32_t send = hi ? pk[4 * s0 + wd] : pk[4 * s1 + wd];
+          const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, m);
+          if (hi)
+            pk[4 * s0 + wd] = recv;
+          else
+            pk[4 * s1 + wd] = recv;
+        }
       }
+    }
+    // Store (B, k): the G lanes of a group write G * 16 contiguous bytes of
+    // one row, chunks B*G .. B*G + G - 1 (32 / G rows per warp instruction).
+    const int row0 = quad * 32 + (lane / G) * G;
+#pragma unroll
+    for (int k = 0; k < G; ++k) {
+      const int row = row0 + k;
+      if (row < w.q_rows) {
+        uint8_t* dst = p.out + (((size_t)(w.q_start + row) * (size_t)p.hq + (size_t)h) * D) * 2 +
+                       (size_t)lid * 16;
+#pragma unroll
+        for (int B = 0; B < N / G; ++B) {
+          const int s = B * G + k;
+          *reinterpret_cast<uint4*>(dst + (size_t)B * G * 16) =
+              make_uint4(pk[4 * s], pk[4 * s + 1], pk[4 * s + 2], pk[4 * s + 3]);
+        }
+      }
+    }
+    if (r < w.q_rows)
       p.lse[(size_t)h * (size_t)p.T + (size_t)(w.q_start + r)] =
           l > 0.f ? (ml.x + __log2f(l)) * 0.69314718055994530942f : -INFINITY;
-    }
     g += (uint32_t)w.n_kt;
   }
 }
