@@ -506,20 +506,28 @@ def sweep(pk, torch, stream, dev):
         out = torch.empty_like(q)
         lse = torch.empty(pack.hq, T, dtype=torch.float32, device=dev)
         ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
-        for _ in range(3):
-            pk.attn_fwd(q, k, v, plan, pack.scale, out=out, lse=lse, workspace=ws)
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-        n = 10
-        torch.cuda.synchronize()
-        ev[0].record(stream)
-        for _ in range(n):
-            pk.attn_fwd(q, k, v, plan, pack.scale, out=out, lse=lse, workspace=ws)
-        ev[1].record(stream)
-        torch.cuda.synchronize()
-        ms = ev[0].elapsed_time(ev[1]) / n
+        def timed(pl):
+            for _ in range(3):
+                pk.attn_fwd(q, k, v, pl, pack.scale, out=out, lse=lse, workspace=ws)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            n = 10
+            torch.cuda.synchronize()
+            ev[0].record(stream)
+            for _ in range(n):
+                pk.attn_fwd(q, k, v, pl, pack.scale, out=out, lse=lse, workspace=ws)
+            ev[1].record(stream)
+            torch.cuda.synchronize()
+            return ev[0].elapsed_time(ev[1]) / n
+        ms = timed(plan)
         fl = plan.useful_flops
         res[name] = {"ms": round(ms, 4), "useful_tflops": round(fl / ms / 1e9, 1),
                      "tokens_per_s": round(T / ms * 1e3), "total_tokens": T}
+        if pack.d == 128:  # the opt-in SM-pair kernel on the same inputs
+            pair = pk.plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d,
+                           device=dev).set_sm_pairs(True)
+            ms2 = timed(pair)
+            res[name]["sm_pairs"] = {"ms": round(ms2, 4), "useful_tflops": round(fl / ms2 / 1e9, 1)}
+            del pair
         del q, k, v, out, lse, plan, ws
         torch.cuda.empty_cache()
     return res

@@ -187,6 +187,28 @@ pk_status pk_plan_create_layout(const pk_layout* layout, int32_t hq, int32_t hkv
 pk_status pk_plan_shard(const pk_plan* full, int32_t rank, int32_t num_ranks, int32_t num_ctas,
                         pk_plan** out);
 
+/*
+ * SM-pair kernel, opt-in (head_dim 128, pk_attn_fwd and the calls built on
+ * it; the FP8 entries keep the one-CTA kernel).  With enable != 0 the
+ * attention runs on clusters of two CTAs on SM pairs: each pair computes
+ * its two query tiles as M = 256 tensor-core products (tcgen05 cta_group::2),
+ * each SM holding half of every key and value tile, so each SM copies half
+ * the key/value bytes per tile.  Results are bit-identical to the one-CTA
+ * kernel.  The plan pairs items that read the same key/value tiles (same
+ * first key row, key/value head and query heads) by their key-tile count;
+ * a pair visits the larger count (the other rows see the extra tiles fully
+ * masked).  Measured on GB300: faster on packs of long sequences (+3 to +4%
+ * on the two 24,832-token sequences of the high-res edit pack), slower on
+ * packs of short ones (-2% on the mixed-resolution pack, -6 to -15% on the
+ * CFG pair), so it is off by default.  The pages have no counterpart; it is
+ * a tuning option of this library.
+ *   PK_ERR_INVALID_ARG for a null plan; PK_ERR_UNSUPPORTED when enabling a
+ *   plan that has no pair schedule (head_dim other than 128, or built for
+ *   fewer than two CTAs).  Takes effect at the next launch; not thread-safe
+ *   against launches running on the plan.
+ */
+pk_status pk_plan_set_sm_pairs(pk_plan* plan, int32_t enable);
+
 /* Bytes of the device image of the plan (work list, per-CTA offsets, the
  * per-row key limit and, for paged keys, the block table). */
 size_t pk_plan_device_bytes(const pk_plan* plan);
@@ -397,6 +419,14 @@ pk_status pk_plan_get_info(const pk_plan* plan, pk_plan_info* info);
 pk_status pk_plan_get_kv_limit(const pk_plan* plan, int32_t* out, int64_t n);
 pk_status pk_plan_get_items(const pk_plan* plan, pk_work_item* items,
                             int64_t n_items, int32_t* cta_offsets,
+                            int64_t n_offsets);
+/* The SM-pair schedule (pk_plan_set_sm_pairs), for tests: *num_pairs and
+ * *num_clusters (0 when the plan has none); with non-null arrays of at
+ * least 2 * num_pairs items and num_clusters + 1 offsets, the
+ * cluster-ordered (rank 0, rank 1) item pairs and the per-cluster offsets
+ * in pairs.  PK_ERR_INVALID_ARG for a null plan or short arrays. */
+pk_status pk_plan_get_pairs(const pk_plan* plan, int32_t* num_pairs, int32_t* num_clusters,
+                            pk_work_item* items, int64_t n_items, int32_t* cluster_offsets,
                             int64_t n_offsets);
 
 /* Element types of pk_lse_merge's tensors. */

@@ -88,6 +88,10 @@ SIGNATURES = {
                                              ctypes.POINTER(_vp)]),
     "pk_plan_shard": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                      ctypes.POINTER(_vp)]),
+    "pk_plan_set_sm_pairs": (ctypes.c_int, [_vp, ctypes.c_int32]),
+    "pk_plan_get_pairs": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int32),
+                                         ctypes.POINTER(ctypes.c_int32), _vp, ctypes.c_int64,
+                                         _vp, ctypes.c_int64]),
     "pk_plan_device_bytes": (ctypes.c_size_t, [_vp]),
     "pk_plan_upload": (ctypes.c_int, [_vp, _vp, ctypes.c_size_t, _vp]),
     "pk_attn_workspace_bytes": (ctypes.c_size_t, [_vp]),

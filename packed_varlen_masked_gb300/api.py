@@ -130,6 +130,30 @@ class Plan:
         """Bytes of attn_fwd_fp8_pv's workspace (the transposed E4M3 values)."""
         return int(self._lib.pk_attn_workspace_bytes_fp8_pv(self._h))
 
+    def set_sm_pairs(self, enable: bool = True) -> "Plan":
+        """Run this plan on SM pairs (pk_plan_set_sm_pairs; head_dim 128):
+        faster on packs of long sequences, slower on short ones, off by
+        default.  Returns the plan."""
+        check(self._lib.pk_plan_set_sm_pairs(self._h, 1 if enable else 0), "pk_plan_set_sm_pairs")
+        return self
+
+    def pairs(self) -> Tuple[np.ndarray, np.ndarray]:
+        """(pair items int32 [2 * num_pairs, 8], rank 0 then rank 1 of each
+        pair, cluster-ordered; cluster offsets int32 [num_clusters + 1], in
+        pairs).  Columns as ``items``."""
+        npairs, ncl = ctypes.c_int32(), ctypes.c_int32()
+        check(self._lib.pk_plan_get_pairs(self._h, ctypes.byref(npairs), ctypes.byref(ncl), None, 0,
+                                          None, 0), "pk_plan_get_pairs")
+        n = 2 * npairs.value
+        items = (WorkItem * max(n, 1))()
+        offs = np.zeros(ncl.value + 1, dtype=np.int32)
+        if ncl.value > 0:
+            check(self._lib.pk_plan_get_pairs(self._h, ctypes.byref(npairs), ctypes.byref(ncl),
+                                              items, n, offs.ctypes.data_as(ctypes.c_void_p),
+                                              offs.size), "pk_plan_get_pairs")
+        arr = np.frombuffer(bytes(items), dtype=np.int32).reshape(-1, 8)[:n].copy()
+        return arr, offs
+
     def kv_limit(self) -> np.ndarray:
         out = np.zeros(max(self.total_tokens, 1), dtype=np.int32)
         check(self._lib.pk_plan_get_kv_limit(self._h, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),

@@ -236,6 +236,81 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint6
   }
 }
 
+// ---- SM pairs (cta_group::2): a cluster of two CTAs on an SM pair -------
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                   "memory");
+}
+// The shared::cluster address of this CTA's shared address `saddr` in CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+// Relaxed arrival on a barrier of another CTA of the cluster: it orders no
+// memory operation, so the caller first completes what the arrival stands
+// for (its TMEM loads and stores).  A release at cluster scope would cost a
+// cluster-wide memory barrier per arrival.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+// Commit of this thread's pair MMAs to the barrier at `bar` in the CTAs of
+// `mask` (bit r: CTA rank r).
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar), "h"(mask)
+      : "memory");
+}
+// Tensor copy into `dst` (a shared::cluster address: this CTA's or the
+// peer's buffer), completing on this CTA's barrier `bar`.
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                                 int c0, int c1, int c2, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+      : "memory");
+}
+// S = Q K^T over the pair, M = 256: each CTA holds its 128 query rows
+// (K-major SW128, 64-column boxes of 128 rows) and half of the key tile (64
+// rows per box, so its boxes are 8 KB apart); each CTA's TMEM gets its rows.
+template <int D>
+__device__ __forceinline__ void issue_qk_pair(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
+  constexpr uint32_t idesc = make_idesc(256, 128, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t oq = (uint64_t)(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
+    const uint64_t ok = (uint64_t)(((kk >> 2) * (kBoxBytes / 2) + (kk & 3) * 32) >> 4);
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(q_desc + oq), "l"(k_desc + ok), "r"(idesc), "r"(kk > 0 ? 1u : 0u)
+        : "memory");
+  }
+}
+// O += P V over the pair: P (fp16) from each CTA's TMEM rows; each CTA holds
+// the values of 64 of the D columns (one MN-major SW128 box of 128 keys).
+template <int D>
+__device__ __forceinline__ void issue_pv_pair(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
+                                              bool accumulate) {
+  constexpr uint32_t idesc = make_idesc_f16(256, D, true);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(p_tmem + (uint32_t)kk * 8u), "l"(v_desc + (uint64_t)(kk * (2048 >> 4))), "r"(idesc),
+        "r"((accumulate || kk > 0) ? 1u : 0u)
+        : "memory");
+}
+
 // O(tmem) (+)= P V: 8 MMAs of 128 x D x 16, fp16 operands.  P (fp16 pairs)
 // is read from TMEM, 8 columns per 16 keys.  V is MN-major with 128-byte swizzle: 16 keys
 // span 2048 bytes, and the second 64-column box (D = 128) is 16384 bytes on.

@@ -75,32 +75,44 @@ constexpr uint32_t kTmemCols = 512;
 // Lanes that write one output row together in the epilogue (16-byte chunks).
 constexpr int kStoreGroup = 8;
 // F8: queries and keys are FP8 E4M3 (one byte per element), values bf16.
-template <int D, bool F8 = false, bool V8 = false>
+// PAIR: the SM-pair kernel (bf16, D = 128): a cluster of two CTAs computes
+// M = 256 products; each CTA holds its own 128 query rows, half of every key
+// tile (64 rows) and half of every value tile (64 of the D columns).
+template <int D, bool F8 = false, bool V8 = false, bool PAIR = false>
 struct Cfg {
-  // Query/key tiles: 128 rows in boxes of 128-byte rows (64 bf16 or 128
-  // FP8 elements); value tiles: 128 rows of D fp16 in 64-column boxes.
+  // Query/key tiles: rows in boxes of 128-byte rows (64 bf16 or 128 FP8
+  // elements); value tiles: 128 rows of D fp16 in 64-column boxes.
   static constexpr int kQKElemsPerBox = F8 ? 128 : 64;
   static constexpr int kQKBoxes = D / kQKElemsPerBox;
-  static constexpr int kQKTileBytes = 128 * D * (F8 ? 1 : 2);
+  static constexpr int kQKTileBytes = 128 * D * (F8 ? 1 : 2);  // a query tile
+  static constexpr int kKRows = PAIR ? 64 : 128;               // key rows per CTA and tile
+  static constexpr int kKBoxBytes = kKRows * 128;
+  static constexpr int kKTileBytes = kKRows * D * (F8 ? 1 : 2);
   // V8: E4M3 values, transposed (one 128-byte row of keys per head-dimension
-  // index), one box per tile; else fp16 values in 64-column boxes.
-  static constexpr int kVBoxes = V8 ? 1 : D / 64;
-  static constexpr int kVTileBytes = 128 * D * (V8 ? 1 : 2);
+  // index), one box per tile; PAIR: one 64-column box (this CTA's half);
+  // else fp16 values in 64-column boxes.
+  static constexpr int kVBoxes = (V8 || PAIR) ? 1 : D / 64;
+  static constexpr int kVTileBytes = PAIR ? 128 * 64 * 2 : 128 * D * (V8 ? 1 : 2);
   // Rings: two query tiles (the next unit's loads during this one), and key
   // and value tiles.  Shared memory stays above half an SM, so exactly one
   // CTA (and one 512-column TMEM allocation) lives on each SM.
-  static constexpr int kKStages = F8 ? 4 : (D == 128 ? 3 : 4);
-  static constexpr int kVStages = V8 ? 4 : (F8 ? 3 : (D == 128 ? 2 : 4));
+  static constexpr int kKStages = PAIR ? 7 : (F8 ? 4 : (D == 128 ? 3 : 4));
+  static constexpr int kVStages = PAIR ? 3 : (V8 ? 4 : (F8 ? 3 : (D == 128 ? 2 : 4)));
   // TMEM columns: S double buffer, P double buffer (16-bit pairs), O.
   static constexpr uint32_t kColS0 = 0;    // S(t) in [128*(t%2), +128)
   static constexpr uint32_t kColP0 = 256;  // P(t) in [256 + 64*(t%2), +64)
   static constexpr uint32_t kColO = 384;   // O in [384, 384 + D)
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = 2 * kQKTileBytes;
-  static constexpr int kOffV = kOffK + kKStages * kQKTileBytes;
+  static constexpr int kOffV = kOffK + kKStages * kKTileBytes;
   static constexpr int kOffBar = kOffV + kVStages * kVTileBytes;
   static_assert(!F8 || D == 128, "FP8 queries/keys need head_dim 128");
   static_assert(!V8 || F8, "E4M3 values come with E4M3 queries and keys");
+  static_assert(!PAIR || (D == 128 && !F8), "the SM-pair kernel is bf16 with head_dim 128");
+  // Arrivals of the softmax (S buffer free, P ready) and the epilogue (O
+  // free): one per thread of the CTA's warpgroup, or, in the pair kernel,
+  // of both CTAs' warpgroups (on the rank-0 CTA's barrier).
+  static constexpr uint32_t kGroupArrivals = PAIR ? 256 : 128;
   // barrier indices
   static constexpr int kQFull = 0, kQEmpty = 2;  // [2] each
   static constexpr int kKFull = 4, kKEmpty = kKFull + kKStages;
@@ -126,13 +138,16 @@ struct Cfg {
 // streams the key/value tiles of its sequence.  A CTA runs the heads of each
 // of its items back to back, so the second head's keys and values come from
 // L2.  Every role walks the same unit sequence.
+// In the pair kernel the items come in (rank 0, rank 1) pairs and each CTA
+// walks its own item of every pair (stride 2).
 struct UnitIter {
   const pk_work_item* items;
-  int it, end, slot;
+  int it, end, slot, stride, rank;
   pk_work_item w;
-  __device__ UnitIter(const pk_work_item* items_, int beg, int end_)
-      : items(items_), it(beg), end(end_), slot(0) {
-    if (it < end) w = items[it];
+  __device__ UnitIter(const pk_work_item* items_, int beg, int end_, int stride_ = 1,
+                      int rank_ = 0)
+      : items(items_), it(beg), end(end_), slot(0), stride(stride_), rank(rank_) {
+    if (it < end) w = items[it * stride + rank];
   }
   __device__ bool valid() const { return it < end; }
   __device__ int head() const { return slot ? w.hq1 : w.hq0; }
@@ -142,7 +157,7 @@ struct UnitIter {
       return;
     }
     slot = 0;
-    if (++it < end) w = items[it];
+    if (++it < end) w = items[it * stride + rank];
   }
 };
 
@@ -150,35 +165,60 @@ struct UnitIter {
 // the ring of key tiles.  Keys and values are re-read by the other query
 // heads of the group and by neighbouring query tiles, so they are kept in L2
 // (evict-last); a query tile is read once (evict-first).
-template <int D, bool F8, bool V8>
+template <int D, bool F8, bool V8, bool PAIR>
 __device__ void producer_qk_role(const KernelParams& p, const CUtensorMap* tm_q,
                                  const CUtensorMap* tm_k, uint32_t sbase, int beg, int end,
                                  const WaitCtl& wc) {
-  using C = Cfg<D, F8, V8>;
+  using C = Cfg<D, F8, V8, PAIR>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
   const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
   uint32_t g = 0, u = 0, k_armed = 0, q_armed = 0;
   bool ok = true;
-  for (UnitIter ui(p.items, beg, end); ui.valid() && ok; ui.next(), ++u) {
+  constexpr int kCtas = PAIR ? 2 : 1;  // pair: this (rank-0) thread loads both CTAs' tiles
+  for (UnitIter ui(p.items, beg, end, kCtas, 0); ui.valid() && ok; ui.next(), ++u) {
     const pk_work_item& w = ui.w;
     const uint32_t qb = u & 1u;
     if (!(ok = mbar_wait(bar(C::kQEmpty + qb), ((u >> 1) & 1u) ^ 1u, wc))) break;
-    mbar_arrive_expect_tx(bar(C::kQFull + qb), C::kQKTileBytes);
+    mbar_arrive_expect_tx(bar(C::kQFull + qb), kCtas * C::kQKTileBytes);
     ++q_armed;
+    if constexpr (PAIR) {
+      // rank r's query rows into rank r's buffer (a partner without rows
+      // reloads the leader's), completing on this CTA's barrier
+      const int q1 = p.items[ui.it * 2 + 1].q_start;
 #pragma unroll
-    for (int h = 0; h < C::kQKBoxes; ++h)
-      tma_load_3d_hint(sbase + C::kOffQ + qb * C::kQKTileBytes + h * kBoxBytes, tm_q,
-                       bar(C::kQFull + qb), h * C::kQKElemsPerBox, ui.head(), w.q_start, stream);
+      for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int h = 0; h < C::kQKBoxes; ++h)
+          tma_load_3d_pair(map_to_rank(sbase + C::kOffQ + qb * C::kQKTileBytes + h * kBoxBytes, r),
+                           tm_q, bar(C::kQFull + qb), h * C::kQKElemsPerBox, ui.head(),
+                           r ? q1 : w.q_start, stream);
+    } else {
+#pragma unroll
+      for (int h = 0; h < C::kQKBoxes; ++h)
+        tma_load_3d_hint(sbase + C::kOffQ + qb * C::kQKTileBytes + h * kBoxBytes, tm_q,
+                         bar(C::kQFull + qb), h * C::kQKElemsPerBox, ui.head(), w.q_start, stream);
+    }
     for (int j = 0; j < w.n_kt; ++j, ++g) {
       const uint32_t st = g % C::kKStages, ph = (g / C::kKStages) & 1u;
       if (!(ok = mbar_wait(bar(C::kKEmpty + st), ph ^ 1u, wc))) break;
-      mbar_arrive_expect_tx(bar(C::kKFull + st), C::kQKTileBytes);
+      mbar_arrive_expect_tx(bar(C::kKFull + st), kCtas * C::kKTileBytes);
       ++k_armed;
+      if constexpr (PAIR) {  // key rows [64 r, 64 r + 64) of the tile to rank r
 #pragma unroll
-      for (int h = 0; h < C::kQKBoxes; ++h)
-        tma_load_3d_hint(sbase + C::kOffK + st * C::kQKTileBytes + h * kBoxBytes, tm_k,
-                         bar(C::kKFull + st), h * C::kQKElemsPerBox, w.hkv, key_tile_row(p, w, j),
-                         keep);
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+          for (int h = 0; h < C::kQKBoxes; ++h)
+            tma_load_3d_pair(
+                map_to_rank(sbase + C::kOffK + st * C::kKTileBytes + h * C::kKBoxBytes, r), tm_k,
+                bar(C::kKFull + st), h * C::kQKElemsPerBox, w.hkv,
+                key_tile_row(p, w, j) + r * C::kKRows, keep);
+      } else {
+#pragma unroll
+        for (int h = 0; h < C::kQKBoxes; ++h)
+          tma_load_3d_hint(sbase + C::kOffK + st * C::kKTileBytes + h * C::kKBoxBytes, tm_k,
+                           bar(C::kKFull + st), h * C::kQKElemsPerBox, w.hkv,
+                           key_tile_row(p, w, j), keep);
+      }
     }
   }
   // Every copy issued must land before the CTA may exit.  After a normal run
@@ -198,22 +238,28 @@ __device__ void producer_qk_role(const KernelParams& p, const CUtensorMap* tm_q,
 
 // V producer (one thread of another warp): the ring of value tiles, so that
 // a value tile waiting for its stage never holds back the next key tile.
-template <int D, bool F8, bool V8>
+template <int D, bool F8, bool V8, bool PAIR>
 __device__ void producer_v_role(const KernelParams& p, const CUtensorMap* tm_v, uint32_t sbase,
                                 int beg, int end, const WaitCtl& wc) {
-  using C = Cfg<D, F8, V8>;
+  using C = Cfg<D, F8, V8, PAIR>;
+  constexpr int kCtas = PAIR ? 2 : 1;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
   const uint64_t keep = l2_policy_evict_last();
   uint32_t g = 0, v_armed = 0;
   bool ok = true;
-  for (UnitIter ui(p.items, beg, end); ui.valid() && ok; ui.next()) {
+  for (UnitIter ui(p.items, beg, end, kCtas, 0); ui.valid() && ok; ui.next()) {
     const pk_work_item& w = ui.w;
     for (int j = 0; j < w.n_kt; ++j, ++g) {
       const uint32_t st = g % C::kVStages, ph = (g / C::kVStages) & 1u;
       if (!(ok = mbar_wait(bar(C::kVEmpty + st), ph ^ 1u, wc))) break;
-      mbar_arrive_expect_tx(bar(C::kVFull + st), C::kVTileBytes);
+      mbar_arrive_expect_tx(bar(C::kVFull + st), kCtas * C::kVTileBytes);
       ++v_armed;
-      if constexpr (V8) {  // (key, head-dimension index, head) view of the transposed copy
+      if constexpr (PAIR) {  // value columns [64 r, 64 r + 64) to rank r
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+          tma_load_3d_pair(map_to_rank(sbase + C::kOffV + st * C::kVTileBytes, r), tm_v,
+                           bar(C::kVFull + st), r * 64, w.hkv, key_tile_row(p, w, j), keep);
+      } else if constexpr (V8) {  // (key, head-dimension index, head) view of the transposed copy
         const int row = p.v8_row ? p.v8_row[ui.it] + j * 128 : key_tile_row(p, w, j);
         tma_load_3d_hint(sbase + C::kOffV + st * C::kVTileBytes, tm_v, bar(C::kVFull + st), row,
                          0, w.hkv, keep);
@@ -240,17 +286,18 @@ __device__ void producer_v_role(const KernelParams& p, const CUtensorMap* tm_v, 
 // S issuer (warp 1): S(t) needs K(t) loaded and S buffer t%2 released by the
 // softmax of tile t-2, so it runs up to two tiles ahead of the softmax and
 // the tensor pipe computes S(t+2) while the softmax works on tile t.
-template <int D, bool F8, bool V8>
+template <int D, bool F8, bool V8, bool PAIR>
 __device__ void mma_s_role(const KernelParams& p, uint32_t sbase, uint32_t tmem, int beg,
                            int end, const WaitCtl& wc) {
-  using C = Cfg<D, F8, V8>;
+  using C = Cfg<D, F8, V8, PAIR>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
   const uint64_t q_desc0 = sdesc(sbase + C::kOffQ, 16, 1024);
   const uint64_t k_desc0 = sdesc(sbase + C::kOffK, 16, 1024);
-  constexpr uint64_t kTileDesc = (uint64_t)(C::kQKTileBytes >> 4);
+  constexpr uint64_t kQTileDesc = (uint64_t)(C::kQKTileBytes >> 4);
+  constexpr uint64_t kKTileDesc = (uint64_t)(C::kKTileBytes >> 4);
   uint32_t t = 0, u = 0;
   bool ok = true;
-  for (UnitIter ui(p.items, beg, end); ui.valid() && ok; ui.next(), ++u) {
+  for (UnitIter ui(p.items, beg, end, PAIR ? 2 : 1, 0); ui.valid() && ok; ui.next(), ++u) {
     const uint32_t n = (uint32_t)ui.w.n_kt, qb = u & 1u;
     if (!(ok = mbar_wait(bar(C::kQFull + qb), (u >> 1) & 1u, wc))) break;
     for (uint32_t j = 0; j < n; ++j, ++t) {
@@ -258,24 +305,35 @@ __device__ void mma_s_role(const KernelParams& p, uint32_t sbase, uint32_t tmem,
       if (!(ok = mbar_wait(bar(C::kKFull + kst), (t / C::kKStages) & 1u, wc))) break;
       if (t >= 2 && !(ok = mbar_wait(bar(C::kSFree + b), ((t >> 1) - 1u) & 1u, wc))) break;
       tc_fence_after();
-      issue_qk<D, F8>(tmem + C::kColS0 + b * 128u, q_desc0 + qb * kTileDesc,
-                  k_desc0 + kst * kTileDesc);
-      tc_commit(bar(C::kSFull + b));
-      tc_commit(bar(C::kKEmpty + kst));
-      if (j + 1 == n) tc_commit(bar(C::kQEmpty + qb));  // last use of this Q buffer
+      if constexpr (PAIR) {  // both CTAs' softmax wait for S; the buffers are this CTA's
+        issue_qk_pair<D>(tmem + C::kColS0 + b * 128u, q_desc0 + qb * kQTileDesc,
+                         k_desc0 + kst * kKTileDesc);
+        tc_commit_pair(bar(C::kSFull + b), 3);
+        tc_commit_pair(bar(C::kKEmpty + kst), 1);
+        if (j + 1 == n) tc_commit_pair(bar(C::kQEmpty + qb), 1);
+      } else {
+        issue_qk<D, F8>(tmem + C::kColS0 + b * 128u, q_desc0 + qb * kQTileDesc,
+                        k_desc0 + kst * kKTileDesc);
+        tc_commit(bar(C::kSFull + b));
+        tc_commit(bar(C::kKEmpty + kst));
+        if (j + 1 == n) tc_commit(bar(C::kQEmpty + qb));  // last use of this Q buffer
+      }
     }
   }
   // Every MMA this thread issued must finish before TMEM is released.
-  tc_commit(bar(C::kMmaDone + 0));
+  if constexpr (PAIR)
+    tc_commit_pair(bar(C::kMmaDone + 0), 1);
+  else
+    tc_commit(bar(C::kMmaDone + 0));
   mbar_wait_drain(bar(C::kMmaDone + 0), 0, wc);
 }
 
 // P V issuer (warp 3): O (+)= P(t) V(t) needs V(t) loaded and P(t) written;
 // a unit's first product overwrites O, after the previous unit's O was read.
-template <int D, bool F8, bool V8>
+template <int D, bool F8, bool V8, bool PAIR>
 __device__ void mma_pv_role(const KernelParams& p, uint32_t sbase, uint32_t tmem, int beg,
                             int end, const WaitCtl& wc) {
-  using C = Cfg<D, F8, V8>;
+  using C = Cfg<D, F8, V8, PAIR>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
   // fp16 values: MN-major, 64-column boxes kBoxBytes apart; E4M3 values:
   // K-major (transposed copy)
@@ -283,7 +341,7 @@ __device__ void mma_pv_role(const KernelParams& p, uint32_t sbase, uint32_t tmem
   constexpr uint64_t kTileDesc = (uint64_t)(C::kVTileBytes >> 4);
   uint32_t t = 0, u = 0;
   bool ok = true;
-  for (UnitIter ui(p.items, beg, end); ui.valid() && ok; ui.next(), ++u) {
+  for (UnitIter ui(p.items, beg, end, PAIR ? 2 : 1, 0); ui.valid() && ok; ui.next(), ++u) {
     const uint32_t n = (uint32_t)ui.w.n_kt;
     for (uint32_t j = 0; j < n; ++j, ++t) {
       const uint32_t vst = t % C::kVStages, b = t & 1u;
@@ -291,24 +349,49 @@ __device__ void mma_pv_role(const KernelParams& p, uint32_t sbase, uint32_t tmem
       if (!(ok = mbar_wait(bar(C::kPReady + b), (t >> 1) & 1u, wc))) break;
       if (j == 0 && !(ok = mbar_wait(bar(C::kOFree), (u & 1u) ^ 1u, wc))) break;
       tc_fence_after();
-      if constexpr (V8)
-        issue_pv_f8<D>(tmem + C::kColO, tmem + C::kColP0 + b * 64u, v_desc0 + vst * kTileDesc,
-                       j > 0);
-      else
-        issue_pv<D>(tmem + C::kColO, tmem + C::kColP0 + b * 64u, v_desc0 + vst * kTileDesc, j > 0);
-      tc_commit(bar(C::kPvDone + b));
-      tc_commit(bar(C::kVEmpty + vst));
+      if constexpr (PAIR) {  // both CTAs' softmax and epilogue wait for P V
+        issue_pv_pair<D>(tmem + C::kColO, tmem + C::kColP0 + b * 64u, v_desc0 + vst * kTileDesc,
+                         j > 0);
+        tc_commit_pair(bar(C::kPvDone + b), 3);
+        tc_commit_pair(bar(C::kVEmpty + vst), 1);
+      } else {
+        if constexpr (V8)
+          issue_pv_f8<D>(tmem + C::kColO, tmem + C::kColP0 + b * 64u, v_desc0 + vst * kTileDesc,
+                         j > 0);
+        else
+          issue_pv<D>(tmem + C::kColO, tmem + C::kColP0 + b * 64u, v_desc0 + vst * kTileDesc,
+                      j > 0);
+        tc_commit(bar(C::kPvDone + b));
+        tc_commit(bar(C::kVEmpty + vst));
+      }
     }
   }
-  tc_commit(bar(C::kMmaDone + 1));
+  if constexpr (PAIR)
+    tc_commit_pair(bar(C::kMmaDone + 1), 1);
+  else
+    tc_commit(bar(C::kMmaDone + 1));
   mbar_wait_drain(bar(C::kMmaDone + 1), 0, wc);
 }
 
+// An arrival of a softmax or epilogue thread on an MMA-side barrier: this
+// CTA's, or in the pair kernel's rank-1 CTA the rank-0 CTA's.  The rank-1
+// arrival is relaxed: what it announces (S or O read out of this CTA's TMEM,
+// or P written into it) has completed before it (every TMEM load and store
+// here is fused with its wait), and the products that follow only touch
+// TMEM.
+template <bool PAIR>
+__device__ __forceinline__ void group_arrive(uint32_t bar, uint32_t rank) {
+  if (PAIR && rank != 0)
+    mbar_arrive_cluster_relaxed(map_to_rank(bar, 0));
+  else
+    mbar_arrive(bar);
+}
+
 // Softmax warpgroup (warps 4-7): thread r owns row r of S, P and O in TMEM.
-template <int D, bool F8, bool V8>
+template <int D, bool F8, bool V8, bool PAIR>
 __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint8_t* sgen, uint32_t tmem,
                              int beg, int end, const WaitCtl& wc) {
-  using C = Cfg<D, F8, V8>;
+  using C = Cfg<D, F8, V8, PAIR>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;  // TMEM lane quadrant this warp may access
@@ -320,10 +403,13 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint8_t* sge
   bool ok = true;
   bool s_ready = false;  // S(t) of the next tile already seen complete
   float2* lm = reinterpret_cast<float2*>(sgen + C::kOffLm);
-  for (UnitIter ui(p.items, beg, end); ui.valid() && ok; ui.next(), ++u) {
+  const uint32_t rank = PAIR ? cluster_rank() : 0u;
+  for (UnitIter ui(p.items, beg, end, PAIR ? 2 : 1, (int)rank); ui.valid() && ok;
+       ui.next(), ++u) {
     const pk_work_item& w = ui.w;
     const bool valid = r < w.q_rows;
-    const int lim = p.kv_limit[w.q_start + (valid ? r : w.q_rows - 1)];
+    // (a pair's rank-1 item may have no rows: its rows see no key)
+    const int lim = w.q_rows > 0 ? p.kv_limit[w.q_start + (valid ? r : w.q_rows - 1)] : -1;
     float m_used = -INFINITY, l = 0.f;
     for (int j = 0; j < w.n_kt; ++j) {
       const uint32_t t = g + (uint32_t)j, b = t & 1u;
@@ -338,7 +424,7 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint8_t* sge
       tmem_ld_x128(tS, sr);
       // S buffer b may now take S(t+2).
       tc_fence_before();
-      mbar_arrive(bar(C::kSFree + b));
+      group_arrive<PAIR>(bar(C::kSFree + b), rank);
       if (j >= w.n_full) {  // partial tile: keys past this row's limit are -inf
         const int nvis = lim - j * 128 + 1;
 #pragma unroll
@@ -455,7 +541,7 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint8_t* sge
       else
         tmem_st_x64(tP, pp);
       tc_fence_before();
-      mbar_arrive(bar(C::kPReady + b));
+      group_arrive<PAIR>(bar(C::kPReady + b), rank);
     }
     if (!ok) break;
     // Hand the unit's row statistics to the epilogue warps, once they have
@@ -474,10 +560,10 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint8_t* sge
 // unit it takes (m, l) from the softmax, waits for the unit's last P V,
 // moves O into registers and frees it for the next unit's first product,
 // then writes O / l as bf16 and the natural-log LSE.
-template <int D, bool F8, bool V8>
+template <int D, bool F8, bool V8, bool PAIR>
 __device__ void epilogue_role(const KernelParams& p, uint32_t sbase, uint8_t* sgen,
                               uint32_t tmem, int beg, int end, const WaitCtl& wc) {
-  using C = Cfg<D, F8, V8>;
+  using C = Cfg<D, F8, V8, PAIR>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;
@@ -486,7 +572,9 @@ __device__ void epilogue_role(const KernelParams& p, uint32_t sbase, uint8_t* sg
   const float2* lm = reinterpret_cast<const float2*>(sgen + C::kOffLm);
   uint32_t g = 0, u = 0;
   bool ok = true;
-  for (UnitIter ui(p.items, beg, end); ui.valid() && ok; ui.next(), ++u) {
+  const uint32_t rank = PAIR ? cluster_rank() : 0u;
+  for (UnitIter ui(p.items, beg, end, PAIR ? 2 : 1, (int)rank); ui.valid() && ok;
+       ui.next(), ++u) {
     const pk_work_item& w = ui.w;
     const int h = ui.head();
     if (!(ok = __all_sync(0xffffffffu, mbar_wait_sleep(bar(C::kLmFull), u & 1u, wc)))) break;
@@ -506,7 +594,7 @@ __device__ void epilogue_role(const KernelParams& p, uint32_t sbase, uint8_t* sg
       tmem_ld_x32(tO + 32u, o1);
     }
     tc_fence_before();
-    mbar_arrive(bar(C::kOFree));
+    group_arrive<PAIR>(bar(C::kOFree), rank);
     const float l = ml.y;
     // a row without keys writes zeros; E4M3 values carry their scale
     const float inv_l = l > 0.f ? p.v_scale / l : 0.f;
@@ -665,12 +753,12 @@ __global__ void __launch_bounds__(256) pk_v8_transpose_kernel(const uint8_t* v8,
   }
 }
 
-template <int D, bool F8, bool V8>
+template <int D, bool F8, bool V8, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     pk_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const KernelParams p) {
-  using C = Cfg<D, F8, V8>;
+  using C = Cfg<D, F8, V8, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1 KB alignment
@@ -679,14 +767,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + C::kOffMisc + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
+  // Pair kernel: CTA rank 0 of each cluster loads both CTAs' tiles and issues
+  // the M = 256 products; both CTAs run their rows' softmax and epilogue.
+  const uint32_t rank = PAIR ? cluster_rank() : 0u;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(C::kQFull + s), 1);
       mbar_init(bar(C::kQEmpty + s), 1);
       mbar_init(bar(C::kSFull + s), 1);
-      mbar_init(bar(C::kSFree + s), 128);
-      mbar_init(bar(C::kPReady + s), 128);
+      mbar_init(bar(C::kSFree + s), C::kGroupArrivals);
+      mbar_init(bar(C::kPReady + s), C::kGroupArrivals);
       mbar_init(bar(C::kPvDone + s), 1);
     }
     for (int s = 0; s < C::kKStages; ++s) {
@@ -697,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(C::kVFull + s), 1);
       mbar_init(bar(C::kVEmpty + s), 1);
     }
-    mbar_init(bar(C::kOFree), 128);
+    mbar_init(bar(C::kOFree), C::kGroupArrivals);
     mbar_init(bar(C::kMmaDone + 0), 1);
     mbar_init(bar(C::kMmaDone + 1), 1);
     mbar_init(bar(C::kLmFull), 128);
@@ -709,47 +800,72 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_v);
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(tmem_holder)),
-                 "r"(kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if constexpr (PAIR) {  // one allocation for the pair: the same columns in both CTAs
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32(tmem_holder)),
+                   "r"(kTmemCols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32(tmem_holder)),
+                   "r"(kTmemCols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
   }
   tc_fence_before();
   __syncthreads();
+  // Pair: both CTAs' barriers exist before either CTA's copies or arrivals
+  // reach them.
+  if constexpr (PAIR) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const int beg = p.cta_offsets[blockIdx.x], end = p.cta_offsets[blockIdx.x + 1];
+  const int unit_set = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int beg = p.cta_offsets[unit_set], end = p.cta_offsets[unit_set + 1];
   const WaitCtl wc{abort_flag, p.status, p.wait_limit_ns};
 
   if (warp < 4) {
-    // Producers and MMA issuers: one thread each, few registers.
+    // Producers and MMA issuers: one thread each, few registers (idle in the
+    // pair's rank-1 CTA).
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsMma));
-    if (warp == 0) {
-      if (lane == 0) producer_qk_role<D, F8, V8>(p, &tm_q, &tm_k, sbase, beg, end, wc);
-    } else if (warp == 1) {
-      if (lane == 0) mma_s_role<D, F8, V8>(p, sbase, tmem, beg, end, wc);
-    } else if (warp == 2) {
-      if (lane == 0) producer_v_role<D, F8, V8>(p, &tm_v, sbase, beg, end, wc);
-    } else {
-      if (lane == 0) mma_pv_role<D, F8, V8>(p, sbase, tmem, beg, end, wc);
+    if (rank == 0) {
+      if (warp == 0) {
+        if (lane == 0) producer_qk_role<D, F8, V8, PAIR>(p, &tm_q, &tm_k, sbase, beg, end, wc);
+      } else if (warp == 1) {
+        if (lane == 0) mma_s_role<D, F8, V8, PAIR>(p, sbase, tmem, beg, end, wc);
+      } else if (warp == 2) {
+        if (lane == 0) producer_v_role<D, F8, V8, PAIR>(p, &tm_v, sbase, beg, end, wc);
+      } else {
+        if (lane == 0) mma_pv_role<D, F8, V8, PAIR>(p, sbase, tmem, beg, end, wc);
+      }
     }
     __syncwarp();
   } else if (warp < 8) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
-    softmax_role<D, F8, V8>(p, sbase, sgen, tmem, beg, end, wc);
+    softmax_role<D, F8, V8, PAIR>(p, sbase, sgen, tmem, beg, end, wc);
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
-    epilogue_role<D, F8, V8>(p, sbase, sgen, tmem, beg, end, wc);
+    epilogue_role<D, F8, V8, PAIR>(p, sbase, sgen, tmem, beg, end, wc);
   }
 
   tc_fence_before();
   __syncthreads();
+  // Pair: the rank-0 CTA's products read and write both CTAs' shared and
+  // tensor memory, and its copies land in both; it leaves this barrier only
+  // after its issuers and producers have drained them, and neither CTA
+  // frees TMEM or exits before that.
+  if constexpr (PAIR) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(kTmemCols)
-                 : "memory");
+    if constexpr (PAIR)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                   "r"(kTmemCols)
+                   : "memory");
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                   "r"(kTmemCols)
+                   : "memory");
   }
 }
 
@@ -803,13 +919,14 @@ EncodeTiledFn get_encode_fn() {
 // (d, H, T) view of a [T][H][d] tensor of 2-byte (bf16, fp16) or 1-byte
 // (FP8) elements, boxes of 128 bytes x 1 head x 128 rows with 128-byte
 // swizzle; rows past T read as zeros.
-bool make_map(CUtensorMap* m, const void* base, int H, int T, int D, CUtensorMapDataType dt) {
+bool make_map(CUtensorMap* m, const void* base, int H, int T, int D, CUtensorMapDataType dt,
+              int box_rows = 128) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
   const cuuint64_t eb = dt == CU_TENSOR_MAP_DATA_TYPE_UINT8 ? 1 : 2;
   const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
   const cuuint64_t strides[2] = {(cuuint64_t)D * eb, (cuuint64_t)H * D * eb};
-  const cuuint32_t box[3] = {(cuuint32_t)(128 / eb), 1, 128};
+  const cuuint32_t box[3] = {(cuuint32_t)(128 / eb), 1, (cuuint32_t)box_rows};
   const cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -915,22 +1032,22 @@ pk_status transpose_values(const pk_plan* plan, const void* v8, void* vt, int sm
 
 // v16: the fp16 values (the workspace convert_values has filled), or with V8
 // the transposed E4M3 copy (transpose_values).
-template <int D, bool F8, bool V8>
+template <int D, bool F8, bool V8, bool PAIR = false>
 pk_status launch(const pk_plan* plan, const void* q, const void* k, const void* v16, void* out,
                  float* lse, float scale, cudaStream_t stream, int32_t* dev_status,
                  float v_scale = 1.0f) {
-  using C = pk::dev::Cfg<D, F8, V8>;
+  using C = pk::dev::Cfg<D, F8, V8, PAIR>;
+  auto kernel = pk::dev::pk_attn_fwd_kernel<D, F8, V8, PAIR>;
   CUtensorMap tq, tk, tv;
   const CUtensorMapDataType qk_dt =
       F8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if (!make_map(&tq, q, plan->hq, plan->T, D, qk_dt) ||
-      !make_map(&tk, k, plan->hkv, plan->Tk, D, qk_dt) ||
+      !make_map(&tk, k, plan->hkv, plan->Tk, D, qk_dt, C::kKRows) ||
       !(V8 ? make_map_v8t(&tv, v16, plan->hkv, plan->v8_rows, D)
            : make_map(&tv, v16, plan->hkv, plan->Tk, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)))
     return PK_ERR_CUDA;
-  if (cudaFuncSetAttribute(pk::dev::pk_attn_fwd_kernel<D, F8, V8>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           C::kSmemBytes) != cudaSuccess) {
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+      cudaSuccess) {
     cudaGetLastError();
     return PK_ERR_CUDA;
   }
@@ -940,7 +1057,7 @@ pk_status launch(const pk_plan* plan, const void* q, const void* k, const void* 
   static std::atomic<int> regs_state{0};  // 0 unknown, 1 fits, 2 does not
   if (regs_state.load() == 0) {
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, pk::dev::pk_attn_fwd_kernel<D, F8, V8>) != cudaSuccess) {
+    if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) {
       cudaGetLastError();
       return PK_ERR_CUDA;
     }
@@ -950,8 +1067,10 @@ pk_status launch(const pk_plan* plan, const void* q, const void* k, const void* 
   if (regs_state.load() != 1) return PK_ERR_UNSUPPORTED;
   const uint8_t* img = static_cast<const uint8_t*>(plan->dev);
   pk::dev::KernelParams kp;
-  kp.items = reinterpret_cast<const pk_work_item*>(img + plan->layout.items_off);
-  kp.cta_offsets = reinterpret_cast<const int32_t*>(img + plan->layout.cta_off_off);
+  kp.items = reinterpret_cast<const pk_work_item*>(
+      img + (PAIR ? plan->layout.pitems_off : plan->layout.items_off));
+  kp.cta_offsets = reinterpret_cast<const int32_t*>(
+      img + (PAIR ? plan->layout.pcta_off_off : plan->layout.cta_off_off));
   kp.kv_limit = reinterpret_cast<const int32_t*>(img + plan->layout.kvlim_off);
   kp.block_table =
       plan->paged ? reinterpret_cast<const int32_t*>(img + plan->layout.table_off) : nullptr;
@@ -965,8 +1084,27 @@ pk_status launch(const pk_plan* plan, const void* q, const void* k, const void* 
   kp.scale_log2 = scale * 1.4426950408889634f;
   kp.v_scale = v_scale;
   kp.wait_limit_ns = g_wait_limit_ns.load();
-  pk::dev::pk_attn_fwd_kernel<D, F8, V8>
-      <<<plan->num_ctas, pk::dev::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, kp);
+  if constexpr (PAIR) {
+    // clusters of two CTAs on SM pairs
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2u * (unsigned)plan->num_clusters);
+    cfg.blockDim = dim3(pk::dev::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kernel, tq, tk, tv, kp) != cudaSuccess) {
+      cudaGetLastError();
+      return PK_ERR_CUDA;
+    }
+    return PK_OK;
+  }
+  kernel<<<plan->num_ctas, pk::dev::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, kp);
   if (cudaGetLastError() != cudaSuccess) return PK_ERR_CUDA;
   return PK_OK;
 }
@@ -1050,7 +1188,11 @@ pk_status pk_attn_fwd_converted(const pk_plan* plan, const void* q, const void* 
     return st;
   if ((st = check_device()) != PK_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (plan->head_dim == 128) return launch<128, false, false>(plan, q, k, v16, out, lse, scale, s, dev_status);
+  if (plan->head_dim == 128) {
+    if (plan->use_pairs && plan->num_clusters > 0)  // pk_plan_set_sm_pairs
+      return launch<128, false, false, true>(plan, q, k, v16, out, lse, scale, s, dev_status);
+    return launch<128, false, false>(plan, q, k, v16, out, lse, scale, s, dev_status);
+  }
   if (plan->head_dim == 64) return launch<64, false, false>(plan, q, k, v16, out, lse, scale, s, dev_status);
   return PK_ERR_UNSUPPORTED;
 }

@@ -23,6 +23,8 @@ struct PlanImageLayout {
   size_t kvlim_off = 0;    // int32[Tq]: last visible key index of the row's key range, -1 none
   size_t table_off = 0;    // int32[num_seqs * blocks_per_seq] when keys are paged
   size_t vblk_off = 0;     // int32[v_blocks.size()]: (pool block, valid rows) the kernel reads
+  size_t pitems_off = 0;   // pk_work_item[2 * num_pairs]: SM-pair items, cluster-ordered
+  size_t pcta_off_off = 0; // int32[num_clusters + 1]
   size_t v8chunk_off = 0;  // int32[v8_chunks.size()]: the E4M3 value transpose's chunks
   size_t v8row_off = 0;    // int32[num_items] (contiguous keys): row of an item's first
                            // key tile in the transposed E4M3 value copy
@@ -68,6 +70,17 @@ struct pk_plan {
   std::vector<int32_t> v8_seq_row;  // contiguous keys: [num_seqs]
   std::vector<pk_work_item> items;         // CTA-ordered
   std::vector<int32_t> cta_offsets;        // [num_ctas + 1]
+  // The same work for SM pairs (head_dim 128, bf16 queries and keys): two
+  // items that read the same key/value tiles (same first key row, key/value
+  // head and query heads) become one pair, run by a cluster of two CTAs as
+  // M = 256 products; the pair visits the larger key-tile count (the other
+  // rows see the extra tiles fully masked).  Stored as consecutive (rank 0,
+  // rank 1) items; a pair without a partner gets a rank-1 item with no rows.
+  // Scheduled longest first over num_clusters = num_ctas / 2 clusters.
+  int32_t num_clusters = 0;
+  bool use_pairs = false;                  // pk_plan_set_sm_pairs
+  std::vector<pk_work_item> pair_items;    // [2 * num_pairs], cluster-ordered
+  std::vector<int32_t> pair_cta_offsets;   // [num_clusters + 1], in pairs
   pk::PlanImageLayout layout;
   std::vector<uint8_t> image;              // host copy of the device image
   void* dev = nullptr;                     // caller's buffer after upload

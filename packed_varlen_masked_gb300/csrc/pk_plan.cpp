@@ -23,6 +23,8 @@
 #include <new>
 #include <numeric>
 #include <queue>
+#include <map>
+#include <array>
 #include <vector>
 
 #include <cuda_runtime_api.h>
@@ -122,8 +124,79 @@ pk_status resolve_num_ctas(int32_t* num_ctas) {
   return PK_OK;
 }
 
-// Longest-processing-time-first schedule of `items` over `num_ctas` CTAs,
-// then the plan's device image.
+// SM-pair items (see pk_plan::pair_items): the items that read the same key
+// and value tiles form a group; within it, ordered by key-tile count (then
+// first row), neighbours pair up, so a pair's two tiles visit about as many
+// key tiles (a text tile that sees one key tile is not paired with an image
+// tile that sees the whole segment).  The pairs, in the order of their
+// groups' first items, are scheduled longest first over `clusters` clusters.
+void schedule_pairs(pk_plan* p, const std::vector<pk_work_item>& items, int32_t clusters) {
+  p->pair_items.clear();
+  p->pair_cta_offsets.clear();
+  p->num_clusters = 0;
+  if (p->head_dim != 128 || clusters < 1 || items.empty()) return;
+  using Key = std::array<int32_t, 4>;
+  std::map<Key, int32_t> group_of;
+  std::vector<std::vector<pk_work_item>> groups;
+  for (const pk_work_item& w : items) {
+    const Key k{w.kv_start, w.hkv, w.hq0, w.hq1};
+    auto it = group_of.find(k);
+    if (it == group_of.end()) {
+      group_of[k] = static_cast<int32_t>(groups.size());
+      groups.push_back({w});
+    } else {
+      groups[it->second].push_back(w);
+    }
+  }
+  std::vector<std::array<pk_work_item, 2>> pairs;
+  for (std::vector<pk_work_item>& g : groups) {
+    std::stable_sort(g.begin(), g.end(), [](const pk_work_item& a, const pk_work_item& b) {
+      return a.n_kt != b.n_kt ? a.n_kt < b.n_kt : a.q_start < b.q_start;
+    });
+    for (size_t i = 0; i < g.size(); i += 2) {
+      std::array<pk_work_item, 2> pr{g[i], g[i]};
+      if (i + 1 < g.size()) {
+        pr[1] = g[i + 1];
+        pr[0].n_kt = pr[1].n_kt = std::max(g[i].n_kt, g[i + 1].n_kt);
+        pr[0].n_full = pr[1].n_full = std::min(g[i].n_full, g[i + 1].n_full);
+      } else {
+        pr[1].q_rows = 0;  // no partner: no rows (its loads read the leader's rows)
+      }
+      pairs.push_back(pr);
+    }
+  }
+  const int32_t n_pairs = static_cast<int32_t>(pairs.size());
+  const int32_t grid = std::min<int32_t>(clusters, n_pairs);
+  p->num_clusters = grid;
+  std::vector<int32_t> order(n_pairs);
+  std::iota(order.begin(), order.end(), 0);
+  std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b2) {
+    return item_cost(pairs[a][0]) > item_cost(pairs[b2][0]);
+  });
+  std::vector<std::vector<int32_t>> per(grid);
+  using Load = std::pair<double, int32_t>;
+  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+  for (int32_t c = 0; c < grid; ++c) heap.push({0.0, c});
+  for (int32_t idx : order) {
+    Load l = heap.top();
+    heap.pop();
+    per[l.second].push_back(idx);
+    l.first += item_cost(pairs[idx][0]);
+    heap.push(l);
+  }
+  p->pair_cta_offsets.assign(grid + 1, 0);
+  p->pair_items.reserve(2 * static_cast<size_t>(n_pairs));
+  for (int32_t c = 0; c < grid; ++c) {
+    for (int32_t idx : per[c]) {
+      p->pair_items.push_back(pairs[idx][0]);
+      p->pair_items.push_back(pairs[idx][1]);
+    }
+    p->pair_cta_offsets[c + 1] = static_cast<int32_t>(p->pair_items.size() / 2);
+  }
+}
+
+// Longest-processing-time-first schedule of `items` over `num_ctas` CTAs
+// (and over num_ctas / 2 SM pairs), then the plan's device image.
 void schedule_and_image(pk_plan* p, std::vector<pk_work_item> items, int32_t num_ctas) {
   const int32_t Tq = p->T;
   // The plan's own work: tiles visited and useful FLOPs (4 d per visible
@@ -166,6 +239,7 @@ void schedule_and_image(pk_plan* p, std::vector<pk_work_item> items, int32_t num
     for (int32_t idx : per_cta[c]) p->items.push_back(items[idx]);
     p->cta_offsets[c + 1] = static_cast<int32_t>(p->items.size());
   }
+  schedule_pairs(p, items, num_ctas / 2);
 
   // Device image.
   pk::PlanImageLayout& IL = p->layout;
@@ -174,7 +248,11 @@ void schedule_and_image(pk_plan* p, std::vector<pk_work_item> items, int32_t num
   IL.kvlim_off = align_up(IL.cta_off_off + sizeof(int32_t) * (grid + 1), pk::kImageAlign);
   IL.table_off = align_up(IL.kvlim_off + sizeof(int32_t) * static_cast<size_t>(Tq), pk::kImageAlign);
   IL.vblk_off = align_up(IL.table_off + sizeof(int32_t) * p->block_table.size(), pk::kImageAlign);
-  IL.v8chunk_off = align_up(IL.vblk_off + sizeof(int32_t) * p->v_blocks.size(), pk::kImageAlign);
+  IL.pitems_off = align_up(IL.vblk_off + sizeof(int32_t) * p->v_blocks.size(), pk::kImageAlign);
+  IL.pcta_off_off =
+      align_up(IL.pitems_off + sizeof(pk_work_item) * p->pair_items.size(), pk::kImageAlign);
+  IL.v8chunk_off = align_up(IL.pcta_off_off + sizeof(int32_t) * p->pair_cta_offsets.size(),
+                            pk::kImageAlign);
   IL.v8row_off = align_up(IL.v8chunk_off + sizeof(int32_t) * p->v8_chunks.size(), pk::kImageAlign);
   // Contiguous keys: an item's key tiles sit in the E4M3 value copy at the
   // copy row of its sequence (the last sequence whose keys start at the
@@ -201,6 +279,12 @@ void schedule_and_image(pk_plan* p, std::vector<pk_work_item> items, int32_t num
   if (!p->v_blocks.empty())
     std::memcpy(p->image.data() + IL.vblk_off, p->v_blocks.data(),
                 sizeof(int32_t) * p->v_blocks.size());
+  if (!p->pair_items.empty()) {
+    std::memcpy(p->image.data() + IL.pitems_off, p->pair_items.data(),
+                sizeof(pk_work_item) * p->pair_items.size());
+    std::memcpy(p->image.data() + IL.pcta_off_off, p->pair_cta_offsets.data(),
+                sizeof(int32_t) * p->pair_cta_offsets.size());
+  }
   if (!p->v8_chunks.empty())
     std::memcpy(p->image.data() + IL.v8chunk_off, p->v8_chunks.data(),
                 sizeof(int32_t) * p->v8_chunks.size());
@@ -566,6 +650,31 @@ pk_status pk_plan_get_info(const pk_plan* p, pk_plan_info* info) {
 pk_status pk_plan_get_kv_limit(const pk_plan* p, int32_t* out, int64_t n) {
   if (p == nullptr || (out == nullptr && p->T > 0) || n < p->T) return PK_ERR_INVALID_ARG;
   if (p->T) std::memcpy(out, p->kv_limit.data(), sizeof(int32_t) * p->T);
+  return PK_OK;
+}
+
+pk_status pk_plan_set_sm_pairs(pk_plan* p, int32_t enable) {
+  if (p == nullptr) return PK_ERR_INVALID_ARG;
+  if (enable && p->num_clusters == 0) return PK_ERR_UNSUPPORTED;
+  p->use_pairs = enable != 0;
+  return PK_OK;
+}
+
+pk_status pk_plan_get_pairs(const pk_plan* p, int32_t* num_pairs, int32_t* num_clusters,
+                            pk_work_item* items, int64_t n_items, int32_t* cluster_offsets,
+                            int64_t n_offsets) {
+  if (p == nullptr || num_pairs == nullptr || num_clusters == nullptr) return PK_ERR_INVALID_ARG;
+  const int64_t ni = static_cast<int64_t>(p->pair_items.size());
+  *num_pairs = static_cast<int32_t>(ni / 2);
+  *num_clusters = p->num_clusters;
+  if (items == nullptr && cluster_offsets == nullptr) return PK_OK;
+  if (items == nullptr || cluster_offsets == nullptr || n_items < ni ||
+      n_offsets < static_cast<int64_t>(p->pair_cta_offsets.size()))
+    return PK_ERR_INVALID_ARG;
+  if (ni) std::memcpy(items, p->pair_items.data(), sizeof(pk_work_item) * ni);
+  if (!p->pair_cta_offsets.empty())
+    std::memcpy(cluster_offsets, p->pair_cta_offsets.data(),
+                sizeof(int32_t) * p->pair_cta_offsets.size());
   return PK_OK;
 }
 

@@ -23,33 +23,57 @@ import pytest
 
 
 class _Bar:
-    def __init__(self, name):
-        self.name, self.c = name, 0  # c: completed phases (count 1: one arrival each)
+    def __init__(self, name, count=1):
+        self.name, self.c = name, 0  # c: completed phases
+        self.count, self.pending = count, 0
 
     def arrive(self):
-        self.c += 1
+        self.pending += 1
+        if self.pending == self.count:
+            self.pending = 0
+            self.c += 1
 
 
-def _run(units, kst, vst, seed, rare, handover_wait=True, abort_at=None):
+def _run(units, kst, vst, seed, rare, handover_wait=True, abort_at=None, pair=False):
     """abort_at: None, or the probability per scheduler round that the abort
-    flag is raised (a wait timing out)."""
+    flag is raised (a wait timing out).  pair: the SM-pair kernel, whose
+    rank-0 CTA loads and issues for both CTAs: its commits of S and P V reach
+    both CTAs' barriers (@0, @1), each CTA's softmax and epilogue wait on
+    their own CTA's barriers, and the S-free, P-ready and O-free barriers (on
+    rank 0) take one arrival from each CTA's warpgroup."""
     rng = random.Random(seed)
+    ranks = (0, 1) if pair else (0,)
+    groups = len(ranks)
     B = {}
+
+    def loc(nm, r):  # a barrier each CTA has its own copy of
+        return f"{nm}@{r}" if pair else nm
+
     for i in range(2):
-        for nm in ("QFull", "QEmpty", "SFull", "SFree", "PReady", "PvDone", "MmaDone"):
+        for nm in ("QFull", "QEmpty", "MmaDone"):
             B[f"{nm}{i}"] = _Bar(f"{nm}{i}")
+        for nm in ("SFree", "PReady"):
+            B[f"{nm}{i}"] = _Bar(f"{nm}{i}", groups)
+        for nm in ("SFull", "PvDone"):
+            for r in ranks:
+                B[loc(f"{nm}{i}", r)] = _Bar(loc(f"{nm}{i}", r))
     for i in range(kst):
         B[f"KFull{i}"], B[f"KEmpty{i}"] = _Bar("KFull"), _Bar("KEmpty")
     for i in range(vst):
         B[f"VFull{i}"], B[f"VEmpty{i}"] = _Bar("VFull"), _Bar("VEmpty")
-    for nm in ("OFree", "LmFull", "LmFree"):
-        B[nm] = _Bar(nm)
+    B["OFree"] = _Bar("OFree", groups)
+    for r in ranks:
+        for nm in ("LmFull", "LmFree"):
+            B[loc(nm, r)] = _Bar(loc(nm, r))
     pipe = []      # MMA commits, completed in order
     copies = []    # TMA copies in flight, completed in any order
     state = {"abort": False}
 
-    def pv_done(t):  # the P-V-done barrier of tile t (two, alternating) and its phase
-        return (f"PvDone{t & 1}", (t >> 1) & 1, t >> 1)
+    def pv_done(t, r=0):  # the P-V-done barrier of tile t (two, alternating) and its phase
+        return (loc(f"PvDone{t & 1}", r), (t >> 1) & 1, t >> 1)
+
+    def everywhere(nm):  # a commit multicast to both CTAs' copies
+        return [loc(nm, r) for r in ranks]
 
     def W(n, par, k):  # bounded wait for phase k of n (parity par); gives up on abort
         return ("wait", n, par, k)
@@ -122,7 +146,8 @@ def _run(units, kst, vst, seed, rare, handover_wait=True, abort_at=None):
                     ok = yield W(f"SFree{b}", ((t >> 1) - 1) & 1, (t >> 1) - 1)
                 if not ok:
                     break
-                yield ("mma", [f"SFull{b}", f"KEmpty{k}"] + ([f"QEmpty{qb}"] if j + 1 == n else []))
+                yield ("mma", everywhere(f"SFull{b}") + [f"KEmpty{k}"] +
+                       ([f"QEmpty{qb}"] if j + 1 == n else []))
                 t += 1
             if not ok:
                 break
@@ -142,49 +167,51 @@ def _run(units, kst, vst, seed, rare, handover_wait=True, abort_at=None):
                     ok = yield W("OFree", (u & 1) ^ 1, u - 1)
                 if not ok:
                     break
-                yield ("mma", [pv_done(t)[0], f"VEmpty{v}"])
+                yield ("mma", everywhere(f"PvDone{t & 1}") + [f"VEmpty{v}"])
                 t += 1
             if not ok:
                 break
         yield ("mma", ["MmaDone1"])
         yield D("MmaDone1", 0, 0)
 
-    def softmax():
+    def softmax(r):
         t = 0
         for u, n in enumerate(units):
             for j in range(n):
                 b = t & 1
-                if not (yield W(f"SFull{b}", (t >> 1) & 1, t >> 1)):
+                if not (yield W(loc(f"SFull{b}", r), (t >> 1) & 1, t >> 1)):
                     return
                 yield A(f"SFree{b}")
                 if j > 0 and rng.random() < rare:  # rescale O after P(t-1) V(t-1)
-                    if not (yield W(*pv_done(t - 1))):
+                    if not (yield W(*pv_done(t - 1, r))):
                         return
                 if t >= 2:  # P buffer b free: P(t-2) V(t-2) done
-                    if not (yield W(*pv_done(t - 2))):
+                    if not (yield W(*pv_done(t - 2, r))):
                         return
                 yield A(f"PReady{b}")
                 t += 1
             if u > 0:
-                if not (yield W("LmFree", (u - 1) & 1, u - 1)):
+                if not (yield W(loc("LmFree", r), (u - 1) & 1, u - 1)):
                     return
-            yield A("LmFull")
+            yield A(loc("LmFull", r))
 
-    def epilogue():
+    def epilogue(r):
         t = 0
         for u, n in enumerate(units):
             t += n
             tl = t - 1
             if handover_wait:
-                if not (yield W("LmFull", u & 1, u)):
+                if not (yield W(loc("LmFull", r), u & 1, u)):
                     return
-            yield A("LmFree")
-            if not (yield W(*pv_done(tl))):
+            yield A(loc("LmFree", r))
+            if not (yield W(*pv_done(tl, r))):
                 return
             yield A("OFree")
 
-    roles = {"qk": producer_qk(), "v": producer_v(), "s": mma_s(), "pv": mma_pv(),
-             "softmax": softmax(), "epilogue": epilogue()}
+    roles = {"qk": producer_qk(), "v": producer_v(), "s": mma_s(), "pv": mma_pv()}
+    for r in ranks:
+        roles[f"softmax{r}"] = softmax(r)
+        roles[f"epilogue{r}"] = epilogue(r)
     cur = {k: None for k in roles}
     done = set()
 
@@ -310,3 +337,22 @@ def test_model_catches_a_skipped_phase():
             assert "passed early" in str(e) or "aliased" in str(e) or "deadlock" in str(e)
             caught += 1
     assert caught >= 30
+
+
+@pytest.mark.parametrize("kst,vst", [(7, 3), (5, 5)])  # SM-pair rings (16 KB halves)
+def test_pair_kernel_barrier_protocol(kst, vst):
+    for seed in range(150):
+        rng = random.Random(5000 + 10 * kst + vst + seed)
+        units = [rng.choice([1, 1, 2, 3, 4, 5, 9, 17]) for _ in range(rng.randint(1, 16))]
+        _run(units, kst, vst, seed, rare=rng.choice([0.0, 0.1, 1.0]), pair=True)
+
+
+@pytest.mark.parametrize("kst,vst", [(7, 3)])
+def test_pair_kernel_abort_path_drains_every_copy_and_mma(kst, vst):
+    aborted = 0
+    for seed in range(300):
+        rng = random.Random(9 + 10 * kst + vst + seed)
+        units = [rng.choice([1, 2, 3, 5, 9, 17]) for _ in range(rng.randint(1, 12))]
+        aborted += _run(units, kst, vst, seed, rare=rng.choice([0.0, 0.1, 1.0]),
+                        abort_at=rng.choice([0.001, 0.01, 0.1, 0.5]), pair=True)
+    assert aborted >= 150
