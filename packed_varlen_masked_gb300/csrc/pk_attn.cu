@@ -9,8 +9,10 @@
 // list of 128-row query tiles, each visiting a prefix of 128-key tiles that
 // are either fully visible (no mask math) or partial (per-element compare).
 // Queries and keys are bf16, or FP8 E4M3 (F8: S = Q K^T on kind::f8f6f4,
-// one dequantisation scale each folded into the softmax scale); values, P
-// and the output are bf16 in both.
+// one dequantisation scale each folded into the softmax scale).  Values and
+// P enter the P V product in fp16 (the values converted from bf16 by a
+// kernel before the launch), or, with V8, both in E4M3 (the values
+// transposed by a kernel before the launch).  The output is bf16.
 //
 // Kernel organisation (one persistent CTA per SM, 12 warps).  The CTA runs
 // its work items' query heads ("units") one after another; a unit is a
@@ -27,14 +29,20 @@
 //               issuers in different warps work concurrently.
 //   warps 4-7   softmax: thread r owns row r of S, P and O in TMEM.  Online
 //               softmax in base 2 with a lazily moved running maximum, P
-//               written as bf16 pairs; at the end of a unit it hands the
+//               written as fp16 pairs; at the end of a unit it hands the
 //               row's (m, l) to the epilogue and goes on to the next unit.
 //   warps 8-11  epilogue: after a unit's last P V, moves O out of TMEM
-//               (freeing it for the next unit), writes O / l as bf16 and
-//               the natural-log LSE.
+//               (freeing it for the next unit), writes O / l as bf16 (whole
+//               128-byte row segments per warp store) and the natural-log
+//               LSE.
 // Registers: the one-thread roles give theirs up (setmaxnreg) to the
 // softmax, whose exponential loop keeps a whole 128-column row of scores
-// and its 64 bf16 pairs live, and to the epilogue, which holds a row of O.
+// and its 64 fp16 pairs live, and to the epilogue, which holds a row of O.
+// PAIR (opt-in, bf16 with D = 128): a cluster of two CTAs on an SM pair
+// computes two query tiles as M = 256 products (tcgen05 cta_group::2); the
+// rank-0 CTA's producers and issuers serve both, each CTA holding half of
+// every key and value tile, and both CTAs run their rows' softmax and
+// epilogue.
 // TMEM columns: S double buffer [0,256), P double buffer [256,384), O
 // [384,384+D).  Because S(t) and P(t) live in different columns and both are
 // double buffered, the S issuer computes S(t+2) as soon as the softmax has
