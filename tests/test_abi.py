@@ -39,7 +39,7 @@ def test_binding_covers_every_declared_symbol():
 
 def test_status_strings():
     lib = pk.load()
-    for code in range(10):
+    for code in range(11):
         assert lib.pk_status_string(code).decode() != "unknown status"
     assert lib.pk_status_string(pk.PK_ERR_TIMEOUT).decode() == "device wait timed out"
 
