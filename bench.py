@@ -553,6 +553,8 @@ def main():
                     help="under torchrun, split the one pack across the ranks (pk_plan_shard: "
                          "whole (sequence, kv head) units per rank, no exchange; strong scaling) "
                          "instead of running one replica per rank")
+    ap.add_argument("--sm-pairs", action="store_true",
+                    help="run the step on the opt-in SM-pair kernel (pk_plan_set_sm_pairs)")
     ap.add_argument("--requests", type=int, default=8,
                     help="requests in the mixed-resolution pack (x2 CFG branches)")
     args = ap.parse_args()
@@ -587,6 +589,8 @@ def main():
     full_plan = plan
     if split:  # this rank's share of the one pack, on the full tensors
         plan = full_plan.shard(rank, world, device=dev)
+    if args.sm_pairs:
+        plan.set_sm_pairs(True)
     out = torch.empty_like(q)
     lse = torch.empty(pack.hq, pack.total_tokens, dtype=torch.float32, device=dev)
     ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
@@ -723,7 +727,7 @@ def main():
     avg_conv_ms = statistics.mean(conv_ms)
     conv_bytes = 2 * plan.workspace_bytes  # read bf16 v, write fp16 v
     conv_gbs = conv_bytes / (avg_conv_ms * 1e-3) / 1e9
-    traffic = load_traffic()
+    traffic = None if args.sm_pairs else load_traffic()  # the capture is of the one-CTA kernel
     info = plan.info
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -743,7 +747,9 @@ def main():
                      "frac_of_sustained": (round(achieved / peaks["bf16_tflops_sustained"], 4)
                                            if peaks.get("bf16_tflops_sustained") else None),
                      "peak_source": peaks["source"] + " (bf16 burst)",
-                     "kernel": "pk_attn_fwd_kernel<128>", "launch_ms_mean": round(avg_launch_ms, 4),
+                     "kernel": ("pk_attn_fwd_kernel<128> on SM pairs" if args.sm_pairs
+                                else "pk_attn_fwd_kernel<128>"),
+                     "launch_ms_mean": round(avg_launch_ms, 4),
                      "launch_ms_median": round(statistics.median(launch_ms), 4),
                      "launch_ms_min": round(min(launch_ms), 4)},
         "value_conversion": {"kernel": "pk_v_to_f16_kernel", "bound": "hbm",
