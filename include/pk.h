@@ -194,10 +194,10 @@ pk_status pk_plan_shard(const pk_plan* full, int32_t rank, int32_t num_ranks, in
  * its two query tiles as M = 256 tensor-core products (tcgen05 cta_group::2),
  * each SM holding half of every key and value tile, so each SM copies half
  * the key/value bytes per tile.  Results are bit-identical to the one-CTA
- * kernel.  The plan pairs items that read the same key/value tiles (same
- * first key row, key/value head and query heads) by their key-tile count;
- * a pair visits the larger count (the other rows see the extra tiles fully
- * masked).  Measured on GB300: faster on packs of long sequences (+3 to +4%
+ * kernel.  The plan pairs, one query head at a time, query tiles that
+ * read the same key/value tiles (same first key row, key/value head and
+ * query head) by their key-tile count; a pair visits the larger count (the
+ * other rows see the extra tiles fully masked).  Measured on GB300: faster on packs of long sequences (+3 to +4%
  * on the two 24,832-token sequences of the high-res edit pack), slower on
  * packs of short ones (-2% on the mixed-resolution pack, -6 to -15% on the
  * CFG pair), so it is off by default.  The pages have no counterpart; it is

@@ -70,13 +70,14 @@ struct pk_plan {
   std::vector<int32_t> v8_seq_row;  // contiguous keys: [num_seqs]
   std::vector<pk_work_item> items;         // CTA-ordered
   std::vector<int32_t> cta_offsets;        // [num_ctas + 1]
-  // The same work for SM pairs (head_dim 128, bf16 queries and keys): two
-  // items that read the same key/value tiles (same first key row, key/value
-  // head and query heads) become one pair, run by a cluster of two CTAs as
-  // M = 256 products; the pair visits the larger key-tile count (the other
-  // rows see the extra tiles fully masked).  Stored as consecutive (rank 0,
-  // rank 1) items; a pair without a partner gets a rank-1 item with no rows.
-  // Scheduled longest first over num_clusters = num_ctas / 2 clusters.
+  // The same work for SM pairs (head_dim 128, bf16 queries and keys): one
+  // query head of two query tiles that read the same key/value tiles (same
+  // first key row, key/value head and query head) per pair, run by a cluster
+  // of two CTAs as M = 256 products; the pair visits the larger key-tile
+  // count (the other rows see the extra tiles fully masked).  Stored as
+  // consecutive (rank 0, rank 1) items with hq1 = -1; a pair without a
+  // partner gets a rank-1 item with no rows.  Scheduled longest first over
+  // num_clusters = num_ctas / 2 clusters.
   int32_t num_clusters = 0;
   bool use_pairs = false;                  // pk_plan_set_sm_pairs
   std::vector<pk_work_item> pair_items;    // [2 * num_pairs], cluster-ordered

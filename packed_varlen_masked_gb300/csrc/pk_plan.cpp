@@ -124,12 +124,15 @@ pk_status resolve_num_ctas(int32_t* num_ctas) {
   return PK_OK;
 }
 
-// SM-pair items (see pk_plan::pair_items): the items that read the same key
-// and value tiles form a group; within it, ordered by key-tile count (then
-// first row), neighbours pair up, so a pair's two tiles visit about as many
-// key tiles (a text tile that sees one key tile is not paired with an image
-// tile that sees the whole segment).  The pairs, in the order of their
-// groups' first items, are scheduled longest first over `clusters` clusters.
+// SM-pair items (see pk_plan::pair_items): each item's query heads are
+// taken one at a time (a pair item is one head of two query tiles, the work
+// of one two-head item, so the 76 clusters get as fine a schedule as the
+// 152 CTAs), and the one-head items that read the same key and value tiles
+// form a group; within it, ordered by key-tile count (then first row),
+// neighbours pair up, so a pair's two tiles visit about as many key tiles (a
+// text tile that sees one key tile is not paired with an image tile that
+// sees the whole segment).  The pairs, in the order of their groups' first
+// items, are scheduled longest first over `clusters` clusters.
 void schedule_pairs(pk_plan* p, const std::vector<pk_work_item>& items, int32_t clusters) {
   p->pair_items.clear();
   p->pair_cta_offsets.clear();
@@ -138,14 +141,20 @@ void schedule_pairs(pk_plan* p, const std::vector<pk_work_item>& items, int32_t 
   using Key = std::array<int32_t, 4>;
   std::map<Key, int32_t> group_of;
   std::vector<std::vector<pk_work_item>> groups;
-  for (const pk_work_item& w : items) {
-    const Key k{w.kv_start, w.hkv, w.hq0, w.hq1};
-    auto it = group_of.find(k);
-    if (it == group_of.end()) {
-      group_of[k] = static_cast<int32_t>(groups.size());
-      groups.push_back({w});
-    } else {
-      groups[it->second].push_back(w);
+  for (const pk_work_item& w0 : items) {
+    for (int hs = 0; hs < 2; ++hs) {  // one query head per pair item (finer schedule)
+      if (hs == 1 && w0.hq1 < 0) break;
+      pk_work_item w = w0;
+      w.hq0 = hs ? w0.hq1 : w0.hq0;
+      w.hq1 = -1;
+      const Key k{w.kv_start, w.hkv, w.hq0, w.hq1};
+      auto it = group_of.find(k);
+      if (it == group_of.end()) {
+        group_of[k] = static_cast<int32_t>(groups.size());
+        groups.push_back({w});
+      } else {
+        groups[it->second].push_back(w);
+      }
     }
   }
   std::vector<std::array<pk_work_item, 2>> pairs;

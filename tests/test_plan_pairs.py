@@ -1,5 +1,5 @@
 """The SM-pair schedule (pk_plan_set_sm_pairs), checked on the host: every
-work item appears once as a rank of a pair, partners read the same key and
+work item's query heads appear once each as a rank of a pair, partners read the same key and
 value tiles, a pair visits the larger key-tile count and masks by the
 smaller full-tile count, items pair with their neighbours by key-tile count,
 and the clusters' offsets cover the pairs."""
@@ -33,9 +33,23 @@ def _key(it):
     return (int(it[KV]), int(it[HK]), int(it[H0]), int(it[H1]))
 
 
+def _one_head_items(items):
+    """The plan's items taken one query head at a time, as the pair schedule
+    takes them."""
+    out = []
+    for it in items:
+        for h in (it[H0], it[H1]):
+            if h < 0:
+                continue
+            x = it.copy()
+            x[H0], x[H1] = h, -1
+            out.append(x)
+    return np.array(out, dtype=np.int32).reshape(-1, 8)
+
+
 @pytest.mark.parametrize("name,plan", _plans(), ids=lambda x: x if isinstance(x, str) else "")
 def test_pairs_cover_every_item_once(name, plan):
-    items, offs = plan.items()
+    items = _one_head_items(plan.items()[0])
     pitems, poffs = plan.pairs()
     npairs = pitems.shape[0] // 2
     assert npairs > 0
@@ -49,7 +63,7 @@ def test_pairs_cover_every_item_once(name, plan):
         by_key[_key(it)].append(it)
     for i in range(npairs):
         a, b = pitems[2 * i], pitems[2 * i + 1]
-        assert _key(a) == _key(b)
+        assert _key(a) == _key(b) and a[H1] == -1
         assert a[NKT] == b[NKT] and a[NF] == b[NF]
         assert a[QR] > 0
         for r in (a, b):
@@ -74,7 +88,7 @@ def test_pairs_cover_every_item_once(name, plan):
 def test_pairing_by_key_tile_count_keeps_the_masked_waste_small(name, plan):
     """Neighbours by key-tile count: the extra (fully masked) tiles a pair
     visits are those of sorted neighbours, a few percent of the work."""
-    items, _ = plan.items()
+    items = _one_head_items(plan.items()[0])
     pitems, _ = plan.pairs()
     by_key = defaultdict(list)
     for it in items:
@@ -122,10 +136,10 @@ def test_shards_have_pair_schedules_of_their_own_items():
     total = 0
     for r in range(3):
         sh = full.shard(r, 3, num_ctas=152, upload=False)
-        items, _ = sh.items()
+        items = _one_head_items(sh.items()[0])
         pitems, _ = sh.pairs()
         rows = {(int(it[Q0]), int(it[H0])) for it in items}
         prow = {(int(it[Q0]), int(it[H0])) for it in pitems if it[QR] > 0}
         assert rows == prow
         total += items.shape[0]
-    assert total == full.items()[0].shape[0]
+    assert total == _one_head_items(full.items()[0]).shape[0]
