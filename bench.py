@@ -528,6 +528,21 @@ def sweep(pk, torch, stream, dev):
             ms2 = timed(pair)
             res[name]["sm_pairs"] = {"ms": round(ms2, 4), "useful_tflops": round(fl / ms2 / 1e9, 1)}
             del pair
+            # FP8 E4M3 queries and keys (per-tensor scales) on the same inputs
+            q8, qs = W.quantize_e4m3(q)
+            k8, ks = W.quantize_e4m3(k)
+            for _ in range(3):
+                pk.attn_fwd_fp8(q8, qs, k8, ks, v, plan, pack.scale, out=out, lse=lse, workspace=ws)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            torch.cuda.synchronize()
+            ev[0].record(stream)
+            for _ in range(10):
+                pk.attn_fwd_fp8(q8, qs, k8, ks, v, plan, pack.scale, out=out, lse=lse, workspace=ws)
+            ev[1].record(stream)
+            torch.cuda.synchronize()
+            ms3 = ev[0].elapsed_time(ev[1]) / 10
+            res[name]["fp8_qk"] = {"ms": round(ms3, 4), "useful_tflops": round(fl / ms3 / 1e9, 1)}
+            del q8, k8
         del q, k, v, out, lse, plan, ws
         torch.cuda.empty_cache()
     return res
