@@ -528,6 +528,13 @@ def sweep(pk, torch, stream, dev):
             ms2 = timed(pair)
             res[name]["sm_pairs"] = {"ms": round(ms2, 4), "useful_tflops": round(fl / ms2 / 1e9, 1)}
             del pair
+            if plan.share_schedule()[0].shape[0] > 0:  # the one-CTA kernel (no K/V sharing)
+                one = pk.plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d,
+                              device=dev).set_kv_share(False)
+                ms4 = timed(one)
+                res[name]["one_cta"] = {"ms": round(ms4, 4),
+                                        "useful_tflops": round(fl / ms4 / 1e9, 1)}
+                del one
             # FP8 E4M3 queries and keys (per-tensor scales) on the same inputs
             q8, qs = W.quantize_e4m3(q)
             k8, ks = W.quantize_e4m3(k)
@@ -568,6 +575,8 @@ def main():
                     help="under torchrun, split the one pack across the ranks (pk_plan_shard: "
                          "whole (sequence, kv head) units per rank, no exchange; strong scaling) "
                          "instead of running one replica per rank")
+    ap.add_argument("--one-cta", action="store_true",
+                    help="run the step on the one-CTA kernel (pk_plan_set_kv_share off)")
     ap.add_argument("--sm-pairs", action="store_true",
                     help="run the step on the opt-in SM-pair kernel (pk_plan_set_sm_pairs)")
     ap.add_argument("--requests", type=int, default=8,
@@ -606,6 +615,9 @@ def main():
         plan = full_plan.shard(rank, world, device=dev)
     if args.sm_pairs:
         plan.set_sm_pairs(True)
+    elif args.one_cta and plan.share_schedule()[0].shape[0] > 0:
+        plan.set_kv_share(False)
+    shared_kv = not args.sm_pairs and not args.one_cta and plan.share_schedule()[0].shape[0] > 0
     out = torch.empty_like(q)
     lse = torch.empty(pack.hq, pack.total_tokens, dtype=torch.float32, device=dev)
     ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
@@ -742,7 +754,8 @@ def main():
     avg_conv_ms = statistics.mean(conv_ms)
     conv_bytes = 2 * plan.workspace_bytes  # read bf16 v, write fp16 v
     conv_gbs = conv_bytes / (avg_conv_ms * 1e-3) / 1e9
-    traffic = None if args.sm_pairs else load_traffic()  # the capture is of the one-CTA kernel
+    # the committed capture is of the default kernel (head-pair clusters)
+    traffic = load_traffic() if shared_kv else None
     info = plan.info
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -763,7 +776,9 @@ def main():
                                            if peaks.get("bf16_tflops_sustained") else None),
                      "peak_source": peaks["source"] + " (bf16 burst)",
                      "kernel": ("pk_attn_fwd_kernel<128> on SM pairs" if args.sm_pairs
-                                else "pk_attn_fwd_kernel<128>"),
+                                else "pk_attn_fwd_kernel<128> on head-pair clusters "
+                                     "(key/value tiles multicast)" if shared_kv
+                                else "pk_attn_fwd_kernel<128>, one CTA per SM"),
                      "launch_ms_mean": round(avg_launch_ms, 4),
                      "launch_ms_median": round(statistics.median(launch_ms), 4),
                      "launch_ms_min": round(min(launch_ms), 4)},
@@ -776,8 +791,9 @@ def main():
         "e2e": e2e,
         "gpu_launches": 2 * args.steps,
         "clocks": clk.summary(),
-        "plan": {k2: info[k2] for k2 in ("num_items", "num_ctas", "num_full_tiles",
-                                          "num_partial_tiles")},
+        "plan": dict({k2: info[k2] for k2 in ("num_items", "num_ctas", "num_full_tiles",
+                                               "num_partial_tiles")},
+                     head_pair_clusters=int(len(plan.share_schedule()[1]) - 1) if shared_kv else 0),
         "per_workload": per_workload,
         "replaced_path": replaced,
         "layouts": layouts,

@@ -209,6 +209,27 @@ pk_status pk_plan_shard(const pk_plan* full, int32_t rank, int32_t num_ranks, in
  */
 pk_status pk_plan_set_sm_pairs(pk_plan* plan, int32_t enable);
 
+/*
+ * Head-pair clusters, on by default where the plan has their schedule
+ * (head_dim 128 and an even number of query heads per key/value head:
+ * every work item then holds two query heads).  A cluster of two CTAs on
+ * neighbouring SMs runs each of its items with one query head per CTA; the
+ * two stream the same key and value tiles, and each CTA copies half of
+ * every tile from global memory into the shared memory of both (TMA
+ * multicast within the cluster), so the pack's keys and values leave L2
+ * half as often.  Each CTA computes exactly what the one-CTA kernel computes
+ * for its head: results are bit-identical with the schedule on or off.
+ * Applies to pk_attn_fwd and the calls built on it, and to
+ * pk_attn_fwd_fp8; pk_plan_set_sm_pairs takes precedence, and
+ * pk_attn_fwd_fp8_pv keeps the one-CTA kernel.  Measured on GB300: +1 to
+ * +3.5% on the d = 128 packs.  The pages have no counterpart; it is a
+ * tuning option of this library.  enable = 0 selects the one-CTA kernel.
+ *   PK_ERR_INVALID_ARG for a null plan; PK_ERR_UNSUPPORTED when enabling a
+ *   plan without the schedule.  Takes effect at the next launch; not
+ *   thread-safe against launches running on the plan.
+ */
+pk_status pk_plan_set_kv_share(pk_plan* plan, int32_t enable);
+
 /* Bytes of the device image of the plan (work list, per-CTA offsets, the
  * per-row key limit and, for paged keys, the block table). */
 size_t pk_plan_device_bytes(const pk_plan* plan);
@@ -428,6 +449,14 @@ pk_status pk_plan_get_items(const pk_plan* plan, pk_work_item* items,
 pk_status pk_plan_get_pairs(const pk_plan* plan, int32_t* num_pairs, int32_t* num_clusters,
                             pk_work_item* items, int64_t n_items, int32_t* cluster_offsets,
                             int64_t n_offsets);
+
+/* The head-pair cluster schedule (pk_plan_set_kv_share), for tests:
+ * *num_clusters (0 when the plan has none, whether enabled or not); with
+ * non-null arrays of at least pk_plan_info.num_items items and
+ * num_clusters + 1 offsets, the cluster-ordered items and the per-cluster
+ * offsets.  PK_ERR_INVALID_ARG for a null plan or short arrays. */
+pk_status pk_plan_get_share(const pk_plan* plan, int32_t* num_clusters, pk_work_item* items,
+                            int64_t n_items, int32_t* cluster_offsets, int64_t n_offsets);
 
 /* Element types of pk_lse_merge's tensors. */
 typedef enum pk_dtype { PK_DTYPE_BF16 = 0, PK_DTYPE_F32 = 1 } pk_dtype;

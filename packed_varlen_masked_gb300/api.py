@@ -137,6 +137,32 @@ class Plan:
         check(self._lib.pk_plan_set_sm_pairs(self._h, 1 if enable else 0), "pk_plan_set_sm_pairs")
         return self
 
+    def set_kv_share(self, enable: bool = True) -> "Plan":
+        """Head-pair clusters sharing each key/value tile (pk_plan_set_kv_share):
+        on by default where the plan has their schedule (head_dim 128, an even
+        number of query heads per key/value head); ``False`` selects the
+        one-CTA kernel.  Bit-identical results either way.  Returns the plan."""
+        check(self._lib.pk_plan_set_kv_share(self._h, 1 if enable else 0), "pk_plan_set_kv_share")
+        return self
+
+    def share_schedule(self) -> Tuple[np.ndarray, np.ndarray]:
+        """(items int32 [num_items, 8], cluster-ordered; cluster offsets int32
+        [num_clusters + 1]) of the head-pair cluster schedule; empty when the
+        plan has none.  Columns as ``items``."""
+        ncl = ctypes.c_int32()
+        check(self._lib.pk_plan_get_share(self._h, ctypes.byref(ncl), None, 0, None, 0),
+              "pk_plan_get_share")
+        if ncl.value == 0:
+            return np.zeros((0, 8), dtype=np.int32), np.zeros(1, dtype=np.int32)
+        n = int(self.info["num_items"])
+        items = (WorkItem * max(n, 1))()
+        offs = np.zeros(ncl.value + 1, dtype=np.int32)
+        check(self._lib.pk_plan_get_share(self._h, ctypes.byref(ncl), items, n,
+                                          offs.ctypes.data_as(ctypes.c_void_p), offs.size),
+              "pk_plan_get_share")
+        arr = np.frombuffer(bytes(items), dtype=np.int32).reshape(-1, 8)[:n].copy()
+        return arr, offs
+
     def pairs(self) -> Tuple[np.ndarray, np.ndarray]:
         """(pair items int32 [2 * num_pairs, 8], rank 0 then rank 1 of each
         pair, cluster-ordered; cluster offsets int32 [num_clusters + 1], in

@@ -43,6 +43,15 @@
 // rank-0 CTA's producers and issuers serve both, each CTA holding half of
 // every key and value tile, and both CTAs run their rows' softmax and
 // epilogue.
+// SHARE (the default at D = 128 where every work item has two query heads):
+// a cluster of two CTAs on neighbouring SMs runs each item with one query
+// head per CTA.  Both stream the same key/value tiles through rings of the
+// same shape; each CTA's producers copy half of every tile (one 64-column
+// box, or for one-box FP8 key tiles 64 of the rows) into the shared memory
+// of both CTAs (TMA multicast), and a ring stage is refilled only after both
+// CTAs' products have read it (each MMA issuer's commit arrives on the
+// stage's empty barrier in both CTAs).  Everything else is the one-CTA
+// kernel, per CTA.
 // TMEM columns: S double buffer [0,256), P double buffer [256,384), O
 // [384,384+D).  Because S(t) and P(t) live in different columns and both are
 // double buffered, the S issuer computes S(t+2) as soon as the softmax has
@@ -86,7 +95,9 @@ constexpr int kStoreGroup = 8;
 // PAIR: the SM-pair kernel (bf16, D = 128): a cluster of two CTAs computes
 // M = 256 products; each CTA holds its own 128 query rows, half of every key
 // tile (64 rows) and half of every value tile (64 of the D columns).
-template <int D, bool F8 = false, bool V8 = false, bool PAIR = false>
+// SHARE: head-pair clusters; each CTA copies half of every key and value
+// tile into both CTAs (see the file comment).
+template <int D, bool F8 = false, bool V8 = false, bool PAIR = false, bool SHARE = false>
 struct Cfg {
   // Query/key tiles: rows in boxes of 128-byte rows (64 bf16 or 128 FP8
   // elements); value tiles: 128 rows of D fp16 in 64-column boxes.
@@ -117,6 +128,10 @@ struct Cfg {
   static_assert(!F8 || D == 128, "FP8 queries/keys need head_dim 128");
   static_assert(!V8 || F8, "E4M3 values come with E4M3 queries and keys");
   static_assert(!PAIR || (D == 128 && !F8), "the SM-pair kernel is bf16 with head_dim 128");
+  static_assert(!SHARE || (D == 128 && !V8 && !PAIR), "head-pair clusters: head_dim 128, 16-bit values");
+  // SHARE: rows per key copy.  Two-box (bf16) key tiles split by boxes, each
+  // CTA copying one whole box; one-box (FP8) key tiles split by rows.
+  static constexpr int kShareKRows = kQKBoxes == 1 ? 64 : 128;
   // Arrivals of the softmax (S buffer free, P ready) and the epilogue (O
   // free): one per thread of the CTA's warpgroup, or, in the pair kernel,
   // of both CTAs' warpgroups (on the rank-0 CTA's barrier).
@@ -147,43 +162,58 @@ struct Cfg {
 // of its items back to back, so the second head's keys and values come from
 // L2.  Every role walks the same unit sequence.
 // In the pair kernel the items come in (rank 0, rank 1) pairs and each CTA
-// walks its own item of every pair (stride 2).
+// walks its own item of every pair (stride 2).  In a head-pair cluster each
+// CTA runs one query head of every item (fixed slot: its cluster rank).
 struct UnitIter {
   const pk_work_item* items;
   int it, end, slot, stride, rank;
+  bool fixed;
   pk_work_item w;
   __device__ UnitIter(const pk_work_item* items_, int beg, int end_, int stride_ = 1,
-                      int rank_ = 0)
-      : items(items_), it(beg), end(end_), slot(0), stride(stride_), rank(rank_) {
+                      int rank_ = 0, int fixed_slot = -1)
+      : items(items_), it(beg), end(end_), slot(fixed_slot < 0 ? 0 : fixed_slot),
+        stride(stride_), rank(rank_), fixed(fixed_slot >= 0) {
     if (it < end) w = items[it * stride + rank];
   }
   __device__ bool valid() const { return it < end; }
   __device__ int head() const { return slot ? w.hq1 : w.hq0; }
   __device__ void next() {
-    if (slot == 0 && w.hq1 >= 0) {
-      slot = 1;
-      return;
+    if (!fixed) {
+      if (slot == 0 && w.hq1 >= 0) {
+        slot = 1;
+        return;
+      }
+      slot = 0;
     }
-    slot = 0;
     if (++it < end) w = items[it * stride + rank];
   }
 };
+
+// The unit iterator of a role: the pair kernel's stride and rank, or a
+// head-pair cluster's fixed slot.
+template <bool PAIR, bool SHARE>
+__device__ __forceinline__ UnitIter role_units(const KernelParams& p, int beg, int end,
+                                               uint32_t pair_rank) {
+  return UnitIter(p.items, beg, end, PAIR ? 2 : 1, PAIR ? (int)pair_rank : 0,
+                  SHARE ? (int)cluster_rank() : -1);
+}
 
 // Q/K producer (one thread): per unit its query tile (double buffered), then
 // the ring of key tiles.  Keys and values are re-read by the other query
 // heads of the group and by neighbouring query tiles, so they are kept in L2
 // (evict-last); a query tile is read once (evict-first).
-template <int D, bool F8, bool V8, bool PAIR>
+template <int D, bool F8, bool V8, bool PAIR, bool SHARE>
 __device__ void producer_qk_role(const KernelParams& p, const CUtensorMap* tm_q,
                                  const CUtensorMap* tm_k, uint32_t sbase, int beg, int end,
                                  const WaitCtl& wc) {
-  using C = Cfg<D, F8, V8, PAIR>;
+  using C = Cfg<D, F8, V8, PAIR, SHARE>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
   const uint64_t keep = l2_policy_evict_last(), stream = l2_policy_evict_first();
   uint32_t g = 0, u = 0, k_armed = 0, q_armed = 0;
   bool ok = true;
   constexpr int kCtas = PAIR ? 2 : 1;  // pair: this (rank-0) thread loads both CTAs' tiles
-  for (UnitIter ui(p.items, beg, end, kCtas, 0); ui.valid() && ok; ui.next(), ++u) {
+  const int srank = SHARE ? (int)cluster_rank() : 0;  // the key box or rows this CTA copies
+  for (UnitIter ui = role_units<PAIR, SHARE>(p, beg, end, 0); ui.valid() && ok; ui.next(), ++u) {
     const pk_work_item& w = ui.w;
     const uint32_t qb = u & 1u;
     if (!(ok = mbar_wait(bar(C::kQEmpty + qb), ((u >> 1) & 1u) ^ 1u, wc))) break;
@@ -211,7 +241,16 @@ __device__ void producer_qk_role(const KernelParams& p, const CUtensorMap* tm_q,
       if (!(ok = mbar_wait(bar(C::kKEmpty + st), ph ^ 1u, wc))) break;
       mbar_arrive_expect_tx(bar(C::kKFull + st), kCtas * C::kKTileBytes);
       ++k_armed;
-      if constexpr (PAIR) {  // key rows [64 r, 64 r + 64) of the tile to rank r
+      if constexpr (SHARE) {  // this CTA's half of the tile, into both CTAs
+        if constexpr (C::kQKBoxes == 2)
+          tma_load_3d_mc(sbase + C::kOffK + st * C::kKTileBytes + srank * C::kKBoxBytes, tm_k,
+                         bar(C::kKFull + st), srank * C::kQKElemsPerBox, w.hkv,
+                         key_tile_row(p, w, j), (uint16_t)3, keep);
+        else
+          tma_load_3d_mc(sbase + C::kOffK + st * C::kKTileBytes + srank * 64 * 128, tm_k,
+                         bar(C::kKFull + st), 0, w.hkv, key_tile_row(p, w, j) + srank * 64,
+                         (uint16_t)3, keep);
+      } else if constexpr (PAIR) {  // key rows [64 r, 64 r + 64) of the tile to rank r
 #pragma unroll
         for (int r = 0; r < 2; ++r)
 #pragma unroll
@@ -234,35 +273,53 @@ __device__ void producer_qk_role(const KernelParams& p, const CUtensorMap* tm_q,
   // after an abort (this thread's or a consumer's) they may be in flight.
   // The last kKStages armings of the ring (and the last two of Q) are the
   // only ones that can be open, each the most recent arming of its stage.
+  // Head-pair cluster: a stage's phase completes only with the other CTA's
+  // half too (see mbar_wait_cluster_drain).
   for (uint32_t k = 1; k <= (uint32_t)C::kKStages && k <= k_armed; ++k) {
     const uint32_t i = k_armed - k;
-    mbar_wait_drain(bar(C::kKFull + i % C::kKStages), (i / C::kKStages) & 1u, wc);
+    if constexpr (SHARE)
+      mbar_wait_cluster_drain(bar(C::kKFull + i % C::kKStages), (i / C::kKStages) & 1u, wc);
+    else
+      mbar_wait_drain(bar(C::kKFull + i % C::kKStages), (i / C::kKStages) & 1u, wc);
   }
   for (uint32_t k = 1; k <= 2u && k <= q_armed; ++k) {
     const uint32_t i = q_armed - k;
     mbar_wait_drain(bar(C::kQFull + (i & 1u)), (i >> 1) & 1u, wc);
   }
+  // Head-pair cluster: the other CTA's last commits (arrivals on this CTA's
+  // empty barriers) land before this CTA may exit.
+  if constexpr (SHARE) {
+    for (uint32_t k = 1; k <= (uint32_t)C::kKStages && k <= k_armed; ++k) {
+      const uint32_t i = k_armed - k;
+      mbar_wait_cluster_drain(bar(C::kKEmpty + i % C::kKStages), (i / C::kKStages) & 1u, wc);
+    }
+  }
 }
 
 // V producer (one thread of another warp): the ring of value tiles, so that
 // a value tile waiting for its stage never holds back the next key tile.
-template <int D, bool F8, bool V8, bool PAIR>
+template <int D, bool F8, bool V8, bool PAIR, bool SHARE>
 __device__ void producer_v_role(const KernelParams& p, const CUtensorMap* tm_v, uint32_t sbase,
                                 int beg, int end, const WaitCtl& wc) {
-  using C = Cfg<D, F8, V8, PAIR>;
+  using C = Cfg<D, F8, V8, PAIR, SHARE>;
   constexpr int kCtas = PAIR ? 2 : 1;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
   const uint64_t keep = l2_policy_evict_last();
   uint32_t g = 0, v_armed = 0;
   bool ok = true;
-  for (UnitIter ui(p.items, beg, end, kCtas, 0); ui.valid() && ok; ui.next()) {
+  const int srank = SHARE ? (int)cluster_rank() : 0;  // the value box this CTA copies
+  for (UnitIter ui = role_units<PAIR, SHARE>(p, beg, end, 0); ui.valid() && ok; ui.next()) {
     const pk_work_item& w = ui.w;
     for (int j = 0; j < w.n_kt; ++j, ++g) {
       const uint32_t st = g % C::kVStages, ph = (g / C::kVStages) & 1u;
       if (!(ok = mbar_wait(bar(C::kVEmpty + st), ph ^ 1u, wc))) break;
       mbar_arrive_expect_tx(bar(C::kVFull + st), kCtas * C::kVTileBytes);
       ++v_armed;
-      if constexpr (PAIR) {  // value columns [64 r, 64 r + 64) to rank r
+      if constexpr (SHARE) {  // this CTA's 64-column box, into both CTAs
+        tma_load_3d_mc(sbase + C::kOffV + st * C::kVTileBytes + srank * kBoxBytes, tm_v,
+                       bar(C::kVFull + st), srank * 64, w.hkv, key_tile_row(p, w, j), (uint16_t)3,
+                       keep);
+      } else if constexpr (PAIR) {  // value columns [64 r, 64 r + 64) to rank r
 #pragma unroll
         for (int r = 0; r < 2; ++r)
           tma_load_3d_pair(map_to_rank(sbase + C::kOffV + st * C::kVTileBytes, r), tm_v,
@@ -281,7 +338,16 @@ __device__ void producer_v_role(const KernelParams& p, const CUtensorMap* tm_v, 
   }
   for (uint32_t k = 1; k <= (uint32_t)C::kVStages && k <= v_armed; ++k) {  // as above
     const uint32_t i = v_armed - k;
-    mbar_wait_drain(bar(C::kVFull + i % C::kVStages), (i / C::kVStages) & 1u, wc);
+    if constexpr (SHARE)
+      mbar_wait_cluster_drain(bar(C::kVFull + i % C::kVStages), (i / C::kVStages) & 1u, wc);
+    else
+      mbar_wait_drain(bar(C::kVFull + i % C::kVStages), (i / C::kVStages) & 1u, wc);
+  }
+  if constexpr (SHARE) {
+    for (uint32_t k = 1; k <= (uint32_t)C::kVStages && k <= v_armed; ++k) {
+      const uint32_t i = v_armed - k;
+      mbar_wait_cluster_drain(bar(C::kVEmpty + i % C::kVStages), (i / C::kVStages) & 1u, wc);
+    }
   }
 }
 
@@ -294,10 +360,10 @@ __device__ void producer_v_role(const KernelParams& p, const CUtensorMap* tm_v, 
 // S issuer (warp 1): S(t) needs K(t) loaded and S buffer t%2 released by the
 // softmax of tile t-2, so it runs up to two tiles ahead of the softmax and
 // the tensor pipe computes S(t+2) while the softmax works on tile t.
-template <int D, bool F8, bool V8, bool PAIR>
+template <int D, bool F8, bool V8, bool PAIR, bool SHARE>
 __device__ void mma_s_role(const KernelParams& p, uint32_t sbase, uint32_t tmem, int beg,
                            int end, const WaitCtl& wc) {
-  using C = Cfg<D, F8, V8, PAIR>;
+  using C = Cfg<D, F8, V8, PAIR, SHARE>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
   const uint64_t q_desc0 = sdesc(sbase + C::kOffQ, 16, 1024);
   const uint64_t k_desc0 = sdesc(sbase + C::kOffK, 16, 1024);
@@ -305,7 +371,7 @@ __device__ void mma_s_role(const KernelParams& p, uint32_t sbase, uint32_t tmem,
   constexpr uint64_t kKTileDesc = (uint64_t)(C::kKTileBytes >> 4);
   uint32_t t = 0, u = 0;
   bool ok = true;
-  for (UnitIter ui(p.items, beg, end, PAIR ? 2 : 1, 0); ui.valid() && ok; ui.next(), ++u) {
+  for (UnitIter ui = role_units<PAIR, SHARE>(p, beg, end, 0); ui.valid() && ok; ui.next(), ++u) {
     const uint32_t n = (uint32_t)ui.w.n_kt, qb = u & 1u;
     if (!(ok = mbar_wait(bar(C::kQFull + qb), (u >> 1) & 1u, wc))) break;
     for (uint32_t j = 0; j < n; ++j, ++t) {
@@ -323,7 +389,10 @@ __device__ void mma_s_role(const KernelParams& p, uint32_t sbase, uint32_t tmem,
         issue_qk<D, F8>(tmem + C::kColS0 + b * 128u, q_desc0 + qb * kQTileDesc,
                         k_desc0 + kst * kKTileDesc);
         tc_commit(bar(C::kSFull + b));
-        tc_commit(bar(C::kKEmpty + kst));
+        if constexpr (SHARE)  // both CTAs' producers refill this stage
+          tc_commit_mc(bar(C::kKEmpty + kst), 3);
+        else
+          tc_commit(bar(C::kKEmpty + kst));
         if (j + 1 == n) tc_commit(bar(C::kQEmpty + qb));  // last use of this Q buffer
       }
     }
@@ -338,10 +407,10 @@ __device__ void mma_s_role(const KernelParams& p, uint32_t sbase, uint32_t tmem,
 
 // P V issuer (warp 3): O (+)= P(t) V(t) needs V(t) loaded and P(t) written;
 // a unit's first product overwrites O, after the previous unit's O was read.
-template <int D, bool F8, bool V8, bool PAIR>
+template <int D, bool F8, bool V8, bool PAIR, bool SHARE>
 __device__ void mma_pv_role(const KernelParams& p, uint32_t sbase, uint32_t tmem, int beg,
                             int end, const WaitCtl& wc) {
-  using C = Cfg<D, F8, V8, PAIR>;
+  using C = Cfg<D, F8, V8, PAIR, SHARE>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
   // fp16 values: MN-major, 64-column boxes kBoxBytes apart; E4M3 values:
   // K-major (transposed copy)
@@ -349,7 +418,7 @@ __device__ void mma_pv_role(const KernelParams& p, uint32_t sbase, uint32_t tmem
   constexpr uint64_t kTileDesc = (uint64_t)(C::kVTileBytes >> 4);
   uint32_t t = 0, u = 0;
   bool ok = true;
-  for (UnitIter ui(p.items, beg, end, PAIR ? 2 : 1, 0); ui.valid() && ok; ui.next(), ++u) {
+  for (UnitIter ui = role_units<PAIR, SHARE>(p, beg, end, 0); ui.valid() && ok; ui.next(), ++u) {
     const uint32_t n = (uint32_t)ui.w.n_kt;
     for (uint32_t j = 0; j < n; ++j, ++t) {
       const uint32_t vst = t % C::kVStages, b = t & 1u;
@@ -370,7 +439,10 @@ __device__ void mma_pv_role(const KernelParams& p, uint32_t sbase, uint32_t tmem
           issue_pv<D>(tmem + C::kColO, tmem + C::kColP0 + b * 64u, v_desc0 + vst * kTileDesc,
                       j > 0);
         tc_commit(bar(C::kPvDone + b));
-        tc_commit(bar(C::kVEmpty + vst));
+        if constexpr (SHARE)
+          tc_commit_mc(bar(C::kVEmpty + vst), 3);
+        else
+          tc_commit(bar(C::kVEmpty + vst));
       }
     }
   }
@@ -396,10 +468,10 @@ __device__ __forceinline__ void group_arrive(uint32_t bar, uint32_t rank) {
 }
 
 // Softmax warpgroup (warps 4-7): thread r owns row r of S, P and O in TMEM.
-template <int D, bool F8, bool V8, bool PAIR>
+template <int D, bool F8, bool V8, bool PAIR, bool SHARE>
 __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint8_t* sgen, uint32_t tmem,
                              int beg, int end, const WaitCtl& wc) {
-  using C = Cfg<D, F8, V8, PAIR>;
+  using C = Cfg<D, F8, V8, PAIR, SHARE>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;  // TMEM lane quadrant this warp may access
@@ -412,7 +484,7 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint8_t* sge
   bool s_ready = false;  // S(t) of the next tile already seen complete
   float2* lm = reinterpret_cast<float2*>(sgen + C::kOffLm);
   const uint32_t rank = PAIR ? cluster_rank() : 0u;
-  for (UnitIter ui(p.items, beg, end, PAIR ? 2 : 1, (int)rank); ui.valid() && ok;
+  for (UnitIter ui = role_units<PAIR, SHARE>(p, beg, end, rank); ui.valid() && ok;
        ui.next(), ++u) {
     const pk_work_item& w = ui.w;
     const bool valid = r < w.q_rows;
@@ -568,10 +640,10 @@ __device__ void softmax_role(const KernelParams& p, uint32_t sbase, uint8_t* sge
 // unit it takes (m, l) from the softmax, waits for the unit's last P V,
 // moves O into registers and frees it for the next unit's first product,
 // then writes O / l as bf16 and the natural-log LSE.
-template <int D, bool F8, bool V8, bool PAIR>
+template <int D, bool F8, bool V8, bool PAIR, bool SHARE>
 __device__ void epilogue_role(const KernelParams& p, uint32_t sbase, uint8_t* sgen,
                               uint32_t tmem, int beg, int end, const WaitCtl& wc) {
-  using C = Cfg<D, F8, V8, PAIR>;
+  using C = Cfg<D, F8, V8, PAIR, SHARE>;
   auto bar = [&](int i) { return sbase + C::kOffBar + 8u * (uint32_t)i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;
@@ -581,7 +653,7 @@ __device__ void epilogue_role(const KernelParams& p, uint32_t sbase, uint8_t* sg
   uint32_t g = 0, u = 0;
   bool ok = true;
   const uint32_t rank = PAIR ? cluster_rank() : 0u;
-  for (UnitIter ui(p.items, beg, end, PAIR ? 2 : 1, (int)rank); ui.valid() && ok;
+  for (UnitIter ui = role_units<PAIR, SHARE>(p, beg, end, rank); ui.valid() && ok;
        ui.next(), ++u) {
     const pk_work_item& w = ui.w;
     const int h = ui.head();
@@ -761,12 +833,12 @@ __global__ void __launch_bounds__(256) pk_v8_transpose_kernel(const uint8_t* v8,
   }
 }
 
-template <int D, bool F8, bool V8, bool PAIR>
+template <int D, bool F8, bool V8, bool PAIR, bool SHARE>
 __global__ void __launch_bounds__(kThreads, 1)
     pk_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const KernelParams p) {
-  using C = Cfg<D, F8, V8, PAIR>;
+  using C = Cfg<D, F8, V8, PAIR, SHARE>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;  // 128-byte swizzle atoms need 1 KB alignment
@@ -788,13 +860,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(C::kPReady + s), C::kGroupArrivals);
       mbar_init(bar(C::kPvDone + s), 1);
     }
+    // SHARE: a ring stage is empty once both CTAs' products have read it.
+    constexpr uint32_t kEmptyArrivals = SHARE ? 2 : 1;
     for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(bar(C::kKFull + s), 1);
-      mbar_init(bar(C::kKEmpty + s), 1);
+      mbar_init(bar(C::kKEmpty + s), kEmptyArrivals);
     }
     for (int s = 0; s < C::kVStages; ++s) {
       mbar_init(bar(C::kVFull + s), 1);
-      mbar_init(bar(C::kVEmpty + s), 1);
+      mbar_init(bar(C::kVEmpty + s), kEmptyArrivals);
     }
     mbar_init(bar(C::kOFree), C::kGroupArrivals);
     mbar_init(bar(C::kMmaDone + 0), 1);
@@ -824,12 +898,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  // Pair: both CTAs' barriers exist before either CTA's copies or arrivals
-  // reach them.
-  if constexpr (PAIR) cluster_sync_all();
+  // Clusters: both CTAs' barriers exist before either CTA's copies or
+  // arrivals reach them.
+  if constexpr (PAIR || SHARE) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const int unit_set = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int unit_set = (PAIR || SHARE) ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int beg = p.cta_offsets[unit_set], end = p.cta_offsets[unit_set + 1];
   const WaitCtl wc{abort_flag, p.status, p.wait_limit_ns};
 
@@ -839,22 +913,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsMma));
     if (rank == 0) {
       if (warp == 0) {
-        if (lane == 0) producer_qk_role<D, F8, V8, PAIR>(p, &tm_q, &tm_k, sbase, beg, end, wc);
+        if (lane == 0) producer_qk_role<D, F8, V8, PAIR, SHARE>(p, &tm_q, &tm_k, sbase, beg, end, wc);
       } else if (warp == 1) {
-        if (lane == 0) mma_s_role<D, F8, V8, PAIR>(p, sbase, tmem, beg, end, wc);
+        if (lane == 0) mma_s_role<D, F8, V8, PAIR, SHARE>(p, sbase, tmem, beg, end, wc);
       } else if (warp == 2) {
-        if (lane == 0) producer_v_role<D, F8, V8, PAIR>(p, &tm_v, sbase, beg, end, wc);
+        if (lane == 0) producer_v_role<D, F8, V8, PAIR, SHARE>(p, &tm_v, sbase, beg, end, wc);
       } else {
-        if (lane == 0) mma_pv_role<D, F8, V8, PAIR>(p, sbase, tmem, beg, end, wc);
+        if (lane == 0) mma_pv_role<D, F8, V8, PAIR, SHARE>(p, sbase, tmem, beg, end, wc);
       }
     }
     __syncwarp();
   } else if (warp < 8) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
-    softmax_role<D, F8, V8, PAIR>(p, sbase, sgen, tmem, beg, end, wc);
+    softmax_role<D, F8, V8, PAIR, SHARE>(p, sbase, sgen, tmem, beg, end, wc);
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
-    epilogue_role<D, F8, V8, PAIR>(p, sbase, sgen, tmem, beg, end, wc);
+    epilogue_role<D, F8, V8, PAIR, SHARE>(p, sbase, sgen, tmem, beg, end, wc);
   }
 
   tc_fence_before();
@@ -862,8 +936,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Pair: the rank-0 CTA's products read and write both CTAs' shared and
   // tensor memory, and its copies land in both; it leaves this barrier only
   // after its issuers and producers have drained them, and neither CTA
-  // frees TMEM or exits before that.
-  if constexpr (PAIR) cluster_sync_all();
+  // frees TMEM or exits before that.  Head-pair cluster: each CTA's copies
+  // land in both CTAs; neither exits before the other has drained.
+  if constexpr (PAIR || SHARE) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
     if constexpr (PAIR)
@@ -1040,17 +1115,17 @@ pk_status transpose_values(const pk_plan* plan, const void* v8, void* vt, int sm
 
 // v16: the fp16 values (the workspace convert_values has filled), or with V8
 // the transposed E4M3 copy (transpose_values).
-template <int D, bool F8, bool V8, bool PAIR = false>
+template <int D, bool F8, bool V8, bool PAIR = false, bool SHARE = false>
 pk_status launch(const pk_plan* plan, const void* q, const void* k, const void* v16, void* out,
                  float* lse, float scale, cudaStream_t stream, int32_t* dev_status,
                  float v_scale = 1.0f) {
-  using C = pk::dev::Cfg<D, F8, V8, PAIR>;
-  auto kernel = pk::dev::pk_attn_fwd_kernel<D, F8, V8, PAIR>;
+  using C = pk::dev::Cfg<D, F8, V8, PAIR, SHARE>;
+  auto kernel = pk::dev::pk_attn_fwd_kernel<D, F8, V8, PAIR, SHARE>;
   CUtensorMap tq, tk, tv;
   const CUtensorMapDataType qk_dt =
       F8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if (!make_map(&tq, q, plan->hq, plan->T, D, qk_dt) ||
-      !make_map(&tk, k, plan->hkv, plan->Tk, D, qk_dt, C::kKRows) ||
+      !make_map(&tk, k, plan->hkv, plan->Tk, D, qk_dt, SHARE ? C::kShareKRows : C::kKRows) ||
       !(V8 ? make_map_v8t(&tv, v16, plan->hkv, plan->v8_rows, D)
            : make_map(&tv, v16, plan->hkv, plan->Tk, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)))
     return PK_ERR_CUDA;
@@ -1076,9 +1151,11 @@ pk_status launch(const pk_plan* plan, const void* q, const void* k, const void* 
   const uint8_t* img = static_cast<const uint8_t*>(plan->dev);
   pk::dev::KernelParams kp;
   kp.items = reinterpret_cast<const pk_work_item*>(
-      img + (PAIR ? plan->layout.pitems_off : plan->layout.items_off));
+      img + (PAIR ? plan->layout.pitems_off
+                  : SHARE ? plan->layout.sitems_off : plan->layout.items_off));
   kp.cta_offsets = reinterpret_cast<const int32_t*>(
-      img + (PAIR ? plan->layout.pcta_off_off : plan->layout.cta_off_off));
+      img + (PAIR ? plan->layout.pcta_off_off
+                  : SHARE ? plan->layout.scta_off_off : plan->layout.cta_off_off));
   kp.kv_limit = reinterpret_cast<const int32_t*>(img + plan->layout.kvlim_off);
   kp.block_table =
       plan->paged ? reinterpret_cast<const int32_t*>(img + plan->layout.table_off) : nullptr;
@@ -1092,10 +1169,11 @@ pk_status launch(const pk_plan* plan, const void* q, const void* k, const void* 
   kp.scale_log2 = scale * 1.4426950408889634f;
   kp.v_scale = v_scale;
   kp.wait_limit_ns = g_wait_limit_ns.load();
-  if constexpr (PAIR) {
-    // clusters of two CTAs on SM pairs
+  if constexpr (PAIR || SHARE) {
+    // clusters of two CTAs on neighbouring SMs
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2u * (unsigned)plan->num_clusters);
+    cfg.gridDim =
+        dim3(2u * (unsigned)(PAIR ? plan->num_clusters : plan->num_share_clusters));
     cfg.blockDim = dim3(pk::dev::kThreads);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = stream;
@@ -1199,6 +1277,9 @@ pk_status pk_attn_fwd_converted(const pk_plan* plan, const void* q, const void* 
   if (plan->head_dim == 128) {
     if (plan->use_pairs && plan->num_clusters > 0)  // pk_plan_set_sm_pairs
       return launch<128, false, false, true>(plan, q, k, v16, out, lse, scale, s, dev_status);
+    if (plan->use_share && plan->num_share_clusters > 0)  // pk_plan_set_kv_share
+      return launch<128, false, false, false, true>(plan, q, k, v16, out, lse, scale, s,
+                                                    dev_status);
     return launch<128, false, false>(plan, q, k, v16, out, lse, scale, s, dev_status);
   }
   if (plan->head_dim == 64) return launch<64, false, false>(plan, q, k, v16, out, lse, scale, s, dev_status);
@@ -1294,6 +1375,10 @@ pk_status pk_attn_fwd_fp8(const pk_plan* plan, const void* q8, float q_scale, co
       PK_OK)
     return st;
   if ((st = check_device()) != PK_OK) return st;
+  if (plan->use_share && plan->num_share_clusters > 0)  // pk_plan_set_kv_share
+    return launch<128, true, false, false, true>(plan, q8, k8, workspace, out, lse, s_all,
+                                                 reinterpret_cast<cudaStream_t>(stream),
+                                                 dev_status);
   return launch<128, true, false>(plan, q8, k8, workspace, out, lse, s_all,
                            reinterpret_cast<cudaStream_t>(stream), dev_status);
 }

@@ -25,6 +25,8 @@ struct PlanImageLayout {
   size_t vblk_off = 0;     // int32[v_blocks.size()]: (pool block, valid rows) the kernel reads
   size_t pitems_off = 0;   // pk_work_item[2 * num_pairs]: SM-pair items, cluster-ordered
   size_t pcta_off_off = 0; // int32[num_clusters + 1]
+  size_t sitems_off = 0;   // pk_work_item[num_items]: head-pair cluster items, cluster-ordered
+  size_t scta_off_off = 0; // int32[num_share_clusters + 1]
   size_t v8chunk_off = 0;  // int32[v8_chunks.size()]: the E4M3 value transpose's chunks
   size_t v8row_off = 0;    // int32[num_items] (contiguous keys): row of an item's first
                            // key tile in the transposed E4M3 value copy
@@ -82,6 +84,16 @@ struct pk_plan {
   bool use_pairs = false;                  // pk_plan_set_sm_pairs
   std::vector<pk_work_item> pair_items;    // [2 * num_pairs], cluster-ordered
   std::vector<int32_t> pair_cta_offsets;   // [num_clusters + 1], in pairs
+  // The same items for head-pair clusters (head_dim 128, every item with
+  // two query heads): a cluster of two CTAs on neighbouring SMs runs each of
+  // its items with one query head per CTA, the two CTAs streaming the same
+  // key/value tiles, each copying half of every tile into both.  Scheduled
+  // longest first over num_share_clusters = num_ctas / 2 clusters; the
+  // default kernel wherever the schedule exists (pk_plan_set_kv_share).
+  int32_t num_share_clusters = 0;
+  bool use_share = false;
+  std::vector<pk_work_item> share_items;   // [num_items], cluster-ordered
+  std::vector<int32_t> share_offsets;      // [num_share_clusters + 1]
   pk::PlanImageLayout layout;
   std::vector<uint8_t> image;              // host copy of the device image
   void* dev = nullptr;                     // caller's buffer after upload

@@ -44,6 +44,29 @@ double item_cost(const pk_work_item& w) {
   return w.hq1 >= 0 ? 2.0 * per_head : per_head;
 }
 
+// Longest-processing-time-first: indices sorted by decreasing cost (ties
+// keep their order, so items streaming the same keys/values start side by
+// side), each given to the least-loaded of `bins` bins.
+std::vector<std::vector<int32_t>> lpt_schedule(const std::vector<double>& cost, int32_t bins) {
+  const int32_t n = static_cast<int32_t>(cost.size());
+  std::vector<int32_t> order(n);
+  std::iota(order.begin(), order.end(), 0);
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int32_t a, int32_t b) { return cost[a] > cost[b]; });
+  std::vector<std::vector<int32_t>> per(bins);
+  using Load = std::pair<double, int32_t>;
+  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+  for (int32_t c = 0; c < bins; ++c) heap.push({0.0, c});
+  for (int32_t idx : order) {
+    Load l = heap.top();
+    heap.pop();
+    per[l.second].push_back(idx);
+    l.first += cost[idx];
+    heap.push(l);
+  }
+  return per;
+}
+
 // Validation of the general layout; fills seg_first[s] (first segment of s)
 // and seq_len[s] (positions covered by its segments).
 pk_status validate_layout(const pk_layout& L, int32_t hq, int32_t hkv, int32_t d,
@@ -177,22 +200,9 @@ void schedule_pairs(pk_plan* p, const std::vector<pk_work_item>& items, int32_t 
   const int32_t n_pairs = static_cast<int32_t>(pairs.size());
   const int32_t grid = std::min<int32_t>(clusters, n_pairs);
   p->num_clusters = grid;
-  std::vector<int32_t> order(n_pairs);
-  std::iota(order.begin(), order.end(), 0);
-  std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b2) {
-    return item_cost(pairs[a][0]) > item_cost(pairs[b2][0]);
-  });
-  std::vector<std::vector<int32_t>> per(grid);
-  using Load = std::pair<double, int32_t>;
-  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
-  for (int32_t c = 0; c < grid; ++c) heap.push({0.0, c});
-  for (int32_t idx : order) {
-    Load l = heap.top();
-    heap.pop();
-    per[l.second].push_back(idx);
-    l.first += item_cost(pairs[idx][0]);
-    heap.push(l);
-  }
+  std::vector<double> cost(n_pairs);
+  for (int32_t i = 0; i < n_pairs; ++i) cost[i] = item_cost(pairs[i][0]);
+  const std::vector<std::vector<int32_t>> per = lpt_schedule(cost, grid);
   p->pair_cta_offsets.assign(grid + 1, 0);
   p->pair_items.reserve(2 * static_cast<size_t>(n_pairs));
   for (int32_t c = 0; c < grid; ++c) {
@@ -204,8 +214,36 @@ void schedule_pairs(pk_plan* p, const std::vector<pk_work_item>& items, int32_t 
   }
 }
 
+// Head-pair cluster items (see pk_plan::share_items): the plan's items as
+// they are, each run by one cluster (a query head per CTA), scheduled
+// longest first over `clusters` clusters.  None unless head_dim is 128 and
+// every item has two query heads.
+void schedule_share(pk_plan* p, const std::vector<pk_work_item>& items, int32_t clusters) {
+  p->share_items.clear();
+  p->share_offsets.clear();
+  p->num_share_clusters = 0;
+  p->use_share = false;
+  if (p->head_dim != 128 || clusters < 1 || items.empty()) return;
+  for (const pk_work_item& w : items)
+    if (w.hq1 < 0) return;
+  const int32_t n = static_cast<int32_t>(items.size());
+  const int32_t grid = std::min<int32_t>(clusters, n);
+  std::vector<double> cost(n);
+  for (int32_t i = 0; i < n; ++i) cost[i] = item_cost(items[i]);
+  const std::vector<std::vector<int32_t>> per = lpt_schedule(cost, grid);
+  p->share_offsets.assign(grid + 1, 0);
+  p->share_items.reserve(n);
+  for (int32_t c = 0; c < grid; ++c) {
+    for (int32_t idx : per[c]) p->share_items.push_back(items[idx]);
+    p->share_offsets[c + 1] = static_cast<int32_t>(p->share_items.size());
+  }
+  p->num_share_clusters = grid;
+  p->use_share = true;
+}
+
 // Longest-processing-time-first schedule of `items` over `num_ctas` CTAs
-// (and over num_ctas / 2 SM pairs), then the plan's device image.
+// (and over num_ctas / 2 SM pairs or head-pair clusters), then the plan's
+// device image.
 void schedule_and_image(pk_plan* p, std::vector<pk_work_item> items, int32_t num_ctas) {
   const int32_t Tq = p->T;
   // The plan's own work: tiles visited and useful FLOPs (4 d per visible
@@ -220,28 +258,12 @@ void schedule_and_image(pk_plan* p, std::vector<pk_work_item> items, int32_t num
     pairs_x_heads += static_cast<double>(pairs) * (w.hq1 >= 0 ? 2 : 1);
   }
   p->useful_flops = 4.0 * p->head_dim * pairs_x_heads;
-  // Longest-processing-time-first: sort by cost (ties keep the items' order,
-  // so items streaming the same keys/values start side by side), then give
-  // each item to the least-loaded CTA.
   const int32_t n_items = static_cast<int32_t>(items.size());
   const int32_t grid = std::min<int32_t>(num_ctas, n_items);
   p->num_ctas = grid;
-  std::vector<int32_t> order(n_items);
-  std::iota(order.begin(), order.end(), 0);
-  std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b2) {
-    return item_cost(items[a]) > item_cost(items[b2]);
-  });
-  std::vector<std::vector<int32_t>> per_cta(grid);
-  using Load = std::pair<double, int32_t>;
-  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
-  for (int32_t c = 0; c < grid; ++c) heap.push({0.0, c});
-  for (int32_t idx : order) {
-    Load l = heap.top();
-    heap.pop();
-    per_cta[l.second].push_back(idx);
-    l.first += item_cost(items[idx]);
-    heap.push(l);
-  }
+  std::vector<double> cost(n_items);
+  for (int32_t i = 0; i < n_items; ++i) cost[i] = item_cost(items[i]);
+  const std::vector<std::vector<int32_t>> per_cta = lpt_schedule(cost, grid);
   p->cta_offsets.assign(grid + 1, 0);
   p->items.reserve(n_items);
   for (int32_t c = 0; c < grid; ++c) {
@@ -249,6 +271,7 @@ void schedule_and_image(pk_plan* p, std::vector<pk_work_item> items, int32_t num
     p->cta_offsets[c + 1] = static_cast<int32_t>(p->items.size());
   }
   schedule_pairs(p, items, num_ctas / 2);
+  schedule_share(p, items, num_ctas / 2);
 
   // Device image.
   pk::PlanImageLayout& IL = p->layout;
@@ -260,7 +283,11 @@ void schedule_and_image(pk_plan* p, std::vector<pk_work_item> items, int32_t num
   IL.pitems_off = align_up(IL.vblk_off + sizeof(int32_t) * p->v_blocks.size(), pk::kImageAlign);
   IL.pcta_off_off =
       align_up(IL.pitems_off + sizeof(pk_work_item) * p->pair_items.size(), pk::kImageAlign);
-  IL.v8chunk_off = align_up(IL.pcta_off_off + sizeof(int32_t) * p->pair_cta_offsets.size(),
+  IL.sitems_off = align_up(IL.pcta_off_off + sizeof(int32_t) * p->pair_cta_offsets.size(),
+                           pk::kImageAlign);
+  IL.scta_off_off =
+      align_up(IL.sitems_off + sizeof(pk_work_item) * p->share_items.size(), pk::kImageAlign);
+  IL.v8chunk_off = align_up(IL.scta_off_off + sizeof(int32_t) * p->share_offsets.size(),
                             pk::kImageAlign);
   IL.v8row_off = align_up(IL.v8chunk_off + sizeof(int32_t) * p->v8_chunks.size(), pk::kImageAlign);
   // Contiguous keys: an item's key tiles sit in the E4M3 value copy at the
@@ -293,6 +320,12 @@ void schedule_and_image(pk_plan* p, std::vector<pk_work_item> items, int32_t num
                 sizeof(pk_work_item) * p->pair_items.size());
     std::memcpy(p->image.data() + IL.pcta_off_off, p->pair_cta_offsets.data(),
                 sizeof(int32_t) * p->pair_cta_offsets.size());
+  }
+  if (!p->share_items.empty()) {
+    std::memcpy(p->image.data() + IL.sitems_off, p->share_items.data(),
+                sizeof(pk_work_item) * p->share_items.size());
+    std::memcpy(p->image.data() + IL.scta_off_off, p->share_offsets.data(),
+                sizeof(int32_t) * p->share_offsets.size());
   }
   if (!p->v8_chunks.empty())
     std::memcpy(p->image.data() + IL.v8chunk_off, p->v8_chunks.data(),
@@ -666,6 +699,29 @@ pk_status pk_plan_set_sm_pairs(pk_plan* p, int32_t enable) {
   if (p == nullptr) return PK_ERR_INVALID_ARG;
   if (enable && p->num_clusters == 0) return PK_ERR_UNSUPPORTED;
   p->use_pairs = enable != 0;
+  return PK_OK;
+}
+
+pk_status pk_plan_set_kv_share(pk_plan* p, int32_t enable) {
+  if (p == nullptr) return PK_ERR_INVALID_ARG;
+  if (enable && p->num_share_clusters == 0) return PK_ERR_UNSUPPORTED;
+  p->use_share = enable != 0;
+  return PK_OK;
+}
+
+pk_status pk_plan_get_share(const pk_plan* p, int32_t* num_clusters, pk_work_item* items,
+                            int64_t n_items, int32_t* cluster_offsets, int64_t n_offsets) {
+  if (p == nullptr || num_clusters == nullptr) return PK_ERR_INVALID_ARG;
+  *num_clusters = p->num_share_clusters;
+  if (items == nullptr && cluster_offsets == nullptr) return PK_OK;
+  const int64_t ni = static_cast<int64_t>(p->share_items.size());
+  if (items == nullptr || cluster_offsets == nullptr || n_items < ni ||
+      n_offsets < static_cast<int64_t>(p->share_offsets.size()))
+    return PK_ERR_INVALID_ARG;
+  if (ni) std::memcpy(items, p->share_items.data(), sizeof(pk_work_item) * ni);
+  if (!p->share_offsets.empty())
+    std::memcpy(cluster_offsets, p->share_offsets.data(),
+                sizeof(int32_t) * p->share_offsets.size());
   return PK_OK;
 }
 

@@ -110,6 +110,33 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, c
   return mbar_wait_slow(bar, parity, c, false);
 }
 
+// Drain wait on a ring barrier of a head-pair cluster (two CTAs filling and
+// emptying each other's ring stages).  After an abort the other CTA may
+// never send its half of a stage or read it, so the awaited phase may never
+// complete; what can still be in flight (this CTA's own copies, the other
+// CTA's last commit arrivals) lands within microseconds.  So the wait is
+// bounded by kDrainLimitNs, or, once the CTA has aborted, by
+// kClusterAbortDrainNs from its start.
+constexpr uint64_t kClusterAbortDrainNs = 2000000ull;
+__device__ __forceinline__ bool mbar_wait_cluster_drain(uint32_t bar, uint32_t parity,
+                                                        const WaitCtl& c) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 15u) == 0) {
+      const uint64_t dt = globaltimer_ns() - t0;
+      const bool aborted = *c.abort_flag != 0;
+      if (aborted && dt > kClusterAbortDrainNs) return false;
+      if (dt > kDrainLimitNs) {
+        *c.abort_flag = 1;
+        if (c.status) atomicCAS(c.status, 0, (int32_t)PK_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
 // Bounded wait for a waiter with nothing else to do (the epilogue warps
 // between units): each try suspends the thread for up to 2 us, so the
 // waiting warps take no issue slots from the softmax warps on the same SM

@@ -356,3 +356,300 @@ def test_pair_kernel_abort_path_drains_every_copy_and_mma(kst, vst):
         aborted += _run(units, kst, vst, seed, rare=rng.choice([0.0, 0.1, 1.0]),
                         abort_at=rng.choice([0.001, 0.01, 0.1, 0.5]), pair=True)
     assert aborted >= 150
+
+
+# ---------------------------------------------------------------------------
+# Head-pair clusters: two CTAs, each running every role of the one-CTA kernel
+# on its own query head of the same items, share the key and value rings.
+# Each CTA's producer arms its own full barrier for the whole tile and copies
+# half of it into both CTAs (a multicast copy lands in the two CTAs
+# independently); each CTA's MMA issuer commits the stage's empty barrier in
+# both CTAs, so a stage is refilled only after both CTAs' products have read
+# it.  Barrier events carry the phase they belong to, and the model fails if
+# one reaches a barrier whose current phase is another: with two senders per
+# ring barrier, that is how a refill racing a slow reader would show.  The
+# arrivals a commit makes in the other CTA travel separately and land later.
+# Before exiting, each producer waits for its ring's last full and empty
+# phases (after an abort those may never complete; the kernel bounds such a
+# drain, and the model lets a wait run out only when nothing else can move,
+# copies and arrivals landing long before any bound expires).  At the
+# cluster barrier nothing may be in flight.
+
+class _TagBar:
+    """A barrier whose phase completes after `count` events, each tagged with
+    the phase it belongs to."""
+
+    def __init__(self, name, count):
+        self.name, self.count, self.c, self.pending = name, count, 0, 0
+
+    def event(self, phase):
+        assert phase == self.c, f"{self.name}: event of phase {phase} while phase {self.c} is open"
+        self.pending += 1
+        if self.pending == self.count:
+            self.pending = 0
+            self.c += 1
+
+
+def _run_share(units, kst, vst, seed, rare, abort_at=None, final_empty_wait=True):
+    rng = random.Random(seed)
+    R = (0, 1)
+    B = {}
+    for r in R:
+        for i in range(2):
+            for nm in ("QFull", "QEmpty", "MmaDone", "SFull", "PvDone"):
+                B[f"{nm}{i}@{r}"] = _Bar(f"{nm}{i}@{r}")
+            for nm in ("SFree", "PReady"):
+                B[f"{nm}{i}@{r}"] = _Bar(f"{nm}{i}@{r}")
+        for nm in ("OFree", "LmFull", "LmFree"):
+            B[f"{nm}@{r}"] = _Bar(f"{nm}@{r}")
+        for i in range(kst):
+            B[f"KFull{i}@{r}"] = _TagBar(f"KFull{i}@{r}", 3)   # arm + two halves
+            B[f"KEmpty{i}@{r}"] = _TagBar(f"KEmpty{i}@{r}", 2)  # both CTAs' commits
+        for i in range(vst):
+            B[f"VFull{i}@{r}"] = _TagBar(f"VFull{i}@{r}", 3)
+            B[f"VEmpty{i}@{r}"] = _TagBar(f"VEmpty{i}@{r}", 2)
+    pipes = {r: [] for r in R}  # per CTA: MMA commits, completed in order
+    inflight = []   # copies and remote commit arrivals, landing in any order
+    abort = {r: False for r in R}
+
+    def hit(target):  # target: name, or (name, phase) for a tagged barrier
+        if isinstance(target, tuple):
+            B[target[0]].event(target[1])
+        else:
+            B[target].arrive()
+
+    def W(n, par, k):
+        return ("wait", n, par, k)
+
+    def D(n, par, k):
+        return ("drain", n, par, k)
+
+    def producer(r, ring, stages, with_q):
+        g = armed = q_armed = 0
+        ok = True
+        for u, n in enumerate(units):
+            if with_q:
+                qb = u & 1
+                ok = yield W(f"QEmpty{qb}@{r}", ((u >> 1) & 1) ^ 1, (u >> 1) - 1)
+                if not ok:
+                    break
+                yield ("copy", [f"QFull{qb}@{r}"])
+                q_armed += 1
+            for _ in range(n):
+                st, ph = g % stages, g // stages
+                ok = yield W(f"{ring}Empty{st}@{r}", (ph & 1) ^ 1, ph - 1)
+                if not ok:
+                    break
+                yield ("arrive", (f"{ring}Full{st}@{r}", ph))
+                yield ("copy", [(f"{ring}Full{st}@{x}", ph) for x in R])
+                armed += 1
+                g += 1
+            if not ok:
+                break
+        for k in range(1, min(stages, armed) + 1):
+            i = armed - k
+            yield D(f"{ring}Full{i % stages}@{r}", (i // stages) & 1, i // stages)
+        for k in range(1, min(2, q_armed) + 1):
+            i = q_armed - k
+            yield D(f"QFull{i & 1}@{r}", (i >> 1) & 1, i >> 1)
+        if final_empty_wait:  # the other CTA's last commits have landed here
+            for k in range(1, min(stages, armed) + 1):
+                i = armed - k
+                yield D(f"{ring}Empty{i % stages}@{r}", (i // stages) & 1, i // stages)
+
+    def mma_s(r):
+        t = 0
+        ok = True
+        for u, n in enumerate(units):
+            qb = u & 1
+            ok = yield W(f"QFull{qb}@{r}", (u >> 1) & 1, u >> 1)
+            if not ok:
+                break
+            for j in range(n):
+                k, b, ph = t % kst, t & 1, t // kst
+                ok = yield W(f"KFull{k}@{r}", ph & 1, ph)
+                if ok and t >= 2:
+                    ok = yield W(f"SFree{b}@{r}", ((t >> 1) - 1) & 1, (t >> 1) - 1)
+                if not ok:
+                    break
+                yield ("mma", [f"SFull{b}@{r}"] + [(f"KEmpty{k}@{x}", ph) for x in R] +
+                       ([f"QEmpty{qb}@{r}"] if j + 1 == n else []))
+                t += 1
+            if not ok:
+                break
+        yield ("mma", [f"MmaDone0@{r}"])
+        yield D(f"MmaDone0@{r}", 0, 0)
+
+    def mma_pv(r):
+        t = 0
+        ok = True
+        for u, n in enumerate(units):
+            for j in range(n):
+                v, b, ph = t % vst, t & 1, t // vst
+                ok = yield W(f"VFull{v}@{r}", ph & 1, ph)
+                if ok:
+                    ok = yield W(f"PReady{b}@{r}", (t >> 1) & 1, t >> 1)
+                if ok and j == 0:
+                    ok = yield W(f"OFree@{r}", (u & 1) ^ 1, u - 1)
+                if not ok:
+                    break
+                yield ("mma", [f"PvDone{b}@{r}"] + [(f"VEmpty{v}@{x}", ph) for x in R])
+                t += 1
+            if not ok:
+                break
+        yield ("mma", [f"MmaDone1@{r}"])
+        yield D(f"MmaDone1@{r}", 0, 0)
+
+    def softmax(r):
+        t = 0
+        for u, n in enumerate(units):
+            for j in range(n):
+                b = t & 1
+                if not (yield W(f"SFull{b}@{r}", (t >> 1) & 1, t >> 1)):
+                    return
+                yield ("arrive", f"SFree{b}@{r}")
+                if j > 0 and rng.random() < rare:
+                    tp = t - 1
+                    if not (yield W(f"PvDone{tp & 1}@{r}", (tp >> 1) & 1, tp >> 1)):
+                        return
+                if t >= 2:
+                    tp = t - 2
+                    if not (yield W(f"PvDone{tp & 1}@{r}", (tp >> 1) & 1, tp >> 1)):
+                        return
+                yield ("arrive", f"PReady{b}@{r}")
+                t += 1
+            if u > 0:
+                if not (yield W(f"LmFree@{r}", (u - 1) & 1, u - 1)):
+                    return
+            yield ("arrive", f"LmFull@{r}")
+
+    def epilogue(r):
+        t = 0
+        for u, n in enumerate(units):
+            t += n
+            tl = t - 1
+            if not (yield W(f"LmFull@{r}", u & 1, u)):
+                return
+            yield ("arrive", f"LmFree@{r}")
+            if not (yield W(f"PvDone{tl & 1}@{r}", (tl >> 1) & 1, tl >> 1)):
+                return
+            yield ("arrive", f"OFree@{r}")
+
+    roles = {}
+    for r in R:
+        roles[(r, "qk")] = producer(r, "K", kst, True)
+        roles[(r, "v")] = producer(r, "V", vst, False)
+        roles[(r, "s")] = mma_s(r)
+        roles[(r, "pv")] = mma_pv(r)
+        roles[(r, "softmax")] = softmax(r)
+        roles[(r, "epilogue")] = epilogue(r)
+    cur = {k: None for k in roles}
+    done = set()
+
+    def advance(k, value):
+        try:
+            cur[k] = roles[k].send(value) if value is not None else next(roles[k])
+        except StopIteration:
+            cur[k] = None
+            done.add(k)
+
+    for k in roles:
+        advance(k, None)
+    rounds = 0
+    while len(done) < len(roles):
+        rounds += 1
+        assert rounds < 400000, "model did not finish"
+        progressed = False
+        for r in R:
+            if abort_at is not None and not abort[r] and rng.random() < abort_at:
+                abort[r] = progressed = True
+            if pipes[r] and rng.random() < 0.5:
+                targets = pipes[r].pop(0)
+                for tg in targets:  # this CTA's barriers now, the other CTA's later
+                    if isinstance(tg, tuple) and not tg[0].endswith(f"@{r}"):
+                        inflight.append(tg)
+                    else:
+                        hit(tg)
+                progressed = True
+        if inflight and rng.random() < 0.5:
+            hit(inflight.pop(rng.randrange(len(inflight))))
+            progressed = True
+        order = [k for k in roles if k not in done]
+        rng.shuffle(order)
+        stuck = []
+        for k in order:
+            r, op = k[0], cur[k]
+            if op[0] == "arrive":
+                hit(op[1])
+                advance(k, True)
+                progressed = True
+            elif op[0] == "mma":
+                pipes[r].append(op[1])
+                advance(k, True)
+                progressed = True
+            elif op[0] == "copy":
+                inflight.extend(op[1])
+                advance(k, True)
+                progressed = True
+            else:
+                kind, nm, par, kk = op
+                c = B[nm].c
+                if (c & 1) != par:
+                    assert c >= kk + 1, f"{k}: wait on {nm} phase {kk} passed early ({c} completed)"
+                    advance(k, True)
+                    progressed = True
+                else:
+                    assert c <= kk, f"{k}: wait on {nm} phase {kk} faces phase {c} (aliased)"
+                    if kind == "wait" and abort[r]:
+                        advance(k, False)
+                        progressed = True
+                    else:
+                        stuck.append(k)
+        if not progressed and not inflight and not any(pipes.values()):
+            # Nothing can move: a bounded wait runs out (a drain wait after
+            # its own, longer, limit) and its CTA aborts.
+            assert stuck, "deadlock with no waiter"
+            assert abort_at is not None, f"deadlock: { {k: cur[k] for k in stuck} }"
+            k = stuck[0]
+            abort[k[0]] = True
+            advance(k, False)
+    # both CTAs have left every role; they pass the cluster barrier and exit
+    assert not any(pipes.values()), f"MMAs still in flight at exit: {pipes}"
+    assert not inflight, f"copies or arrivals still in flight at exit: {inflight}"
+    return abort[0] or abort[1]
+
+
+@pytest.mark.parametrize("kst,vst", [(3, 2), (4, 3)])  # bf16 and FP8 queries/keys rings
+def test_share_cluster_barrier_protocol(kst, vst):
+    for seed in range(120):
+        rng = random.Random(7000 + 10 * kst + vst + seed)
+        units = [rng.choice([1, 1, 2, 3, 4, 5, 9, 17]) for _ in range(rng.randint(1, 16))]
+        assert not _run_share(units, kst, vst, seed, rare=rng.choice([0.0, 0.1, 1.0]))
+
+
+@pytest.mark.parametrize("kst,vst", [(3, 2)])
+def test_share_cluster_abort_path(kst, vst):
+    """Timeouts at random moments in either CTA: both CTAs leave, and nothing
+    is in flight when they pass the cluster barrier."""
+    aborted = 0
+    for seed in range(250):
+        rng = random.Random(11 + 10 * kst + vst + seed)
+        units = [rng.choice([1, 2, 3, 5, 9, 17]) for _ in range(rng.randint(1, 12))]
+        aborted += _run_share(units, kst, vst, seed, rare=rng.choice([0.0, 0.1, 1.0]),
+                              abort_at=rng.choice([0.001, 0.01, 0.1, 0.5]))
+    assert aborted >= 120
+
+
+def test_share_model_catches_a_missing_final_wait():
+    """Plant a mistake (the producers skip the wait for the other CTA's last
+    commits): some run must end with an arrival still in flight."""
+    caught = 0
+    for seed in range(80):
+        rng = random.Random(300 + seed)
+        units = [rng.choice([1, 2, 3, 5]) for _ in range(rng.randint(1, 6))]
+        try:
+            _run_share(units, 3, 2, seed, 0.1, final_empty_wait=False)
+        except AssertionError as e:
+            assert "in flight" in str(e)
+            caught += 1
+    assert caught >= 10
