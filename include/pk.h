@@ -197,11 +197,13 @@ pk_status pk_plan_shard(const pk_plan* full, int32_t rank, int32_t num_ranks, in
  * kernel.  The plan pairs, one query head at a time, query tiles that
  * read the same key/value tiles (same first key row, key/value head and
  * query head) by their key-tile count; a pair visits the larger count (the
- * other rows see the extra tiles fully masked).  Measured on GB300: faster on packs of long sequences (+3 to +4%
- * on the two 24,832-token sequences of the high-res edit pack), slower on
- * packs of short ones (-2% on the mixed-resolution pack, -6 to -15% on the
- * CFG pair), so it is off by default.  The pages have no counterpart; it is
- * a tuning option of this library.
+ * other rows see the extra tiles fully masked).  Measured on GB300 against
+ * the one-CTA kernel: faster on packs of long sequences (+3 to +4% on the
+ * two 24,832-token sequences of the high-res edit pack), slower on packs of
+ * short ones (-2% on the mixed-resolution pack, -6 to -15% on the CFG
+ * pair); the default head-pair clusters (pk_plan_set_kv_share) are faster
+ * than it on every pack measured, so it is off by default.  The pages have
+ * no counterpart; it is a tuning option of this library.
  *   PK_ERR_INVALID_ARG for a null plan; PK_ERR_UNSUPPORTED when enabling a
  *   plan that has no pair schedule (head_dim other than 128, or built for
  *   fewer than two CTAs).  Takes effect at the next launch; not thread-safe

@@ -132,8 +132,9 @@ class Plan:
 
     def set_sm_pairs(self, enable: bool = True) -> "Plan":
         """Run this plan on SM pairs (pk_plan_set_sm_pairs; head_dim 128):
-        faster on packs of long sequences, slower on short ones, off by
-        default.  Returns the plan."""
+        against the one-CTA kernel faster on packs of long sequences and
+        slower on short ones; slower than the default head-pair clusters on
+        every pack measured, off by default.  Returns the plan."""
         check(self._lib.pk_plan_set_sm_pairs(self._h, 1 if enable else 0), "pk_plan_set_sm_pairs")
         return self
 
