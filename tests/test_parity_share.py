@@ -81,6 +81,21 @@ def test_share_fp8_equals_the_one_cta_kernel(name):
     _assert_identical(*_both(pack, None, None, v.cuda(), fp8=(q8.cuda(), qs, k8.cuda(), ks)))
 
 
+@pytest.mark.parametrize("ctas", [2, 7, 24])
+def test_share_with_few_clusters(ctas):
+    """Plans built for few CTAs: one to twelve clusters, each running many
+    items back to back (and an odd CTA count, whose last CTA the clusters
+    leave out)."""
+    pack = W.CONFIGS["cfg_pair"]()
+    q, k, v = W.make_qkv(pack, device="cuda")
+    args = (pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d)
+    one = pk.plan(*args, num_ctas=ctas).set_kv_share(False)
+    share = pk.plan(*args, num_ctas=ctas)
+    assert len(share.share_schedule()[1]) - 1 == ctas // 2
+    _assert_identical(pk.attn_fwd(q, k, v, one, pack.scale, check_status=True),
+                      pk.attn_fwd(q, k, v, share, pack.scale, check_status=True))
+
+
 def test_share_against_the_oracle():
     pack = _packs()[-1]
     q, k, v = W.make_qkv(pack)
