@@ -213,8 +213,8 @@ pk_status pk_plan_set_sm_pairs(pk_plan* plan, int32_t enable);
 
 /*
  * Head-pair clusters, on by default where the plan has their schedule
- * (head_dim 128 and an even number of query heads per key/value head:
- * every work item then holds two query heads).  A cluster of two CTAs on
+ * (an even number of query heads per key/value head: every work item then
+ * holds two query heads; head_dim 64 or 128).  A cluster of two CTAs on
  * neighbouring SMs runs each of its items with one query head per CTA; the
  * two stream the same key and value tiles, and each CTA copies half of
  * every tile from global memory into the shared memory of both (TMA
@@ -224,7 +224,7 @@ pk_status pk_plan_set_sm_pairs(pk_plan* plan, int32_t enable);
  * Applies to pk_attn_fwd and the calls built on it, and to
  * pk_attn_fwd_fp8; pk_plan_set_sm_pairs takes precedence, and
  * pk_attn_fwd_fp8_pv keeps the one-CTA kernel.  Measured on GB300: +1 to
- * +3.5% on the d = 128 packs.  The pages have no counterpart; it is a
+ * +8% on the d = 128 packs.  The pages have no counterpart; it is a
  * tuning option of this library.  enable = 0 selects the one-CTA kernel.
  *   PK_ERR_INVALID_ARG for a null plan; PK_ERR_UNSUPPORTED when enabling a
  *   plan without the schedule.  Takes effect at the next launch; not

@@ -140,8 +140,8 @@ class Plan:
 
     def set_kv_share(self, enable: bool = True) -> "Plan":
         """Head-pair clusters sharing each key/value tile (pk_plan_set_kv_share):
-        on by default where the plan has their schedule (head_dim 128, an even
-        number of query heads per key/value head); ``False`` selects the
+        on by default where the plan has their schedule (an even number of
+        query heads per key/value head); ``False`` selects the
         one-CTA kernel.  Bit-identical results either way.  Returns the plan."""
         check(self._lib.pk_plan_set_kv_share(self._h, 1 if enable else 0), "pk_plan_set_kv_share")
         return self

@@ -43,11 +43,11 @@
 // rank-0 CTA's producers and issuers serve both, each CTA holding half of
 // every key and value tile, and both CTAs run their rows' softmax and
 // epilogue.
-// SHARE (the default at D = 128 where every work item has two query heads):
+// SHARE (the default where every work item has two query heads):
 // a cluster of two CTAs on neighbouring SMs runs each item with one query
 // head per CTA.  Both stream the same key/value tiles through rings of the
 // same shape; each CTA's producers copy half of every tile (one 64-column
-// box, or for one-box FP8 key tiles 64 of the rows) into the shared memory
+// box, or for one-box tiles 64 of the rows) into the shared memory
 // of both CTAs (TMA multicast), and a ring stage is refilled only after both
 // CTAs' products have read it (each MMA issuer's commit arrives on the
 // stage's empty barrier in both CTAs).  Everything else is the one-CTA
@@ -134,10 +134,12 @@ struct Cfg {
   static_assert(!F8 || D == 128, "FP8 queries/keys need head_dim 128");
   static_assert(!V8 || F8, "E4M3 values come with E4M3 queries and keys");
   static_assert(!PAIR || (D == 128 && !F8), "the SM-pair kernel is bf16 with head_dim 128");
-  static_assert(!SHARE || (D == 128 && !V8 && !PAIR), "head-pair clusters: head_dim 128, 16-bit values");
-  // SHARE: rows per key copy.  Two-box (bf16) key tiles split by boxes, each
-  // CTA copying one whole box; one-box (FP8) key tiles split by rows.
+  static_assert(!SHARE || (!V8 && !PAIR), "head-pair clusters: 16-bit values, one CTA per head");
+  // SHARE: rows per key and value copy.  Two-box tiles (bf16 keys and the
+  // values at D = 128) split by boxes, each CTA copying one whole box;
+  // one-box tiles (FP8 keys, D = 64) split by rows, 64 each.
   static constexpr int kShareKRows = kQKBoxes == 1 ? 64 : 128;
+  static constexpr int kShareVRows = kVBoxes == 1 ? 64 : 128;
   // Arrivals of the softmax (S buffer free, P ready) and the epilogue (O
   // free): one per thread of the CTA's warpgroup, or, in the pair kernel,
   // of both CTAs' warpgroups (on the rank-0 CTA's barrier).
@@ -321,10 +323,15 @@ __device__ void producer_v_role(const KernelParams& p, const CUtensorMap* tm_v, 
       if (!(ok = mbar_wait(bar(C::kVEmpty + st), ph ^ 1u, wc))) break;
       mbar_arrive_expect_tx(bar(C::kVFull + st), kCtas * C::kVTileBytes);
       ++v_armed;
-      if constexpr (SHARE) {  // this CTA's 64-column box, into both CTAs
-        tma_load_3d_mc(sbase + C::kOffV + st * C::kVTileBytes + srank * kBoxBytes, tm_v,
-                       bar(C::kVFull + st), srank * 64, w.hkv, key_tile_row(p, w, j), (uint16_t)3,
-                       keep);
+      if constexpr (SHARE) {  // this CTA's half of the tile, into both CTAs
+        if constexpr (C::kVBoxes == 2)
+          tma_load_3d_mc(sbase + C::kOffV + st * C::kVTileBytes + srank * kBoxBytes, tm_v,
+                         bar(C::kVFull + st), srank * 64, w.hkv, key_tile_row(p, w, j),
+                         (uint16_t)3, keep);
+        else
+          tma_load_3d_mc(sbase + C::kOffV + st * C::kVTileBytes + srank * 64 * 128, tm_v,
+                         bar(C::kVFull + st), 0, w.hkv, key_tile_row(p, w, j) + srank * 64,
+                         (uint16_t)3, keep);
       } else if constexpr (PAIR) {  // value columns [64 r, 64 r + 64) to rank r
 #pragma unroll
         for (int r = 0; r < 2; ++r)
@@ -1133,7 +1140,8 @@ pk_status launch(const pk_plan* plan, const void* q, const void* k, const void* 
   if (!make_map(&tq, q, plan->hq, plan->T, D, qk_dt) ||
       !make_map(&tk, k, plan->hkv, plan->Tk, D, qk_dt, SHARE ? C::kShareKRows : C::kKRows) ||
       !(V8 ? make_map_v8t(&tv, v16, plan->hkv, plan->v8_rows, D)
-           : make_map(&tv, v16, plan->hkv, plan->Tk, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16)))
+           : make_map(&tv, v16, plan->hkv, plan->Tk, D, CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                      SHARE ? C::kShareVRows : 128)))
     return PK_ERR_CUDA;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
       cudaSuccess) {
@@ -1288,7 +1296,12 @@ pk_status pk_attn_fwd_converted(const pk_plan* plan, const void* q, const void* 
                                                     dev_status);
     return launch<128, false, false>(plan, q, k, v16, out, lse, scale, s, dev_status);
   }
-  if (plan->head_dim == 64) return launch<64, false, false>(plan, q, k, v16, out, lse, scale, s, dev_status);
+  if (plan->head_dim == 64) {
+    if (plan->use_share && plan->num_share_clusters > 0)  // pk_plan_set_kv_share
+      return launch<64, false, false, false, true>(plan, q, k, v16, out, lse, scale, s,
+                                                   dev_status);
+    return launch<64, false, false>(plan, q, k, v16, out, lse, scale, s, dev_status);
+  }
   return PK_ERR_UNSUPPORTED;
 }
 

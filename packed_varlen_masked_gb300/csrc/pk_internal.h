@@ -84,8 +84,8 @@ struct pk_plan {
   bool use_pairs = false;                  // pk_plan_set_sm_pairs
   std::vector<pk_work_item> pair_items;    // [2 * num_pairs], cluster-ordered
   std::vector<int32_t> pair_cta_offsets;   // [num_clusters + 1], in pairs
-  // The same items for head-pair clusters (head_dim 128, every item with
-  // two query heads): a cluster of two CTAs on neighbouring SMs runs each of
+  // The same items for head-pair clusters (every item with two query
+  // heads): a cluster of two CTAs on neighbouring SMs runs each of
   // its items with one query head per CTA, the two CTAs streaming the same
   // key/value tiles, each copying half of every tile into both.  Scheduled
   // longest first over num_share_clusters = num_ctas / 2 clusters; the

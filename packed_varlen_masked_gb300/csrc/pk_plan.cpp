@@ -216,14 +216,14 @@ void schedule_pairs(pk_plan* p, const std::vector<pk_work_item>& items, int32_t 
 
 // Head-pair cluster items (see pk_plan::share_items): the plan's items as
 // they are, each run by one cluster (a query head per CTA), scheduled
-// longest first over `clusters` clusters.  None unless head_dim is 128 and
-// every item has two query heads.
+// longest first over `clusters` clusters.  None unless every item has two
+// query heads.
 void schedule_share(pk_plan* p, const std::vector<pk_work_item>& items, int32_t clusters) {
   p->share_items.clear();
   p->share_offsets.clear();
   p->num_share_clusters = 0;
   p->use_share = false;
-  if (p->head_dim != 128 || clusters < 1 || items.empty()) return;
+  if (clusters < 1 || items.empty()) return;
   for (const pk_work_item& w : items)
     if (w.hq1 < 0) return;
   const int32_t n = static_cast<int32_t>(items.size());

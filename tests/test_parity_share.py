@@ -1,5 +1,5 @@
 """GPU parity of the head-pair clusters (pk_plan_set_kv_share, the default
-at head_dim 128 where every work item holds two query heads).  Each CTA of
+wherever every work item holds two query heads).  Each CTA of
 a cluster runs the one-CTA kernel's arithmetic, in the same order, on its
 query head; only the copies of the key and value tiles are shared.  So the
 outputs must equal the one-CTA kernel's bit for bit (the default path is
@@ -45,8 +45,9 @@ def _assert_identical(a, b):
 
 def _packs():
     rng = np.random.default_rng(91)
-    packs = [W.random_pack(rng, 5, 900, hq=hq, hkv=hkv, d=128, name=f"rnd{i}-h{hq}-{hkv}")
-             for i, (hq, hkv) in enumerate([(8, 2), (4, 2), (2, 1), (16, 2), (8, 4)])]
+    packs = [W.random_pack(rng, 5, 900, hq=hq, hkv=hkv, d=d, name=f"rnd{i}-h{hq}-{hkv}-d{d}")
+             for i, (hq, hkv, d) in enumerate([(8, 2, 128), (4, 2, 128), (2, 1, 128), (16, 2, 128),
+                                               (8, 4, 128), (8, 2, 64), (4, 2, 64)])]
     packs += [
         W.Pack("odd-tiles", [[(W.TEXT, 1)], [], [(W.IMAGE, 129)], [(W.TEXT, 128), (W.IMAGE, 257)],
                              [(W.IMAGE, 383), (W.TEXT, 1)]], hq=4, hkv=2, d=128, seed=41),
