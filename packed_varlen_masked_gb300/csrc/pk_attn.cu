@@ -115,14 +115,15 @@ struct Cfg {
   // Rings: two query tiles (the next unit's loads during this one), and key
   // and value tiles.  Shared memory stays above half an SM, so exactly one
   // CTA (and one 512-column TMEM allocation) lives on each SM.  In head-pair
-  // clusters a stage waits for the slower CTA of the two: there bf16 takes
-  // two key and three value stages (0.5 to 1.5 % faster than three and two)
-  // and FP8 queries/keys five key stages of 16 KB and three value stages (0.3
-  // to 1 % faster than four and three).
+  // clusters a stage waits for the slower CTA of the two: there bf16 at
+  // D = 128 takes two key and three value stages (0.5 to 1.5 % faster than
+  // three and two) and FP8 queries/keys five key stages of 16 KB and three
+  // value stages (0.3 to 1 % faster than four and three); D = 64 keeps the
+  // one-CTA kernel's four and four.
   static constexpr int kKStages =
-      SHARE ? (F8 ? 5 : 2) : PAIR ? 7 : (F8 ? 4 : (D == 128 ? 3 : 4));
+      SHARE ? (D == 64 ? 4 : (F8 ? 5 : 2)) : PAIR ? 7 : (F8 ? 4 : (D == 128 ? 3 : 4));
   static constexpr int kVStages =
-      SHARE ? 3 : PAIR ? 3 : (V8 ? 4 : (F8 ? 3 : (D == 128 ? 2 : 4)));
+      SHARE ? (D == 64 ? 4 : 3) : PAIR ? 3 : (V8 ? 4 : (F8 ? 3 : (D == 128 ? 2 : 4)));
   // TMEM columns: S double buffer, P double buffer (16-bit pairs), O.
   static constexpr uint32_t kColS0 = 0;    // S(t) in [128*(t%2), +128)
   static constexpr uint32_t kColP0 = 256;  // P(t) in [256 + 64*(t%2), +64)

@@ -619,7 +619,7 @@ def _run_share(units, kst, vst, seed, rare, abort_at=None, final_empty_wait=True
     return abort[0] or abort[1]
 
 
-@pytest.mark.parametrize("kst,vst", [(2, 3), (5, 3), (3, 2)])  # bf16, FP8 queries/keys; other
+@pytest.mark.parametrize("kst,vst", [(2, 3), (5, 3), (4, 4), (3, 2)])  # bf16, FP8 q/k, d 64; other
 def test_share_cluster_barrier_protocol(kst, vst):
     for seed in range(120):
         rng = random.Random(7000 + 10 * kst + vst + seed)
