@@ -18,9 +18,9 @@
 // its work items' query heads ("units") one after another; a unit is a
 // 128-row query tile streaming the key/value tiles of its sequence.
 //   warp 0      TMA producer of the query tiles (double buffered) and of a
-//               3-stage ring of key tiles; warp 2: TMA producer of a 2-stage
-//               ring of value tiles (128-byte swizzled boxes, one per 64
-//               columns of the head dimension).
+//               ring of key tiles; warp 2: TMA producer of a ring of value
+//               tiles (128-byte swizzled boxes, one per 64 columns of the
+//               head dimension; ring depths in Cfg).
 //   warp 1      allocates the 512 TMEM columns; one thread issues every
 //               S(t) = Q K(t)^T (both operands K-major in shared memory).
 //   warp 3      one thread issues every O += P(t) V(t) (P read from TMEM, V
@@ -167,9 +167,9 @@ struct Cfg {
 };
 
 // A unit of work is one query head of a work item: a 128-row query tile that
-// streams the key/value tiles of its sequence.  A CTA runs the heads of each
-// of its items back to back, so the second head's keys and values come from
-// L2.  Every role walks the same unit sequence.
+// streams the key/value tiles of its sequence.  A CTA on its own runs the
+// heads of each of its items back to back, so the second head's keys and
+// values come from L2.  Every role walks the same unit sequence.
 // In the pair kernel the items come in (rank 0, rank 1) pairs and each CTA
 // walks its own item of every pair (stride 2).  In a head-pair cluster each
 // CTA runs one query head of every item (fixed slot: its cluster rank).
