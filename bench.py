@@ -100,6 +100,19 @@ def load_traffic():
     return float(m_b.group(1))
 
 
+# TMA multicast (the head-pair clusters' shared key/value copies) runs only in
+# single-GPU runs: on more than one GPU every plan here takes the one-CTA
+# kernel.
+SINGLE_GPU = True
+
+
+def cta_plan(plan):
+    """The plan as this run may launch it (see SINGLE_GPU)."""
+    if not SINGLE_GPU and plan.share_schedule()[0].shape[0] > 0:
+        plan.set_kv_share(False)
+    return plan
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons during a region."""
 
@@ -409,8 +422,8 @@ def layouts_bench(pk, torch, stream, dev, pack, q, k, v, reps=10):
     for name, kk, vv, kw in (("prefix", k, v, {}),
                              ("prefix_paged", kp, vp,
                               {"block_table": table, "num_kv_rows": kp.shape[0]})):
-        pl = pk.plan_layout(cu_q, cu, sg, pack.hq, pack.hkv, pack.d, q_pos0=q_pos0, k_pos0=z,
-                            device=dev, **kw)
+        pl = cta_plan(pk.plan_layout(cu_q, cu, sg, pack.hq, pack.hkv, pack.d, q_pos0=q_pos0,
+                                     k_pos0=z, device=dev, **kw))
         out = torch.empty_like(qs)
         lse = torch.empty(pack.hq, qs.shape[0], dtype=torch.float32, device=dev)
         ws = torch.empty(pl.workspace_bytes, dtype=torch.uint8, device=dev)
@@ -437,7 +450,7 @@ def fp8_bench(pk, torch, stream, dev, pack, q, k, v, reps=10):
     bf16 values."""
     q8, qs = W.quantize_e4m3(q)
     k8, ks = W.quantize_e4m3(k)
-    plan = pk.plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d, device=dev)
+    plan = cta_plan(pk.plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d, device=dev))
     out = torch.empty_like(q)
     lse = torch.empty(pack.hq, pack.total_tokens, dtype=torch.float32, device=dev)
     ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
@@ -502,7 +515,8 @@ def sweep(pk, torch, stream, dev):
         q = torch.randn(T, pack.hq, pack.d, device=dev, generator=g).bfloat16() * pack.q_mult
         k = torch.randn(T, pack.hkv, pack.d, device=dev, generator=g).bfloat16()
         v = torch.randn(T, pack.hkv, pack.d, device=dev, generator=g).bfloat16()
-        plan = pk.plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d, device=dev)
+        plan = cta_plan(pk.plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d,
+                                device=dev))
         out = torch.empty_like(q)
         lse = torch.empty(pack.hq, T, dtype=torch.float32, device=dev)
         ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
@@ -528,7 +542,7 @@ def sweep(pk, torch, stream, dev):
             ms2 = timed(pair)
             res[name]["sm_pairs"] = {"ms": round(ms2, 4), "useful_tflops": round(fl / ms2 / 1e9, 1)}
             del pair
-            if plan.share_schedule()[0].shape[0] > 0:  # the one-CTA kernel (no K/V sharing)
+            if SINGLE_GPU and plan.share_schedule()[0].shape[0] > 0:  # one CTA per SM, no sharing
                 one = pk.plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d,
                               device=dev).set_kv_share(False)
                 ms4 = timed(one)
@@ -586,6 +600,8 @@ def main():
         ap.error("--warmup must be >= 3")
 
     world, rank, local = dist_setup(args)
+    global SINGLE_GPU
+    SINGLE_GPU = world == 1
     pack = (W.mixed_resolution(requests=args.requests) if args.workload == "mixed_resolution"
             else W.CONFIGS[args.workload]())
 
@@ -608,16 +624,17 @@ def main():
 
     q, k, v = W.make_qkv(pack)
     q, k, v = q.to(dev), k.to(dev), v.to(dev)
-    plan = pk.plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d, device=dev)
+    plan = cta_plan(pk.plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d, device=dev))
     split = args.split and world > 1
     full_plan = plan
     if split:  # this rank's share of the one pack, on the full tensors
-        plan = full_plan.shard(rank, world, device=dev)
+        plan = cta_plan(full_plan.shard(rank, world, device=dev))
     if args.sm_pairs:
         plan.set_sm_pairs(True)
     elif args.one_cta and plan.share_schedule()[0].shape[0] > 0:
         plan.set_kv_share(False)
-    shared_kv = not args.sm_pairs and not args.one_cta and plan.share_schedule()[0].shape[0] > 0
+    shared_kv = (SINGLE_GPU and not args.sm_pairs and not args.one_cta
+                 and plan.share_schedule()[0].shape[0] > 0)
     out = torch.empty_like(q)
     lse = torch.empty(pack.hq, pack.total_tokens, dtype=torch.float32, device=dev)
     ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
