@@ -97,6 +97,43 @@ def test_share_with_few_clusters(ctas):
                       pk.attn_fwd(q, k, v, share, pack.scale, check_status=True))
 
 
+def _sweep_packs():
+    rng = np.random.default_rng(2024)
+    out = []
+    for i in range(24):
+        hkv = int(rng.choice([1, 2, 4]))
+        group = int(rng.choice([2, 4, 8]))
+        d = int(rng.choice([64, 128]))
+        out.append(W.random_pack(rng, int(rng.integers(1, 7)), int(rng.integers(40, 1600)),
+                                 hq=hkv * group, hkv=hkv, d=d,
+                                 name=f"sweep{i}-h{hkv * group}-{hkv}-d{d}"))
+    return out
+
+
+@pytest.mark.parametrize("pack", _sweep_packs(), ids=lambda p: p.name)
+def test_share_random_sweep(pack):
+    """Seeded random packs over group sizes 2 to 8, one to four key/value
+    heads and both head dimensions; FP8 queries and keys too at d = 128."""
+    q, k, v = W.make_qkv(pack, device="cuda")
+    _assert_identical(*_both(pack, q, k, v))
+    if pack.d == 128:
+        q8, qs = W.quantize_e4m3(q)
+        k8, ks = W.quantize_e4m3(k)
+        _assert_identical(*_both(pack, None, None, v, fp8=(q8, qs, k8, ks)))
+
+
+def test_share_d64_against_the_oracle():
+    pack = W.Pack("share-d64", [[(W.TEXT, 70), (W.IMAGE, 300)], [(W.IMAGE, 129), (W.TEXT, 5)]],
+                  hq=8, hkv=2, d=64, seed=46)
+    q, k, v = W.make_qkv(pack)
+    out_o, lse_o = oracle.attention(q, k, v, pack.cu_seqlens, pack.segments, pack.hq, pack.hkv,
+                                    pack.d, pack.scale)
+    plan = pk.plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d)
+    assert plan.share_schedule()[0].shape[0] > 0
+    out, lse = pk.attn_fwd(q.cuda(), k.cuda(), v.cuda(), plan, pack.scale, check_status=True)
+    check(pack.name, out.float().cpu().numpy(), lse.cpu().numpy(), out_o, lse_o)
+
+
 def test_share_against_the_oracle():
     pack = _packs()[-1]
     q, k, v = W.make_qkv(pack)
