@@ -255,7 +255,8 @@ size_t pk_attn_workspace_bytes_fp8_pv(const pk_plan* plan);
 /*
  * Launch the attention forward on `stream` (asynchronous): two kernels, the
  * conversion of the value rows the plan reads from bf16 to fp16 into the
- * workspace, then the attention.
+ * workspace, then the attention (on head-pair clusters where the plan has
+ * their schedule, see pk_plan_set_kv_share; one CTA per SM otherwise).
  *   q, k, v   : device bf16 tensors as described above.
  *   out, lse  : device outputs as described above.
  *   scale     : softmax scale, finite and > 0 (usually 1/sqrt(head_dim)).
