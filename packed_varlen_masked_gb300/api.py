@@ -144,7 +144,16 @@ class Plan:
         query heads per key/value head); ``False`` selects the
         one-CTA kernel.  Bit-identical results either way.  Returns the plan."""
         check(self._lib.pk_plan_set_kv_share(self._h, 1 if enable else 0), "pk_plan_set_kv_share")
+        self._kv_share_off = not enable
         return self
+
+    @property
+    def kv_share(self) -> bool:
+        """Whether launches of this plan run on head-pair clusters: the plan
+        has their schedule and ``set_kv_share(False)`` has not been called
+        (``set_sm_pairs(True)`` takes precedence at launch)."""
+        return (not getattr(self, "_kv_share_off", False)
+                and self.share_schedule()[0].shape[0] > 0)
 
     def share_schedule(self) -> Tuple[np.ndarray, np.ndarray]:
         """(items int32 [num_items, 8], cluster-ordered; cluster offsets int32

@@ -157,3 +157,22 @@ def test_two_gloo_ranks_split_one_pack_into_a_partition(tmp_path):
     assert sorted(map(tuple, got.tolist())) == sorted(map(tuple, full.tolist()))
     fl = np.load(tmp_path / "flops.npy")
     assert fl[0] == pytest.approx(fl[1], rel=1e-12)
+
+
+def test_multi_gpu_runs_build_plans_for_the_one_cta_kernel():
+    """TMA multicast stays in single-GPU runs: with more than one rank the
+    bench takes every plan off the head-pair clusters."""
+    import bench
+    import packed_varlen_masked_gb300 as pk
+    import workloads as W
+    pack = W.cfg_pair()
+    saved = bench.SINGLE_GPU
+    try:
+        for single, expect in ((True, True), (False, False)):
+            bench.SINGLE_GPU = single
+            plan = bench.cta_plan(pk.Plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv,
+                                          pack.d, num_ctas=152, upload=False))
+            assert plan.kv_share == expect
+            assert plan.share_schedule()[0].shape[0] > 0  # the schedule stays
+    finally:
+        bench.SINGLE_GPU = saved

@@ -43,6 +43,7 @@ def _plans():
 
 @pytest.mark.parametrize("name,plan", _plans(), ids=lambda x: x if isinstance(x, str) else "")
 def test_share_schedule_holds_every_item_once(name, plan):
+    assert plan.kv_share  # on by default wherever the schedule exists
     items, _ = plan.items()
     sitems, soffs = plan.share_schedule()
     assert sitems.shape == items.shape
@@ -74,10 +75,12 @@ def test_no_share_schedule_without_two_heads_per_item(hq, hkv, d, ctas):
     plan = pk.Plan(pack.cu_seqlens, pack.segments, hq, hkv, d, num_ctas=ctas, upload=False)
     sitems, soffs = plan.share_schedule()
     assert sitems.shape[0] == 0 and len(soffs) == 1
+    assert not plan.kv_share
     with pytest.raises(pk.PKError) as e:
         plan.set_kv_share(True)
     assert e.value.status == pk.PK_ERR_UNSUPPORTED
     plan.set_kv_share(False)  # the one-CTA kernel: always allowed
+    assert not plan.kv_share
 
 
 def test_shards_have_their_own_share_schedule():
