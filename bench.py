@@ -108,7 +108,7 @@ SINGLE_GPU = True
 
 def cta_plan(plan):
     """The plan as this run may launch it (see SINGLE_GPU)."""
-    if not SINGLE_GPU and plan.share_schedule()[0].shape[0] > 0:
+    if not SINGLE_GPU and plan.kv_share:
         plan.set_kv_share(False)
     return plan
 
@@ -542,7 +542,7 @@ def sweep(pk, torch, stream, dev):
             ms2 = timed(pair)
             res[name]["sm_pairs"] = {"ms": round(ms2, 4), "useful_tflops": round(fl / ms2 / 1e9, 1)}
             del pair
-            if SINGLE_GPU and plan.share_schedule()[0].shape[0] > 0:  # one CTA per SM, no sharing
+            if plan.kv_share:  # the same inputs on one CTA per SM, without the sharing
                 one = pk.plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d,
                               device=dev).set_kv_share(False)
                 ms4 = timed(one)
@@ -631,10 +631,9 @@ def main():
         plan = cta_plan(full_plan.shard(rank, world, device=dev))
     if args.sm_pairs:
         plan.set_sm_pairs(True)
-    elif args.one_cta and plan.share_schedule()[0].shape[0] > 0:
+    elif args.one_cta and plan.kv_share:
         plan.set_kv_share(False)
-    shared_kv = (SINGLE_GPU and not args.sm_pairs and not args.one_cta
-                 and plan.share_schedule()[0].shape[0] > 0)
+    shared_kv = plan.kv_share and not args.sm_pairs
     out = torch.empty_like(q)
     lse = torch.empty(pack.hq, pack.total_tokens, dtype=torch.float32, device=dev)
     ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
