@@ -212,9 +212,10 @@ pk_status pk_plan_shard(const pk_plan* full, int32_t rank, int32_t num_ranks, in
 pk_status pk_plan_set_sm_pairs(pk_plan* plan, int32_t enable);
 
 /*
- * Head-pair clusters, on by default where the plan has their schedule
- * (an even number of query heads per key/value head: every work item then
- * holds two query heads; head_dim 64 or 128).  A cluster of two CTAs on
+ * Head-pair clusters, on by default at head_dim 128 where the plan has
+ * their schedule (an even number of query heads per key/value head: every
+ * work item then holds two query heads); available, off by default, at
+ * head_dim 64, where they measured 1.7% slower than one CTA per SM.  A cluster of two CTAs on
  * neighbouring SMs runs each of its items with one query head per CTA; the
  * two stream the same key and value tiles, and each CTA copies half of
  * every tile from global memory into the shared memory of both (TMA
@@ -231,6 +232,11 @@ pk_status pk_plan_set_sm_pairs(pk_plan* plan, int32_t enable);
  *   thread-safe against launches running on the plan.
  */
 pk_status pk_plan_set_kv_share(pk_plan* plan, int32_t enable);
+
+/* 1 when launches of the plan run on head-pair clusters (their schedule
+ * exists and pk_plan_set_kv_share has them on; pk_plan_set_sm_pairs still
+ * takes precedence), else 0 (also for a null plan). */
+int32_t pk_plan_kv_share(const pk_plan* plan);
 
 /* Bytes of the device image of the plan (work list, per-CTA offsets, the
  * per-row key limit and, for paged keys, the block table). */
@@ -255,8 +261,8 @@ size_t pk_attn_workspace_bytes_fp8_pv(const pk_plan* plan);
 /*
  * Launch the attention forward on `stream` (asynchronous): two kernels, the
  * conversion of the value rows the plan reads from bf16 to fp16 into the
- * workspace, then the attention (on head-pair clusters where the plan has
- * their schedule, see pk_plan_set_kv_share; one CTA per SM otherwise).
+ * workspace, then the attention (on head-pair clusters when
+ * pk_plan_kv_share(plan) is 1, one CTA per SM otherwise).
  *   q, k, v   : device bf16 tensors as described above.
  *   out, lse  : device outputs as described above.
  *   scale     : softmax scale, finite and > 0 (usually 1/sqrt(head_dim)).

@@ -90,6 +90,7 @@ SIGNATURES = {
                                      ctypes.POINTER(_vp)]),
     "pk_plan_set_sm_pairs": (ctypes.c_int, [_vp, ctypes.c_int32]),
     "pk_plan_set_kv_share": (ctypes.c_int, [_vp, ctypes.c_int32]),
+    "pk_plan_kv_share": (ctypes.c_int32, [_vp]),
     "pk_plan_get_share": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int32), _vp, ctypes.c_int64,
                                          _vp, ctypes.c_int64]),
     "pk_plan_get_pairs": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int32),

@@ -140,20 +140,18 @@ class Plan:
 
     def set_kv_share(self, enable: bool = True) -> "Plan":
         """Head-pair clusters sharing each key/value tile (pk_plan_set_kv_share):
-        on by default where the plan has their schedule (an even number of
-        query heads per key/value head); ``False`` selects the
+        on by default at head_dim 128 where the plan has their schedule (an
+        even number of query heads per key/value head), opt-in at 64;
+        ``False`` selects the
         one-CTA kernel.  Bit-identical results either way.  Returns the plan."""
         check(self._lib.pk_plan_set_kv_share(self._h, 1 if enable else 0), "pk_plan_set_kv_share")
-        self._kv_share_off = not enable
         return self
 
     @property
     def kv_share(self) -> bool:
-        """Whether launches of this plan run on head-pair clusters: the plan
-        has their schedule and ``set_kv_share(False)`` has not been called
-        (``set_sm_pairs(True)`` takes precedence at launch)."""
-        return (not getattr(self, "_kv_share_off", False)
-                and self.share_schedule()[0].shape[0] > 0)
+        """Whether launches of this plan run on head-pair clusters
+        (pk_plan_kv_share; ``set_sm_pairs(True)`` takes precedence)."""
+        return bool(self._lib.pk_plan_kv_share(self._h))
 
     def share_schedule(self) -> Tuple[np.ndarray, np.ndarray]:
         """(items int32 [num_items, 8], cluster-ordered; cluster offsets int32

@@ -89,7 +89,8 @@ struct pk_plan {
   // its items with one query head per CTA, the two CTAs streaming the same
   // key/value tiles, each copying half of every tile into both.  Scheduled
   // longest first over num_share_clusters = num_ctas / 2 clusters; the
-  // default kernel wherever the schedule exists (pk_plan_set_kv_share).
+  // default kernel at head_dim 128 wherever the schedule exists, opt-in at
+  // 64 (pk_plan_set_kv_share).
   int32_t num_share_clusters = 0;
   bool use_share = false;
   std::vector<pk_work_item> share_items;   // [num_items], cluster-ordered

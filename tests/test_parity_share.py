@@ -1,5 +1,6 @@
-"""GPU parity of the head-pair clusters (pk_plan_set_kv_share, the default
-wherever every work item holds two query heads).  Each CTA of
+"""GPU parity of the head-pair clusters (pk_plan_set_kv_share: the default
+at head_dim 128 wherever every work item holds two query heads, opt-in at
+64).  Each CTA of
 a cluster runs the one-CTA kernel's arithmetic, in the same order, on its
 query head; only the copies of the key and value tiles are shared.  So the
 outputs must equal the one-CTA kernel's bit for bit (the default path is
@@ -24,8 +25,8 @@ def _both(pack, q, k, v, plan_args=None, plan_kw=None, fp8=None):
     mk = (lambda: pk.plan_layout(*plan_args, **plan_kw)) if plan_kw is not None else \
         (lambda: pk.plan(*plan_args))
     one = mk().set_kv_share(False)
-    share = mk()
-    assert share.share_schedule()[0].shape[0] > 0
+    share = mk().set_kv_share(True)  # the default at d = 128, opt-in at 64
+    assert share.kv_share
     res = []
     for plan in (one, share):
         if fp8 is None:
@@ -92,7 +93,7 @@ def test_share_with_few_clusters(ctas):
     args = (pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d)
     one = pk.plan(*args, num_ctas=ctas).set_kv_share(False)
     share = pk.plan(*args, num_ctas=ctas)
-    assert len(share.share_schedule()[1]) - 1 == ctas // 2
+    assert share.kv_share and len(share.share_schedule()[1]) - 1 == ctas // 2
     _assert_identical(pk.attn_fwd(q, k, v, one, pack.scale, check_status=True),
                       pk.attn_fwd(q, k, v, share, pack.scale, check_status=True))
 
@@ -129,7 +130,8 @@ def test_share_d64_against_the_oracle():
     out_o, lse_o = oracle.attention(q, k, v, pack.cu_seqlens, pack.segments, pack.hq, pack.hkv,
                                     pack.d, pack.scale)
     plan = pk.plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d)
-    assert plan.share_schedule()[0].shape[0] > 0
+    assert not plan.kv_share  # opt-in at d = 64
+    plan.set_kv_share(True)
     out, lse = pk.attn_fwd(q.cuda(), k.cuda(), v.cuda(), plan, pack.scale, check_status=True)
     check(pack.name, out.float().cpu().numpy(), lse.cpu().numpy(), out_o, lse_o)
 
@@ -140,7 +142,7 @@ def test_share_against_the_oracle():
     out_o, lse_o = oracle.attention(q, k, v, pack.cu_seqlens, pack.segments, pack.hq, pack.hkv,
                                     pack.d, pack.scale)
     plan = pk.plan(pack.cu_seqlens, pack.segments, pack.hq, pack.hkv, pack.d)
-    assert plan.share_schedule()[0].shape[0] > 0
+    assert plan.kv_share  # the default at d = 128
     out, lse = pk.attn_fwd(q.cuda(), k.cuda(), v.cuda(), plan, pack.scale, check_status=True)
     check(pack.name + "/share", out.float().cpu().numpy(), lse.cpu().numpy(), out_o, lse_o)
 

@@ -43,7 +43,12 @@ def _plans():
 
 @pytest.mark.parametrize("name,plan", _plans(), ids=lambda x: x if isinstance(x, str) else "")
 def test_share_schedule_holds_every_item_once(name, plan):
-    assert plan.kv_share  # on by default wherever the schedule exists
+    # on by default at head_dim 128 wherever the schedule exists, opt-in at 64
+    assert plan.kv_share == (plan.head_dim == 128)
+    plan.set_kv_share(True)
+    assert plan.kv_share
+    plan.set_kv_share(False)
+    assert not plan.kv_share
     items, _ = plan.items()
     sitems, soffs = plan.share_schedule()
     assert sitems.shape == items.shape
